@@ -1,0 +1,296 @@
+"""Thin Python binding of libspecfold.so (include/specfold.h).
+
+Argument marshalling only: torch tensors are passed by data pointer, the
+stream is torch's current CUDA stream, and every step runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is missing, loading
+it raises.  Function names match the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Sequence
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libspecfold.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "specfold.h")
+
+OK, EINVAL, EALIGN, ECAPACITY, EUNSUPPORTED, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6
+DEV_TIMEOUT, DEV_BAD_PARENT = 1, 2
+BF16, F32 = 0, 1
+STAGE_EVENTS = 11
+STAGE_NAMES = ("gate", "select", "rmsnorm1", "qkv", "attention", "out_proj", "rmsnorm2", "gate_up",
+               "down", "fold_fill")
+
+
+class SpecfoldError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {code} ({status_string(code)})")
+
+
+class specfold_dims(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("rms_eps", ctypes.c_float),
+                ("dtype", ctypes.c_int)]
+
+
+class specfold_weights(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_void_p) for k in
+                ("g1", "w_q", "w_k", "w_v", "w_o", "g2", "w_gate", "w_up", "w_down")]
+
+
+class specfold_kv_view(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("token_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64)]
+
+
+class specfold_ws_layout(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_size_t) for k in
+                ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "x1", "q",
+                 "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "total")]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIG = {
+    "specfold_gate": (_I, [_I, _P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "specfold_resolve": (_I, [_P, _P, _I, _I, _P, _P, _P]),
+    "specfold_pack": (_I, [_I, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "specfold_qkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_attention": (_I, [_P, _P, specfold_kv_view, specfold_kv_view, _I, _P, _P, _P, _P, _P, _I, _I,
+                                _P, _P, ctypes.c_size_t, _P]),
+    "specfold_out_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_ffn": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_layer_forward": (_I, [_P, _P, _P, _P, _I, _I, specfold_kv_view, specfold_kv_view, _I,
+                                    ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "specfold_linear": (_I, [_I, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
+    "specfold_linear_workspace_size": (ctypes.c_size_t, [_I, _I]),
+    "specfold_workspace_layout": (_I, [_P, _I, _I, _P]),
+    "specfold_get_status": (_I, [_P, _P, _P]),
+    "specfold_read_n_packed": (_I, [_P, _I, _I, _P, _P, _P]),
+    "specfold_status_string": (ctypes.c_char_p, [_I]),
+    "specfold_launch_count": (ctypes.c_uint64, []),
+    "specfold_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+}
+
+_lib = None
+
+
+def lib(path: str = LIB_PATH):
+    """Load libspecfold.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -m diffusion_branch_speculative_gb300.build)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIG.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions(path: str = HEADER) -> list:
+    """Names of the functions include/specfold.h declares."""
+    txt = open(path).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|uint64_t|const char\*)\s+(specfold_\w+)\s*\(", txt, re.M)))
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().specfold_status_string(code).decode()
+    except Exception:  # library not loadable: still give a message
+        return "status"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise SpecfoldError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float32:
+        return F32
+    raise ValueError(f"unsupported dtype {t}")
+
+
+def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16) -> specfold_dims:
+    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype)
+
+
+def make_weights(w: dict) -> specfold_weights:
+    return specfold_weights(*[ctypes.c_void_p(w[k].data_ptr()) for k in
+                              ("g1", "w_q", "w_k", "w_v", "w_o", "g2", "w_gate", "w_up", "w_down")])
+
+
+def kv_view(t: Optional[torch.Tensor]) -> specfold_kv_view:
+    """A [P, n_kv, hd] strided view (last dim contiguous), passed without copy."""
+    if t is None or t.numel() == 0:
+        return specfold_kv_view(None, 8, 8)
+    assert t.dim() == 3 and t.stride(2) == 1, "prefix view must be [P, n_kv, hd] with unit last stride"
+    return specfold_kv_view(t.data_ptr(), t.stride(0), t.stride(1))
+
+
+def workspace_size(dims: specfold_dims, B: int, L: int) -> int:
+    return int(lib().specfold_workspace_size(ctypes.byref(dims), B, L))
+
+
+def workspace_layout(dims: specfold_dims, B: int, L: int) -> specfold_ws_layout:
+    lo = specfold_ws_layout()
+    _check(lib().specfold_workspace_layout(ctypes.byref(dims), B, L, ctypes.byref(lo)), "specfold_workspace_layout")
+    return lo
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled byte workspace (the library needs it zeroed once)."""
+    return torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)[: nbytes]
+
+
+# ------------------------------------------------------------ entry points --
+
+def specfold_gate(H: torch.Tensor, parent: torch.Tensor, tau: float, fold: torch.Tensor,
+                  rel: Optional[torch.Tensor] = None, stream=None):
+    B, L, d = H.shape
+    _check(lib().specfold_gate(dtype_code(H.dtype), _ptr(H), _ptr(parent), B, L, d, float(tau), _ptr(fold),
+                               _ptr(rel), _stream(stream)), "specfold_gate")
+
+
+def specfold_resolve(fold: torch.Tensor, parent: torch.Tensor, B: int, L: int, src: torch.Tensor,
+                     status: Optional[torch.Tensor] = None, stream=None):
+    _check(lib().specfold_resolve(_ptr(fold), _ptr(parent), B, L, _ptr(src), _ptr(status), _stream(stream)),
+           "specfold_resolve")
+
+
+def specfold_pack(fold, H, g1, eps, packed_idx, slot_of_row, n_dev, X1, stream=None):
+    B, L, d = H.shape
+    _check(lib().specfold_pack(dtype_code(H.dtype), _ptr(fold), _ptr(H), _ptr(g1), float(eps), B, L, d,
+                               _ptr(packed_idx), _ptr(slot_of_row), _ptr(n_dev), _ptr(X1), _stream(stream)),
+           "specfold_pack")
+
+
+def specfold_qkv(dims, weights, X1, packed_idx, n_dev, B, L, Q, blockK, blockV, ws, stream=None):
+    _check(lib().specfold_qkv(ctypes.byref(dims), ctypes.byref(weights), _ptr(X1), _ptr(packed_idx), _ptr(n_dev),
+                              B, L, _ptr(Q), _ptr(blockK), _ptr(blockV), _ptr(ws), ws.numel(), _stream(stream)),
+           "specfold_qkv")
+
+
+def specfold_attention(dims, Q, prefK, prefV, P, blockK, blockV, src, packed_idx, n_dev, B, L, O, ws, stream=None):
+    _check(lib().specfold_attention(ctypes.byref(dims), _ptr(Q), kv_view(prefK), kv_view(prefV), P, _ptr(blockK),
+                                    _ptr(blockV), _ptr(src), _ptr(packed_idx), _ptr(n_dev), B, L, _ptr(O), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "specfold_attention")
+
+
+def specfold_out_proj(dims, weights, O, packed_idx, n_dev, H_in, B, L, A, ws, stream=None):
+    _check(lib().specfold_out_proj(ctypes.byref(dims), ctypes.byref(weights), _ptr(O), _ptr(packed_idx),
+                                   _ptr(n_dev), _ptr(H_in), B, L, _ptr(A), _ptr(ws), ws.numel(), _stream(stream)),
+           "specfold_out_proj")
+
+
+def specfold_ffn(dims, weights, A, packed_idx, n_dev, H_in, src, fold, B, L, H_out, ws, stream=None):
+    _check(lib().specfold_ffn(ctypes.byref(dims), ctypes.byref(weights), _ptr(A), _ptr(packed_idx), _ptr(n_dev),
+                              _ptr(H_in), _ptr(src), _ptr(fold), B, L, _ptr(H_out), _ptr(ws), ws.numel(),
+                              _stream(stream)), "specfold_ffn")
+
+
+def specfold_layer_forward(dims, weights, H_in, parent, prefK, prefV, P, tau, H_out, ws,
+                           events: Optional[Sequence] = None, stream=None):
+    B, L, _ = H_in.shape
+    ev = None
+    if events is not None:
+        assert len(events) == STAGE_EVENTS
+        ev = (ctypes.c_void_p * STAGE_EVENTS)(*[e.cuda_event for e in events])
+    _check(lib().specfold_layer_forward(ctypes.byref(dims), ctypes.byref(weights), _ptr(H_in), _ptr(parent), B, L,
+                                        kv_view(prefK), kv_view(prefV), P, float(tau), _ptr(H_out), _ptr(ws),
+                                        ws.numel(), ev, _stream(stream)), "specfold_layer_forward")
+
+
+def specfold_linear(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor, ws: torch.Tensor, stream=None):
+    M, K = X.shape
+    N = W.shape[0]
+    _check(lib().specfold_linear(dtype_code(X.dtype), _ptr(X), _ptr(W), M, N, K, _ptr(Y), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "specfold_linear")
+
+
+def linear_workspace_size(M: int, N: int) -> int:
+    return int(lib().specfold_linear_workspace_size(M, N))
+
+
+def specfold_get_status(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    rc = lib().specfold_get_status(_ptr(ws), ctypes.byref(v), _stream(stream))
+    if rc not in (OK, EDEVICE):
+        raise SpecfoldError(rc, "specfold_get_status")
+    return int(v.value)
+
+
+def specfold_launch_count() -> int:
+    return int(lib().specfold_launch_count())
+
+
+def specfold_selftest_timeout(status: torch.Tensor, wait_ns: int, stream=None):
+    _check(lib().specfold_selftest_timeout(_ptr(status), int(wait_ns), _stream(stream)), "specfold_selftest_timeout")
+
+
+# ------------------------------------------------------------ convenience --
+
+class FoldedLayer:
+    """One folded verification layer: weights on the device plus a workspace.
+
+    forward(H_in, parent, tau) runs S1..S10 through specfold_layer_forward and
+    returns H_out; intermediates can be read back with `view(name)`.
+    """
+
+    def __init__(self, dims: specfold_dims, weights: dict, B: int, L: int, prefK=None, prefV=None, device="cuda"):
+        self.dims = dims
+        self.w = weights
+        self.cw = make_weights(weights)
+        self.B, self.L = B, L
+        self.prefK, self.prefV = prefK, prefV
+        self.P = 0 if prefK is None else prefK.shape[0]
+        self.lo = workspace_layout(dims, B, L)
+        self.ws = alloc_workspace(self.lo.total, device)
+
+    def forward(self, H_in, parent, tau, H_out=None, events=None, stream=None):
+        if H_out is None:
+            H_out = torch.empty_like(H_in)
+        specfold_layer_forward(self.dims, self.cw, H_in, parent, self.prefK, self.prefV, self.P, tau, H_out,
+                               self.ws, events=events, stream=stream)
+        return H_out
+
+    def view(self, name: str, dtype=None, shape=None) -> torch.Tensor:
+        """A tensor view of one workspace section (see specfold_ws_layout)."""
+        names = [f[0] for f in specfold_ws_layout._fields_]
+        off = getattr(self.lo, name)
+        nxt = min([getattr(self.lo, k) for k in names if getattr(self.lo, k) > off] + [self.lo.total])
+        raw = self.ws[off:nxt]
+        if dtype is not None:
+            es = torch.empty((), dtype=dtype).element_size()
+            raw = raw[: (raw.numel() // es) * es].view(dtype)
+        if shape is not None:
+            n = 1
+            for s in shape:
+                n *= s
+            raw = raw[:n].view(*shape)
+        return raw
+
+    def n_packed(self) -> int:
+        return int(self.view("n_packed", torch.int32)[0].item())
+
+    def status(self) -> int:
+        return specfold_get_status(self.ws)

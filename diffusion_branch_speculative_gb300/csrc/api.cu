@@ -1,0 +1,580 @@
+// C ABI of the folded multi-branch verification layer: argument checks,
+// workspace layout, TMA descriptor encoding and the stage-by-stage launch
+// sequence of specfold_layer_forward.  Everything is asynchronous on the
+// caller's stream; nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "sf_internal.h"
+
+namespace sf {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 0 || dev >= 64) return 1;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 1;
+  }
+  return cached[dev];
+}
+
+int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? SPECFOLD_OK : SPECFOLD_ECUDA; }
+
+// ------------------------------------------------------------ TMA maps --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride_elems,
+                uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SPECFOLD_ECUDA;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_stride_elems * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPECFOLD_OK : SPECFOLD_ECUDA;
+}
+
+int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim, uint64_t heads, uint64_t tokens,
+                uint64_t head_stride, uint64_t token_stride, uint32_t box_tokens) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return SPECFOLD_ECUDA;
+  const cuuint64_t dims[3] = {dim, heads, tokens};
+  const cuuint64_t strides[2] = {head_stride * 2, token_stride * 2};
+  const cuuint32_t box[3] = {64, 1, box_tokens};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPECFOLD_OK : SPECFOLD_ECUDA;
+}
+
+// ------------------------------------------------------------- checks --
+static bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static int esize(int dtype) { return dtype == SPECFOLD_BF16 ? 2 : 4; }
+static bool dtype_ok(int dtype) { return dtype == SPECFOLD_BF16 || dtype == SPECFOLD_F32; }
+
+static int check_rows(int B, int L) {
+  if (B < 1 || L < 1) return SPECFOLD_EINVAL;
+  if (static_cast<long long>(B) * L > SPECFOLD_MAX_ROWS) return SPECFOLD_ECAPACITY;
+  return SPECFOLD_OK;
+}
+
+static int check_dims(const specfold_dims* d) {
+  if (!d) return SPECFOLD_EINVAL;
+  if (!dtype_ok(d->dtype)) return SPECFOLD_EINVAL;
+  if (d->d_model <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 || d->ffn_dim <= 0)
+    return SPECFOLD_EINVAL;
+  if (!(d->rms_eps >= 0.f) || std::isinf(d->rms_eps)) return SPECFOLD_EINVAL;
+  if (d->head_dim != 64 && d->head_dim != 128) return SPECFOLD_EUNSUPPORTED;
+  if (d->n_q_heads % d->n_kv_heads) return SPECFOLD_EUNSUPPORTED;
+  if (d->d_model % 256) return SPECFOLD_EUNSUPPORTED;
+  if ((d->n_q_heads * d->head_dim) % 128 || (d->n_kv_heads * d->head_dim) % 128) return SPECFOLD_EUNSUPPORTED;
+  if (d->ffn_dim % 128) return SPECFOLD_EUNSUPPORTED;
+  return SPECFOLD_OK;
+}
+
+static int check_weights(const specfold_weights* w) {
+  if (!w) return SPECFOLD_EINVAL;
+  const void* ps[9] = {w->g1, w->w_q, w->w_k, w->w_v, w->w_o, w->g2, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : ps) {
+    if (!p) return SPECFOLD_EINVAL;
+    if (!a16(p)) return SPECFOLD_EALIGN;
+  }
+  return SPECFOLD_OK;
+}
+
+static int check_view(const specfold_kv_view& v, int P) {
+  if (P == 0) return SPECFOLD_OK;
+  if (!v.ptr) return SPECFOLD_EINVAL;
+  if (!a16(v.ptr)) return SPECFOLD_EALIGN;
+  if (v.token_stride <= 0 || v.head_stride <= 0) return SPECFOLD_EINVAL;
+  if (v.token_stride % 8 || v.head_stride % 8) return SPECFOLD_EALIGN;
+  return SPECFOLD_OK;
+}
+
+#define SF_TRY(x)              \
+  do {                         \
+    const int _rc = (x);       \
+    if (_rc) return _rc;       \
+  } while (0)
+
+// ------------------------------------------------------ workspace layout --
+static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+static int gemm_counters_for_layer(const specfold_dims* d, int R) {
+  int c = gemm_counters_needed(R, d->n_q_heads * d->head_dim + 2 * d->n_kv_heads * d->head_dim, EPI_QKV);
+  c = std::max(c, gemm_counters_needed(R, d->d_model, EPI_RESID_PACKED));
+  c = std::max(c, gemm_counters_needed(R, d->ffn_dim, EPI_SWIGLU));
+  return c;
+}
+
+static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) {
+  const size_t R = static_cast<size_t>(B) * L;
+  const size_t e = esize(d->dtype);
+  const size_t nq = static_cast<size_t>(d->n_q_heads) * d->head_dim;
+  const size_t nkv = static_cast<size_t>(d->n_kv_heads) * d->head_dim;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += up256(bytes);
+    return at;
+  };
+  o->status = take(4);
+  o->n_packed = take(4);
+  o->fold = take(R);
+  o->rel = take(R * 4);
+  o->src = take(R * 4);
+  o->packed_idx = take(R * 4);
+  o->slot_of_row = take(R * 4);
+  o->x1 = take(R * d->d_model * e);
+  o->q = take(R * nq * e);
+  o->block_k = take(R * nkv * e);
+  o->block_v = take(R * nkv * e);
+  o->attn_o = take(R * nq * e);
+  o->a = take(R * d->d_model * e);
+  o->x2 = take(R * d->d_model * e);
+  o->g = take(R * d->ffn_dim * e);
+  o->gemm_scratch = take(static_cast<size_t>(gemm_counters_for_layer(d, static_cast<int>(R))) * 4);
+  take(gemm_partial_floats() * 4);
+  o->total = off;
+}
+
+struct Scratch {
+  int* counters;
+  int counters_len;
+  float* partial;
+  size_t partial_len;
+};
+
+static Scratch layer_scratch(void* ws, const specfold_dims* d, int B, int L, const specfold_ws_layout& lo) {
+  Scratch s;
+  const int R = B * L;
+  s.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch);
+  s.counters_len = gemm_counters_for_layer(d, R);
+  s.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch +
+                                       up256(static_cast<size_t>(s.counters_len) * 4));
+  s.partial_len = gemm_partial_floats();
+  return s;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+static void fill_scratch(GemmCall& c, const Scratch& s, uint32_t* status) {
+  c.counters = s.counters;
+  c.counters_len = s.counters_len;
+  c.partial = s.partial;
+  c.partial_len = s.partial_len;
+  c.status = status;
+}
+
+// ---------------------------------------------------------- stage bodies --
+static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const void* X1, const int32_t* packed_idx,
+                     const int32_t* n_dev, int R, void* Q, void* bK, void* bV, const Scratch& s, uint32_t* status,
+                     cudaStream_t st) {
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.epi = EPI_QKV;
+  c.A = X1;
+  c.Mcap = R;
+  c.K = d->d_model;
+  c.n_dev = n_dev;
+  c.nb = 3;
+  c.b[0] = w->w_q;
+  c.b[1] = w->w_k;
+  c.b[2] = w->w_v;
+  c.b_rows[0] = d->n_q_heads * d->head_dim;
+  c.b_rows[1] = c.b_rows[2] = d->n_kv_heads * d->head_dim;
+  c.N = c.b_rows[0] + 2 * c.b_rows[1];
+  c.Y = Q;
+  c.Yk = bK;
+  c.Yv = bV;
+  c.row_idx = packed_idx;
+  c.n_q = d->n_q_heads;
+  c.n_kv = d->n_kv_heads;
+  c.hd = d->head_dim;
+  fill_scratch(c, s, status);
+  return launch_gemm(c, st);
+}
+
+static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
+                           const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
+                           const int32_t* n_dev, int B, int L, void* O, uint32_t* status, cudaStream_t st) {
+  AttnCall a;
+  memset(&a, 0, sizeof(a));
+  a.Q = Q;
+  a.pk = pk;
+  a.pv = pv;
+  a.P = P;
+  a.blockK = bK;
+  a.blockV = bV;
+  a.src = src;
+  a.packed_idx = packed_idx;
+  a.n_dev = n_dev;
+  a.B = B;
+  a.L = L;
+  a.n_q = d->n_q_heads;
+  a.n_kv = d->n_kv_heads;
+  a.hd = d->head_dim;
+  a.O = O;
+  a.status = status;
+  return launch_attention(a, st);
+}
+
+static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, const void* O,
+                          const int32_t* packed_idx, const int32_t* n_dev, const void* H_in, int R, void* A,
+                          const Scratch& s, uint32_t* status, cudaStream_t st) {
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.epi = EPI_RESID_PACKED;
+  c.A = O;
+  c.Mcap = R;
+  c.K = d->n_q_heads * d->head_dim;
+  c.n_dev = n_dev;
+  c.nb = 1;
+  c.b[0] = w->w_o;
+  c.b_rows[0] = d->d_model;
+  c.N = d->d_model;
+  c.Y = A;
+  c.ldy = d->d_model;
+  c.resid = H_in;
+  c.ldr = d->d_model;
+  c.row_idx = packed_idx;
+  fill_scratch(c, s, status);
+  return launch_gemm(c, st);
+}
+
+static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const void* A, const int32_t* packed_idx,
+                     const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int R,
+                     void* H_out, void* X2, void* G, const Scratch& s, uint32_t* status, cudaStream_t st,
+                     void* const* ev, int ev0) {
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+  SF_TRY(launch_rmsnorm_rows(d->dtype, A, nullptr, n_dev, R, d->d_model, w->g2, d->rms_eps, X2, st));
+  mark(ev0 + 1);
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.epi = EPI_SWIGLU;
+  c.A = X2;
+  c.Mcap = R;
+  c.K = d->d_model;
+  c.n_dev = n_dev;
+  c.nb = 2;
+  c.b[0] = w->w_gate;
+  c.b[1] = w->w_up;
+  c.b_rows[0] = c.b_rows[1] = d->ffn_dim;
+  c.N = d->ffn_dim;
+  c.Y = G;
+  c.ldy = d->ffn_dim;
+  fill_scratch(c, s, status);
+  SF_TRY(launch_gemm(c, st));
+  mark(ev0 + 2);
+  memset(&c, 0, sizeof(c));
+  c.epi = EPI_RESID_SCATTER;
+  c.A = G;
+  c.Mcap = R;
+  c.K = d->ffn_dim;
+  c.n_dev = n_dev;
+  c.nb = 1;
+  c.b[0] = w->w_down;
+  c.b_rows[0] = d->d_model;
+  c.N = d->d_model;
+  c.Y = H_out;
+  c.ldy = d->d_model;
+  c.resid = A;
+  c.ldr = d->d_model;
+  c.row_idx = packed_idx;
+  fill_scratch(c, s, status);
+  SF_TRY(launch_gemm(c, st));
+  mark(ev0 + 3);
+  SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
+  mark(ev0 + 4);
+  return SPECFOLD_OK;
+}
+
+}  // namespace sf
+
+using namespace sf;
+
+// ======================================================================
+extern "C" {
+
+size_t specfold_workspace_size(const specfold_dims* dims, int B, int L) {
+  if (check_dims(dims) || check_rows(B, L)) return 0;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  return lo.total;
+}
+
+int specfold_workspace_layout(const specfold_dims* dims, int B, int L, specfold_ws_layout* out) {
+  if (!out) return SPECFOLD_EINVAL;
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  layout(dims, B, L, out);
+  return SPECFOLD_OK;
+}
+
+size_t specfold_linear_workspace_size(int M, int N) {
+  if (M <= 0 || N <= 0) return 0;
+  return 256 + up256(static_cast<size_t>(gemm_counters_needed(M, N, EPI_STORE)) * 4) + gemm_partial_floats() * 4;
+}
+
+int specfold_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                  uint8_t* fold, float* rel_opt, void* stream) {
+  if (!dtype_ok(dtype) || !H || !parent || !fold) return SPECFOLD_EINVAL;
+  SF_TRY(check_rows(B, L));
+  if (d <= 0) return SPECFOLD_EINVAL;
+  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;  // rejects NaN too
+  if (d % 256) return SPECFOLD_EUNSUPPORTED;
+  if (!a16(H)) return SPECFOLD_EALIGN;
+  return launch_gate(dtype, H, parent, B, L, d, tau, fold, rel_opt, static_cast<cudaStream_t>(stream));
+}
+
+int specfold_resolve(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src, uint32_t* status_opt,
+                     void* stream) {
+  if (!fold || !parent || !src) return SPECFOLD_EINVAL;
+  SF_TRY(check_rows(B, L));
+  return launch_select(fold, parent, B, L, src, nullptr, nullptr, nullptr, status_opt,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1, float eps, int B, int L, int d,
+                  int32_t* packed_idx, int32_t* slot_of_row, int32_t* n_dev, void* X1, void* stream) {
+  if (!dtype_ok(dtype) || !fold || !H || !g1 || !packed_idx || !slot_of_row || !n_dev || !X1)
+    return SPECFOLD_EINVAL;
+  SF_TRY(check_rows(B, L));
+  if (d <= 0 || !(eps >= 0.f)) return SPECFOLD_EINVAL;
+  if (d % 256) return SPECFOLD_EUNSUPPORTED;
+  if (!a16(H) || !a16(g1) || !a16(X1)) return SPECFOLD_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // pack alone: every row is its own source unless folded (no parent walk),
+  // so the scan runs on fold with a trivial parent table of the root only.
+  SF_TRY(launch_select(fold, nullptr, B, L, nullptr, packed_idx, slot_of_row, n_dev, nullptr, st));
+  return launch_rmsnorm_rows(dtype, H, packed_idx, n_dev, B * L, d, g1, eps, X1, st);
+}
+
+int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const void* X1, const int32_t* packed_idx,
+                 const int32_t* n_dev, int B, int L, void* Q, void* blockK, void* blockV, void* ws, size_t ws_bytes,
+                 void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  SF_TRY(check_weights(w));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!X1 || !packed_idx || !n_dev || !Q || !blockK || !blockV || !ws) return SPECFOLD_EINVAL;
+  if (!a16(X1) || !a16(Q) || !a16(blockK) || !a16(blockV) || !a16(ws)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  return stage_qkv(dims, w, X1, packed_idx, n_dev, B * L, Q, blockK, blockV, s, at<uint32_t>(ws, lo.status),
+                   static_cast<cudaStream_t>(stream));
+}
+
+int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_view prefK, specfold_kv_view prefV,
+                       int P, const void* blockK, const void* blockV, const int32_t* src, const int32_t* packed_idx,
+                       const int32_t* n_dev, int B, int L, void* O, void* ws, size_t ws_bytes, void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (P < 0 || !Q || !blockK || !blockV || !src || !packed_idx || !n_dev || !O || !ws) return SPECFOLD_EINVAL;
+  SF_TRY(check_view(prefK, P));
+  SF_TRY(check_view(prefV, P));
+  if (!a16(Q) || !a16(blockK) || !a16(blockV) || !a16(O)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.status + 256) return SPECFOLD_ECAPACITY;
+  return stage_attention(dims, Q, prefK, prefV, P, blockK, blockV, src, packed_idx, n_dev, B, L, O,
+                         at<uint32_t>(ws, lo.status), static_cast<cudaStream_t>(stream));
+}
+
+int specfold_out_proj(const specfold_dims* dims, const specfold_weights* w, const void* O, const int32_t* packed_idx,
+                      const int32_t* n_dev, const void* H_in, int B, int L, void* A, void* ws, size_t ws_bytes,
+                      void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  SF_TRY(check_weights(w));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!O || !packed_idx || !n_dev || !H_in || !A || !ws) return SPECFOLD_EINVAL;
+  if (!a16(O) || !a16(H_in) || !a16(A)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  return stage_out_proj(dims, w, O, packed_idx, n_dev, H_in, B * L, A, s, at<uint32_t>(ws, lo.status),
+                        static_cast<cudaStream_t>(stream));
+}
+
+int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const void* A, const int32_t* packed_idx,
+                 const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int B, int L,
+                 void* H_out, void* ws, size_t ws_bytes, void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  SF_TRY(check_weights(w));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!A || !packed_idx || !n_dev || !H_in || !src || !fold || !H_out || !ws) return SPECFOLD_EINVAL;
+  if (!a16(A) || !a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  return stage_ffn(dims, w, A, packed_idx, n_dev, H_in, src, fold, B * L, H_out, at<void>(ws, lo.x2),
+                   at<void>(ws, lo.g), s, at<uint32_t>(ws, lo.status), static_cast<cudaStream_t>(stream), nullptr,
+                   0);
+}
+
+int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                           const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV, int P,
+                           float tau, void* H_out, void* ws, size_t ws_bytes, void* const* stage_events,
+                           void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  SF_TRY(check_weights(w));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!H_in || !parent || !H_out || !ws || P < 0) return SPECFOLD_EINVAL;
+  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
+  SF_TRY(check_view(prefK, P));
+  SF_TRY(check_view(prefV, P));
+  if (!a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int R = B * L;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  uint32_t* status = at<uint32_t>(ws, lo.status);
+  uint8_t* fold = at<uint8_t>(ws, lo.fold);
+  int32_t* src = at<int32_t>(ws, lo.src);
+  int32_t* pidx = at<int32_t>(ws, lo.packed_idx);
+  int32_t* n_dev = at<int32_t>(ws, lo.n_packed);
+  auto mark = [&](int i) {
+    if (stage_events) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
+  };
+  mark(0);
+  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st));
+  mark(1);
+  SF_TRY(launch_select(fold, parent, B, L, src, pidx, at<int32_t>(ws, lo.slot_of_row), n_dev, status, st));
+  mark(2);
+  SF_TRY(launch_rmsnorm_rows(dims->dtype, H_in, pidx, n_dev, R, dims->d_model, w->g1, dims->rms_eps,
+                             at<void>(ws, lo.x1), st));
+  mark(3);
+  SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
+                   at<void>(ws, lo.block_v), s, status, st));
+  mark(4);
+  SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
+                         at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status, st));
+  mark(5);
+  SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st));
+  mark(6);
+  return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
+                   at<void>(ws, lo.g), s, status, st, stage_events, 6);
+}
+
+int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (dtype != SPECFOLD_BF16) return dtype_ok(dtype) ? SPECFOLD_EUNSUPPORTED : SPECFOLD_EINVAL;
+  if (!X || !W || !Y || !ws || M <= 0 || N <= 0 || K <= 0) return SPECFOLD_EINVAL;
+  if (K % 64 || N % 128) return SPECFOLD_EUNSUPPORTED;
+  if (!a16(X) || !a16(W) || !a16(Y) || !a16(ws)) return SPECFOLD_EALIGN;
+  if (ws_bytes < specfold_linear_workspace_size(M, N)) return SPECFOLD_ECAPACITY;
+  GemmCall c;
+  memset(&c, 0, sizeof(c));
+  c.epi = EPI_STORE;
+  c.A = X;
+  c.Mcap = M;
+  c.K = K;
+  c.n_dev = nullptr;
+  c.nb = 1;
+  c.b[0] = W;
+  c.b_rows[0] = N;
+  c.N = N;
+  c.Y = Y;
+  c.ldy = N;
+  c.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 256);
+  c.counters_len = gemm_counters_needed(M, N, EPI_STORE);
+  c.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256 + up256(static_cast<size_t>(c.counters_len) * 4));
+  c.partial_len = gemm_partial_floats();
+  c.status = static_cast<uint32_t*>(ws);
+  return launch_gemm(c, static_cast<cudaStream_t>(stream));
+}
+
+int specfold_get_status(void* ws, uint32_t* status_out, void* stream) {
+  if (!ws) return SPECFOLD_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return SPECFOLD_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SPECFOLD_ECUDA;
+  if (status_out) *status_out = v;
+  if (v) {
+    if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess) return SPECFOLD_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SPECFOLD_ECUDA;
+    return SPECFOLD_EDEVICE;
+  }
+  return SPECFOLD_OK;
+}
+
+int specfold_read_n_packed(const void* ws, int B, int L, const specfold_dims* dims, int32_t* n_out, void* stream) {
+  if (!ws || !n_out) return SPECFOLD_EINVAL;
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(n_out, static_cast<const uint8_t*>(ws) + lo.n_packed, 4, cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return SPECFOLD_ECUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? SPECFOLD_OK : SPECFOLD_ECUDA;
+}
+
+const char* specfold_status_string(int s) {
+  switch (s) {
+    case SPECFOLD_OK: return "ok";
+    case SPECFOLD_EINVAL: return "invalid argument";
+    case SPECFOLD_EALIGN: return "pointer or stride not 16-byte aligned";
+    case SPECFOLD_ECAPACITY: return "capacity exceeded (workspace or rows)";
+    case SPECFOLD_EUNSUPPORTED: return "shape not supported by the kernels";
+    case SPECFOLD_ECUDA: return "CUDA runtime error";
+    case SPECFOLD_EDEVICE: return "device reported an error (see status bits)";
+    default: return "unknown status";
+  }
+}
+
+uint64_t specfold_launch_count(void) { return g_launches.load(); }
+
+int specfold_selftest_timeout(uint32_t* status, uint64_t wait_ns, void* stream) {
+  if (!status) return SPECFOLD_EINVAL;
+  if (wait_ns > 1000000000ull) wait_ns = 1000000000ull;
+  return launch_timeout_probe(status, wait_ns, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+// Folded attention (S5) on the 5th-generation tensor cores.
+//
+// One CTA takes 128 query rows of one KV head: row m = k*g + j is query head
+// (h*g + j) of packed row k, so a tile mixes the GQA group and consecutive
+// packed rows, which may belong to several branches.  Keys are streamed in
+// blocks of 128:
+//   * the shared prefix (all branches see it) through a 3-D TMA map over the
+//     caller's strided view -- never copied per branch;
+//   * then the L block keys of every branch present in the tile, gathered
+//     through the provenance table (key j of branch b is row src[b*L + j] of
+//     the block K/V), with scores of other branches' keys masked.
+// S = Q K^T and O_blk = P V run as tcgen05.mma into TMEM (two S and two O
+// buffers so the next S overlaps the softmax); four softmax warps own one
+// query row per thread, keep the running max/sum and the output accumulator
+// in registers, and write P (bf16) to shared memory for the P V product.
+//
+// Roles (256 threads): warps 0-2 load (TMA for prefix and Q, gathers for
+// block keys), warp 3 allocates TMEM and issues MMAs, warps 4-7 softmax
+// (warp w may only touch TMEM lanes 32*(w%4) .. +31).  Eight warps keep two
+// warps per SM sub-partition, so a softmax thread can hold its 128-float
+// output row in registers.
+#include "sf_device.cuh"
+#include "sf_internal.h"
+
+#include <cmath>
+#include <cstring>
+
+namespace sf {
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kLoaders = 96;
+constexpr int kAtom = 128 * 128;  // one 128-row x 128-byte swizzle block
+
+struct AttnParams {
+  CUtensorMap mapQ;
+  CUtensorMap mapK;
+  CUtensorMap mapV;
+  const __nv_bfloat16* bK;
+  const __nv_bfloat16* bV;
+  const int32_t* src;
+  const int32_t* packed_idx;
+  const int32_t* n_dev;
+  __nv_bfloat16* O;
+  int P, L, R, n_kv, g, n_q;
+  float sl2;  // log2(e) / sqrt(hd)
+  uint32_t* status;
+};
+
+template <int HD>
+struct ACfg {
+  static constexpr int NATOM = HD / 64;
+  static constexpr int Q_BYTES = kAtom * NATOM;
+  static constexpr int KV_BYTES = kAtom * NATOM;  // one K (or V) tile of 128 keys
+  static constexpr int P_BYTES = 2 * kAtom;       // 128 rows x 128 keys bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = Q_BYTES;          // stage s: K at +2s*KV, V at +(2s+1)*KV
+  static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
+  static constexpr int OFF_META = OFF_P + P_BYTES;          // int [2][128]
+  static constexpr int OFF_BAR = OFF_META + 2 * 128 * 4;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = 256;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = ACfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_free = bars + 7;    // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_full = bars + 10;   // [2]
+  uint64_t* o_free = bars + 12;   // [2]
+  uint64_t* drain = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* okflag = abort_flag + 1;  // [2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.x * 128;
+  const int g = p.g, L = p.L;
+  const int n = min(max(p.n_dev[0], 0), p.R);
+  const int rows_total = n * g;
+  if (m0 >= rows_total) return;
+  const int k_lo = m0 / g;
+  const int k_hi = min(n - 1, (m0 + 127) / g);
+  const int B = p.R / L;
+  const int b_lo = min(max(p.packed_idx[k_lo] / L, 0), B - 1);
+  const int b_hi = min(max(p.packed_idx[k_hi] / L, b_lo), B - 1);
+  const int keys_blk = (b_hi - b_lo + 1) * L;
+  const int NBP = (p.P + 127) / 128;
+  const int NB = NBP + (keys_blk + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&kv_full[i]), 1);
+      mbar_init(smem_u32(&kv_empty[i]), 1);
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_free[i]), 128);
+      mbar_init(smem_u32(&o_full[i]), 1);
+      mbar_init(smem_u32(&o_free[i]), 128);
+    }
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 3) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sP = smem + C::OFF_P;
+
+  if (warp < 3) {
+    // ------------------------------------------------------------ loaders --
+    const int lt = threadIdx.x;
+    if (lt == 0) {
+      prefetch_tmap(&p.mapQ);
+      if (NBP > 0) {
+        prefetch_tmap(&p.mapK);
+        prefetch_tmap(&p.mapV);
+      }
+      mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
+      for (int a = 0; a < C::NATOM; ++a)
+        tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + m0);
+    }
+    int issued_tma = -1;
+    for (int j = 0; j < NB; ++j) {
+      const int st = j & 1;
+      if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((j >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+      named_bar_sync(1, kLoaders);
+      if (!okflag[st]) break;
+      uint8_t* sK = smem + C::OFF_KV + (2 * st) * C::KV_BYTES;
+      uint8_t* sV = sK + C::KV_BYTES;
+      if (j < NBP) {
+        if (lt == 0) {
+          const uint32_t fb = smem_u32(&kv_full[st]);
+          mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+          for (int a = 0; a < C::NATOM; ++a) {
+            tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, j * 128);
+            tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, j * 128);
+          }
+          issued_tma = j;
+        }
+      } else {
+        for (int kr = lt; kr < 128; kr += kLoaders) {
+          const int e = (j - NBP) * 128 + kr;
+          int bb = -1;
+          const uint4* krow = nullptr;
+          const uint4* vrow = nullptr;
+          if (e < keys_blk) {
+            const int b = b_lo + e / L;
+            const int s = p.src[b * L + (e - (e / L) * L)];
+            if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
+              bb = b;
+              const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
+              krow = reinterpret_cast<const uint4*>(p.bK + off);
+              vrow = reinterpret_cast<const uint4*>(p.bV + off);
+            }
+          }
+          meta[st * 128 + kr] = bb;
+#pragma unroll
+          for (int c16 = 0; c16 < HD / 8; ++c16) {
+            const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
+            const uint4 vv = vrow ? __ldg(vrow + c16) : make_uint4(0, 0, 0, 0);
+            const int off = (c16 >> 3) * kAtom + kr * 128 + (((c16 & 7) ^ (kr & 7)) << 4);
+            *reinterpret_cast<uint4*>(sK + off) = kv;
+            *reinterpret_cast<uint4*>(sV + off) = vv;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kLoaders);
+        if (lt == 0) mbar_arrive(smem_u32(&kv_full[st]));
+      }
+    }
+    if (lt == 0 && *abort_flag && issued_tma >= 0) {
+      int never = 0;
+      mbar_wait(smem_u32(&kv_full[issued_tma & 1]), (issued_tma >> 1) & 1, &never, nullptr, 10000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax --
+    const int qw = warp & 3;
+    const int row = qw * 32 + lane;
+    const int m = m0 + row;
+    const bool valid = m < rows_total;
+    const int k = valid ? m / g : 0;
+    const int hg = m - (m / g) * g;
+    const int my_b = valid ? p.packed_idx[k] / L : -2;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    float o[HD];
+#pragma unroll
+    for (int e = 0; e < HD; ++e) o[e] = 0.f;
+    float m_run = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+    for (int j = 0; j < NB && ok; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(smem_u32(&s_full[sb]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      const bool prefix = j < NBP;
+      if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const int* mb = meta + sb * 128;
+      const int key0 = j * 128;
+      const uint32_t ts = tmem + lane_off + sb * 128;
+      // pass 1: row max of the unmasked scores
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(ts + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int key = c * 32 + e;
+          const bool keep = prefix ? (key0 + key < p.P) : (mb[key] == my_b);
+          if (keep) mx = fmaxf(mx, __uint_as_float(r[e]));
+        }
+      }
+      const float m_new = fmaxf(m_run, mx * p.sl2);
+      // fold the previous block's P V into the accumulator (also frees P)
+      if (j >= 1) {
+        const int ob = (j - 1) & 1;
+        if (!mbar_wait(smem_u32(&o_full[ob]), ((j - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&o_free[ob]));
+      }
+      const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
+      l *= alpha;
+      // pass 2: probabilities -> bf16 P tile (K-major, 128-byte swizzle)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(ts + c * 32, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int key = c * 32 + e + t;
+            const bool keep = prefix ? (key0 + key < p.P) : (mb[key] == my_b);
+            pv[t] = keep ? ex2(fmaf(__uint_as_float(r[e + t]), p.sl2, -m_new)) : 0.f;
+            l += pv[t];
+          }
+          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
+          const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s_free[sb]));
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(p_full));
+      m_run = m_new;
+      alpha_prev = alpha;
+    }
+    if (ok) {
+      const int ob = (NB - 1) & 1;
+      if (mbar_wait(smem_u32(&o_full[ob]), ((NB - 1) >> 1) & 1, abort_flag, p.status)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
+        }
+        if (valid) {
+          const float inv = 1.f / l;
+          uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
+                                                static_cast<size_t>(h * g + hg) * HD);
+#pragma unroll
+          for (int q8 = 0; q8 < HD / 8; ++q8)
+            dst[q8] = make_uint4(pack_bf16x2(o[8 * q8] * inv, o[8 * q8 + 1] * inv),
+                                 pack_bf16x2(o[8 * q8 + 2] * inv, o[8 * q8 + 3] * inv),
+                                 pack_bf16x2(o[8 * q8 + 4] * inv, o[8 * q8 + 5] * inv),
+                                 pack_bf16x2(o[8 * q8 + 6] * inv, o[8 * q8 + 7] * inv));
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, HD, true);
+      bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.status);
+      const uint32_t aQ = smem_u32(sQ);
+      const uint32_t aP = smem_u32(sP);
+      auto issue_pv = [&](int i) -> bool {
+        if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
+        const int ob = i & 1;
+        if (!mbar_wait(smem_u32(&o_free[ob]), ((i >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (i & 1) + 1) * C::KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          tc_mma_f16(tmem + C::COL_O + ob * HD,
+                     sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&o_full[ob]));
+        tc_commit(smem_u32(&kv_empty[i & 1]));
+        return true;
+      };
+      for (int j = 0; j < NB && ok; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(smem_u32(&kv_full[st]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&s_free[st]), ((j >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * st) * C::KV_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          tc_mma_f16(tmem + st * 128,
+                     sdesc_sw128(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                     sdesc_sw128(aK + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&s_full[st]));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(NB - 1);
+      tc_commit(smem_u32(drain));
+      int never = 0;
+      mbar_wait(smem_u32(drain), 0, &never, nullptr, 10000000ull);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 3) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int HD>
+int run_attn(const AttnCall& c, cudaStream_t st) {
+  using C = ACfg<HD>;
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  const int R = c.B * c.L;
+  const int g = c.n_q / c.n_kv;
+  int rc = make_map_2d(&p.mapQ, c.Q, static_cast<uint64_t>(c.n_kv) * R * g, HD, HD, 128);
+  if (rc) return rc;
+  if (c.P > 0) {
+    rc = make_map_3d(&p.mapK, c.pk.ptr, HD, c.n_kv, c.P, c.pk.head_stride, c.pk.token_stride, 128);
+    if (rc) return rc;
+    rc = make_map_3d(&p.mapV, c.pv.ptr, HD, c.n_kv, c.P, c.pv.head_stride, c.pv.token_stride, 128);
+    if (rc) return rc;
+  }
+  p.bK = static_cast<const __nv_bfloat16*>(c.blockK);
+  p.bV = static_cast<const __nv_bfloat16*>(c.blockV);
+  p.src = c.src;
+  p.packed_idx = c.packed_idx;
+  p.n_dev = c.n_dev;
+  p.O = static_cast<__nv_bfloat16*>(c.O);
+  p.P = c.P;
+  p.L = c.L;
+  p.R = R;
+  p.n_kv = c.n_kv;
+  p.g = g;
+  p.n_q = c.n_q;
+  p.sl2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  p.status = c.status;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
+      return SPECFOLD_ECUDA;
+    attr_done[dev] = 1;
+  }
+  const dim3 grid((R * g + 127) / 128, c.n_kv);
+  attn_kernel<HD><<<grid, kAttnThreads, C::SMEM_BYTES, st>>>(p);
+  count_launch();
+  return check_launch();
+}
+
+}  // namespace
+
+int launch_attention(const AttnCall& c, cudaStream_t st) {
+  if (c.hd == 128) return run_attn<128>(c, st);
+  if (c.hd == 64) return run_attn<64>(c, st);
+  return SPECFOLD_EUNSUPPORTED;
+}
+
+}  // namespace sf

@@ -1,0 +1,373 @@
+// Row-wise kernels of the folded layer: the residual gate (S1), provenance
+// resolve + pack scan (S2, S3), the RMSNorm gathers (S3, S7) and the fold-fill
+// of folded rows (S10).  All are HBM-bound: one warp per row, 16-byte
+// vectorised coalesced loads, fp32 warp-shuffle reductions.
+#include "sf_device.cuh"
+#include "sf_internal.h"
+
+namespace sf {
+namespace {
+
+template <typename T>
+struct VecT;
+template <>
+struct VecT<__nv_bfloat16> {
+  static constexpr int N = 8;  // elements per 16-byte vector
+  SF_DEV static void unpack(const uint4& u, float (&f)[8]) {
+    f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+    f[4] = bf16lo(u.z); f[5] = bf16hi(u.z); f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+  }
+  SF_DEV static uint4 pack(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+template <>
+struct VecT<float> {
+  static constexpr int N = 4;
+  SF_DEV static void unpack(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  SF_DEV static uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+SF_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int kRowWarps = 8;  // warps (rows) per block of the row kernels
+
+// ------------------------------------------------------------------ S1 gate --
+// One warp per row (b, i).  Child row and parent row are streamed once each
+// (the parent row is shared by all its children and is normally an L2 hit).
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d,
+            float tau, uint8_t* __restrict__ fold, float* __restrict__ rel) {
+  using V = VecT<T>;
+  const int row = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B * L) return;
+  const int b = row / L, i = row - b * L;
+  const int p = b > 0 ? parent[b] : -1;
+  if (b == 0 || p < 0 || p >= b) {  // root, or a parent the resolver will reject
+    if (lane == 0) {
+      fold[row] = 0;
+      if (rel) rel[row] = -1.f;
+    }
+    return;
+  }
+  const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(row) * d);
+  const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(p) * L + i) * d);
+  const int nv = d / V::N;
+  float num = 0.f, den = 0.f;
+  constexpr int U = 4;
+  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+    uint4 cv[U], pv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * 32;
+      if (v < nv) {
+        cv[u] = __ldg(c + v);
+        pv[u] = __ldg(q + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * 32;
+      if (v < nv) {
+        float fc[V::N], fp[V::N];
+        V::unpack(cv[u], fc);
+        V::unpack(pv[u], fp);
+#pragma unroll
+        for (int e = 0; e < V::N; ++e) {
+          const float df = fc[e] - fp[e];
+          num = fmaf(df, df, num);
+          den = fmaf(fp[e], fp[e], den);
+        }
+      }
+    }
+  }
+  num = warp_sum(num);
+  den = warp_sum(den);
+  if (lane == 0) {
+    const bool f = (num < tau * tau * den) || (num == 0.f && tau > 0.f);
+    fold[row] = f ? 1 : 0;
+    if (rel) rel[row] = den > 0.f ? sqrtf(num / den) : (num == 0.f ? 0.f : __int_as_float(0x7f800000));
+  }
+}
+
+// --------------------------------------------------- S2 + S3 resolve / scan --
+// One block.  A row is recomputed iff fold[r] == 0, it is a root row, or its
+// branch's parent is invalid (the chain cannot continue).  src follows the
+// fold chain through first parents.  The packed list is an exclusive scan of
+// the recomputed flags in row order, each thread owning a contiguous segment.
+constexpr int kSelectThreads = 1024;
+
+// Branch whose row (., i) ends the fold chain that starts at (b, i).  Without
+// a parent table (pack alone) a folded non-root row is simply not recomputed.
+SF_DEV int chain_end(const uint8_t* fold, const int32_t* parent, int b, int i, int L) {
+  if (!parent) return (b > 0 && fold[b * L + i]) ? -1 : b;
+  int s = b;
+  while (s > 0 && fold[s * L + i]) {
+    const int p = parent[s];
+    if (p < 0 || p >= s) break;
+    s = p;
+  }
+  return s;
+}
+
+__global__ void __launch_bounds__(kSelectThreads)
+select_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ parent, int B, int L,
+              int32_t* __restrict__ src, int32_t* __restrict__ packed_idx,
+              int32_t* __restrict__ slot, int32_t* __restrict__ n_dev, uint32_t* status) {
+  __shared__ int s_bad;
+  __shared__ int s_warp[kSelectThreads / 32];
+  const int tid = threadIdx.x;
+  const int R = B * L;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int b = tid; parent && b < B; b += kSelectThreads) {
+    const int p = parent[b];
+    if ((b == 0 && p != -1) || (b > 0 && (p < 0 || p >= b))) atomicOr(&s_bad, 1);
+  }
+  const int ipt = (R + kSelectThreads - 1) / kSelectThreads;
+  const int r0 = min(R, tid * ipt), r1 = min(R, r0 + ipt);
+  int cnt = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int b = r / L, i = r - b * L;
+    const int s = chain_end(fold, parent, b, i, L);
+    const int sr = s < 0 ? -1 : s * L + i;
+    if (src) src[r] = sr;
+    cnt += (sr == r);
+  }
+  // block exclusive scan of cnt
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    s_warp[lane] = v;  // inclusive warp totals
+  }
+  __syncthreads();
+  int off = (w > 0 ? s_warp[w - 1] : 0) + incl - cnt;
+  for (int r = r0; r < r1; ++r) {
+    const int b = r / L, i = r - b * L;
+    const int s = chain_end(fold, parent, b, i, L);
+    const bool act = s >= 0 && (s * L + i) == r;
+    if (act) {
+      if (packed_idx) packed_idx[off] = r;
+      if (slot) slot[r] = off;
+      ++off;
+    } else if (slot) {
+      slot[r] = -1;
+    }
+  }
+  if (tid == kSelectThreads - 1 && n_dev) n_dev[0] = s_warp[31];
+  if (tid == 0 && s_bad && status) atomicOr(status, SPECFOLD_DEV_BAD_PARENT);
+}
+
+// ------------------------------------------------------- RMSNorm gathers --
+// Y[k] = X[idx[k]] * g / sqrt(mean(X^2) + eps), one warp per output row; the
+// row is held in registers between the reduction and the scaled store.
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(kRowWarps * 32)
+rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ n_dev, int R, int d, const T* __restrict__ g,
+                    float eps, T* __restrict__ Y) {
+  using V = VecT<T>;
+  const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
+  if (k >= n) return;
+  const int r = idx ? idx[k] : k;
+  const uint4* x = reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * d);
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  uint4* y = reinterpret_cast<uint4*>(Y + static_cast<size_t>(k) * d);
+  const int nv = d / V::N;
+  const int per_lane = (nv + 31) / 32;
+  uint4 v[MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    if (j < per_lane && lane + 32 * j < nv) v[j] = __ldg(x + lane + 32 * j);
+  }
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    if (j < per_lane && lane + 32 * j < nv) {
+      float f[V::N];
+      V::unpack(v[j], f);
+#pragma unroll
+      for (int e = 0; e < V::N; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    const int vi = lane + 32 * j;
+    if (j < per_lane && vi < nv) {
+      float f[V::N], gf[V::N];
+      V::unpack(v[j], f);
+      V::unpack(__ldg(gv + vi), gf);
+#pragma unroll
+      for (int e = 0; e < V::N; ++e) f[e] = f[e] * inv * gf[e];
+      y[vi] = V::pack(f);
+    }
+  }
+}
+
+// -------------------------------------------------------------- S10 fill --
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ src,
+                 const T* __restrict__ Hin, T* __restrict__ Hout, int R, int d) {
+  using V = VecT<T>;
+  const int r = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R || !fold[r]) return;
+  const int s = src[r];
+  if (s == r || s < 0 || s >= R) return;
+  const uint4* os = reinterpret_cast<const uint4*>(Hout + static_cast<size_t>(s) * d);
+  const uint4* ir = reinterpret_cast<const uint4*>(Hin + static_cast<size_t>(r) * d);
+  const uint4* is = reinterpret_cast<const uint4*>(Hin + static_cast<size_t>(s) * d);
+  uint4* orow = reinterpret_cast<uint4*>(Hout + static_cast<size_t>(r) * d);
+  const int nv = d / V::N;
+  constexpr int U = 2;
+  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+    uint4 a[U], b[U], c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nv) {
+        a[u] = os[v];
+        b[u] = __ldg(ir + v);
+        c[u] = __ldg(is + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nv) {
+        float fa[V::N], fb[V::N], fc[V::N];
+        V::unpack(a[u], fa);
+        V::unpack(b[u], fb);
+        V::unpack(c[u], fc);
+#pragma unroll
+        for (int e = 0; e < V::N; ++e) fa[e] = fa[e] + (fb[e] - fc[e]);
+        orow[v] = V::pack(fa);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------ bounded-wait probe --
+__global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing arrives on this barrier: the wait has to run out.
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, wait_ns);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                uint8_t* fold, float* rel, cudaStream_t st) {
+  const int R = B * L;
+  const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
+  if (dtype == SPECFOLD_BF16)
+    gate_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(H), parent, B, L, d, tau, fold, rel);
+  else
+    gate_kernel<float><<<grid, block, 0, st>>>(static_cast<const float*>(H), parent, B, L, d, tau,
+                                               fold, rel);
+  count_launch();
+  return check_launch();
+}
+
+int launch_select(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src,
+                  int32_t* packed_idx, int32_t* slot, int32_t* n_dev, uint32_t* status,
+                  cudaStream_t st) {
+  select_kernel<<<1, kSelectThreads, 0, st>>>(fold, parent, B, L, src, packed_idx, slot, n_dev,
+                                              status);
+  count_launch();
+  return check_launch();
+}
+
+template <typename T>
+static void rmsnorm_dispatch(const void* X, const int32_t* idx, const int32_t* n_dev, int R,
+                             int d, const void* g, float eps, void* Y, cudaStream_t st) {
+  const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
+  const int per_lane = (d / VecT<T>::N + 31) / 32;
+  const T* x = static_cast<const T*>(X);
+  const T* gg = static_cast<const T*>(g);
+  T* y = static_cast<T*>(Y);
+  if (per_lane <= 4)
+    rmsnorm_rows_kernel<T, 4><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+  else if (per_lane <= 8)
+    rmsnorm_rows_kernel<T, 8><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+  else if (per_lane <= 16)
+    rmsnorm_rows_kernel<T, 16><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+  else
+    rmsnorm_rows_kernel<T, 32><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+}
+
+int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
+                        int R, int d, const void* g, float eps, void* Y, cudaStream_t st) {
+  const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
+  if (per_lane > 32) return SPECFOLD_EUNSUPPORTED;
+  if (dtype == SPECFOLD_BF16)
+    rmsnorm_dispatch<__nv_bfloat16>(X, idx, n_dev, R, d, g, eps, Y, st);
+  else
+    rmsnorm_dispatch<float>(X, idx, n_dev, R, d, g, eps, Y, st);
+  count_launch();
+  return check_launch();
+}
+
+int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const void* H_in,
+                     void* H_out, int R, int d, cudaStream_t st) {
+  const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
+  if (dtype == SPECFOLD_BF16)
+    fold_fill_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
+        fold, src, static_cast<const __nv_bfloat16*>(H_in), static_cast<__nv_bfloat16*>(H_out), R,
+        d);
+  else
+    fold_fill_kernel<float><<<grid, block, 0, st>>>(fold, src, static_cast<const float*>(H_in),
+                                                    static_cast<float*>(H_out), R, d);
+  count_launch();
+  return check_launch();
+}
+
+int launch_timeout_probe(uint32_t* status, uint64_t wait_ns, cudaStream_t st) {
+  timeout_probe_kernel<<<1, 32, 0, st>>>(status, wait_ns);
+  count_launch();
+  return check_launch();
+}
+
+}  // namespace sf

@@ -1,0 +1,100 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "specfold.h"
+
+namespace sf {
+
+// ---- launch bookkeeping ----
+void count_launch(int n = 1);
+int num_sms();                        // SMs of the current device (cached per device)
+int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a launch
+
+// ---- row-wise kernels (rowwise.cu) ----
+// gate: fold/rel per row; dtype bf16 or f32.
+int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                uint8_t* fold, float* rel, cudaStream_t st);
+// resolve + pack scan in one block; any output may be null.
+int launch_select(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src,
+                  int32_t* packed_idx, int32_t* slot, int32_t* n_dev, uint32_t* status,
+                  cudaStream_t st);
+// Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
+int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
+                        int R, int d, const void* g, float eps, void* Y, cudaStream_t st);
+// H_out[r] = H_out[s] + H_in[r] - H_in[s] for folded rows r, s = src[r].
+int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const void* H_in,
+                     void* H_out, int R, int d, cudaStream_t st);
+int launch_timeout_probe(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
+
+// ---- tcgen05 GEMM (gemm_tc.cu) ----
+enum GemmEpi : int {
+  EPI_STORE = 0,          // Y[k][c] = acc                      (plain, identity rows)
+  EPI_QKV = 1,            // Q head-group layout, K/V rows at row_idx[k]
+  EPI_RESID_PACKED = 2,   // Y[k][c] = acc + resid[row_idx[k]][c]
+  EPI_SWIGLU = 3,         // Y[k][f] = silu(acc_gate) * acc_up
+  EPI_RESID_SCATTER = 4,  // Y[row_idx[k]][c] = acc + resid[k][c]
+};
+
+struct GemmCall {
+  int epi;
+  const void* A;          // [Mcap, K] bf16 row-major
+  int Mcap;               // rows of A (and of the row-indexed outputs)
+  int K;
+  const int32_t* n_dev;   // rows to compute (device); null -> Mcap
+  // B operands: `nb` weights stacked along N; for SWIGLU, b[0] = gate, b[1] = up
+  const void* b[3];
+  int b_rows[3];
+  int nb;
+  int N;                  // total output columns (SWIGLU: F)
+  // epilogue
+  void* Y;
+  long long ldy;
+  const void* resid;
+  long long ldr;
+  const int32_t* row_idx;
+  void* Yk;               // QKV: block K / V outputs
+  void* Yv;
+  int n_q, n_kv, hd;      // QKV head layout
+  // scratch: tile counters (zero on entry, left zero) and fp32 partial sums
+  int* counters;
+  int counters_len;
+  float* partial;
+  size_t partial_len;     // floats, >= gemm_partial_floats()
+  uint32_t* status;
+};
+size_t gemm_partial_floats();
+int gemm_counters_needed(int Mcap, int N, int epi);
+int launch_gemm(const GemmCall& c, cudaStream_t st);
+
+// ---- tcgen05 attention (attn_tc.cu) ----
+struct AttnCall {
+  const void* Q;          // [n_kv, R*g, hd]
+  specfold_kv_view pk, pv;
+  int P;
+  const void* blockK;     // [R, n_kv, hd]
+  const void* blockV;
+  const int32_t* src;
+  const int32_t* packed_idx;
+  const int32_t* n_dev;
+  int B, L, n_q, n_kv, hd;
+  void* O;                // [R, n_q*hd]
+  uint32_t* status;
+};
+int launch_attention(const AttnCall& c, cudaStream_t st);
+
+// ---- TMA descriptors (api.cu) ----
+// 2-D bf16 map over a row-major [rows, cols] matrix with a {64, box_rows}
+// box and 128-byte swizzle.
+int make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                uint64_t row_stride_elems, uint32_t box_rows);
+// 3-D bf16 map {dim, heads, tokens} with strides in elements and a
+// {64, 1, box_tokens} box, 128-byte swizzle.
+int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim, uint64_t heads, uint64_t tokens,
+                uint64_t head_stride, uint64_t token_stride, uint32_t box_tokens);
+
+}  // namespace sf

@@ -1,0 +1,253 @@
+/*
+ * specfold.h -- C ABI of the GB300 (sm_103a) folded multi-branch verification
+ * layer (SpecFold).
+ *
+ * The layer is one bidirectional transformer layer (RMSNorm, GQA attention,
+ * SwiGLU FFN) evaluated over B draft branches of one L-token block that share
+ * a prefix KV cache.  Rows whose layer input barely differs from the parent
+ * branch are folded: they reuse the computed source row's output plus their
+ * own input difference.  All other rows are packed into one batch and
+ * recomputed.  Sources: the SpecFold explainer (blog.ontle.kr/blog/358) --
+ * "observation" paragraph with Fig. 2 (the gate metric), the "mechanism"
+ * paragraph (gate, packed batch, shared prefix cache without copies) and the
+ * implementation note (gate, provenance and attention kernels, GQA,
+ * zero-copy strided view); and the iitog.ru summary "SpecFold ускоряет
+ * диффузионные языковые модели до 1,99x", key facts (folded attention and
+ * FFN that keep the residual hidden states).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers owned by the caller unless stated.  The
+ *     library never allocates device memory; scratch comes from a caller
+ *     workspace (specfold_workspace_size) that must be zero-filled once after
+ *     allocation (cudaMemset) and is left reusable by every successful call.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, 0 = legacy
+ *     default stream) and returns a status: 0 on success, a negative
+ *     SPECFOLD_E* code for an error detected on the host before anything was
+ *     launched.  Errors detected on the device (a bounded wait that ran out,
+ *     an invalid draft-graph parent, a count beyond capacity) set bits in
+ *     the workspace's device status word; read them with specfold_get_status.
+ *   - Rows are r = b*L + i for branch b (0 = root / main branch) and block
+ *     position i.  R = B*L is the row capacity.  The number of packed rows n
+ *     stays on the device (n_dev) and kernels are sized for n = R, so a call
+ *     never synchronises with the host.
+ *   - Element type: dims.dtype.  SPECFOLD_BF16 is supported by every entry
+ *     point.  All activations, weights and the prefix view use that type;
+ *     accumulation is fp32.
+ *   - Matrices are row-major.  Weights use the [out, in] layout.
+ *   - Alignment: every pointer is 16-byte aligned; the prefix view strides are
+ *     multiples of 8 elements (SPECFOLD_EALIGN otherwise).
+ */
+#ifndef SPECFOLD_H
+#define SPECFOLD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host status codes ---- */
+#define SPECFOLD_OK            0
+#define SPECFOLD_EINVAL       -1   /* null pointer, negative size, tau < 0 or NaN, ... */
+#define SPECFOLD_EALIGN       -2   /* pointer or stride not 16-byte aligned */
+#define SPECFOLD_ECAPACITY    -3   /* workspace too small, or B*L above SPECFOLD_MAX_ROWS */
+#define SPECFOLD_EUNSUPPORTED -4   /* shape outside the kernels' tiling (see each call) */
+#define SPECFOLD_ECUDA        -5   /* a CUDA runtime call failed (launch, attribute, ...) */
+#define SPECFOLD_EDEVICE      -6   /* specfold_get_status: the device status word is non-zero */
+
+/* ---- device status bits (specfold_get_status) ---- */
+#define SPECFOLD_DEV_TIMEOUT    1u  /* a bounded wait inside a kernel ran out; outputs invalid */
+#define SPECFOLD_DEV_BAD_PARENT 2u  /* parent[b] outside [0, b) for b > 0, or parent[0] != -1 */
+
+#define SPECFOLD_MAX_ROWS 16384     /* largest B*L */
+
+typedef enum { SPECFOLD_BF16 = 0, SPECFOLD_F32 = 1 } specfold_dtype;
+
+/* Layer shape.  Constraints (SPECFOLD_EUNSUPPORTED otherwise): head_dim is 64
+ * or 128; n_q_heads % n_kv_heads == 0; d_model % 256 == 0;
+ * (n_q_heads*head_dim) % 128 == 0; (n_kv_heads*head_dim) % 128 == 0;
+ * ffn_dim % 128 == 0. */
+typedef struct {
+  int d_model;      /* hidden size d */
+  int n_q_heads;    /* query heads */
+  int n_kv_heads;   /* key/value heads (GQA group g = n_q_heads / n_kv_heads) */
+  int head_dim;     /* hd */
+  int ffn_dim;      /* SwiGLU inner width F */
+  float rms_eps;    /* RMSNorm epsilon (>= 0) */
+  int dtype;        /* specfold_dtype */
+} specfold_dims;
+
+/* Layer weights (device, [out, in] row-major, dims.dtype). */
+typedef struct {
+  const void* g1;      /* [d]            RMSNorm before attention */
+  const void* w_q;     /* [n_q*hd, d] */
+  const void* w_k;     /* [n_kv*hd, d] */
+  const void* w_v;     /* [n_kv*hd, d] */
+  const void* w_o;     /* [d, n_q*hd] */
+  const void* g2;      /* [d]            RMSNorm before the FFN */
+  const void* w_gate;  /* [F, d] */
+  const void* w_up;    /* [F, d] */
+  const void* w_down;  /* [d, F] */
+} specfold_weights;
+
+/* Zero-copy strided view of the shared prefix K (or V): element
+ * (token t, kv head h, dim j) is ptr[t*token_stride + h*head_stride + j].
+ * Any slice of a larger (e.g. fused K/V) cache can be passed without a copy. */
+typedef struct {
+  const void* ptr;
+  int64_t token_stride;   /* elements, multiple of 8 */
+  int64_t head_stride;    /* elements, multiple of 8 */
+} specfold_kv_view;
+
+/* Byte offsets of the intermediates inside a layer workspace (for
+ * inspection; all relative to the workspace base). */
+typedef struct {
+  size_t status;       /* uint32 device status word */
+  size_t n_packed;     /* int32 n */
+  size_t fold;         /* uint8  [R] */
+  size_t rel;          /* float  [R] */
+  size_t src;          /* int32  [R] */
+  size_t packed_idx;   /* int32  [R] (first n valid) */
+  size_t slot_of_row;  /* int32  [R] (-1 for folded rows) */
+  size_t x1;           /* [R, d]        RMSNorm1 of packed rows */
+  size_t q;            /* [n_kv, R*g, hd]  queries, head-group major */
+  size_t block_k;      /* [R, n_kv, hd]  keys of recomputed rows (row r) */
+  size_t block_v;      /* [R, n_kv, hd] */
+  size_t attn_o;       /* [R, n_q*hd]   attention output, packed rows */
+  size_t a;            /* [R, d]        attention sublayer output, packed rows */
+  size_t x2;           /* [R, d]        RMSNorm2 of a */
+  size_t g;            /* [R, F]        silu(x2 Wg) * (x2 Wu) */
+  size_t gemm_scratch; /* split-K partial sums and tile counters */
+  size_t total;        /* total bytes */
+} specfold_ws_layout;
+
+/* Number of stage events specfold_layer_forward records when given them. */
+#define SPECFOLD_STAGE_EVENTS 11
+
+/* ------------------------------------------------------------------ */
+/* S1 gate.  Explainer, Fig. 2 paragraph: r(b,i) = |H_b[i] - H_p[i]| / |H_p[i]|
+ * on the layer input, p = parent[b] (the first parent of a multi-parent
+ * node).  fold[r] = 1 iff sum(delta^2) < tau^2 * sum(H_p^2), or the row equals
+ * its parent row and tau > 0 (so tau = 0 folds nothing).  Root rows: fold 0,
+ * rel -1.  A parent outside [0, b) makes the row recompute (fold 0).
+ *   H       [B, L, d] dims-dtype          parent  int32 [B]
+ *   fold    uint8 [B*L] (out)             rel_opt float [B*L] (out, may be NULL)
+ * d % 256 == 0. */
+int specfold_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d,
+                  float tau, uint8_t* fold, float* rel_opt, void* stream);
+
+/* S2 resolve.  Explainer, implementation note (provenance kernel): src[r] = r
+ * for a recomputed row, else src of the same position in the parent branch,
+ * following the fold chain to the row actually computed.  A bad parent
+ * (outside [0, b)) ends the chain at that row and sets SPECFOLD_DEV_BAD_PARENT
+ * in *status_opt (device uint32, may be NULL).
+ *   fold uint8 [B*L], parent int32 [B] -> src int32 [B*L] */
+int specfold_resolve(const uint8_t* fold, const int32_t* parent, int B, int L,
+                     int32_t* src, uint32_t* status_opt, void* stream);
+
+/* S3 pack.  Explainer, "mechanism" paragraph and implementation note: every
+ * recomputed row of every branch goes into one packed batch, branch-major and
+ * position-ascending (increasing r), and is RMS-normalised:
+ *   X1[k] = H[packed_idx[k]] * g1 / sqrt(mean(H^2) + eps)
+ *   fold uint8 [B*L], H [B, L, d], g1 [d]
+ *   -> packed_idx int32 [B*L] (first n valid), slot_of_row int32 [B*L]
+ *      (-1 for folded rows), n_dev int32 [1], X1 [B*L, d] (first n rows). */
+int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1, float eps,
+                  int B, int L, int d, int32_t* packed_idx, int32_t* slot_of_row,
+                  int32_t* n_dev, void* X1, void* stream);
+
+/* S4 QKV projection of the packed rows (one transformer layer's attention
+ * input projections).  Q goes to the head-group-major layout
+ * Q[h_kv][k*g + j][hd] (query head h_kv*g + j of packed row k, R*g rows per
+ * KV head); keys/values of packed row k go to row packed_idx[k] of
+ * blockK/blockV [B*L, n_kv, hd].  Rows of folded positions are not written.
+ * ws: a layer workspace (split-K scratch, status). */
+int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const void* X1,
+                 const int32_t* packed_idx, const int32_t* n_dev, int B, int L,
+                 void* Q, void* blockK, void* blockV, void* ws, size_t ws_bytes, void* stream);
+
+/* S5 folded attention.  Explainer, implementation note: FlashAttention-style
+ * streaming with GQA; the shared prefix K/V is read through the strided view
+ * (never copied per branch); packed row k of branch b attends to all P prefix
+ * keys and to the L block keys of its own branch, block key j being row
+ * src[b*L + j] of blockK/blockV (a folded position uses its resolved source's
+ * key/value).  No mask inside the block, no attention across branches,
+ * softmax scale 1/sqrt(hd).
+ *   Q as written by specfold_qkv -> O [B*L, n_q*hd] (packed rows, first n). */
+int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_view prefK,
+                       specfold_kv_view prefV, int P, const void* blockK, const void* blockV,
+                       const int32_t* src, const int32_t* packed_idx, const int32_t* n_dev,
+                       int B, int L, void* O, void* ws, size_t ws_bytes, void* stream);
+
+/* S6 output projection + residual: A[k] = H[packed_idx[k]] + O[k] w_o^T. */
+int specfold_out_proj(const specfold_dims* dims, const specfold_weights* w, const void* O,
+                      const int32_t* packed_idx, const int32_t* n_dev, const void* H_in,
+                      int B, int L, void* A, void* ws, size_t ws_bytes, void* stream);
+
+/* S7-S10 folded FFN.  iitog.ru summary (key facts) and explainer
+ * ("keep own difference"): for packed rows
+ *   X2 = rmsnorm(A) * g2;  G = silu(X2 Wg^T) * (X2 Wu^T);
+ *   H_out[packed_idx[k]] = A[k] + G[k] Wd^T
+ * then for every folded row r with s = src[r]:
+ *   H_out[r] = H_out[s] + (H_in[r] - H_in[s]).
+ * X2 and G live in the workspace. */
+int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const void* A,
+                 const int32_t* packed_idx, const int32_t* n_dev, const void* H_in,
+                 const int32_t* src, const uint8_t* fold, int B, int L, void* H_out,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* S1-S10: the whole folded layer.  H_in [B, L, d], parent int32 [B] (first
+ * parents, parent[0] = -1, parent[b] < b), prefix views of P tokens, tau >= 0
+ * (0 = folding off: the dense multi-branch verify through the same kernels).
+ * Writes H_out [B, L, d]; intermediates stay in ws (specfold_workspace_layout).
+ * stage_events: NULL, or SPECFOLD_STAGE_EVENTS cudaEvent_t handles recorded
+ * on `stream` before each of the ten kernels and after the last. */
+int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
+                           const void* H_in, const int32_t* parent, int B, int L,
+                           specfold_kv_view prefK, specfold_kv_view prefV, int P, float tau,
+                           void* H_out, void* ws, size_t ws_bytes,
+                           void* const* stage_events, void* stream);
+
+/* Plain packed GEMM through the same tcgen05 engine: Y[M, N] = X[M, K] W^T
+ * with W [N, K]; Y in dims-dtype.  K % 64 == 0, N % 128 == 0. */
+int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for a layer of this shape and B*L rows (host only, no GPU
+ * needed).  0 if the shape is invalid. */
+size_t specfold_workspace_size(const specfold_dims* dims, int B, int L);
+
+/* Workspace bytes for specfold_linear with M rows and N columns. */
+size_t specfold_linear_workspace_size(int M, int N);
+
+/* Offsets of the intermediates for this shape.  Returns SPECFOLD_OK or
+ * SPECFOLD_EINVAL / SPECFOLD_EUNSUPPORTED. */
+int specfold_workspace_layout(const specfold_dims* dims, int B, int L, specfold_ws_layout* out);
+
+/* Synchronises `stream`, copies the workspace's device status word to
+ * *status_out (may be NULL) and clears it.  Returns SPECFOLD_OK if it was 0,
+ * SPECFOLD_EDEVICE if not, SPECFOLD_ECUDA if the copy failed. */
+int specfold_get_status(void* ws, uint32_t* status_out, void* stream);
+
+/* Reads the packed-row count n of the last layer call on `stream`
+ * (synchronises the stream). */
+int specfold_read_n_packed(const void* ws, int B, int L, const specfold_dims* dims,
+                           int32_t* n_out, void* stream);
+
+/* Static string for a status code. */
+const char* specfold_status_string(int status);
+
+/* Kernels this library has launched in this process (host counter). */
+uint64_t specfold_launch_count(void);
+
+/* Self-test of the bounded-wait path: launches one block that waits on an
+ * mbarrier nobody arrives at, for at most wait_ns nanoseconds (capped at
+ * 1e9); the wait runs out, the kernel sets SPECFOLD_DEV_TIMEOUT in *status
+ * (device uint32) and returns.  The GPU context stays usable. */
+int specfold_selftest_timeout(uint32_t* status, uint64_t wait_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECFOLD_H */

@@ -1,0 +1,205 @@
+"""CUDA path vs the CPU oracle, through the C-ABI (GPU only).
+
+Bars (the benchmark spec): gate decisions, provenance and packed index lists are
+bit-exact (rows within 1e-4 relative of tau are reported and take the GPU's
+decision on both sides); bf16 outputs are within 2e-2 relative L2.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_branch_speculative_gb300 import binding, synth
+from oracle import specfold_oracle as orc
+from tests.gpu_cases import (TOL, DeviceInputs, bf16, oracle_with_gpu_decisions, read_intermediates, rel_l2,
+                             run_layer, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    binding.lib()
+
+
+def check_layer(inp, tau, rows=None, inter=True):
+    dev = DeviceInputs(inp)
+    lay, out = run_layer(dev, tau)
+    assert lay.status() == 0
+    gi = read_intermediates(lay, dev)
+    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows)
+    assert n_bad == 0, f"{n_bad} gate decisions differ away from tau"
+    B, L, D = inp.H.shape
+    R = B * L
+    # S1: relative differences (fp32 on the GPU) and decisions
+    nonroot = np.arange(R) >= L
+    rg, ro = gi["rel"][nonroot], res["rel"].reshape(-1)[nonroot]
+    fin = np.isfinite(ro)
+    np.testing.assert_allclose(rg[fin], ro[fin], rtol=1e-4, atol=1e-6)
+    assert np.array_equal(gi["fold"], res["fold"].reshape(-1))
+    # S2/S3: provenance and packed list, bit-exact
+    assert np.array_equal(gi["src"], res["src"])
+    assert gi["n"] == res["n"]
+    assert np.array_equal(gi["packed_idx"], res["packed_idx"])
+    assert np.array_equal(gi["slot"], res["slot"])
+    m = {"n": gi["n"], "near_tau": n_near}
+    if inter:
+        act = res["act_rows"]
+        k = gi["slot"][act]
+        m["X1"] = rel_l2(gi["X1"][k], res["X1"])
+        m["Q"] = rel_l2(gi["Q"][k], res["Q"])
+        m["K"] = rel_l2(gi["bK"][act], np.stack([res["K_rows"][r] for r in act]))
+        m["V"] = rel_l2(gi["bV"][act], np.stack([res["V_rows"][r] for r in act]))
+        m["attnO"] = rel_l2(gi["attnO"][k], res["attnO"])
+        m["A"] = rel_l2(gi["A"][k], res["A"])
+        m["X2"] = rel_l2(gi["X2"][k], res["X2"])
+        m["G"] = rel_l2(gi["G"][k], res["G"])
+    Hg = to_np(out).reshape(R, D)
+    Hin = inp.H.reshape(R, D).astype(np.float64)
+    rr = res["out_rows"]
+    m["H_out"] = rel_l2(Hg[rr], res["out"])
+    m["delta"] = rel_l2(Hg[rr] - Hin[rr], res["out"] - Hin[rr])
+    for key, val in m.items():
+        if key not in ("n", "near_tau"):
+            assert val < TOL, (key, val, m)
+    return m, lay, out
+
+
+# ------------------------------------------------------------ GEMM engine --
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (100, 256, 512), (300, 384, 1024), (129, 3584, 3584),
+                                   (64, 3584, 18944), (2048, 1024, 4096)])
+def test_linear_matches_fp64(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    X = synth.round_bf16(rng.standard_normal((M, K)).astype(np.float32))
+    W = synth.round_bf16((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    Xd, Wd = bf16(X), bf16(W)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = binding.alloc_workspace(binding.linear_workspace_size(M, N))
+    binding.specfold_linear(Xd, Wd, Y, ws)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    assert rel_l2(to_np(Y), ref) < 5e-3
+    # a second call reuses the self-resetting split-K counters
+    Y2 = torch.empty_like(Y)
+    binding.specfold_linear(Xd, Wd, Y2, ws)
+    assert torch.equal(Y, Y2)
+    assert binding.specfold_get_status(ws) == 0
+
+
+# ------------------------------------------------ standalone S1/S2/S3 calls --
+
+@pytest.mark.parametrize("name,tau", [("tiny", 0.05), ("7b_layer", 0.05), ("3b_layer", 0.05)])
+def test_gate_resolve_pack_standalone(name, tau):
+    inp = synth.make_layer_inputs(name, seed=1, dtype="bf16")
+    dev = DeviceInputs(inp)
+    B, L, D = inp.H.shape
+    R = B * L
+    fold = torch.empty(R, dtype=torch.uint8, device="cuda")
+    rel = torch.empty(R, dtype=torch.float32, device="cuda")
+    binding.specfold_gate(dev.H, dev.parent, tau, fold, rel)
+    f0, r0 = orc.gate(inp.H, inp.parent, np.float32(tau))
+    near = orc.near_tau_rows(r0, float(np.float32(tau)))
+    fg = fold.cpu().numpy().astype(bool).reshape(B, L)
+    assert np.array_equal(fg[~near], f0[~near])
+    # resolve/pack on the oracle's decisions (GPU's at near-tau rows)
+    f_use = np.where(near, fg, f0)
+    fold_d = torch.from_numpy(f_use.reshape(-1).astype(np.uint8)).cuda()
+    src = torch.empty(R, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.specfold_resolve(fold_d, dev.parent, B, L, src, status)
+    assert np.array_equal(src.cpu().numpy(), orc.resolve(f_use, inp.parent))
+    pidx = torch.empty(R, dtype=torch.int32, device="cuda")
+    slot = torch.empty(R, dtype=torch.int32, device="cuda")
+    n_dev = torch.empty(1, dtype=torch.int32, device="cuda")
+    X1 = torch.empty(R, D, dtype=torch.bfloat16, device="cuda")
+    binding.specfold_pack(fold_d, dev.H, dev.W["g1"], inp.dims.eps, pidx, slot, n_dev, X1)
+    idx, sl, n = orc.pack(f_use)
+    assert int(n_dev.item()) == n
+    assert np.array_equal(pidx.cpu().numpy()[:n], idx)
+    assert np.array_equal(slot.cpu().numpy(), sl)
+    x1 = orc.rmsnorm(inp.H.reshape(R, D)[idx], inp.weights["g1"], inp.dims.eps)
+    assert rel_l2(to_np(X1[:n]), x1) < 5e-3
+    assert int(status.item()) == 0
+
+
+def test_bad_parent_sets_status():
+    inp = synth.make_layer_inputs("tiny", seed=0, dtype="bf16")
+    B, L = 4, 16
+    fold = torch.ones(B * L, dtype=torch.uint8, device="cuda")
+    parent = torch.tensor([-1, 0, 2, 1], dtype=torch.int32, device="cuda")   # parent[2] = 2 is invalid
+    src = torch.empty(B * L, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.specfold_resolve(fold, parent, B, L, src, status)
+    s = src.cpu().numpy().reshape(B, L)
+    assert int(status.item()) & binding.DEV_BAD_PARENT
+    assert np.all(s[0] == np.arange(L)) and np.all(s[1] == np.arange(L))
+    assert np.all(s[2] == 2 * L + np.arange(L))          # chain stops at the bad link
+    assert np.all(s[3] == np.arange(L))                  # 3 -> 1 -> 0
+
+
+# --------------------------------------------------------- whole layer ----
+
+@pytest.mark.parametrize("tau", [0.0, 0.05, 0.2])
+def test_layer_small(tau):
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=512, P=64, L=16, levels=(1, 2, 2))
+    m, _, _ = check_layer(synth.make_layer_inputs(w, seed=3), tau)
+    if tau == 0.0:
+        assert m["n"] == 5 * 16
+
+
+def test_layer_ragged_hd128():
+    """P and L not multiples of the tiles, several branches per query tile."""
+    w = synth.small_workload(d=512, n_q=8, n_kv=2, hd=128, F=384, P=100, L=12, levels=(1, 3, 4, 3),
+                             reveals=(1, 2), second_parent=True)
+    check_layer(synth.make_layer_inputs(w, seed=5), 0.05)
+
+
+def test_layer_no_prefix():
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=256, P=0, L=8, levels=(1, 2))
+    check_layer(synth.make_layer_inputs(w, seed=2), 0.05)
+
+
+def test_layer_tiny_workload_bf16():
+    check_layer(synth.make_layer_inputs("tiny", seed=0, dtype="bf16"), 0.05)
+
+
+@pytest.mark.parametrize("tau", [0.0, 0.02, 0.05, 0.1])
+def test_layer_7b(tau):
+    m, _, _ = check_layer(synth.make_layer_inputs("7b_layer", seed=0), tau)
+    print("7b", tau, m)
+
+
+def test_layer_3b():
+    m, _, _ = check_layer(synth.make_layer_inputs("3b_layer", seed=0), 0.05)
+    print("3b", m)
+
+
+@pytest.mark.parametrize("frac,n_expect", [(0.0, 32), (0.25, 536), (1.0, 2048)])
+def test_layer_stress_sampled(frac, n_expect):
+    inp = synth.make_layer_inputs("stress", seed=0, forced_frac=frac)
+    rng = np.random.default_rng(1)
+    R = inp.H.shape[0] * inp.H.shape[1]
+    rows = sorted(set(rng.choice(R, size=24, replace=False).tolist()) | {0, R - 1})
+    m, _, _ = check_layer(inp, 0.05, rows=rows)
+    assert m["n"] == n_expect
+    print("stress", frac, m)
+
+
+def test_deterministic_bitwise():
+    inp = synth.make_layer_inputs("7b_layer", seed=4)
+    dev = DeviceInputs(inp)
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, dev.pk, dev.pv)
+    a = lay.forward(dev.H, dev.parent, 0.05).clone()
+    b = lay.forward(dev.H, dev.parent, 0.05).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_timeout_selftest_reports_and_context_survives():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.specfold_selftest_timeout(status, 20_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) & binding.DEV_TIMEOUT
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum().item()) == 8.0
