@@ -1,0 +1,430 @@
+"""Benchmark: verified branch-tokens/s of the folded verification layer.
+
+One step = one folded-layer call (gate, resolve, pack + RMSNorm1, QKV, folded
+attention, output projection, RMSNorm2, SwiGLU, down projection, fold-fill)
+over one batch of B branches x L block tokens, on the 7B-like single-layer
+workload: d 3584, 28/4 heads x 128, SwiGLU 18944, prefix 512, L 32, 8
+branches on a depth-3 directed draft graph, seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--tau T] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  value = B*L*steps*N / (max over ranks of the
+summed device time of the K steps), inputs resident in HBM; L2 is flushed
+(256 MiB write) between steps, outside the timed events.  e2e = the same
+metric through the public API with pinned host buffers, including the
+host->device copy of H_in/parent and the device->host copy of H_out.
+--impl reference times the CPU oracle on this host's cores instead.
+Multi-GPU: independent replicas, one per rank (no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verified branch-tokens/s per layer"
+UNIT = "branch-tokens/s"
+FLUSH_BYTES = 256 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="7b_layer")
+    ap.add_argument("--tau", type=float, default=0.05)
+    ap.add_argument("--frac", type=float, default=None, help="forced recompute fraction (stress workload)")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(w, tau, frac=None):
+    d = w.dims
+    s = (f"{w.name}: d={d.d} heads={d.n_q}/{d.n_kv}x{d.hd} ffn={d.F} P={w.P} L={w.L} B={w.B} "
+         f"levels={'/'.join(map(str, w.levels))} tau={tau}")
+    if frac is not None:
+        s += f" forced_frac={frac}"
+    return s
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]), "src": "measured"}
+    except Exception:
+        return dict(PEAKS_FALLBACK, src="fallback")
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if t0 - 0.15 <= t <= t1 + 0.15] or [l for _, l in self.lines[-5:]]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[2]))
+                mx = float(f[3])
+                for nm, v in zip(names, f[6:10]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- roofline data --
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "sf_device.cuh"):
+        with open(os.path.join(ROOT, "diffusion_branch_speculative_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (profiles/<kernel>__<workload>.md)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def stage_roofline(name, dims, n, R, us, peaks):
+    """Algorithmic work of one launch of a stage and its bound."""
+    d, F, e = dims.d, dims.F, 2
+    nq, nkv = dims.n_q * dims.hd, dims.n_kv * dims.hd
+    if name == "gate_up":
+        flops = 2.0 * n * d * 2 * F
+        byts = 2 * F * d * e + n * d * e + n * F * e
+    elif name == "down":
+        flops = 2.0 * n * F * d
+        byts = d * F * e + n * F * e + 2 * n * d * e + n * 4
+    elif name == "qkv":
+        flops = 2.0 * n * d * (nq + 2 * nkv)
+        byts = (nq + 2 * nkv) * d * e + n * d * e + n * (nq + 2 * nkv) * e
+    elif name == "out_proj":
+        flops = 2.0 * n * nq * d
+        byts = d * nq * e + n * nq * e + 2 * n * d * e
+    else:
+        return None
+    t = us * 1e-6
+    t_mem = byts / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if t_mem >= t_tc:
+        a = byts / t / 1e9
+        return {"bound": "hbm", "achieved": round(a, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(a / peaks["hbm_gbs"], 4), "algorithmic_bytes": int(byts)}
+    a = flops / t / 1e12
+    return {"bound": "tensor", "achieved": round(a, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(a / peaks["bf16_tflops"], 4), "algorithmic_flops": flops}
+
+
+# ------------------------------------------------------------- our arm ----
+def run_ours(args, rank, world):
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    w = synth.WORKLOADS[args.workload]
+    inp = synth.make_layer_inputs(w, seed=args.seed + rank, forced_frac=args.frac)
+    d = inp.dims
+    B, L, D = inp.H.shape
+    R = B * L
+    dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
+    H = to(inp.H)
+    parent = torch.from_numpy(inp.parent.astype(np.int32)).cuda()
+    W = {k: to(v) for k, v in inp.weights.items()}
+    cache = to(inp.prefix.cache)
+    o, P = inp.prefix.offset, inp.prefix.P
+    pk, pv = (cache[o:o + P, 0], cache[o:o + P, 1]) if P else (None, None)
+    lay = binding.FoldedLayer(dims, W, B, L, pk, pv)
+    Hout = torch.empty_like(H)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed_steps(tau, steps, warmup, stage_ev=False, clocks=None):
+        for _ in range(warmup):
+            lay.forward(H, parent, tau, Hout)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)] for _ in range(steps)] \
+            if stage_ev else None
+        if st_ev:  # torch creates the CUDA event at its first record
+            for row in st_ev:
+                for e in row:
+                    e.record(stream)
+        barrier()
+        torch.cuda.synchronize()
+        l0 = binding.specfold_launch_count()
+        t0 = time.time()
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            lay.forward(H, parent, tau, Hout, events=st_ev[i] if st_ev else None)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        launches = binding.specfold_launch_count() - l0
+        ms = [a.elapsed_time(b) for a, b in evs]
+        stages = None
+        if st_ev:
+            stages = {}
+            for si, nm in enumerate(binding.STAGE_NAMES):
+                stages[nm] = statistics.mean(e[si].elapsed_time(e[si + 1]) for e in st_ev) * 1e3
+        return sum(ms), ms, launches, stages, (t0, t1)
+
+    # headline: tau from the command line, stage events on
+    sampler = ClockSampler(dev_index)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, ms, launches, stages, (t0, t1) = timed_steps(args.tau, args.steps, args.warmup, stage_ev=True)
+    clocks = sampler.stop(t0, t1)
+    assert lay.status() == 0, "device status set"
+    n = lay.n_packed()
+    total_ms_max = total_ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms_max = float(t.item())
+    value = B * L * args.steps * world / (total_ms_max * 1e-3)
+
+    # dominant kernel of the step
+    gemm_stages = ("qkv", "out_proj", "gate_up", "down")
+    top = max(stages, key=stages.get)
+    rf = stage_roofline(top, d, n, R, stages[top], peaks) if top in gemm_stages else None
+    if rf is None:
+        top = max(gemm_stages, key=lambda s: stages[s])
+        rf = stage_roofline(top, d, n, R, stages[top], peaks)
+    rf["kernel"] = f"gemm_kernel ({top})"
+    rf["us_per_launch"] = round(stages[top], 2)
+    rf["peak_src"] = f"{peaks['src']} ({'MEASURED_PEAKS.json burst' if peaks['src'] == 'measured' else 'recipe fallback'})"
+    rf["traffic"] = committed_traffic(f"gemm_{top}", args.workload)
+    rf["stage_share"] = round(stages[top] / sum(stages.values()), 3)
+
+    # e2e through the public API with pinned host buffers
+    H_host = torch.empty(H.shape, dtype=torch.bfloat16, pin_memory=True)
+    H_host.copy_(H.cpu())
+    par_host = parent.cpu().pin_memory()
+    out_host = torch.empty(H.shape, dtype=torch.bfloat16, pin_memory=True)
+    H_e, par_e, out_e = torch.empty_like(H), torch.empty_like(parent), torch.empty_like(H)
+    e2e_steps = max(1, min(args.steps, 500))
+    for _ in range(3):
+        H_e.copy_(H_host, non_blocking=True)
+        par_e.copy_(par_host, non_blocking=True)
+        lay.forward(H_e, par_e, args.tau, out_e)
+        out_host.copy_(out_e, non_blocking=True)
+    torch.cuda.synchronize()
+    e_ms = []
+    barrier()
+    for _ in range(e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        H_e.copy_(H_host, non_blocking=True)
+        par_e.copy_(par_host, non_blocking=True)
+        lay.forward(H_e, par_e, args.tau, out_e)
+        out_host.copy_(out_e, non_blocking=True)
+        b.record(stream)
+        e_ms.append((a, b))
+    torch.cuda.synchronize()
+    e_total = sum(a.elapsed_time(b) for a, b in e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_total = float(t.item())
+    assert torch.equal(out_host.cuda(), Hout), "e2e output differs from the resident run"
+    e2e = {"value": round(B * L * e2e_steps * world / (e_total * 1e-3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": int(H.numel() * 2 + parent.numel() * 4),
+           "d2h_bytes_per_step": int(Hout.numel() * 2), "steps": e2e_steps}
+
+    # recompute-fraction sweep (tau = 0 is the dense multi-branch verify)
+    sweep = []
+    if not args.no_sweep:
+        for tau in ([0.0] + list(w.taus)):
+            tot, _, _, st, _ = timed_steps(tau, max(50, min(args.steps, 300)), 5, stage_ev=True)
+            steps_s = max(50, min(args.steps, 300))
+            nn = lay.n_packed()
+            sweep.append({"tau": tau, "n_packed": nn, "rho": round(nn / R, 4),
+                          "us_per_step": round(tot / steps_s * 1e3, 2),
+                          "tokens_per_s": round(R * steps_s / (tot * 1e-3), 1),
+                          "stages_us": {k: round(v, 2) for k, v in st.items()}})
+        dense = next(s for s in sweep if s["tau"] == 0.0)["us_per_step"]
+        for s in sweep:
+            s["time_vs_dense"] = round(s["us_per_step"] / dense, 4)
+    return {
+        "value": value, "ms_per_step": total_ms_max / args.steps, "n_packed": n, "R": R, "w": w,
+        "stages": stages, "roofline": rf, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+        "sweep": sweep, "inp": inp,
+    }
+
+
+# -------------------------------------------------------- oracle on CPU ----
+def oracle_sample(inp, tau, rows_per_step, steps, budget_s=None):
+    """Time the CPU oracle producing `rows_per_step` output rows per step."""
+    from oracle import specfold_oracle as orc
+    d = inp.dims
+    W64 = {k: np.asarray(v, np.float64) for k, v in inp.weights.items()}
+    pk = np.asarray(inp.prefix.K, np.float64)
+    pv = np.asarray(inp.prefix.V, np.float64)
+    H = inp.H.astype(np.float64)
+    R = H.shape[0] * H.shape[1]
+    rng = np.random.default_rng(7)
+    done, t_total = 0, 0.0
+    for i in range(steps):
+        rows = rng.choice(R, size=rows_per_step, replace=False)
+        t0 = time.perf_counter()
+        orc.layer_forward(H, inp.parent, W64, pk, pv, float(np.float32(tau)), d.eps, d.n_kv, d.hd, rows=rows)
+        t_total += time.perf_counter() - t0
+        done += rows_per_step
+        if budget_s is not None and t_total > budget_s:
+            break
+    return done, t_total
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        from diffusion_branch_speculative_gb300 import synth
+        w = synth.WORKLOADS[args.workload]
+        inp = synth.make_layer_inputs(w, seed=args.seed, forced_frac=args.frac)
+        R = w.B * w.L
+        rows_per_step = 1
+        oracle_sample(inp, args.tau, rows_per_step, max(1, min(args.warmup, 2)))
+        done, secs = oracle_sample(inp, args.tau, rows_per_step, args.steps)
+        val = done / secs
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(val, 3), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w, args.tau, args.frac), "B": w.B, "L": w.L, "P": w.P,
+                       "tau": args.tau, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{rows_per_step} seeded output row(s) of the {R}-row step per timed step "
+                                       f"(numpy float64, all BLAS threads)"},
+            "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    r = run_ours(args, rank, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows_per_step = 8
+        done, secs = oracle_sample(r["inp"], args.tau, rows_per_step, 1000, budget_s=15.0)
+        cpu = {"value": round(done / secs, 3), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{done} seeded output rows ({rows_per_step} per oracle call) of the "
+                         f"{r['R']}-row step, numpy float64, ~15 s"}
+    if rank == 0:
+        w = r["w"]
+        line = {
+            "metric": METRIC, "value": round(r["value"], 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(w, args.tau, args.frac), "B": w.B, "L": w.L, "P": w.P,
+                       "tau": args.tau, "n_packed": r["n_packed"], "recompute_fraction": round(r["n_packed"] / r["R"], 4),
+                       "l2": "flushed between steps (256 MiB write outside the timed events)",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_step": round(r["ms_per_step"] * 1e3, 2),
+            "roofline": r["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": r["e2e"],
+            "gpu_launches": r["gpu_launches"],
+            "clocks": r["clocks"],
+            "stages_us": {k: round(v, 2) for k, v in r["stages"].items()},
+            "sweep": r["sweep"],
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

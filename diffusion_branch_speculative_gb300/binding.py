@@ -214,7 +214,10 @@ def specfold_layer_forward(dims, weights, H_in, parent, prefK, prefV, P, tau, H_
     ev = None
     if events is not None:
         assert len(events) == STAGE_EVENTS
-        ev = (ctypes.c_void_p * STAGE_EVENTS)(*[e.cuda_event for e in events])
+        handles = [e.cuda_event for e in events]
+        if not all(handles):
+            raise ValueError("stage events must exist already (torch creates them at their first record())")
+        ev = (ctypes.c_void_p * STAGE_EVENTS)(*handles)
     _check(lib().specfold_layer_forward(ctypes.byref(dims), ctypes.byref(weights), _ptr(H_in), _ptr(parent), B, L,
                                         kv_view(prefK), kv_view(prefV), P, float(tau), _ptr(H_out), _ptr(ws),
                                         ws.numel(), ev, _stream(stream)), "specfold_layer_forward")

@@ -129,13 +129,6 @@ static int check_view(const specfold_kv_view& v, int P) {
 // ------------------------------------------------------ workspace layout --
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-static int gemm_counters_for_layer(const specfold_dims* d, int R) {
-  int c = gemm_counters_needed(R, d->n_q_heads * d->head_dim + 2 * d->n_kv_heads * d->head_dim, EPI_QKV);
-  c = std::max(c, gemm_counters_needed(R, d->d_model, EPI_RESID_PACKED));
-  c = std::max(c, gemm_counters_needed(R, d->ffn_dim, EPI_SWIGLU));
-  return c;
-}
-
 static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) {
   const size_t R = static_cast<size_t>(B) * L;
   const size_t e = esize(d->dtype);
@@ -162,25 +155,21 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->a = take(R * d->d_model * e);
   o->x2 = take(R * d->d_model * e);
   o->g = take(R * d->ffn_dim * e);
-  o->gemm_scratch = take(static_cast<size_t>(gemm_counters_for_layer(d, static_cast<int>(R))) * 4);
-  take(gemm_partial_floats() * 4);
+  o->gemm_scratch = take(gemm_partial_floats() * 4);
   o->total = off;
 }
 
 struct Scratch {
-  int* counters;
-  int counters_len;
   float* partial;
   size_t partial_len;
 };
 
 static Scratch layer_scratch(void* ws, const specfold_dims* d, int B, int L, const specfold_ws_layout& lo) {
   Scratch s;
-  const int R = B * L;
-  s.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch);
-  s.counters_len = gemm_counters_for_layer(d, R);
-  s.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch +
-                                       up256(static_cast<size_t>(s.counters_len) * 4));
+  (void)d;
+  (void)B;
+  (void)L;
+  s.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch);
   s.partial_len = gemm_partial_floats();
   return s;
 }
@@ -191,8 +180,6 @@ static T* at(void* ws, size_t off) {
 }
 
 static void fill_scratch(GemmCall& c, const Scratch& s, uint32_t* status) {
-  c.counters = s.counters;
-  c.counters_len = s.counters_len;
   c.partial = s.partial;
   c.partial_len = s.partial_len;
   c.status = status;
@@ -347,7 +334,7 @@ int specfold_workspace_layout(const specfold_dims* dims, int B, int L, specfold_
 
 size_t specfold_linear_workspace_size(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
-  return 256 + up256(static_cast<size_t>(gemm_counters_needed(M, N, EPI_STORE)) * 4) + gemm_partial_floats() * 4;
+  return 256 + gemm_partial_floats() * 4;
 }
 
 int specfold_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
@@ -520,9 +507,7 @@ int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K
   c.N = N;
   c.Y = Y;
   c.ldy = N;
-  c.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + 256);
-  c.counters_len = gemm_counters_needed(M, N, EPI_STORE);
-  c.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256 + up256(static_cast<size_t>(c.counters_len) * 4));
+  c.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
   c.partial_len = gemm_partial_floats();
   c.status = static_cast<uint32_t*>(ws);
   return launch_gemm(c, static_cast<cudaStream_t>(stream));

@@ -7,8 +7,9 @@
 // One CTA per SM loops over work units (m-tile, k-split, n-tile).  The number
 // of packed rows n is read on the device, so the decomposition adapts to the
 // recompute fraction without a host round trip: when the m x n tiles cannot
-// fill the SMs, the K loop is split and the last CTA to finish a tile sums the
-// fp32 partials in a fixed order (deterministic) and runs the epilogue.
+// fill the SMs, the K loop is split across CTAs, each writes its fp32 partial
+// tile, and a second, fully parallel kernel sums the partials in a fixed
+// order (deterministic) and runs the fused epilogue.
 //
 // Roles (192 threads): warp 0 issues TMA loads into a multi-stage ring of
 // 128-byte-swizzled tiles; warp 1 allocates TMEM and issues tcgen05.mma
@@ -18,6 +19,7 @@
 #include "sf_device.cuh"
 #include "sf_internal.h"
 
+#include <algorithm>
 #include <cstring>
 
 namespace sf {
@@ -57,23 +59,24 @@ struct GemmParams {
   void* Yv;
   int n_q, n_kv, hd, g, R;
   float* partial;
-  int* counters;
   uint32_t* status;
 };
 
 SF_DEV float silu(float x) { return x / (1.f + ex2(-x * 1.4426950408889634f)); }
 
-SF_DEV void store32_bf16(__nv_bfloat16* dst, const float (&v)[32]) {
+template <int W>
+SF_DEV void store_bf16(__nv_bfloat16* dst, const float (&v)[W]) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < W / 8; ++q)
     d4[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                        pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
-SF_DEV void add32_bf16(const __nv_bfloat16* src, float (&v)[32]) {
+template <int W>
+SF_DEV void add_bf16(const __nv_bfloat16* src, float (&v)[W]) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < W / 8; ++q) {
     const uint4 u = __ldg(s4 + q);
     v[8 * q + 0] += bf16lo(u.x); v[8 * q + 1] += bf16hi(u.x);
     v[8 * q + 2] += bf16lo(u.y); v[8 * q + 3] += bf16hi(u.y);
@@ -82,39 +85,50 @@ SF_DEV void add32_bf16(const __nv_bfloat16* src, float (&v)[32]) {
   }
 }
 
-// Epilogue of one 32-column chunk of packed row k.  c = first output column
-// (first feature for SWIGLU, where v holds gate and u holds up values).
-template <int EPI>
-SF_DEV void epi_chunk(const GemmParams& p, int k, int c, float (&v)[32], const float (&u)[32]) {
+// Epilogue of W consecutive output columns of packed row k.  c = first output
+// column (first feature for SWIGLU, where v holds gate and u holds up values).
+template <int EPI, int W>
+SF_DEV void epi_chunk(const GemmParams& p, int k, int c, float (&v)[W], const float (&u)[W]) {
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
   if constexpr (EPI == EPI_STORE) {
-    store32_bf16(Y + static_cast<size_t>(k) * p.ldy + c, v);
+    store_bf16<W>(Y + static_cast<size_t>(k) * p.ldy + c, v);
   } else if constexpr (EPI == EPI_RESID_PACKED) {
     const int r = p.row_idx[k];
-    add32_bf16(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(r) * p.ldr + c, v);
-    store32_bf16(Y + static_cast<size_t>(k) * p.ldy + c, v);
+    add_bf16<W>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(r) * p.ldr + c, v);
+    store_bf16<W>(Y + static_cast<size_t>(k) * p.ldy + c, v);
   } else if constexpr (EPI == EPI_RESID_SCATTER) {
     const int r = p.row_idx[k];
-    add32_bf16(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + c, v);
-    store32_bf16(Y + static_cast<size_t>(r) * p.ldy + c, v);
+    add_bf16<W>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + c, v);
+    store_bf16<W>(Y + static_cast<size_t>(r) * p.ldy + c, v);
   } else if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = silu(v[e]) * u[e];
-    store32_bf16(Y + static_cast<size_t>(k) * p.ldy + c, v);
-  } else {  // EPI_QKV
+    for (int e = 0; e < W; ++e) v[e] = silu(v[e]) * u[e];
+    store_bf16<W>(Y + static_cast<size_t>(k) * p.ldy + c, v);
+  } else {  // EPI_QKV: W columns never straddle a head (hd % 32 == 0)
     const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
     if (c < nq) {
       const int head = c / p.hd, j = c - head * p.hd;
       const int hk = head / p.g, hg = head - hk * p.g;
-      store32_bf16(Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j, v);
+      store_bf16<W>(Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j, v);
     } else {
       const int r = p.row_idx[k];
       const bool is_k = c < nq + nkv;
       const int cc = is_k ? c - nq : c - nq - nkv;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
-      store32_bf16(dst + static_cast<size_t>(r) * nkv + cc, v);
+      store_bf16<W>(dst + static_cast<size_t>(r) * nkv + cc, v);
     }
   }
+}
+
+// Split factor of the K loop for n packed rows: only when the m x n tiles
+// cannot fill the grid, and never below kMinKbPerSplit k-blocks per split.
+SF_DEV int split_factor(int tiles, int grid, int KB) {
+  int S = 1;
+  if (tiles > 0 && tiles < grid) {
+    S = min(grid / tiles, KB / kMinKbPerSplit);
+    S = max(1, min(S, kMaxSplits));
+  }
+  return S;
 }
 
 struct Unit {
@@ -147,18 +161,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = abort_flag + 1;    // accumulator-ready broadcast
-  volatile int* s_last = abort_flag + 2;  // split-K "last CTA of the tile" broadcast
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
   const int KB = p.K / kBK;
-  int S = 1;
-  if (tiles > 0 && tiles < static_cast<int>(gridDim.x)) {
-    S = min(static_cast<int>(gridDim.x) / tiles, KB / kMinKbPerSplit);
-    S = max(1, min(S, kMaxSplits));
-  }
+  const int S = split_factor(tiles, static_cast<int>(gridDim.x), KB);
   const int U = tiles * S;
   if (static_cast<int>(blockIdx.x) >= U) return;
 
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
           if (valid) {
             if (S == 1) {
-              epi_chunk<EPI>(p, k, w.nt * (BN / 2) + ch * 32, vg, vu);
+              epi_chunk<EPI, 32>(p, k, w.nt * (BN / 2) + ch * 32, vg, vu);
             } else {
               float4* pg = reinterpret_cast<float4*>(part + ch * 32);
               float4* pu = reinterpret_cast<float4*>(part + BN / 2 + ch * 32);
@@ -329,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
           if (valid) {
             if (S == 1) {
-              epi_chunk<EPI>(p, k, w.nt * BN + ch * 32, v, v);
+              epi_chunk<EPI, 32>(p, k, w.nt * BN + ch * 32, v, v);
             } else {
               float4* pp = reinterpret_cast<float4*>(part + ch * 32);
 #pragma unroll
@@ -340,54 +349,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce[ab]));
-      if (S > 1) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (et == 0) *s_last = (atomicAdd(&p.counters[w.tile], 1) == S - 1) ? 1 : 0;
-        named_bar_sync(1, 128);
-        const bool last = *s_last != 0;
-        if (last) {
-          __threadfence();
-          const float* base = p.partial + static_cast<size_t>(w.tile) * S * kBM * BN +
-                              static_cast<size_t>(row) * BN;
-          if (valid) {
-            if constexpr (EPI == EPI_SWIGLU) {
-              for (int ch = 0; ch < BN / 64; ++ch) {
-                float vg[32], vu[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) vg[e] = vu[e] = 0.f;
-                for (int s = 0; s < S; ++s) {
-                  const float4* pg = reinterpret_cast<const float4*>(base + static_cast<size_t>(s) * kBM * BN + ch * 32);
-                  const float4* pu = reinterpret_cast<const float4*>(base + static_cast<size_t>(s) * kBM * BN + BN / 2 + ch * 32);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) {
-                    const float4 a = __ldcg(pg + e), b = __ldcg(pu + e);
-                    vg[4 * e] += a.x; vg[4 * e + 1] += a.y; vg[4 * e + 2] += a.z; vg[4 * e + 3] += a.w;
-                    vu[4 * e] += b.x; vu[4 * e + 1] += b.y; vu[4 * e + 2] += b.z; vu[4 * e + 3] += b.w;
-                  }
-                }
-                epi_chunk<EPI>(p, k, w.nt * (BN / 2) + ch * 32, vg, vu);
-              }
-            } else {
-              for (int ch = 0; ch < BN / 32; ++ch) {
-                float v[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0.f;
-                for (int s = 0; s < S; ++s) {
-                  const float4* pp = reinterpret_cast<const float4*>(base + static_cast<size_t>(s) * kBM * BN + ch * 32);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) {
-                    const float4 a = __ldcg(pp + e);
-                    v[4 * e] += a.x; v[4 * e + 1] += a.y; v[4 * e + 2] += a.z; v[4 * e + 3] += a.w;
-                  }
-                }
-                epi_chunk<EPI>(p, k, w.nt * BN + ch * 32, v, v);
-              }
-            }
-          }
-          if (et == 0) p.counters[w.tile] = 0;  // ready for the next call
-        }
-      }
     }
   }
 
@@ -396,6 +357,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Sums the S fp32 partial tiles of a split-K GEMM in split order and runs the
+// epilogue.  One thread per (packed row, 8 output columns); all partial loads
+// of a thread are issued before the adds.  Returns at once when the GEMM ran
+// unsplit (S recomputed from the same n and grid).
+template <int BN, int EPI>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
+  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int Mt = (n + kBM - 1) / kBM;
+  const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
+  if (S <= 1) return;
+  constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;   // output columns per tile
+  const int groups = (p.Nt * TW) / 8;
+  const long long total = static_cast<long long>(n) * groups;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(idx / groups);
+    const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
+    const int nt = c / TW, tc = c - nt * TW;
+    const int m = k / kBM, row = k - m * kBM;
+    const float* base = p.partial + (static_cast<size_t>(m * p.Nt + nt) * S) * kBM * BN +
+                        static_cast<size_t>(row) * BN + tc;
+    float v[8], u[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = u[e] = 0.f;
+#pragma unroll
+    for (int s0 = 0; s0 < kMaxSplits; s0 += 8) {
+      if (s0 >= S) break;
+      float4 a[8][2], b[8][2];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (s0 + q < S) {
+          const float4* src = reinterpret_cast<const float4*>(base + static_cast<size_t>(s0 + q) * kBM * BN);
+          a[q][0] = __ldcg(src);
+          a[q][1] = __ldcg(src + 1);
+          if constexpr (EPI == EPI_SWIGLU) {
+            b[q][0] = __ldcg(src + BN / 8);
+            b[q][1] = __ldcg(src + BN / 8 + 1);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (s0 + q < S) {
+          v[0] += a[q][0].x; v[1] += a[q][0].y; v[2] += a[q][0].z; v[3] += a[q][0].w;
+          v[4] += a[q][1].x; v[5] += a[q][1].y; v[6] += a[q][1].z; v[7] += a[q][1].w;
+          if constexpr (EPI == EPI_SWIGLU) {
+            u[0] += b[q][0].x; u[1] += b[q][0].y; u[2] += b[q][0].z; u[3] += b[q][0].w;
+            u[4] += b[q][1].x; u[5] += b[q][1].y; u[6] += b[q][1].z; u[7] += b[q][1].w;
+          }
+        }
+      }
+    }
+    epi_chunk<EPI, 8>(p, k, nt * TW + tc, v, u);
   }
 }
 
@@ -431,10 +448,7 @@ int run_gemm(const GemmCall& c, cudaStream_t st) {
   p.hd = c.hd;
   p.g = c.n_kv > 0 ? c.n_q / c.n_kv : 1;
   p.R = c.Mcap;
-  // the counters must cover every tile this call can have (n = Mcap)
-  if (static_cast<long long>((c.Mcap + kBM - 1) / kBM) * p.Nt > c.counters_len) return SPECFOLD_ECAPACITY;
-  if (c.partial_len < static_cast<size_t>(kMaxGrid) * kBM * 256) return SPECFOLD_ECAPACITY;
-  p.counters = c.counters;
+  if (c.partial_len < gemm_partial_floats()) return SPECFOLD_ECAPACITY;
   p.partial = c.partial;
   p.status = c.status;
 
@@ -450,7 +464,17 @@ int run_gemm(const GemmCall& c, cudaStream_t st) {
   const int grid = min(num_sms(), kMaxGrid);
   gemm_kernel<BN, EPI><<<grid, kGemmThreads, Cf::SMEM_BYTES, st>>>(p);
   count_launch();
-  return check_launch();
+  if (check_launch()) return SPECFOLD_ECUDA;
+  // a split is possible only if even one m-tile leaves SMs idle
+  if (p.Nt < grid && p.K / kBK >= 2 * kMinKbPerSplit) {
+    constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
+    const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
+    const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
+    splitk_reduce_kernel<BN, EPI><<<std::max(rgrid, 1), 256, 0, st>>>(p, grid);
+    count_launch();
+    return check_launch();
+  }
+  return SPECFOLD_OK;
 }
 
 template <int EPI>
@@ -460,13 +484,9 @@ int run_epi(const GemmCall& c, int BN, cudaStream_t st) {
 
 }  // namespace
 
+// fp32 partial tiles: at most one per persistent CTA (a split happens only
+// when tiles * S <= grid).
 size_t gemm_partial_floats() { return static_cast<size_t>(kMaxGrid) * kBM * 256; }
-
-int gemm_counters_needed(int Mcap, int N, int epi) {
-  const int BN = 128;  // the smaller tile gives the larger count
-  const int Nt = epi == EPI_SWIGLU ? N / (BN / 2) : N / BN;
-  return ((Mcap + kBM - 1) / kBM) * Nt;
-}
 
 int launch_gemm(const GemmCall& c, cudaStream_t st) {
   if (c.K <= 0 || c.K % kBK || c.Mcap <= 0 || c.N <= 0) return SPECFOLD_EUNSUPPORTED;

@@ -46,7 +46,7 @@ constexpr int kRowWarps = 8;  // warps (rows) per block of the row kernels
 // ------------------------------------------------------------------ S1 gate --
 // One warp per row (b, i).  Child row and parent row are streamed once each
 // (the parent row is shared by all its children and is normally an L2 hit).
-template <typename T>
+template <typename T, int MAXV>
 __global__ void __launch_bounds__(kRowWarps * 32)
 gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d,
             float tau, uint8_t* __restrict__ fold, float* __restrict__ rel) {
@@ -67,20 +67,20 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
   const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(p) * L + i) * d);
   const int nv = d / V::N;
   float num = 0.f, den = 0.f;
-  constexpr int U = 4;
-  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
-    uint4 cv[U], pv[U];
+  // the whole row is in flight at once (the kernel is latency-bound otherwise)
+  for (int v0 = 0; v0 < nv; v0 += 32 * MAXV) {
+    uint4 cv[MAXV], pv[MAXV];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * 32;
+    for (int u = 0; u < MAXV; ++u) {
+      const int v = v0 + lane + u * 32;
       if (v < nv) {
         cv[u] = __ldg(c + v);
         pv[u] = __ldg(q + v);
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + u * 32;
+    for (int u = 0; u < MAXV; ++u) {
+      const int v = v0 + lane + u * 32;
       if (v < nv) {
         float fc[V::N], fp[V::N];
         V::unpack(cv[u], fc);
@@ -195,14 +195,21 @@ rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
   using V = VecT<T>;
   const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (k >= R) return;
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  const int nv = d / V::N;
+  const int per_lane = (nv + 31) / 32;
+  // the gains do not depend on the packed list: start them first
+  uint4 gw[MAXV];
+#pragma unroll
+  for (int j = 0; j < MAXV; ++j) {
+    if (j < per_lane && lane + 32 * j < nv) gw[j] = __ldg(gv + lane + 32 * j);
+  }
   const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
   if (k >= n) return;
   const int r = idx ? idx[k] : k;
   const uint4* x = reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * d);
-  const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* y = reinterpret_cast<uint4*>(Y + static_cast<size_t>(k) * d);
-  const int nv = d / V::N;
-  const int per_lane = (nv + 31) / 32;
   uint4 v[MAXV];
   float ss = 0.f;
 #pragma unroll
@@ -226,7 +233,7 @@ rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
     if (j < per_lane && vi < nv) {
       float f[V::N], gf[V::N];
       V::unpack(v[j], f);
-      V::unpack(__ldg(gv + vi), gf);
+      V::unpack(gw[j], gf);
 #pragma unroll
       for (int e = 0; e < V::N; ++e) f[e] = f[e] * inv * gf[e];
       y[vi] = V::pack(f);
@@ -250,7 +257,7 @@ fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ s
   const uint4* is = reinterpret_cast<const uint4*>(Hin + static_cast<size_t>(s) * d);
   uint4* orow = reinterpret_cast<uint4*>(Hout + static_cast<size_t>(r) * d);
   const int nv = d / V::N;
-  constexpr int U = 2;
+  constexpr int U = 8;
   for (int v0 = lane; v0 < nv; v0 += 32 * U) {
     uint4 a[U], b[U], c[U];
 #pragma unroll
@@ -301,12 +308,20 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
                 uint8_t* fold, float* rel, cudaStream_t st) {
   const int R = B * L;
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
-  if (dtype == SPECFOLD_BF16)
-    gate_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(H), parent, B, L, d, tau, fold, rel);
-  else
-    gate_kernel<float><<<grid, block, 0, st>>>(static_cast<const float*>(H), parent, B, L, d, tau,
-                                               fold, rel);
+  const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
+  if (dtype == SPECFOLD_BF16) {
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
+    if (per_lane <= 8)
+      gate_kernel<__nv_bfloat16, 8><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+    else
+      gate_kernel<__nv_bfloat16, 16><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+  } else {
+    const float* h = static_cast<const float*>(H);
+    if (per_lane <= 8)
+      gate_kernel<float, 8><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+    else
+      gate_kernel<float, 16><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+  }
   count_launch();
   return check_launch();
 }

@@ -60,15 +60,12 @@ struct GemmCall {
   void* Yk;               // QKV: block K / V outputs
   void* Yv;
   int n_q, n_kv, hd;      // QKV head layout
-  // scratch: tile counters (zero on entry, left zero) and fp32 partial sums
-  int* counters;
-  int counters_len;
+  // scratch: fp32 split-K partial tiles
   float* partial;
   size_t partial_len;     // floats, >= gemm_partial_floats()
   uint32_t* status;
 };
 size_t gemm_partial_floats();
-int gemm_counters_needed(int Mcap, int N, int epi);
 int launch_gemm(const GemmCall& c, cudaStream_t st);
 
 // ---- tcgen05 attention (attn_tc.cu) ----

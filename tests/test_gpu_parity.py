@@ -60,8 +60,14 @@ def check_layer(inp, tau, rows=None, inter=True):
     rr = res["out_rows"]
     m["H_out"] = rel_l2(Hg[rr], res["out"])
     m["delta"] = rel_l2(Hg[rr] - Hin[rr], res["out"] - Hin[rr])
+    # The layer's own contribution (H_out - H_in) can be small next to H, so
+    # the bf16 rounding of H_out alone may exceed 2e-2 of it: bound the error
+    # by 2e-2 of the contribution plus twice that rounding floor.
+    err = np.linalg.norm(Hg[rr] - res["out"])
+    floor = np.linalg.norm(synth.round_bf16(res["out"].astype(np.float32)) - res["out"])
+    assert err <= TOL * np.linalg.norm(res["out"] - Hin[rr]) + 2.0 * floor, m
     for key, val in m.items():
-        if key not in ("n", "near_tau"):
+        if key not in ("n", "near_tau", "delta"):
             assert val < TOL, (key, val, m)
     return m, lay, out
 
