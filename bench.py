@@ -1,7 +1,8 @@
 """Benchmark: verified branch-tokens/s of the folded verification layer.
 
 One step = one folded-layer call (gate, resolve, pack + RMSNorm1, QKV, folded
-attention, output projection, RMSNorm2, SwiGLU, down projection, fold-fill)
+attention, output projection + RMSNorm2, SwiGLU, down projection, fold-fill),
+replayed as the library's CUDA graph of specfold_layer_forward
 over one batch of B branches x L block tokens, on the 7B-like single-layer
 workload: d 3584, 28/4 heads x 128, SwiGLU 18944, prefix 512, L 32, 8
 branches on a depth-3 directed draft graph, seeded synthetic inputs.
@@ -10,7 +11,8 @@ branches on a depth-3 directed draft graph, seeded synthetic inputs.
 
 Prints one JSON line (rank 0).  value = B*L*steps*N / (max over ranks of the
 summed device time of the K steps), inputs resident in HBM; L2 is flushed
-(256 MiB write) between steps, outside the timed events.  e2e = the same
+between steps (a 256 MiB write, then a 256 MiB read so the written lines are
+evicted too), outside the timed events.  e2e = the same
 metric through the public API with pinned host buffers, including the
 host->device copy of H_in/parent and the device->host copy of H_out.
 --impl reference times the CPU oracle on this host's cores instead.
@@ -168,7 +170,7 @@ def stage_roofline(name, dims, n, R, us, peaks):
     elif name == "qkv":
         flops = 2.0 * n * d * (nq + 2 * nkv)
         byts = (nq + 2 * nkv) * d * e + n * d * e + n * (nq + 2 * nkv) * e
-    elif name == "out_proj":
+    elif name == "out_proj_norm":
         flops = 2.0 * n * nq * d
         byts = d * nq * e + n * nq * e + 2 * n * d * e
     else:
@@ -208,7 +210,14 @@ def run_ours(args, rank, world):
     pk, pv = (cache[o:o + P, 0], cache[o:o + P, 1]) if P else (None, None)
     lay = binding.FoldedLayer(dims, W, B, L, pk, pv)
     Hout = torch.empty_like(H)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        # write a buffer larger than L2, then read another one so the dirty
+        # lines of the first are written back before the timed region starts
+        flush_w.zero_()
+        flush_r.sum()
     stream = torch.cuda.current_stream()
     peaks = load_peaks()
 
@@ -217,43 +226,43 @@ def run_ours(args, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    def timed_steps(tau, steps, warmup, stage_ev=False, clocks=None):
+    def timed_steps(tau, steps, warmup):
+        """K graph replays of the layer, each bracketed by event-record nodes
+        inside the graph (first and last node), L2 flushed before each."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
+        for e in ev:  # torch creates the CUDA event at its first record
+            e.record(stream)
+        graph = lay.graph(H, parent, tau, Hout, events=ev)
         for _ in range(warmup):
-            lay.forward(H, parent, tau, Hout)
+            flush()
+            graph.launch()
         torch.cuda.synchronize()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)] for _ in range(steps)] \
-            if stage_ev else None
-        if st_ev:  # torch creates the CUDA event at its first record
-            for row in st_ev:
-                for e in row:
-                    e.record(stream)
         barrier()
         torch.cuda.synchronize()
         l0 = binding.specfold_launch_count()
         t0 = time.time()
+        ms = []
+        st_sum = [0.0] * (binding.STAGE_EVENTS - 1)
         for i in range(steps):
-            flush.zero_()
-            evs[i][0].record(stream)
-            lay.forward(H, parent, tau, Hout, events=st_ev[i] if st_ev else None)
-            evs[i][1].record(stream)
+            flush()
+            graph.launch()
+            ev[-1].synchronize()
+            ms.append(ev[0].elapsed_time(ev[-1]))
+            for si in range(binding.STAGE_EVENTS - 1):
+                st_sum[si] += ev[si].elapsed_time(ev[si + 1])
         torch.cuda.synchronize()
         barrier()
         t1 = time.time()
         launches = binding.specfold_launch_count() - l0
-        ms = [a.elapsed_time(b) for a, b in evs]
-        stages = None
-        if st_ev:
-            stages = {}
-            for si, nm in enumerate(binding.STAGE_NAMES):
-                stages[nm] = statistics.mean(e[si].elapsed_time(e[si + 1]) for e in st_ev) * 1e3
+        graph.close()
+        stages = {nm: st_sum[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)}
         return sum(ms), ms, launches, stages, (t0, t1)
 
     # headline: tau from the command line, stage events on
     sampler = ClockSampler(dev_index)
     sampler.start()
     time.sleep(0.3)
-    total_ms, ms, launches, stages, (t0, t1) = timed_steps(args.tau, args.steps, args.warmup, stage_ev=True)
+    total_ms, ms, launches, stages, (t0, t1) = timed_steps(args.tau, args.steps, args.warmup)
     clocks = sampler.stop(t0, t1)
     assert lay.status() == 0, "device status set"
     n = lay.n_packed()
@@ -266,7 +275,7 @@ def run_ours(args, rank, world):
     value = B * L * args.steps * world / (total_ms_max * 1e-3)
 
     # dominant kernel of the step
-    gemm_stages = ("qkv", "out_proj", "gate_up", "down")
+    gemm_stages = ("qkv", "out_proj_norm", "gate_up", "down")
     top = max(stages, key=stages.get)
     rf = stage_roofline(top, d, n, R, stages[top], peaks) if top in gemm_stages else None
     if rf is None:
@@ -284,26 +293,30 @@ def run_ours(args, rank, world):
     par_host = parent.cpu().pin_memory()
     out_host = torch.empty(H.shape, dtype=torch.bfloat16, pin_memory=True)
     H_e, par_e, out_e = torch.empty_like(H), torch.empty_like(parent), torch.empty_like(H)
+    H_e.copy_(H)
+    par_e.copy_(parent)
+    e_graph = lay.graph(H_e, par_e, args.tau, out_e)
     e2e_steps = max(1, min(args.steps, 500))
     for _ in range(3):
         H_e.copy_(H_host, non_blocking=True)
         par_e.copy_(par_host, non_blocking=True)
-        lay.forward(H_e, par_e, args.tau, out_e)
+        e_graph.launch()
         out_host.copy_(out_e, non_blocking=True)
     torch.cuda.synchronize()
     e_ms = []
     barrier()
     for _ in range(e2e_steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         H_e.copy_(H_host, non_blocking=True)
         par_e.copy_(par_host, non_blocking=True)
-        lay.forward(H_e, par_e, args.tau, out_e)
+        e_graph.launch()
         out_host.copy_(out_e, non_blocking=True)
         b.record(stream)
         e_ms.append((a, b))
     torch.cuda.synchronize()
+    e_graph.close()
     e_total = sum(a.elapsed_time(b) for a, b in e_ms)
     if world > 1:
         import torch.distributed as dist
@@ -319,7 +332,7 @@ def run_ours(args, rank, world):
     sweep = []
     if not args.no_sweep:
         for tau in ([0.0] + list(w.taus)):
-            tot, _, _, st, _ = timed_steps(tau, max(50, min(args.steps, 300)), 5, stage_ev=True)
+            tot, _, _, st, _ = timed_steps(tau, max(50, min(args.steps, 300)), 5)
             steps_s = max(50, min(args.steps, 300))
             nn = lay.n_packed()
             sweep.append({"tau": tau, "n_packed": nn, "rho": round(nn / R, 4),
@@ -408,7 +421,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": workload_desc(w, args.tau, args.frac), "B": w.B, "L": w.L, "P": w.P,
                        "tau": args.tau, "n_packed": r["n_packed"], "recompute_fraction": round(r["n_packed"] / r["R"], 4),
-                       "l2": "flushed between steps (256 MiB write outside the timed events)",
+                       "l2": "flushed between steps (256 MiB write + 256 MiB read, outside the timed events)",
                        "parallelism": f"replicas x{world}"},
             "us_per_step": round(r["ms_per_step"] * 1e3, 2),
             "roofline": r["roofline"],

@@ -21,9 +21,8 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "specfold.h")
 OK, EINVAL, EALIGN, ECAPACITY, EUNSUPPORTED, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6
 DEV_TIMEOUT, DEV_BAD_PARENT = 1, 2
 BF16, F32 = 0, 1
-STAGE_EVENTS = 11
-STAGE_NAMES = ("gate", "select", "rmsnorm1", "qkv", "attention", "out_proj", "rmsnorm2", "gate_up",
-               "down", "fold_fill")
+STAGE_EVENTS = 9
+STAGE_NAMES = ("gate", "select_pack", "qkv", "attention", "out_proj_norm", "gate_up", "down", "fold_fill")
 
 
 class SpecfoldError(RuntimeError):
@@ -50,7 +49,7 @@ class specfold_kv_view(ctypes.Structure):
 class specfold_ws_layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in
                 ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "x1", "q",
-                 "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "total")]
+                 "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "attn_scratch", "total")]
 
 
 _P = ctypes.c_void_p
@@ -75,6 +74,10 @@ _SIG = {
     "specfold_status_string": (ctypes.c_char_p, [_I]),
     "specfold_launch_count": (ctypes.c_uint64, []),
     "specfold_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+    "specfold_layer_graph_create": (_I, [_P, _P, _P, _P, _I, _I, specfold_kv_view, specfold_kv_view, _I,
+                                         ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "specfold_graph_launch": (_I, [_P, _P]),
+    "specfold_graph_destroy": (_I, [_P]),
 }
 
 _lib = None
@@ -250,6 +253,45 @@ def specfold_selftest_timeout(status: torch.Tensor, wait_ns: int, stream=None):
     _check(lib().specfold_selftest_timeout(_ptr(status), int(wait_ns), _stream(stream)), "specfold_selftest_timeout")
 
 
+class LayerGraph:
+    """A captured specfold_layer_forward call (specfold_layer_graph_create):
+    launch() replays all of its kernels with one graph launch.  Inputs are read
+    from, and outputs written to, the buffers given at capture."""
+
+    def __init__(self, dims, weights, H_in, parent, prefK, prefV, P, tau, H_out, ws,
+                 events: Optional[Sequence] = None):
+        B, L, _ = H_in.shape
+        ev = None
+        if events is not None:
+            handles = [e.cuda_event for e in events]
+            if len(handles) != STAGE_EVENTS or not all(handles):
+                raise ValueError("need SPECFOLD_STAGE_EVENTS recorded-once events")
+            ev = (ctypes.c_void_p * STAGE_EVENTS)(*handles)
+        self._keep = (dims, weights, H_in, parent, prefK, prefV, H_out, ws, events, ev)
+        h = ctypes.c_void_p()
+        torch.cuda.synchronize()
+        _check(lib().specfold_layer_graph_create(ctypes.byref(dims), ctypes.byref(weights), _ptr(H_in), _ptr(parent),
+                                                 B, L, kv_view(prefK), kv_view(prefV), P, float(tau), _ptr(H_out),
+                                                 _ptr(ws), ws.numel(), ev, ctypes.byref(h)),
+               "specfold_layer_graph_create")
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(lib().specfold_graph_launch(self._h, _stream(stream)), "specfold_graph_launch")
+
+    def close(self):
+        if self._h:
+            torch.cuda.synchronize()
+            lib().specfold_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 # ------------------------------------------------------------ convenience --
 
 class FoldedLayer:
@@ -291,6 +333,11 @@ class FoldedLayer:
                 n *= s
             raw = raw[:n].view(*shape)
         return raw
+
+    def graph(self, H_in, parent, tau, H_out, events=None) -> LayerGraph:
+        """Capture forward(H_in, parent, tau, H_out) as one replayable graph."""
+        return LayerGraph(self.dims, self.cw, H_in, parent, self.prefK, self.prefV, self.P, tau, H_out, self.ws,
+                          events=events)
 
     def n_packed(self) -> int:
         return int(self.view("n_packed", torch.int32)[0].item())

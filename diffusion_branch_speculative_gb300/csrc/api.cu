@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "sf_internal.h"
 
@@ -156,6 +157,8 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->x2 = take(R * d->d_model * e);
   o->g = take(R * d->ffn_dim * e);
   o->gemm_scratch = take(gemm_partial_floats() * 4);
+  o->attn_scratch = take(attn_partial_bytes(static_cast<int>(R), d->n_q_heads / d->n_kv_heads, d->n_kv_heads,
+                                            d->head_dim));
   o->total = off;
 }
 
@@ -183,6 +186,17 @@ static void fill_scratch(GemmCall& c, const Scratch& s, uint32_t* status) {
   c.partial = s.partial;
   c.partial_len = s.partial_len;
   c.status = status;
+}
+
+// Stage events: recorded as graph event nodes while the stream is being
+// captured (a plain record would become a capture-internal dependency).
+static void record_stage_event(void* ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
 }
 
 // ---------------------------------------------------------- stage bodies --
@@ -216,7 +230,8 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
 
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
                            const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
-                           const int32_t* n_dev, int B, int L, void* O, uint32_t* status, cudaStream_t st) {
+                           const int32_t* n_dev, int B, int L, void* O, uint32_t* status, void* part,
+                           size_t part_bytes, cudaStream_t st) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
   a.Q = Q;
@@ -235,12 +250,14 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
   a.hd = d->head_dim;
   a.O = O;
   a.status = status;
+  a.part = part;
+  a.part_bytes = part_bytes;
   return launch_attention(a, st);
 }
 
 static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, const void* O,
                           const int32_t* packed_idx, const int32_t* n_dev, const void* H_in, int R, void* A,
-                          const Scratch& s, uint32_t* status, cudaStream_t st) {
+                          const Scratch& s, uint32_t* status, cudaStream_t st, void* X2_fused = nullptr) {
   GemmCall c;
   memset(&c, 0, sizeof(c));
   c.epi = EPI_RESID_PACKED;
@@ -258,18 +275,22 @@ static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, con
   c.ldr = d->d_model;
   c.row_idx = packed_idx;
   fill_scratch(c, s, status);
+  if (X2_fused) {
+    const RowNorm rn{w->g2, d->rms_eps, X2_fused};
+    return launch_gemm(c, st, &rn);
+  }
   return launch_gemm(c, st);
 }
 
 static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const void* A, const int32_t* packed_idx,
                      const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int R,
                      void* H_out, void* X2, void* G, const Scratch& s, uint32_t* status, cudaStream_t st,
-                     void* const* ev, int ev0) {
+                     void* const* ev, int ev0, bool x2_ready) {
   auto mark = [&](int i) {
-    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    if (ev) record_stage_event(ev[i], st);
   };
-  SF_TRY(launch_rmsnorm_rows(d->dtype, A, nullptr, n_dev, R, d->d_model, w->g2, d->rms_eps, X2, st));
-  mark(ev0 + 1);
+  if (!x2_ready)
+    SF_TRY(launch_rmsnorm_rows(d->dtype, A, nullptr, n_dev, R, d->d_model, w->g2, d->rms_eps, X2, st));
   GemmCall c;
   memset(&c, 0, sizeof(c));
   c.epi = EPI_SWIGLU;
@@ -286,7 +307,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.ldy = d->ffn_dim;
   fill_scratch(c, s, status);
   SF_TRY(launch_gemm(c, st));
-  mark(ev0 + 2);
+  mark(ev0 + 1);
   memset(&c, 0, sizeof(c));
   c.epi = EPI_RESID_SCATTER;
   c.A = G;
@@ -304,9 +325,9 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.row_idx = packed_idx;
   fill_scratch(c, s, status);
   SF_TRY(launch_gemm(c, st));
-  mark(ev0 + 3);
+  mark(ev0 + 2);
   SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
-  mark(ev0 + 4);
+  mark(ev0 + 3);
   return SPECFOLD_OK;
 }
 
@@ -352,8 +373,8 @@ int specfold_resolve(const uint8_t* fold, const int32_t* parent, int B, int L, i
                      void* stream) {
   if (!fold || !parent || !src) return SPECFOLD_EINVAL;
   SF_TRY(check_rows(B, L));
-  return launch_select(fold, parent, B, L, src, nullptr, nullptr, nullptr, status_opt,
-                       static_cast<cudaStream_t>(stream));
+  return launch_select_pack(SPECFOLD_BF16, fold, parent, B, L, 0, nullptr, nullptr, 0.f, src, nullptr, nullptr,
+                            nullptr, nullptr, status_opt, static_cast<cudaStream_t>(stream));
 }
 
 int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1, float eps, int B, int L, int d,
@@ -365,10 +386,9 @@ int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1,
   if (d % 256) return SPECFOLD_EUNSUPPORTED;
   if (!a16(H) || !a16(g1) || !a16(X1)) return SPECFOLD_EALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // pack alone: every row is its own source unless folded (no parent walk),
-  // so the scan runs on fold with a trivial parent table of the root only.
-  SF_TRY(launch_select(fold, nullptr, B, L, nullptr, packed_idx, slot_of_row, n_dev, nullptr, st));
-  return launch_rmsnorm_rows(dtype, H, packed_idx, n_dev, B * L, d, g1, eps, X1, st);
+  // pack alone: no parent walk -- a folded non-root row is not recomputed
+  return launch_select_pack(dtype, fold, nullptr, B, L, d, H, g1, eps, nullptr, packed_idx, slot_of_row, n_dev, X1,
+                            nullptr, st);
 }
 
 int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const void* X1, const int32_t* packed_idx,
@@ -400,9 +420,10 @@ int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_vie
   if (!a16(Q) || !a16(blockK) || !a16(blockV) || !a16(O)) return SPECFOLD_EALIGN;
   specfold_ws_layout lo;
   layout(dims, B, L, &lo);
-  if (ws_bytes < lo.status + 256) return SPECFOLD_ECAPACITY;
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
   return stage_attention(dims, Q, prefK, prefV, P, blockK, blockV, src, packed_idx, n_dev, B, L, O,
-                         at<uint32_t>(ws, lo.status), static_cast<cudaStream_t>(stream));
+                         at<uint32_t>(ws, lo.status), at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch,
+                         static_cast<cudaStream_t>(stream));
 }
 
 int specfold_out_proj(const specfold_dims* dims, const specfold_weights* w, const void* O, const int32_t* packed_idx,
@@ -437,7 +458,7 @@ int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const voi
   const Scratch s = layer_scratch(ws, dims, B, L, lo);
   return stage_ffn(dims, w, A, packed_idx, n_dev, H_in, src, fold, B * L, H_out, at<void>(ws, lo.x2),
                    at<void>(ws, lo.g), s, at<uint32_t>(ws, lo.status), static_cast<cudaStream_t>(stream), nullptr,
-                   0);
+                   0, false);
 }
 
 int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
@@ -465,26 +486,26 @@ int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
   int32_t* pidx = at<int32_t>(ws, lo.packed_idx);
   int32_t* n_dev = at<int32_t>(ws, lo.n_packed);
   auto mark = [&](int i) {
-    if (stage_events) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
+    if (stage_events) record_stage_event(stage_events[i], st);
   };
   mark(0);
   SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st));
   mark(1);
-  SF_TRY(launch_select(fold, parent, B, L, src, pidx, at<int32_t>(ws, lo.slot_of_row), n_dev, status, st));
+  SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
+                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st));
   mark(2);
-  SF_TRY(launch_rmsnorm_rows(dims->dtype, H_in, pidx, n_dev, R, dims->d_model, w->g1, dims->rms_eps,
-                             at<void>(ws, lo.x1), st));
-  mark(3);
   SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
                    at<void>(ws, lo.block_v), s, status, st));
-  mark(4);
+  mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
-                         at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status, st));
+                         at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
+  mark(4);
+  SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
+                        at<void>(ws, lo.x2)));
   mark(5);
-  SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st));
-  mark(6);
   return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
-                   at<void>(ws, lo.g), s, status, st, stage_events, 6);
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true);
 }
 
 int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y, void* ws, size_t ws_bytes,
@@ -511,6 +532,74 @@ int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K
   c.partial_len = gemm_partial_floats();
   c.status = static_cast<uint32_t*>(ws);
   return launch_gemm(c, static_cast<cudaStream_t>(stream));
+}
+
+struct specfold_graph_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  uint64_t kernels;  // kernels per replay
+};
+
+int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                                const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV,
+                                int P, float tau, void* H_out, void* ws, size_t ws_bytes, void* const* stage_events,
+                                specfold_graph* graph) {
+  if (!graph) return SPECFOLD_EINVAL;
+  *graph = nullptr;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return SPECFOLD_ECUDA;
+  // one eager call first: kernel attributes are set and arguments checked
+  // outside the capture
+  int rc = specfold_layer_forward(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, ws_bytes, nullptr, s);
+  if (rc == SPECFOLD_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = SPECFOLD_ECUDA;
+  if (rc != SPECFOLD_OK) {
+    cudaStreamDestroy(s);
+    return rc;
+  }
+  const uint64_t k0 = g_launches.load();
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return SPECFOLD_ECUDA;
+  }
+  rc = specfold_layer_forward(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, ws_bytes, stage_events,
+                              s);
+  const cudaError_t ce = cudaStreamEndCapture(s, &g);
+  const uint64_t kernels = g_launches.load() - k0;
+  g_launches.fetch_sub(kernels);  // captured, not launched
+  cudaStreamDestroy(s);
+  if (rc != SPECFOLD_OK || ce != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    return rc != SPECFOLD_OK ? rc : SPECFOLD_ECUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return SPECFOLD_ECUDA;
+  }
+  specfold_graph h = new (std::nothrow) specfold_graph_s{g, exec, kernels};
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(g);
+    return SPECFOLD_ECAPACITY;
+  }
+  *graph = h;
+  return SPECFOLD_OK;
+}
+
+int specfold_graph_launch(specfold_graph graph, void* stream) {
+  if (!graph) return SPECFOLD_EINVAL;
+  if (cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SPECFOLD_ECUDA;
+  count_launch(static_cast<int>(graph->kernels));
+  return SPECFOLD_OK;
+}
+
+int specfold_graph_destroy(specfold_graph graph) {
+  if (!graph) return SPECFOLD_EINVAL;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
+  return SPECFOLD_OK;
 }
 
 int specfold_get_status(void* ws, uint32_t* status_out, void* stream) {

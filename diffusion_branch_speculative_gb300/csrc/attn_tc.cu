@@ -22,6 +22,7 @@
 #include "sf_device.cuh"
 #include "sf_internal.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 
@@ -30,6 +31,7 @@ namespace {
 
 constexpr int kAttnThreads = 256;
 constexpr int kLoaders = 96;
+constexpr int kSmBudget = 160;  // SM count the split sizing plans for (>= one GB300)
 constexpr int kAtom = 128 * 128;  // one 128-row x 128-byte swizzle block
 
 struct AttnParams {
@@ -45,7 +47,20 @@ struct AttnParams {
   int P, L, R, n_kv, g, n_q;
   float sl2;  // log2(e) / sqrt(hd)
   uint32_t* status;
+  // split-KV: up to sp_max CTAs share one (query tile, kv head); each writes
+  // an unnormalised partial (o, running max m in log2 units, sum l)
+  int sp_max;
+  int num_sms;
+  float* part_o;    // [tiles_x * n_kv * sp_max][128][hd]
+  float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
 };
+
+// Number of key-range splits for n packed rows: enough CTAs to cover the SMs.
+SF_DEV int attn_splits(int rows_total, int n_kv, int sp_max, int num_sms) {
+  const int tiles = ((rows_total + 127) / 128) * n_kv;
+  if (tiles <= 0) return 1;
+  return max(1, min(sp_max, (num_sms + tiles - 1) / tiles));
+}
 
 template <int HD>
 struct ACfg {
@@ -67,7 +82,10 @@ template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = ACfg<HD>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base; plain pointer arithmetic on the shared array keeps
+  // every derived pointer in the shared state space (shared, not generic,
+  // loads and stores)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
@@ -98,6 +116,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int keys_blk = (b_hi - b_lo + 1) * L;
   const int NBP = (p.P + 127) / 128;
   const int NB = NBP + (keys_blk + 127) / 128;
+  // this CTA's share of the key blocks
+  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms);
+  const int z = blockIdx.z;
+  if (z >= SP) return;
+  const int jb = (z * NB) / SP;
+  const int NT = ((z + 1) * NB) / SP - jb;
+  const size_t pslot = (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * p.sp_max + z;
+  if (NT == 0) {  // empty key range: a neutral partial
+    for (int i = threadIdx.x; i < 128 * HD; i += kAttnThreads) p.part_o[pslot * 128 * HD + i] = 0.f;
+    for (int i = threadIdx.x; i < 128; i += kAttnThreads) {
+      p.part_ml[(pslot * 128 + i) * 2] = -INFINITY;
+      p.part_ml[(pslot * 128 + i) * 2 + 1] = 0.f;
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -139,9 +172,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + m0);
     }
     int issued_tma = -1;
-    for (int j = 0; j < NB; ++j) {
-      const int st = j & 1;
-      if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((j >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+    for (int t = 0; t < NT; ++t) {
+      const int j = jb + t;
+      const int st = t & 1;
+      if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((t >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
       named_bar_sync(1, kLoaders);
       if (!okflag[st]) break;
       uint8_t* sK = smem + C::OFF_KV + (2 * st) * C::KV_BYTES;
@@ -154,7 +188,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, j * 128);
             tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, j * 128);
           }
-          issued_tma = j;
+          issued_tma = t;
         }
       } else {
         for (int kr = lt; kr < 128; kr += kLoaders) {
@@ -206,40 +240,64 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     for (int e = 0; e < HD; ++e) o[e] = 0.f;
     float m_run = -INFINITY, l = 0.f, alpha_prev = 1.f;
     bool ok = true;
-    for (int j = 0; j < NB && ok; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(smem_u32(&s_full[sb]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+    for (int t = 0; t < NT && ok; ++t) {
+      const int j = jb + t;
+      const int sb = t & 1;
+      if (!mbar_wait(smem_u32(&s_full[sb]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      __syncwarp();
       const bool prefix = j < NBP;
-      if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      __syncwarp();
       tc_fence_after();
-      const int* mb = meta + sb * 128;
       const int key0 = j * 128;
       const uint32_t ts = tmem + lane_off + sb * 128;
-      // pass 1: row max of the unmasked scores
+      // visibility of the 128 keys as four 32-bit masks (bit e of km[c]: key
+      // 32c + e): prefix keys below P, block keys of this row's own branch
+      uint32_t km[4];
+      if (prefix) {
+        const int lim = p.P - key0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int v = lim - c * 32;
+          km[c] = v >= 32 ? 0xffffffffu : (v <= 0 ? 0u : ((1u << v) - 1u));
+        }
+      } else {
+        const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t mk = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int4 v = mb4[c * 8 + q];
+            mk |= (static_cast<uint32_t>(v.x == my_b) << (4 * q)) | (static_cast<uint32_t>(v.y == my_b) << (4 * q + 1)) |
+                  (static_cast<uint32_t>(v.z == my_b) << (4 * q + 2)) | (static_cast<uint32_t>(v.w == my_b) << (4 * q + 3));
+          }
+          km[c] = mk;
+        }
+      }
+      // pass 1: row max of the visible scores
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(ts + c * 32, r);
-        tmem_ld_wait();
+        tmem_ld_wait(r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = c * 32 + e;
-          const bool keep = prefix ? (key0 + key < p.P) : (mb[key] == my_b);
-          if (keep) mx = fmaxf(mx, __uint_as_float(r[e]));
-        }
+        for (int e = 0; e < 32; ++e)
+          mx = fmaxf(mx, ((km[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY);
       }
       const float m_new = fmaxf(m_run, mx * p.sl2);
       // fold the previous block's P V into the accumulator (also frees P)
-      if (j >= 1) {
-        const int ob = (j - 1) & 1;
-        if (!mbar_wait(smem_u32(&o_full[ob]), ((j - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (t >= 1) {
+        const int ob = (t - 1) & 1;
+        if (!mbar_wait(smem_u32(&o_full[ob]), ((t - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        __syncwarp();
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
         }
@@ -253,17 +311,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(ts + c * 32, r);
-        tmem_ld_wait();
+        tmem_ld_wait(r);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float pv[2];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const int key = c * 32 + e + t;
-            const bool keep = prefix ? (key0 + key < p.P) : (mb[key] == my_b);
-            pv[t] = keep ? ex2(fmaf(__uint_as_float(r[e + t]), p.sl2, -m_new)) : 0.f;
-            l += pv[t];
+          for (int u = 0; u < 2; ++u) {
+            const float x = ex2(fmaf(__uint_as_float(r[e + u]), p.sl2, -m_new));
+            pv[u] = ((km[c] >> (e + u)) & 1u) ? x : 0.f;
+            l += pv[u];
           }
           pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
         }
@@ -282,18 +339,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       alpha_prev = alpha;
     }
     if (ok) {
-      const int ob = (NB - 1) & 1;
-      if (mbar_wait(smem_u32(&o_full[ob]), ((NB - 1) >> 1) & 1, abort_flag, p.status)) {
+      const int ob = (NT - 1) & 1;
+      if (mbar_wait(smem_u32(&o_full[ob]), ((NT - 1) >> 1) & 1, abort_flag, p.status)) {
+        __syncwarp();
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
         }
-        if (valid) {
+        if (SP > 1) {
+          float* po = p.part_o + (pslot * 128 + row) * HD;
+#pragma unroll
+          for (int q4 = 0; q4 < HD / 4; ++q4)
+            reinterpret_cast<float4*>(po)[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          p.part_ml[(pslot * 128 + row) * 2] = m_run;
+          p.part_ml[(pslot * 128 + row) * 2 + 1] = l;
+        } else if (valid) {
           const float inv = 1.f / l;
           uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
                                                 static_cast<size_t>(h * g + hg) * HD);
@@ -314,7 +379,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.status);
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aP = smem_u32(sP);
-      auto issue_pv = [&](int i) -> bool {
+      auto issue_pv = [&](int i) -> bool {  // i: local block index
         if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
         const int ob = i & 1;
         if (!mbar_wait(smem_u32(&o_free[ob]), ((i >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
@@ -330,10 +395,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         tc_commit(smem_u32(&kv_empty[i & 1]));
         return true;
       };
-      for (int j = 0; j < NB && ok; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(smem_u32(&kv_full[st]), (j >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&s_free[st]), ((j >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+      for (int t = 0; t < NT && ok; ++t) {
+        const int st = t & 1;
+        if (!mbar_wait(smem_u32(&kv_full[st]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&s_free[st]), ((t >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * st) * C::KV_BYTES);
 #pragma unroll
@@ -343,9 +408,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                      sdesc_sw128(aK + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
         tc_commit(smem_u32(&s_full[st]));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
       }
-      if (ok) issue_pv(NB - 1);
+      if (ok) issue_pv(NT - 1);
       tc_commit(smem_u32(drain));
       int never = 0;
       mbar_wait(smem_u32(drain), 0, &never, nullptr, 10000000ull);
@@ -358,6 +423,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   if (warp == 3) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Merges the split-KV partials: for each (query row, kv head, 8 dims),
+// O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p, int tiles_x) {
+  const int n = min(max(p.n_dev[0], 0), p.R);
+  const int rows_total = n * p.g;
+  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms);
+  if (SP <= 1) return;
+  constexpr int DG = HD / 8;
+  const long long total = static_cast<long long>(rows_total) * p.n_kv * DG;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int dg = static_cast<int>(idx % DG);
+    const long long rest = idx / DG;
+    const int m = static_cast<int>(rest % rows_total);
+    const int h = static_cast<int>(rest / rows_total);
+    const int row = m & 127;
+    const size_t pb = (static_cast<size_t>(h) * tiles_x + (m >> 7)) * p.sp_max;
+    float M = -INFINITY;
+    for (int z = 0; z < SP; ++z) M = fmaxf(M, __ldcg(p.part_ml + ((pb + z) * 128 + row) * 2));
+    float l = 0.f, acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int z = 0; z < SP; ++z) {
+      const float mz = __ldcg(p.part_ml + ((pb + z) * 128 + row) * 2);
+      if (mz == -INFINITY) continue;
+      const float wz = ex2(mz - M);
+      l = fmaf(__ldcg(p.part_ml + ((pb + z) * 128 + row) * 2 + 1), wz, l);
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + ((pb + z) * 128 + row) * HD + dg * 8);
+      const float4 a = __ldcg(src), b = __ldcg(src + 1);
+      acc[0] = fmaf(a.x, wz, acc[0]); acc[1] = fmaf(a.y, wz, acc[1]);
+      acc[2] = fmaf(a.z, wz, acc[2]); acc[3] = fmaf(a.w, wz, acc[3]);
+      acc[4] = fmaf(b.x, wz, acc[4]); acc[5] = fmaf(b.y, wz, acc[5]);
+      acc[6] = fmaf(b.z, wz, acc[6]); acc[7] = fmaf(b.w, wz, acc[7]);
+    }
+    const float inv = 1.f / l;
+    const int k = m / p.g, hg = m - k * p.g;
+    uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
+                                          static_cast<size_t>(h * p.g + hg) * HD + dg * 8);
+    *dst = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                      pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
   }
 }
 
@@ -390,6 +499,14 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   p.n_q = c.n_q;
   p.sl2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   p.status = c.status;
+  const int tiles_x = (R * g + 127) / 128;
+  p.sp_max = attn_sp_max(R, g, c.n_kv);
+  p.num_sms = num_sms();
+  if (p.sp_max > 1) {
+    if (!c.part || c.part_bytes < attn_partial_bytes(R, g, c.n_kv, HD)) return SPECFOLD_ECAPACITY;
+    p.part_o = static_cast<float*>(c.part);
+    p.part_ml = p.part_o + static_cast<size_t>(tiles_x) * c.n_kv * p.sp_max * 128 * HD;
+  }
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -399,13 +516,36 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
-  const dim3 grid((R * g + 127) / 128, c.n_kv);
+  const dim3 grid(tiles_x, c.n_kv, p.sp_max);
   attn_kernel<HD><<<grid, kAttnThreads, C::SMEM_BYTES, st>>>(p);
   count_launch();
-  return check_launch();
+  if (check_launch()) return SPECFOLD_ECUDA;
+  if (p.sp_max > 1) {
+    const long long work = static_cast<long long>(R) * g * c.n_kv * (HD / 8);
+    const int cg = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
+    attn_combine_kernel<HD><<<std::max(cg, 1), 256, 0, st>>>(p, tiles_x);
+    count_launch();
+    return check_launch();
+  }
+  return SPECFOLD_OK;
 }
 
 }  // namespace
+
+// Largest split count for this shape: enough (query tile, head, split) CTAs
+// to cover about four waves of SMs when every row is packed, at most 16.
+int attn_sp_max(int R, int g, int n_kv) {
+  const int tiles = ((R * g + 127) / 128) * n_kv;
+  const int want = (4 * kSmBudget + tiles - 1) / tiles;
+  return std::max(1, std::min(16, want));
+}
+
+size_t attn_partial_bytes(int R, int g, int n_kv, int hd) {
+  const int sp = attn_sp_max(R, g, n_kv);
+  if (sp <= 1) return 0;
+  const size_t slots = static_cast<size_t>((R * g + 127) / 128) * n_kv * sp;
+  return slots * 128 * (hd + 2) * sizeof(float);
+}
 
 int launch_attention(const AttnCall& c, cudaStream_t st) {
   if (c.hd == 128) return run_attn<128>(c, st);

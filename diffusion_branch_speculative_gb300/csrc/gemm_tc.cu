@@ -40,7 +40,8 @@ struct Cfg {
   static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int EPI_STAGE_BYTES = 4 * 32 * 33 * 4;  // per epilogue warp: 32 x 32 fp32, padded
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EPI_STAGE_BYTES + 1024;
 };
 
 struct GemmParams {
@@ -62,7 +63,7 @@ struct GemmParams {
   uint32_t* status;
 };
 
-SF_DEV float silu(float x) { return x / (1.f + ex2(-x * 1.4426950408889634f)); }
+SF_DEV float silu(float x) { return __fdividef(x, 1.f + ex2(-x * 1.4426950408889634f)); }
 
 template <int W>
 SF_DEV void store_bf16(__nv_bfloat16* dst, const float (&v)[W]) {
@@ -131,6 +132,38 @@ SF_DEV int split_factor(int tiles, int grid, int KB) {
   return S;
 }
 
+// Epilogue of one output element (row k, column c); for SWIGLU x is the
+// gate value and u the up value of feature c.
+template <int EPI>
+SF_DEV void epi_elem(const GemmParams& p, int k, int c, float x, float u) {
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+  const __nv_bfloat16* Rz = static_cast<const __nv_bfloat16*>(p.resid);
+  if constexpr (EPI == EPI_STORE) {
+    Y[static_cast<size_t>(k) * p.ldy + c] = __float2bfloat16_rn(x);
+  } else if constexpr (EPI == EPI_RESID_PACKED) {
+    const int r = p.row_idx[k];
+    Y[static_cast<size_t>(k) * p.ldy + c] = __float2bfloat16_rn(x + __bfloat162float(Rz[static_cast<size_t>(r) * p.ldr + c]));
+  } else if constexpr (EPI == EPI_RESID_SCATTER) {
+    const int r = p.row_idx[k];
+    Y[static_cast<size_t>(r) * p.ldy + c] = __float2bfloat16_rn(x + __bfloat162float(Rz[static_cast<size_t>(k) * p.ldr + c]));
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    Y[static_cast<size_t>(k) * p.ldy + c] = __float2bfloat16_rn(silu(x) * u);
+  } else {  // EPI_QKV
+    const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+    if (c < nq) {
+      const int head = c / p.hd, j = c - head * p.hd;
+      const int hk = head / p.g, hg = head - hk * p.g;
+      Y[((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j] = __float2bfloat16_rn(x);
+    } else {
+      const int r = p.row_idx[k];
+      const bool is_k = c < nq + nkv;
+      const int cc = is_k ? c - nq : c - nq - nkv;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
+      dst[static_cast<size_t>(r) * nkv + cc] = __float2bfloat16_rn(x);
+    }
+  }
+}
+
 struct Unit {
   int m, s, nt, kb0, kb1, tile;
 };
@@ -151,7 +184,8 @@ template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, kept in the shared state space (see attn_tc.cu)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
@@ -161,6 +195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = abort_flag + 1;    // accumulator-ready broadcast
+  float* epi_stage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
@@ -286,7 +321,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // --------------------------------------------------------- epilogue --
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int et = threadIdx.x - 64;    // 0..127
-    const int row = q * 32 + lane;
     uint32_t t = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++t) {
       const Unit w = decode(u, Mt, S, p.Nt, KB);
@@ -296,56 +330,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       const bool ok = *s_ok != 0;
       named_bar_sync(1, 128);
       if (!ok) break;
+      __syncwarp();
       tc_fence_after();
-      const int k = w.m * kBM + row;
-      const bool valid = k < n;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
-      float* part = p.partial + (static_cast<size_t>(w.tile) * S + w.s) * kBM * BN +
-                    static_cast<size_t>(row) * BN;
-      if constexpr (EPI == EPI_SWIGLU) {
-        for (int ch = 0; ch < BN / 64; ++ch) {
-          uint32_t rg[32], ru[32];
-          tmem_ld32(tb + ch * 32, rg);
-          tmem_ld32(tb + BN / 2 + ch * 32, ru);
-          tmem_ld_wait();
-          float vg[32], vu[32];
+      // Each 32-column chunk of the warp's 32 rows goes through a padded smem
+      // transpose so that lane j then handles column j of one row at a time:
+      // every store (and residual load) of the warp is one contiguous segment.
+      float* stg = epi_stage + q * (32 * 33);
+      const int row0 = w.m * kBM + q * 32;          // first packed row of this warp
+      const int rows_here = min(32, n - row0);      // valid rows (may be <= 0)
+      float* prow = p.partial + (static_cast<size_t>(w.tile) * S + w.s) * kBM * BN + static_cast<size_t>(q * 32) * BN;
+      constexpr int NCH = EPI == EPI_SWIGLU ? BN / 64 : BN / 32;
+      for (int ch = 0; ch < NCH; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tb + ch * 32, r);
+        tmem_ld_wait(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            vg[e] = __uint_as_float(rg[e]);
-            vu[e] = __uint_as_float(ru[e]);
+        for (int e = 0; e < 32; ++e) stg[lane * 33 + e] = __uint_as_float(r[e]);
+        float gt[32];  // SWIGLU: gate values of column `lane`, one per row
+        if constexpr (EPI == EPI_SWIGLU) {
+          // the up half of the tile: same rows, columns BN/2 further on
+          uint32_t r2[32];
+          tmem_ld32(tb + BN / 2 + ch * 32, r2);
+          tmem_ld_wait(r2);
+          __syncwarp();
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) gt[rr] = stg[rr * 33 + lane];
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stg[lane * 33 + e] = __uint_as_float(r2[e]);
+        }
+        __syncwarp();
+        if (S == 1) {
+          const int cbase = EPI == EPI_SWIGLU ? w.nt * (BN / 2) + ch * 32 : w.nt * BN + ch * 32;
+#pragma unroll
+          for (int rr = 0; rr < 32; ++rr) {
+            if (rr < rows_here) {
+              const float x = stg[rr * 33 + lane];
+              if constexpr (EPI == EPI_SWIGLU)
+                epi_elem<EPI>(p, row0 + rr, cbase + lane, gt[rr], x);
+              else
+                epi_elem<EPI>(p, row0 + rr, cbase + lane, x, 0.f);
+            }
           }
-          if (valid) {
-            if (S == 1) {
-              epi_chunk<EPI, 32>(p, k, w.nt * (BN / 2) + ch * 32, vg, vu);
-            } else {
-              float4* pg = reinterpret_cast<float4*>(part + ch * 32);
-              float4* pu = reinterpret_cast<float4*>(part + BN / 2 + ch * 32);
+        } else {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                pg[e] = make_float4(vg[4 * e], vg[4 * e + 1], vg[4 * e + 2], vg[4 * e + 3]);
-                pu[e] = make_float4(vu[4 * e], vu[4 * e + 1], vu[4 * e + 2], vu[4 * e + 3]);
+          for (int rr = 0; rr < 32; ++rr) {
+            if (rr < rows_here) {
+              if constexpr (EPI == EPI_SWIGLU) {
+                prow[static_cast<size_t>(rr) * BN + ch * 32 + lane] = gt[rr];
+                prow[static_cast<size_t>(rr) * BN + BN / 2 + ch * 32 + lane] = stg[rr * 33 + lane];
+              } else {
+                prow[static_cast<size_t>(rr) * BN + ch * 32 + lane] = stg[rr * 33 + lane];
               }
             }
           }
         }
-      } else {
-        for (int ch = 0; ch < BN / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tb + ch * 32, r);
-          tmem_ld_wait();
-          float v[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
-          if (valid) {
-            if (S == 1) {
-              epi_chunk<EPI, 32>(p, k, w.nt * BN + ch * 32, v, v);
-            } else {
-              float4* pp = reinterpret_cast<float4*>(part + ch * 32);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) pp[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            }
-          }
-        }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&acce[ab]));
@@ -416,8 +457,91 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   }
 }
 
+// Output-projection finish (S6 + S7): one block per packed row k.  When the
+// GEMM was split, sums the partials in split order, adds the residual row
+// H[row_idx[k]] and writes A[k] (bf16); when it was not, A[k] is already
+// written by the GEMM epilogue.  Either way the block then RMS-normalises the
+// bf16 row: X2[k] = A[k] * g2 / sqrt(mean(A[k]^2) + eps).
+template <int BN, int GPT>
+__global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_constant__ GemmParams p, int gemm_grid,
+                                                             const __nv_bfloat16* __restrict__ g2, float eps,
+                                                             __nv_bfloat16* __restrict__ X2) {
+  __shared__ float s_red[8];
+  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int k = blockIdx.x;
+  if (k >= n) return;
+  const int Mt = (n + kBM - 1) / kBM;
+  const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
+  const int groups = p.N / 8;
+  const int m = k / kBM, row = k - m * kBM;
+  __nv_bfloat16* Arow = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(k) * p.ldy;
+  float v[GPT][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int gi = threadIdx.x + 256 * j;
+    if (gi >= groups) break;
+    const int c = gi * 8;
+    if (S > 1) {
+      const int nt = c / BN, tc = c - nt * BN;
+      const float* base = p.partial + (static_cast<size_t>(m * p.Nt + nt) * S) * kBM * BN +
+                          static_cast<size_t>(row) * BN + tc;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int s0 = 0; s0 < S; s0 += 4) {
+        float4 a4[4][2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (s0 + q < S) {
+            const float4* src = reinterpret_cast<const float4*>(base + static_cast<size_t>(s0 + q) * kBM * BN);
+            a4[q][0] = __ldcg(src);
+            a4[q][1] = __ldcg(src + 1);
+          }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (s0 + q < S) {
+            acc[0] += a4[q][0].x; acc[1] += a4[q][0].y; acc[2] += a4[q][0].z; acc[3] += a4[q][0].w;
+            acc[4] += a4[q][1].x; acc[5] += a4[q][1].y; acc[6] += a4[q][1].z; acc[7] += a4[q][1].w;
+          }
+      }
+      add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(p.row_idx[k]) * p.ldr + c, acc);
+      store_bf16<8>(Arow + c, acc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[j][e] = __bfloat162float(__float2bfloat16_rn(acc[e]));
+    } else {
+      const uint4 u = *reinterpret_cast<const uint4*>(Arow + c);
+      v[j][0] = bf16lo(u.x); v[j][1] = bf16hi(u.x); v[j][2] = bf16lo(u.y); v[j][3] = bf16hi(u.y);
+      v[j][4] = bf16lo(u.z); v[j][5] = bf16hi(u.z); v[j][6] = bf16lo(u.w); v[j][7] = bf16hi(u.w);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(v[j][e], v[j][e], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += s_red[w];
+  const float inv = rsqrtf(tot / static_cast<float>(p.N) + eps);
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int gi = threadIdx.x + 256 * j;
+    if (gi >= groups) break;
+    const int c = gi * 8;
+    const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g2 + c));
+    float o[8];
+    o[0] = v[j][0] * inv * bf16lo(gu.x); o[1] = v[j][1] * inv * bf16hi(gu.x);
+    o[2] = v[j][2] * inv * bf16lo(gu.y); o[3] = v[j][3] * inv * bf16hi(gu.y);
+    o[4] = v[j][4] * inv * bf16lo(gu.z); o[5] = v[j][5] * inv * bf16hi(gu.z);
+    o[6] = v[j][6] * inv * bf16lo(gu.w); o[7] = v[j][7] * inv * bf16hi(gu.w);
+    store_bf16<8>(X2 + static_cast<size_t>(k) * p.N + c, o);
+  }
+}
+
 template <int BN, int EPI>
-int run_gemm(const GemmCall& c, cudaStream_t st) {
+int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   using Cf = Cfg<BN>;
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -465,8 +589,25 @@ int run_gemm(const GemmCall& c, cudaStream_t st) {
   gemm_kernel<BN, EPI><<<grid, kGemmThreads, Cf::SMEM_BYTES, st>>>(p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
+  if constexpr (EPI == EPI_RESID_PACKED) {
+    if (rn) {
+      const int groups = c.N / 8;
+      if (groups > 4 * 256 || c.N % 8) return SPECFOLD_EUNSUPPORTED;
+      const dim3 g(c.Mcap), b(256);
+      const __nv_bfloat16* g2 = static_cast<const __nv_bfloat16*>(rn->gain);
+      __nv_bfloat16* x2 = static_cast<__nv_bfloat16*>(rn->out);
+      if (groups <= 256)
+        outproj_finish_kernel<BN, 1><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+      else if (groups <= 512)
+        outproj_finish_kernel<BN, 2><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+      else
+        outproj_finish_kernel<BN, 4><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+      count_launch();
+      return check_launch();
+    }
+  }
   // a split is possible only if even one m-tile leaves SMs idle
-  if (p.Nt < grid && p.K / kBK >= 2 * kMinKbPerSplit) {
+  if (grid / p.Nt >= 2 && p.K / kBK >= 2 * kMinKbPerSplit) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
@@ -478,8 +619,8 @@ int run_gemm(const GemmCall& c, cudaStream_t st) {
 }
 
 template <int EPI>
-int run_epi(const GemmCall& c, int BN, cudaStream_t st) {
-  return BN == 256 ? run_gemm<256, EPI>(c, st) : run_gemm<128, EPI>(c, st);
+int run_epi(const GemmCall& c, int BN, cudaStream_t st, const RowNorm* rn = nullptr) {
+  return BN == 256 ? run_gemm<256, EPI>(c, st, rn) : run_gemm<128, EPI>(c, st, rn);
 }
 
 }  // namespace
@@ -488,7 +629,7 @@ int run_epi(const GemmCall& c, int BN, cudaStream_t st) {
 // when tiles * S <= grid).
 size_t gemm_partial_floats() { return static_cast<size_t>(kMaxGrid) * kBM * 256; }
 
-int launch_gemm(const GemmCall& c, cudaStream_t st) {
+int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   if (c.K <= 0 || c.K % kBK || c.Mcap <= 0 || c.N <= 0) return SPECFOLD_EUNSUPPORTED;
   int BN = 128;
   switch (c.epi) {
@@ -512,7 +653,7 @@ int launch_gemm(const GemmCall& c, cudaStream_t st) {
   BN = c.N % 256 == 0 ? 256 : 128;
   switch (c.epi) {
     case EPI_STORE: return run_epi<EPI_STORE>(c, BN, st);
-    case EPI_RESID_PACKED: return run_epi<EPI_RESID_PACKED>(c, BN, st);
+    case EPI_RESID_PACKED: return run_epi<EPI_RESID_PACKED>(c, BN, st, rn);
     case EPI_RESID_SCATTER: return run_epi<EPI_RESID_SCATTER>(c, BN, st);
     default: return SPECFOLD_EINVAL;
   }

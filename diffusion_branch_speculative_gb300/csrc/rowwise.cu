@@ -103,122 +103,35 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
   }
 }
 
-// --------------------------------------------------- S2 + S3 resolve / scan --
-// One block.  A row is recomputed iff fold[r] == 0, it is a root row, or its
-// branch's parent is invalid (the chain cannot continue).  src follows the
-// fold chain through first parents.  The packed list is an exclusive scan of
-// the recomputed flags in row order, each thread owning a contiguous segment.
-constexpr int kSelectThreads = 1024;
-
-// Branch whose row (., i) ends the fold chain that starts at (b, i).  Without
-// a parent table (pack alone) a folded non-root row is simply not recomputed.
-SF_DEV int chain_end(const uint8_t* fold, const int32_t* parent, int b, int i, int L) {
-  if (!parent) return (b > 0 && fold[b * L + i]) ? -1 : b;
-  int s = b;
-  while (s > 0 && fold[s * L + i]) {
-    const int p = parent[s];
-    if (p < 0 || p >= s) break;
-    s = p;
-  }
-  return s;
-}
-
-__global__ void __launch_bounds__(kSelectThreads)
-select_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ parent, int B, int L,
-              int32_t* __restrict__ src, int32_t* __restrict__ packed_idx,
-              int32_t* __restrict__ slot, int32_t* __restrict__ n_dev, uint32_t* status) {
-  __shared__ int s_bad;
-  __shared__ int s_warp[kSelectThreads / 32];
-  const int tid = threadIdx.x;
-  const int R = B * L;
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
-  for (int b = tid; parent && b < B; b += kSelectThreads) {
-    const int p = parent[b];
-    if ((b == 0 && p != -1) || (b > 0 && (p < 0 || p >= b))) atomicOr(&s_bad, 1);
-  }
-  const int ipt = (R + kSelectThreads - 1) / kSelectThreads;
-  const int r0 = min(R, tid * ipt), r1 = min(R, r0 + ipt);
-  int cnt = 0;
-  for (int r = r0; r < r1; ++r) {
-    const int b = r / L, i = r - b * L;
-    const int s = chain_end(fold, parent, b, i, L);
-    const int sr = s < 0 ? -1 : s * L + i;
-    if (src) src[r] = sr;
-    cnt += (sr == r);
-  }
-  // block exclusive scan of cnt
-  const int lane = tid & 31, w = tid >> 5;
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) s_warp[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int v = s_warp[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
-    }
-    s_warp[lane] = v;  // inclusive warp totals
-  }
-  __syncthreads();
-  int off = (w > 0 ? s_warp[w - 1] : 0) + incl - cnt;
-  for (int r = r0; r < r1; ++r) {
-    const int b = r / L, i = r - b * L;
-    const int s = chain_end(fold, parent, b, i, L);
-    const bool act = s >= 0 && (s * L + i) == r;
-    if (act) {
-      if (packed_idx) packed_idx[off] = r;
-      if (slot) slot[r] = off;
-      ++off;
-    } else if (slot) {
-      slot[r] = -1;
-    }
-  }
-  if (tid == kSelectThreads - 1 && n_dev) n_dev[0] = s_warp[31];
-  if (tid == 0 && s_bad && status) atomicOr(status, SPECFOLD_DEV_BAD_PARENT);
-}
-
-// ------------------------------------------------------- RMSNorm gathers --
-// Y[k] = X[idx[k]] * g / sqrt(mean(X^2) + eps), one warp per output row; the
-// row is held in registers between the reduction and the scaled store.
+// ------------------------------------------------------- RMSNorm of a row --
+// Loads the gains (independent of the packed list) into registers.
 template <typename T, int MAXV>
-__global__ void __launch_bounds__(kRowWarps * 32)
-rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
-                    const int32_t* __restrict__ n_dev, int R, int d, const T* __restrict__ g,
-                    float eps, T* __restrict__ Y) {
+SF_DEV void load_gains(const T* g, int d, int lane, uint4 (&gw)[MAXV]) {
   using V = VecT<T>;
-  const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (k >= R) return;
   const uint4* gv = reinterpret_cast<const uint4*>(g);
   const int nv = d / V::N;
-  const int per_lane = (nv + 31) / 32;
-  // the gains do not depend on the packed list: start them first
-  uint4 gw[MAXV];
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    if (j < per_lane && lane + 32 * j < nv) gw[j] = __ldg(gv + lane + 32 * j);
-  }
-  const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
-  if (k >= n) return;
-  const int r = idx ? idx[k] : k;
-  const uint4* x = reinterpret_cast<const uint4*>(X + static_cast<size_t>(r) * d);
-  uint4* y = reinterpret_cast<uint4*>(Y + static_cast<size_t>(k) * d);
+  for (int j = 0; j < MAXV; ++j)
+    if (lane + 32 * j < nv) gw[j] = __ldg(gv + lane + 32 * j);
+}
+
+// y = x * g / sqrt(mean(x^2) + eps) for one row, one warp; the whole row is
+// loaded before the reduction and held in registers until the scaled store.
+template <typename T, int MAXV>
+SF_DEV void norm_row(const T* __restrict__ xrow, const uint4 (&gw)[MAXV], int d, float eps,
+                     T* __restrict__ yrow, int lane) {
+  using V = VecT<T>;
+  const uint4* x = reinterpret_cast<const uint4*>(xrow);
+  uint4* y = reinterpret_cast<uint4*>(yrow);
+  const int nv = d / V::N;
   uint4 v[MAXV];
   float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j) {
-    if (j < per_lane && lane + 32 * j < nv) v[j] = __ldg(x + lane + 32 * j);
-  }
+  for (int j = 0; j < MAXV; ++j)
+    if (lane + 32 * j < nv) v[j] = __ldg(x + lane + 32 * j);
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
-    if (j < per_lane && lane + 32 * j < nv) {
+    if (lane + 32 * j < nv) {
       float f[V::N];
       V::unpack(v[j], f);
 #pragma unroll
@@ -230,7 +143,7 @@ rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
     const int vi = lane + 32 * j;
-    if (j < per_lane && vi < nv) {
+    if (vi < nv) {
       float f[V::N], gf[V::N];
       V::unpack(v[j], f);
       V::unpack(gw[j], gf);
@@ -239,6 +152,132 @@ rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
       y[vi] = V::pack(f);
     }
   }
+}
+
+// --------------------------------------------- S2 + S3 resolve / pack ------
+// A row is recomputed iff fold[r] == 0, it is a root row, or its branch's
+// parent is invalid (the chain cannot continue); src follows the fold chain
+// through first parents to the recomputed row.  The packed list is the
+// exclusive scan of the recomputed flags in row order.
+//
+// Every block recomputes the whole (cheap: R flags, short chains) resolve and
+// scan in shared memory, writes its share of src / slot / packed_idx, and then
+// gathers and RMS-normalises its eight packed rows -- so resolve, scan and the
+// RMSNorm1 gather are one launch with no inter-block wait.
+constexpr int kPackThreads = kRowWarps * 32;
+
+// Branch whose row (., i) ends the fold chain that starts at (b, i), or -1
+// when, without a parent table (pack alone), a folded non-root row is simply
+// not recomputed.
+SF_DEV int chain_end(const uint8_t* fold, const int32_t* parent, int b, int i, int L) {
+  if (!parent) return (b > 0 && fold[b * L + i]) ? -1 : b;
+  int s = b;
+  while (s > 0 && fold[s * L + i]) {
+    const int p = parent[s];
+    if (p < 0 || p >= s) break;
+    s = p;
+  }
+  return s;
+}
+
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(kPackThreads)
+select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ parent, int B, int L,
+                   int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
+                   int32_t* __restrict__ src, int32_t* __restrict__ packed_idx, int32_t* __restrict__ slot,
+                   int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status) {
+  extern __shared__ int smem_i[];
+  __shared__ int s_warp[kPackThreads / 32];
+  __shared__ int s_bad;
+  const int R = B * L;
+  int* s_src = smem_i;          // [R] source row (-1: not recomputed, no source)
+  int* s_slot = smem_i + R;     // [R] packed slot or -1
+  int* s_inv = smem_i + 2 * R;  // [R] row of packed slot k
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  uint4 gw[MAXV];
+  if (X1) load_gains<T, MAXV>(g1, d, lane, gw);
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int b = tid; parent && b < B; b += kPackThreads) {
+      const int p = parent[b];
+      if ((b == 0 && p != -1) || (b > 0 && (p < 0 || p >= b))) atomicOr(&s_bad, 1);
+    }
+  const int ipt = (R + kPackThreads - 1) / kPackThreads;
+  const int r0 = min(R, tid * ipt), r1 = min(R, r0 + ipt);
+  int cnt = 0;
+  for (int r = r0; r < r1; ++r) {
+    const int b = r / L, i = r - b * L;
+    const int sb = chain_end(fold, parent, b, i, L);
+    const int sr = sb < 0 ? -1 : sb * L + i;
+    s_src[r] = sr;
+    cnt += (sr == r);
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s_warp[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int v = lane < kPackThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane < kPackThreads / 32) s_warp[lane] = v;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int n = s_warp[kPackThreads / 32 - 1];
+  int off = (w > 0 ? s_warp[w - 1] : 0) + incl - cnt;
+  for (int r = r0; r < r1; ++r) {
+    if (s_src[r] == r) {
+      s_slot[r] = off;
+      s_inv[off] = r;
+      ++off;
+    } else {
+      s_slot[r] = -1;
+    }
+  }
+  __syncthreads();
+  // this block's share of the global outputs
+  const int chunk = (R + gridDim.x - 1) / gridDim.x;
+  const int c0 = min(R, static_cast<int>(blockIdx.x) * chunk), c1 = min(R, c0 + chunk);
+  for (int r = c0 + tid; r < c1; r += kPackThreads) {
+    if (src) src[r] = s_src[r];
+    if (slot) slot[r] = s_slot[r];
+    if (packed_idx && s_slot[r] >= 0) packed_idx[s_slot[r]] = r;
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    if (n_dev) n_dev[0] = n;
+    if (s_bad && status) atomicOr(status, SPECFOLD_DEV_BAD_PARENT);
+  }
+  // RMSNorm1 gather of this block's packed rows
+  if (X1) {
+    const int k = blockIdx.x * kRowWarps + w;
+    if (k < n) norm_row<T, MAXV>(H + static_cast<size_t>(s_inv[k]) * d, gw, d, eps, X1 + static_cast<size_t>(k) * d, lane);
+  }
+}
+
+// ------------------------------------------------------- RMSNorm rows --
+// Y[k] = X[idx ? idx[k] : k] * g / sqrt(mean(X^2) + eps) for k < n.
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(kRowWarps * 32)
+rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ n_dev, int R, int d, const T* __restrict__ g,
+                    float eps, T* __restrict__ Y) {
+  const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (k >= R) return;
+  uint4 gw[MAXV];
+  load_gains<T, MAXV>(g, d, lane, gw);   // independent of the packed list: first
+  const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
+  if (k >= n) return;
+  const int r = idx ? idx[k] : k;
+  norm_row<T, MAXV>(X + static_cast<size_t>(r) * d, gw, d, eps, Y + static_cast<size_t>(k) * d, lane);
 }
 
 // -------------------------------------------------------------- S10 fill --
@@ -326,18 +365,58 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
   return check_launch();
 }
 
-int launch_select(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src,
-                  int32_t* packed_idx, int32_t* slot, int32_t* n_dev, uint32_t* status,
-                  cudaStream_t st) {
-  select_kernel<<<1, kSelectThreads, 0, st>>>(fold, parent, B, L, src, packed_idx, slot, n_dev,
-                                              status);
+template <typename T, int MAXV>
+static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
+                              const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
+                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st) {
+  const int R = B * L;
+  const size_t smem = static_cast<size_t>(3) * R * sizeof(int);
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(select_pack_kernel<T, MAXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             3 * SPECFOLD_MAX_ROWS * static_cast<int>(sizeof(int))) != cudaSuccess)
+      return SPECFOLD_ECUDA;
+    attr_done[dev] = 1;
+  }
+  const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
+  select_pack_kernel<T, MAXV><<<grid, block, smem, st>>>(fold, parent, B, L, d, static_cast<const T*>(H),
+                                                          static_cast<const T*>(g1), eps, src, packed_idx, slot,
+                                                          n_dev, static_cast<T*>(X1), status);
   count_launch();
   return check_launch();
 }
 
 template <typename T>
-static void rmsnorm_dispatch(const void* X, const int32_t* idx, const int32_t* n_dev, int R,
-                             int d, const void* g, float eps, void* Y, cudaStream_t st) {
+static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
+                                const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
+                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st) {
+  const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
+  if (per_lane <= 4)
+    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+  if (per_lane <= 8)
+    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+  if (per_lane <= 16)
+    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+  if (per_lane <= 32)
+    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+  return SPECFOLD_EUNSUPPORTED;
+}
+
+int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
+                       const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot, int32_t* n_dev,
+                       void* X1, uint32_t* status, cudaStream_t st) {
+  if (dtype == SPECFOLD_BF16)
+    return select_pack_dispatch<__nv_bfloat16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1,
+                                               status, st);
+  return select_pack_dispatch<float>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status,
+                                     st);
+}
+
+template <typename T>
+static void rmsnorm_dispatch(const void* X, const int32_t* idx, const int32_t* n_dev, int R, int d, const void* g,
+                             float eps, void* Y, cudaStream_t st) {
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
   const int per_lane = (d / VecT<T>::N + 31) / 32;
   const T* x = static_cast<const T*>(X);

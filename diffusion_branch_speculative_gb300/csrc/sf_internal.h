@@ -19,10 +19,11 @@ int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a l
 // gate: fold/rel per row; dtype bf16 or f32.
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
                 uint8_t* fold, float* rel, cudaStream_t st);
-// resolve + pack scan in one block; any output may be null.
-int launch_select(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src,
-                  int32_t* packed_idx, int32_t* slot, int32_t* n_dev, uint32_t* status,
-                  cudaStream_t st);
+// resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
+// given); parent may be null (pack alone); any output may be null.
+int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
+                       const void* H, const void* g1, float eps, int32_t* src, int32_t* packed_idx,
+                       int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st);
 // Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
                         int R, int d, const void* g, float eps, void* Y, cudaStream_t st);
@@ -66,7 +67,14 @@ struct GemmCall {
   uint32_t* status;
 };
 size_t gemm_partial_floats();
-int launch_gemm(const GemmCall& c, cudaStream_t st);
+// Optional RMSNorm of the finished rows of an EPI_RESID_PACKED GEMM (the
+// output projection): out[k] = Y[k] * gain / sqrt(mean(Y[k]^2) + eps).
+struct RowNorm {
+  const void* gain;
+  float eps;
+  void* out;
+};
+int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn = nullptr);
 
 // ---- tcgen05 attention (attn_tc.cu) ----
 struct AttnCall {
@@ -81,7 +89,11 @@ struct AttnCall {
   int B, L, n_q, n_kv, hd;
   void* O;                // [R, n_q*hd]
   uint32_t* status;
+  void* part;             // split-KV partials (attn_partial_bytes)
+  size_t part_bytes;
 };
+int attn_sp_max(int R, int g, int n_kv);
+size_t attn_partial_bytes(int R, int g, int n_kv, int hd);
 int launch_attention(const AttnCall& c, cudaStream_t st);
 
 // ---- TMA descriptors (api.cu) ----

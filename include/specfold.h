@@ -118,12 +118,16 @@ typedef struct {
   size_t a;            /* [R, d]        attention sublayer output, packed rows */
   size_t x2;           /* [R, d]        RMSNorm2 of a */
   size_t g;            /* [R, F]        silu(x2 Wg) * (x2 Wu) */
-  size_t gemm_scratch; /* split-K partial sums and tile counters */
+  size_t gemm_scratch; /* fp32 split-K partial sums */
+  size_t attn_scratch; /* fp32 split-KV attention partials */
   size_t total;        /* total bytes */
 } specfold_ws_layout;
 
-/* Number of stage events specfold_layer_forward records when given them. */
-#define SPECFOLD_STAGE_EVENTS 11
+/* Number of stage events specfold_layer_forward records when given them:
+ * before the gate, after the gate, after resolve + pack + RMSNorm1, after the
+ * QKV projection, after attention, after the output projection (+ RMSNorm2),
+ * after the SwiGLU GEMM, after the down projection, after the fold-fill. */
+#define SPECFOLD_STAGE_EVENTS 9
 
 /* ------------------------------------------------------------------ */
 /* S1 gate.  Explainer, Fig. 2 paragraph: r(b,i) = |H_b[i] - H_p[i]| / |H_p[i]|
@@ -202,12 +206,30 @@ int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const voi
  * (0 = folding off: the dense multi-branch verify through the same kernels).
  * Writes H_out [B, L, d]; intermediates stay in ws (specfold_workspace_layout).
  * stage_events: NULL, or SPECFOLD_STAGE_EVENTS cudaEvent_t handles recorded
- * on `stream` before each of the ten kernels and after the last. */
+ * on `stream` at the stage boundaries listed at SPECFOLD_STAGE_EVENTS. */
 int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
                            const void* H_in, const int32_t* parent, int B, int L,
                            specfold_kv_view prefK, specfold_kv_view prefV, int P, float tau,
                            void* H_out, void* ws, size_t ws_bytes,
                            void* const* stage_events, void* stream);
+
+/* CUDA graph of one specfold_layer_forward call.  The library captures the
+ * whole launch sequence once (on a private stream, thread-local capture) and
+ * replays it with a single graph launch, which removes the per-kernel host
+ * launch cost.  Every pointer, the shape, tau and the optional stage events
+ * are fixed at creation: to run on new inputs, write them into the same H_in
+ * / parent buffers before each launch.  Returns SPECFOLD_OK and sets *graph,
+ * or an error code (nothing is captured then). */
+typedef struct specfold_graph_s* specfold_graph;
+int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weights* w,
+                                const void* H_in, const int32_t* parent, int B, int L,
+                                specfold_kv_view prefK, specfold_kv_view prefV, int P, float tau,
+                                void* H_out, void* ws, size_t ws_bytes,
+                                void* const* stage_events, specfold_graph* graph);
+/* Enqueue one replay on `stream`. */
+int specfold_graph_launch(specfold_graph graph, void* stream);
+/* Release the graph (after its launches have completed). */
+int specfold_graph_destroy(specfold_graph graph);
 
 /* Plain packed GEMM through the same tcgen05 engine: Y[M, N] = X[M, K] W^T
  * with W [N, K]; Y in dims-dtype.  K % 64 == 0, N % 128 == 0. */

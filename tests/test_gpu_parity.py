@@ -209,3 +209,95 @@ def test_timeout_selftest_reports_and_context_survives():
     assert int(status.item()) & binding.DEV_TIMEOUT
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum().item()) == 8.0
+
+
+@pytest.mark.parametrize("name", ["7b_layer", "small"])
+def test_standalone_stage_calls_chain(name):
+    """S1..S10 through the per-stage entry points (gate, resolve, pack, qkv,
+    attention, out_proj, ffn) match the oracle and the fused layer call."""
+    if name == "small":
+        w = synth.small_workload(d=512, n_q=8, n_kv=2, hd=128, F=384, P=100, L=12, levels=(1, 3, 4))
+        inp = synth.make_layer_inputs(w, seed=8)
+    else:
+        inp = synth.make_layer_inputs(name, seed=2)
+    tau = 0.05
+    dev = DeviceInputs(inp)
+    d = inp.dims
+    B, L, D = inp.H.shape
+    R = B * L
+    g = d.n_q // d.n_kv
+    ws = binding.alloc_workspace(binding.workspace_size(dev.dims, B, L))
+    cw = binding.make_weights(dev.W)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    bf = dict(dtype=torch.bfloat16, device="cuda")
+    fold = torch.empty(R, dtype=torch.uint8, device="cuda")
+    src, pidx, slot = torch.empty(R, **i32), torch.empty(R, **i32), torch.empty(R, **i32)
+    n_dev = torch.empty(1, **i32)
+    X1 = torch.empty(R, D, **bf)
+    Q = torch.empty(d.n_kv, R * g, d.hd, **bf)
+    bK, bV = torch.zeros(R, d.n_kv, d.hd, **bf), torch.zeros(R, d.n_kv, d.hd, **bf)
+    O = torch.empty(R, d.n_q * d.hd, **bf)
+    A = torch.empty(R, D, **bf)
+    Hout = torch.empty_like(dev.H)
+    binding.specfold_gate(dev.H, dev.parent, tau, fold)
+    binding.specfold_resolve(fold, dev.parent, B, L, src)
+    binding.specfold_pack(fold, dev.H, dev.W["g1"], d.eps, pidx, slot, n_dev, X1)
+    binding.specfold_qkv(dev.dims, cw, X1, pidx, n_dev, B, L, Q, bK, bV, ws)
+    binding.specfold_attention(dev.dims, Q, dev.pk, dev.pv, dev.P, bK, bV, src, pidx, n_dev, B, L, O, ws)
+    binding.specfold_out_proj(dev.dims, cw, O, pidx, n_dev, dev.H, B, L, A, ws)
+    binding.specfold_ffn(dev.dims, cw, A, pidx, n_dev, dev.H, src, fold, B, L, Hout, ws)
+    torch.cuda.synchronize()
+    assert binding.specfold_get_status(ws) == 0
+    gf = fold.cpu().numpy().astype(bool)
+    res, _, n_bad = oracle_with_gpu_decisions(inp, tau, gf)
+    assert n_bad == 0
+    assert np.array_equal(src.cpu().numpy(), res["src"])
+    n = int(n_dev.item())
+    assert n == res["n"]
+    assert rel_l2(to_np(A[:n]), res["A"]) < TOL
+    assert rel_l2(to_np(Hout).reshape(R, D), res["out"]) < TOL
+    # same result as the fused layer call
+    lay, out = run_layer(dev, tau)
+    assert rel_l2(to_np(Hout), to_np(out)) < 2e-3
+
+
+def test_graph_replay_matches_eager_and_tracks_inputs():
+    inp = synth.make_layer_inputs("7b_layer", seed=6)
+    dev = DeviceInputs(inp)
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, dev.pk, dev.pv)
+    eager = lay.forward(dev.H, dev.parent, 0.05).clone()
+    H = dev.H.clone()
+    out = torch.empty_like(H)
+    g = lay.graph(H, dev.parent, 0.05, out)
+    n0 = binding.specfold_launch_count()
+    g.launch()
+    torch.cuda.synchronize()
+    assert binding.specfold_launch_count() - n0 >= 9
+    assert torch.equal(out, eager)
+    # new inputs written into the captured buffer are picked up by the replay
+    inp2 = synth.make_layer_inputs("7b_layer", seed=7)
+    H.copy_(bf16(inp2.H))
+    g.launch()
+    torch.cuda.synchronize()
+    eager2 = lay.forward(H, dev.parent, 0.05)
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager2)
+    g.close()
+
+
+def test_graph_with_stage_events():
+    inp = synth.make_layer_inputs("small" if False else "tiny", seed=1, dtype="bf16")
+    dev = DeviceInputs(inp)
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, dev.pk, dev.pv)
+    out = torch.empty_like(dev.H)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
+    for e in ev:
+        e.record()
+    g = lay.graph(dev.H, dev.parent, 0.05, out, events=ev)
+    for _ in range(3):
+        g.launch()
+        ev[-1].synchronize()
+        times = [ev[i].elapsed_time(ev[i + 1]) for i in range(binding.STAGE_EVENTS - 1)]
+        assert all(t >= 0 for t in times) and sum(times) > 0
+    g.close()
+    assert torch.equal(out, lay.forward(dev.H, dev.parent, 0.05))
