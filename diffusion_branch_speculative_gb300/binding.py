@@ -66,6 +66,7 @@ _SIG = {
     "specfold_layer_forward": (_I, [_P, _P, _P, _P, _I, _I, specfold_kv_view, specfold_kv_view, _I,
                                     ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "specfold_linear": (_I, [_I, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_linear_noalloc": (_I, [_I, _P, _P, _I, _I, _I, _P, _P]),
     "specfold_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
     "specfold_linear_workspace_size": (ctypes.c_size_t, [_I, _I]),
     "specfold_workspace_layout": (_I, [_P, _I, _I, _P]),
@@ -231,6 +232,14 @@ def specfold_linear(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor, ws: torch
     N = W.shape[0]
     _check(lib().specfold_linear(dtype_code(X.dtype), _ptr(X), _ptr(W), M, N, K, _ptr(Y), _ptr(ws), ws.numel(),
                                  _stream(stream)), "specfold_linear")
+
+
+def specfold_linear_noalloc(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor, stream=None):
+    """Y = X W^T without a workspace (the library's static device scratch)."""
+    M, K = X.shape
+    N = W.shape[0]
+    _check(lib().specfold_linear_noalloc(dtype_code(X.dtype), _ptr(X), _ptr(W), M, N, K, _ptr(Y), _stream(stream)),
+           "specfold_linear_noalloc")
 
 
 def linear_workspace_size(M: int, N: int) -> int:

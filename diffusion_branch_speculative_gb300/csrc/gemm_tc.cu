@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 namespace sf {
 namespace {
@@ -660,3 +661,100 @@ int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
 }
 
 }  // namespace sf
+
+// ===================================================================== //
+// specfold_linear_noalloc: the plain GEMM for callers that cannot allocate
+// device memory.  Its only scratch, the fp32 split-K partial tiles, lives in
+// this file-scope device array, which every GPU that loads the library keeps
+// until the process exits.  The persistent grid is capped so that the partial
+// tiles of any split fit in it.
+// ===================================================================== //
+namespace sf {
+namespace {
+
+constexpr size_t kNoAllocBytes = static_cast<size_t>(16) << 20;                  // 16 MiB
+constexpr int kNoAllocGrid = static_cast<int>(kNoAllocBytes / (kBM * 256 * 4));  // 128 CTAs
+constexpr int kNoAllocMaxRows = SPECFOLD_MAX_ROWS;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device with that
+// device current (in host code the symbol itself is only a host stand-in).
+void* noalloc_scratch_ptr() {
+  static std::mutex mu;
+  static void* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+template <int BN>
+int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* Y, cudaStream_t st) {
+  using Cf = Cfg<BN>;
+  const int grid = std::min(num_sms(), kNoAllocGrid);
+  // a split writes at most one 128 x BN fp32 tile per CTA of the capped grid
+  if (static_cast<size_t>(grid) * kBM * BN * 4 > kNoAllocBytes) return SPECFOLD_ECAPACITY;
+  void* scratch = noalloc_scratch_ptr();
+  if (!scratch) return SPECFOLD_ECUDA;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  int rc = make_map_2d(&p.mapA, X, M, K, K, kBM);
+  if (rc) return rc;
+  rc = make_map_2d(&p.mapB[0], W, N, K, K, BN / 2);
+  if (rc) return rc;
+  p.nb = 1;
+  p.K = K;
+  p.Mcap = M;
+  p.N = N;
+  p.Nt = N / BN;
+  p.n_dev = nullptr;
+  p.Y = Y;
+  p.ldy = N;
+  p.R = M;
+  p.g = 1;
+  p.partial = static_cast<float*>(scratch);  // written in full before it is read: nothing to clear
+  p.status = nullptr;
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cf::SMEM_BYTES) != cudaSuccess)
+      return SPECFOLD_ECUDA;
+    attr_done[dev] = 1;
+  }
+  gemm_kernel<BN, EPI_STORE><<<grid, kGemmThreads, Cf::SMEM_BYTES, st>>>(p);
+  count_launch();
+  if (check_launch()) return SPECFOLD_ECUDA;
+  if (grid / p.Nt >= 2 && K / kBK >= 2 * kMinKbPerSplit) {
+    const long long work = static_cast<long long>(M) * (p.Nt * BN / 8);
+    const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
+    splitk_reduce_kernel<BN, EPI_STORE><<<std::max(rgrid, 1), 256, 0, st>>>(p, grid);
+    count_launch();
+    return check_launch();
+  }
+  return SPECFOLD_OK;
+}
+
+}  // namespace
+}  // namespace sf
+
+extern "C" int specfold_linear_noalloc(int dtype, const void* X, const void* W, int M, int N, int K, void* Y,
+                                       void* stream) {
+  using namespace sf;
+  if (dtype != SPECFOLD_BF16 && dtype != SPECFOLD_F32) return SPECFOLD_EINVAL;
+  if (dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!X || !W || !Y || M <= 0 || N <= 0 || K <= 0) return SPECFOLD_EINVAL;
+  if (M > kNoAllocMaxRows) return SPECFOLD_ECAPACITY;
+  if (K % kBK || N % 128) return SPECFOLD_EUNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W) | reinterpret_cast<uintptr_t>(Y)) & 15u)
+    return SPECFOLD_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return N % 256 == 0 ? run_linear_noalloc<256>(X, W, M, N, K, Y, st) : run_linear_noalloc<128>(X, W, M, N, K, Y, st);
+}

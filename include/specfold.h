@@ -236,6 +236,27 @@ int specfold_graph_destroy(specfold_graph graph);
 int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* The plain GEMM of specfold_linear for callers that cannot allocate device
+ * memory: a plain C caller that holds only its inputs and outputs and has no
+ * allocator, or code running where cudaMalloc is not allowed (inside a CUDA
+ * stream capture, or a runtime that forbids allocation after warm-up).  The
+ * SpecFold pages have no counterpart; this is a library convenience.
+ * Y[M, N] = X[M, K] W^T exactly as specfold_linear computes it, with no
+ * workspace argument: the split-K scratch is a 16 MiB static device array
+ * inside the library, held by every GPU that loads it until the process
+ * exits.  Limits: M <= SPECFOLD_MAX_ROWS (larger M: SPECFOLD_ECAPACITY);
+ * K % 64 == 0 and N % 128 == 0 (SPECFOLD_EUNSUPPORTED); at most 128 CTAs, so
+ * it can be slower than specfold_linear on large problems.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the one array: calls that overlap on the GPU (other
+ * streams, or other host threads) race and must be serialised by the caller.
+ * The scratch is fully rewritten before it is read, so a call needs nothing
+ * cleared from the previous one.  A bounded wait that runs out cannot be
+ * reported (there is no status word). */
+int specfold_linear_noalloc(int dtype, const void* X, const void* W, int M, int N, int K, void* Y,
+                            void* stream);
+
 /* Workspace bytes for a layer of this shape and B*L rows (host only, no GPU
  * needed).  0 if the shape is invalid. */
 size_t specfold_workspace_size(const specfold_dims* dims, int B, int L);
