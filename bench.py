@@ -226,12 +226,19 @@ def run_ours(args, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    def timed_steps(tau, steps, warmup):
-        """K graph replays of the layer, each bracketed by event-record nodes
-        inside the graph (first and last node), L2 flushed before each."""
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
-        for e in ev:  # torch creates the CUDA event at its first record
-            e.record(stream)
+    def timed_steps(tau, steps, warmup, stage_events=False):
+        """K replays of the layer's CUDA graph, L2 flushed before each.
+
+        Without stage events the step is bracketed by events recorded on the
+        stream around the graph launch (the flush ahead of it keeps the GPU
+        busy while the host submits).  With stage events the graph itself
+        carries event-record nodes at every stage boundary, for the per-stage
+        breakdown."""
+        ev = None
+        if stage_events:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
+            for e in ev:  # torch creates the CUDA event at its first record
+                e.record(stream)
         graph = lay.graph(H, parent, tau, Hout, events=ev)
         for _ in range(warmup):
             flush()
@@ -243,27 +250,38 @@ def run_ours(args, rank, world):
         t0 = time.time()
         ms = []
         st_sum = [0.0] * (binding.STAGE_EVENTS - 1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
         for i in range(steps):
             flush()
-            graph.launch()
-            ev[-1].synchronize()
-            ms.append(ev[0].elapsed_time(ev[-1]))
-            for si in range(binding.STAGE_EVENTS - 1):
-                st_sum[si] += ev[si].elapsed_time(ev[si + 1])
+            if stage_events:
+                graph.launch()
+                ev[-1].synchronize()
+                ms.append(ev[0].elapsed_time(ev[-1]))
+                for si in range(binding.STAGE_EVENTS - 1):
+                    st_sum[si] += ev[si].elapsed_time(ev[si + 1])
+            else:
+                a.record(stream)
+                graph.launch()
+                b.record(stream)
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
         torch.cuda.synchronize()
         barrier()
         t1 = time.time()
         launches = binding.specfold_launch_count() - l0
         graph.close()
-        stages = {nm: st_sum[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)}
+        stages = {nm: st_sum[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)} if stage_events else None
         return sum(ms), ms, launches, stages, (t0, t1)
 
     # headline: tau from the command line, stage events on
     sampler = ClockSampler(dev_index)
     sampler.start()
     time.sleep(0.3)
-    total_ms, ms, launches, stages, (t0, t1) = timed_steps(args.tau, args.steps, args.warmup)
+    total_ms, ms, launches, _, (t0, t1) = timed_steps(args.tau, args.steps, args.warmup)
     clocks = sampler.stop(t0, t1)
+    # per-stage breakdown (graph with event-record nodes at stage boundaries)
+    _, _, _, stages, _ = timed_steps(args.tau, max(50, min(args.steps, 500)), 5, stage_events=True)
     assert lay.status() == 0, "device status set"
     n = lay.n_packed()
     total_ms_max = total_ms
@@ -332,8 +350,9 @@ def run_ours(args, rank, world):
     sweep = []
     if not args.no_sweep:
         for tau in ([0.0] + list(w.taus)):
-            tot, _, _, st, _ = timed_steps(tau, max(50, min(args.steps, 300)), 5)
             steps_s = max(50, min(args.steps, 300))
+            tot, _, _, _, _ = timed_steps(tau, steps_s, 5)
+            _, _, _, st, _ = timed_steps(tau, steps_s, 5, stage_events=True)
             nn = lay.n_packed()
             sweep.append({"tau": tau, "n_packed": nn, "rho": round(nn / R, 4),
                           "us_per_step": round(tot / steps_s * 1e3, 2),

@@ -4,10 +4,12 @@
 // caller's stream; nothing here allocates device memory.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
 
+#include "sf_device.cuh"
 #include "sf_internal.h"
 
 namespace sf {
@@ -26,6 +28,14 @@ int num_sms() {
     cached[dev] = v > 0 ? v : 1;
   }
   return cached[dev];
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("SPECFOLD_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? SPECFOLD_OK : SPECFOLD_ECUDA; }

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   volatile int* okflag = abort_flag + 1;  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.y;
   const int m0 = blockIdx.x * 128;
   const int g = p.g, L = p.L;
@@ -430,6 +432,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 // O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p, int tiles_x) {
+  pdl_wait();
+  pdl_trigger();
   const int n = min(max(p.n_dev[0], 0), p.R);
   const int rows_total = n * p.g;
   const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms);
@@ -444,22 +448,37 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     const int h = static_cast<int>(rest / rows_total);
     const int row = m & 127;
     const size_t pb = (static_cast<size_t>(h) * tiles_x + (m >> 7)) * p.sp_max;
+    // every load of the row is issued before any arithmetic
+    float mz[16], lz[16];
+    float4 oa[16], ob[16];
+#pragma unroll
+    for (int z = 0; z < 16; ++z) {
+      if (z < SP) {
+        const float* ml = p.part_ml + ((pb + z) * 128 + row) * 2;
+        mz[z] = __ldcg(ml);
+        lz[z] = __ldcg(ml + 1);
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + ((pb + z) * 128 + row) * HD + dg * 8);
+        oa[z] = __ldcg(src);
+        ob[z] = __ldcg(src + 1);
+      }
+    }
     float M = -INFINITY;
-    for (int z = 0; z < SP; ++z) M = fmaxf(M, __ldcg(p.part_ml + ((pb + z) * 128 + row) * 2));
+#pragma unroll
+    for (int z = 0; z < 16; ++z)
+      if (z < SP) M = fmaxf(M, mz[z]);
     float l = 0.f, acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int z = 0; z < SP; ++z) {
-      const float mz = __ldcg(p.part_ml + ((pb + z) * 128 + row) * 2);
-      if (mz == -INFINITY) continue;
-      const float wz = ex2(mz - M);
-      l = fmaf(__ldcg(p.part_ml + ((pb + z) * 128 + row) * 2 + 1), wz, l);
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + ((pb + z) * 128 + row) * HD + dg * 8);
-      const float4 a = __ldcg(src), b = __ldcg(src + 1);
-      acc[0] = fmaf(a.x, wz, acc[0]); acc[1] = fmaf(a.y, wz, acc[1]);
-      acc[2] = fmaf(a.z, wz, acc[2]); acc[3] = fmaf(a.w, wz, acc[3]);
-      acc[4] = fmaf(b.x, wz, acc[4]); acc[5] = fmaf(b.y, wz, acc[5]);
-      acc[6] = fmaf(b.z, wz, acc[6]); acc[7] = fmaf(b.w, wz, acc[7]);
+#pragma unroll
+    for (int z = 0; z < 16; ++z) {
+      if (z < SP && mz[z] != -INFINITY) {
+        const float wz = ex2(mz[z] - M);
+        l = fmaf(lz[z], wz, l);
+        acc[0] = fmaf(oa[z].x, wz, acc[0]); acc[1] = fmaf(oa[z].y, wz, acc[1]);
+        acc[2] = fmaf(oa[z].z, wz, acc[2]); acc[3] = fmaf(oa[z].w, wz, acc[3]);
+        acc[4] = fmaf(ob[z].x, wz, acc[4]); acc[5] = fmaf(ob[z].y, wz, acc[5]);
+        acc[6] = fmaf(ob[z].z, wz, acc[6]); acc[7] = fmaf(ob[z].w, wz, acc[7]);
+      }
     }
     const float inv = 1.f / l;
     const int k = m / p.g, hg = m - k * p.g;
@@ -517,13 +536,13 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
     attr_done[dev] = 1;
   }
   const dim3 grid(tiles_x, c.n_kv, p.sp_max);
-  attn_kernel<HD><<<grid, kAttnThreads, C::SMEM_BYTES, st>>>(p);
+  launch_k(attn_kernel<HD>, dim3(grid), dim3(kAttnThreads), C::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
   if (p.sp_max > 1) {
     const long long work = static_cast<long long>(R) * g * c.n_kv * (HD / 8);
     const int cg = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
-    attn_combine_kernel<HD><<<std::max(cg, 1), 256, 0, st>>>(p, tiles_x);
+    launch_k(attn_combine_kernel<HD>, dim3(std::max(cg, 1)), dim3(256), 0, st, p, tiles_x);
     count_launch();
     return check_launch();
   }

@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   float* epi_stage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
@@ -408,6 +410,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 // unsplit (S recomputed from the same n and grid).
 template <int BN, int EPI>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
+  pdl_wait();
+  pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int Mt = (n + kBM - 1) / kBM;
   const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
@@ -468,6 +472,8 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
                                                              const __nv_bfloat16* __restrict__ g2, float eps,
                                                              __nv_bfloat16* __restrict__ X2) {
   __shared__ float s_red[8];
+  pdl_wait();
+  pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int k = blockIdx.x;
   if (k >= n) return;
@@ -587,7 +593,7 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
     attr_done[dev] = 1;
   }
   const int grid = min(num_sms(), kMaxGrid);
-  gemm_kernel<BN, EPI><<<grid, kGemmThreads, Cf::SMEM_BYTES, st>>>(p);
+  launch_k(gemm_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
   if constexpr (EPI == EPI_RESID_PACKED) {
@@ -598,11 +604,11 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
       const __nv_bfloat16* g2 = static_cast<const __nv_bfloat16*>(rn->gain);
       __nv_bfloat16* x2 = static_cast<__nv_bfloat16*>(rn->out);
       if (groups <= 256)
-        outproj_finish_kernel<BN, 1><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+        launch_k(outproj_finish_kernel<BN, 1>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       else if (groups <= 512)
-        outproj_finish_kernel<BN, 2><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+        launch_k(outproj_finish_kernel<BN, 2>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       else
-        outproj_finish_kernel<BN, 4><<<g, b, 0, st>>>(p, grid, g2, rn->eps, x2);
+        launch_k(outproj_finish_kernel<BN, 4>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       count_launch();
       return check_launch();
     }
@@ -612,7 +618,7 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
-    splitk_reduce_kernel<BN, EPI><<<std::max(rgrid, 1), 256, 0, st>>>(p, grid);
+    launch_k(splitk_reduce_kernel<BN, EPI>, dim3(std::max(rgrid, 1)), dim3(256), 0, st, p, grid);
     count_launch();
     return check_launch();
   }
@@ -729,13 +735,13 @@ int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* 
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
-  gemm_kernel<BN, EPI_STORE><<<grid, kGemmThreads, Cf::SMEM_BYTES, st>>>(p);
+  launch_k(gemm_kernel<BN, EPI_STORE>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
   if (grid / p.Nt >= 2 && K / kBK >= 2 * kMinKbPerSplit) {
     const long long work = static_cast<long long>(M) * (p.Nt * BN / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
-    splitk_reduce_kernel<BN, EPI_STORE><<<std::max(rgrid, 1), 256, 0, st>>>(p, grid);
+    launch_k(splitk_reduce_kernel<BN, EPI_STORE>, dim3(std::max(rgrid, 1)), dim3(256), 0, st, p, grid);
     count_launch();
     return check_launch();
   }

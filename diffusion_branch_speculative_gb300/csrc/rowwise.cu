@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d,
             float tau, uint8_t* __restrict__ fold, float* __restrict__ rel) {
   using V = VecT<T>;
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * L) return;
@@ -195,7 +197,9 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
   int* s_inv = smem_i + 2 * R;  // [R] row of packed slot k
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   uint4 gw[MAXV];
-  if (X1) load_gains<T, MAXV>(g1, d, lane, gw);
+  if (X1) load_gains<T, MAXV>(g1, d, lane, gw);   // weights: independent of earlier kernels
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) s_bad = 0;
   __syncthreads();
   if (blockIdx.x == 0)
@@ -271,9 +275,11 @@ rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
                     float eps, T* __restrict__ Y) {
   const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (k >= R) return;
   uint4 gw[MAXV];
-  load_gains<T, MAXV>(g, d, lane, gw);   // independent of the packed list: first
+  if (k < R) load_gains<T, MAXV>(g, d, lane, gw);   // weights: independent of earlier kernels
+  pdl_wait();
+  pdl_trigger();
+  if (k >= R) return;
   const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
   if (k >= n) return;
   const int r = idx ? idx[k] : k;
@@ -286,6 +292,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ src,
                  const T* __restrict__ Hin, T* __restrict__ Hout, int R, int d) {
   using V = VecT<T>;
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= R || !fold[r]) return;
@@ -351,15 +359,15 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
   if (dtype == SPECFOLD_BF16) {
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
     if (per_lane <= 8)
-      gate_kernel<__nv_bfloat16, 8><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+      launch_k(gate_kernel<__nv_bfloat16, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel);
     else
-      gate_kernel<__nv_bfloat16, 16><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+      launch_k(gate_kernel<__nv_bfloat16, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel);
   } else {
     const float* h = static_cast<const float*>(H);
     if (per_lane <= 8)
-      gate_kernel<float, 8><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+      launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel);
     else
-      gate_kernel<float, 16><<<grid, block, 0, st>>>(h, parent, B, L, d, tau, fold, rel);
+      launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel);
   }
   count_launch();
   return check_launch();
@@ -381,7 +389,7 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
     attr_done[dev] = 1;
   }
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
-  select_pack_kernel<T, MAXV><<<grid, block, smem, st>>>(fold, parent, B, L, d, static_cast<const T*>(H),
+  launch_k(select_pack_kernel<T, MAXV>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
                                                           n_dev, static_cast<T*>(X1), status);
   count_launch();
@@ -423,13 +431,13 @@ static void rmsnorm_dispatch(const void* X, const int32_t* idx, const int32_t* n
   const T* gg = static_cast<const T*>(g);
   T* y = static_cast<T*>(Y);
   if (per_lane <= 4)
-    rmsnorm_rows_kernel<T, 4><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+    launch_k(rmsnorm_rows_kernel<T, 4>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
   else if (per_lane <= 8)
-    rmsnorm_rows_kernel<T, 8><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+    launch_k(rmsnorm_rows_kernel<T, 8>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
   else if (per_lane <= 16)
-    rmsnorm_rows_kernel<T, 16><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+    launch_k(rmsnorm_rows_kernel<T, 16>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
   else
-    rmsnorm_rows_kernel<T, 32><<<grid, block, 0, st>>>(x, idx, n_dev, R, d, gg, eps, y);
+    launch_k(rmsnorm_rows_kernel<T, 32>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
 }
 
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
@@ -448,11 +456,11 @@ int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const v
                      void* H_out, int R, int d, cudaStream_t st) {
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
   if (dtype == SPECFOLD_BF16)
-    fold_fill_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
+    launch_k(fold_fill_kernel<__nv_bfloat16>, dim3(grid), dim3(block), 0, st, 
         fold, src, static_cast<const __nv_bfloat16*>(H_in), static_cast<__nv_bfloat16*>(H_out), R,
         d);
   else
-    fold_fill_kernel<float><<<grid, block, 0, st>>>(fold, src, static_cast<const float*>(H_in),
+    launch_k(fold_fill_kernel<float>, dim3(grid), dim3(block), 0, st, fold, src, static_cast<const float*>(H_in),
                                                     static_cast<float*>(H_out), R, d);
   count_launch();
   return check_launch();

@@ -73,6 +73,13 @@ SF_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32
   }
 }
 
+// Programmatic dependent launch: every kernel of the library waits for the
+// grids it depends on before touching their outputs (griddepcontrol.wait is a
+// no-op when the launch carried no programmatic dependency), then lets the
+// next kernel in the stream start launching.
+SF_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+SF_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 SF_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -219,5 +226,25 @@ SF_DEV uint32_t pack_bf16x2(float lo, float hi) {
 }
 SF_DEV float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 SF_DEV float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Host: launch with programmatic stream serialisation, so the kernel's
+// launch and prologue overlap the previous kernel in the stream (disabled by
+// SPECFOLD_PDL=0 in the environment).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace sf
