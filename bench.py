@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stress", action="store_true", help="skip the stress-workload recompute-fraction sweep")
     return ap.parse_args()
 
 
@@ -226,7 +227,7 @@ def run_ours(args, rank, world):
             import torch.distributed as dist
             dist.barrier()
 
-    def timed_steps(tau, steps, warmup, stage_events=False):
+    def timed_steps(tau, steps, warmup, stage_events=False, only=None):
         """K replays of the layer's CUDA graph, L2 flushed before each.
 
         Without stage events the step is bracketed by events recorded on the
@@ -239,6 +240,8 @@ def run_ours(args, rank, world):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
             for e in ev:  # torch creates the CUDA event at its first record
                 e.record(stream)
+        if only is not None:  # just the boundaries around one stage
+            ev = [e if i in (only, only + 1) else None for i, e in enumerate(ev)]
         graph = lay.graph(H, parent, tau, Hout, events=ev)
         for _ in range(warmup):
             flush()
@@ -254,7 +257,11 @@ def run_ours(args, rank, world):
         b = torch.cuda.Event(enable_timing=True)
         for i in range(steps):
             flush()
-            if stage_events:
+            if stage_events and only is not None:
+                graph.launch()
+                ev[only + 1].synchronize()
+                st_sum[only] += ev[only].elapsed_time(ev[only + 1])
+            elif stage_events:
                 graph.launch()
                 ev[-1].synchronize()
                 ms.append(ev[0].elapsed_time(ev[-1]))
@@ -272,6 +279,8 @@ def run_ours(args, rank, world):
         launches = binding.specfold_launch_count() - l0
         graph.close()
         stages = {nm: st_sum[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)} if stage_events else None
+        if only is not None:
+            stages = {binding.STAGE_NAMES[only]: st_sum[only] / steps * 1e3}
         return sum(ms), ms, launches, stages, (t0, t1)
 
     # headline: tau from the command line, stage events on
@@ -299,8 +308,13 @@ def run_ours(args, rank, world):
     if rf is None:
         top = max(gemm_stages, key=lambda s: stages[s])
         rf = stage_roofline(top, d, n, R, stages[top], peaks)
+    # re-time that stage with event nodes only at its two boundaries (each
+    # event node in a graph costs microseconds of its own)
+    only = binding.STAGE_NAMES.index(top)
+    _, _, _, st_top, _ = timed_steps(args.tau, max(50, min(args.steps, 500)), 5, stage_events=True, only=only)
+    rf = stage_roofline(top, d, n, R, st_top[top], peaks)
     rf["kernel"] = f"gemm_kernel ({top})"
-    rf["us_per_launch"] = round(stages[top], 2)
+    rf["us_per_launch"] = round(st_top[top], 2)
     rf["peak_src"] = f"{peaks['src']} ({'MEASURED_PEAKS.json burst' if peaks['src'] == 'measured' else 'recipe fallback'})"
     rf["traffic"] = committed_traffic(f"gemm_{top}", args.workload)
     rf["stage_share"] = round(stages[top] / sum(stages.values()), 3)
@@ -361,11 +375,68 @@ def run_ours(args, rank, world):
         dense = next(s for s in sweep if s["tau"] == 0.0)["us_per_step"]
         for s in sweep:
             s["time_vs_dense"] = round(s["us_per_step"] / dense, 4)
+    stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
     return {
+        "stress_sweep": stress,
         "value": value, "ms_per_step": total_ms_max / args.steps, "n_packed": n, "R": R, "w": w,
         "stages": stages, "roofline": rf, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "sweep": sweep, "inp": inp,
     }
+
+
+def stress_sweep(args, flush, barrier):
+    """µs per verify step against the recompute fraction on the stress
+    workload (prefix 8192, 64 branches): forced fractions of non-root rows
+    above tau = 0.05, and tau = 0 (dense multi-branch verify) for reference."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+    w = synth.WORKLOADS["stress"]
+    base = synth.make_layer_inputs(w, seed=args.seed, forced_frac=0.0)
+    d = base.dims
+    B, L, D = base.H.shape
+    dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
+    W = {k: to(v) for k, v in base.weights.items()}
+    cache = to(base.prefix.cache)
+    o, P = base.prefix.offset, base.prefix.P
+    lay = binding.FoldedLayer(dims, W, B, L, cache[o:o + P, 0], cache[o:o + P, 1])
+    H = torch.empty(B, L, D, dtype=torch.bfloat16, device="cuda")
+    parent = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(H)
+    stream = torch.cuda.current_stream()
+    steps = max(20, min(args.steps, 100))
+    rows = []
+    for frac, tau in [(0.0, 0.0)] + [(f, 0.05) for f in w.forced_fracs]:
+        br = synth.make_branches(w, np.random.default_rng(args.seed + 17), forced_frac=frac)
+        H.copy_(to(br.H))
+        parent.copy_(torch.from_numpy(br.graph.parent.astype(np.int32)))
+        g = lay.graph(H, parent, tau, out)
+        for _ in range(3):
+            flush()
+            g.launch()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(steps):
+            flush()
+            a.record(stream)
+            g.launch()
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        g.close()
+        nn = lay.n_packed()
+        rows.append({"forced_frac": frac if tau > 0 else None, "tau": tau, "n_packed": nn,
+                     "rho": round(nn / (B * L), 4), "us_per_step": round(tot / steps * 1e3, 2),
+                     "tokens_per_s": round(B * L * steps / (tot * 1e-3), 1)})
+    dense = rows[0]["us_per_step"]
+    for r in rows:
+        r["time_vs_dense"] = round(r["us_per_step"] / dense, 4)
+    del lay, W, cache
+    torch.cuda.empty_cache()
+    return rows
 
 
 # -------------------------------------------------------- oracle on CPU ----
@@ -450,6 +521,7 @@ def main():
             "clocks": r["clocks"],
             "stages_us": {k: round(v, 2) for k, v in r["stages"].items()},
             "sweep": r["sweep"],
+            "stress_sweep": r["stress_sweep"],
         }
         print(json.dumps(line))
     if world > 1:

@@ -272,9 +272,11 @@ class LayerGraph:
         B, L, _ = H_in.shape
         ev = None
         if events is not None:
-            handles = [e.cuda_event for e in events]
-            if len(handles) != STAGE_EVENTS or not all(handles):
-                raise ValueError("need SPECFOLD_STAGE_EVENTS recorded-once events")
+            if len(events) != STAGE_EVENTS:
+                raise ValueError("need SPECFOLD_STAGE_EVENTS entries (None skips a boundary)")
+            handles = [None if e is None else e.cuda_event for e in events]
+            if not all(h for e, h in zip(events, handles) if e is not None):
+                raise ValueError("stage events must exist already (torch creates them at their first record())")
             ev = (ctypes.c_void_p * STAGE_EVENTS)(*handles)
         self._keep = (dims, weights, H_in, parent, prefK, prefV, H_out, ws, events, ev)
         h = ctypes.c_void_p()

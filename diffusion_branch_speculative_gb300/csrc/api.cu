@@ -2,6 +2,7 @@
 // workspace layout, TMA descriptor encoding and the stage-by-stage launch
 // sequence of specfold_layer_forward.  Everything is asynchronous on the
 // caller's stream; nothing here allocates device memory.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -28,6 +29,15 @@ int num_sms() {
     cached[dev] = v > 0 ? v : 1;
   }
   return cached[dev];
+}
+
+// SPECFOLD_L2PF=0 in the environment turns the layer's L2 weight prefetch off.
+static bool l2pf_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("SPECFOLD_L2PF");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 bool pdl_enabled() {
@@ -137,6 +147,9 @@ static int check_view(const specfold_kv_view& v, int P) {
     if (_rc) return _rc;       \
   } while (0)
 
+// Bytes of the SwiGLU weights (gate + up) pulled into L2 during attention.
+static constexpr size_t kPrefetchFfnBytes = static_cast<size_t>(64) << 20;
+
 // ------------------------------------------------------ workspace layout --
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -201,6 +214,7 @@ static void fill_scratch(GemmCall& c, const Scratch& s, uint32_t* status) {
 // Stage events: recorded as graph event nodes while the stream is being
 // captured (a plain record would become a capture-internal dependency).
 static void record_stage_event(void* ev, cudaStream_t st) {
+  if (!ev) return;  // entries may be NULL: only the given boundaries are recorded
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   cudaStreamIsCapturing(st, &cs);
   if (cs == cudaStreamCaptureStatusActive)
@@ -241,7 +255,7 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
                            const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
                            const int32_t* n_dev, int B, int L, void* O, uint32_t* status, void* part,
-                           size_t part_bytes, cudaStream_t st) {
+                           size_t part_bytes, cudaStream_t st, const L2Prefetch* prefetch = nullptr) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
   a.Q = Q;
@@ -262,6 +276,7 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
   a.status = status;
   a.part = part;
   a.part_bytes = part_bytes;
+  if (prefetch) a.prefetch = *prefetch;
   return launch_attention(a, st);
 }
 
@@ -498,8 +513,20 @@ int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
   auto mark = [&](int i) {
     if (stage_events) record_stage_event(stage_events[i], st);
   };
+  // L2 prefetch plan: the attention projections are pulled in while the
+  // (latency-bound) gate and pack run, the head of the SwiGLU weights while
+  // attention runs.  The layer still reads every weight byte from HBM once.
+  const size_t e = esize(dims->dtype);
+  const size_t d_ = dims->d_model;
+  const size_t nq = static_cast<size_t>(dims->n_q_heads) * dims->head_dim;
+  const size_t nkv = static_cast<size_t>(dims->n_kv_heads) * dims->head_dim;
+  const size_t ffn_head = std::min(static_cast<size_t>(dims->ffn_dim) * d_ * e, kPrefetchFfnBytes / 2);
+  L2Prefetch pf_gate = {{w->w_q, w->w_k, w->w_v, w->w_o},
+                        {nq * d_ * e, nkv * d_ * e, nkv * d_ * e, d_ * nq * e}};
+  L2Prefetch pf_attn = {{w->w_gate, w->w_up, nullptr, nullptr}, {ffn_head, ffn_head, 0, 0}};
   mark(0);
-  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st));
+  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
+                     l2pf_enabled() ? &pf_gate : nullptr));
   mark(1);
   SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
                             at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st));
@@ -509,7 +536,8 @@ int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
   mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
-                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st,
+                         l2pf_enabled() ? &pf_attn : nullptr));
   mark(4);
   SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
                         at<void>(ws, lo.x2)));

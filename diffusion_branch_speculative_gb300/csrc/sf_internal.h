@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "specfold.h"
+#include "sf_device.cuh"
 
 namespace sf {
 
@@ -18,7 +19,7 @@ int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a l
 // ---- row-wise kernels (rowwise.cu) ----
 // gate: fold/rel per row; dtype bf16 or f32.
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
-                uint8_t* fold, float* rel, cudaStream_t st);
+                uint8_t* fold, float* rel, cudaStream_t st, const struct L2Prefetch* prefetch = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
 // given); parent may be null (pack alone); any output may be null.
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
@@ -91,6 +92,7 @@ struct AttnCall {
   uint32_t* status;
   void* part;             // split-KV partials (attn_partial_bytes)
   size_t part_bytes;
+  L2Prefetch prefetch;    // optional: weights to pull into L2 meanwhile
 };
 int attn_sp_max(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);

@@ -206,7 +206,8 @@ int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const voi
  * (0 = folding off: the dense multi-branch verify through the same kernels).
  * Writes H_out [B, L, d]; intermediates stay in ws (specfold_workspace_layout).
  * stage_events: NULL, or SPECFOLD_STAGE_EVENTS cudaEvent_t handles recorded
- * on `stream` at the stage boundaries listed at SPECFOLD_STAGE_EVENTS. */
+ * on `stream` at the stage boundaries listed at SPECFOLD_STAGE_EVENTS; a NULL
+ * entry skips that boundary. */
 int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
                            const void* H_in, const int32_t* parent, int B, int L,
                            specfold_kv_view prefK, specfold_kv_view prefV, int P, float tau,
