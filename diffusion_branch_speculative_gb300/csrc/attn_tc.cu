@@ -9,10 +9,10 @@
 //   * then the L block keys of every branch present in the tile, gathered
 //     through the provenance table (key j of branch b is row src[b*L + j] of
 //     the block K/V), with scores of other branches' keys masked.
-// S = Q K^T and O_blk = P V run as tcgen05.mma into TMEM (two S and two O
-// buffers so the next S overlaps the softmax); four softmax warps own one
-// query row per thread, keep the running max/sum and the output accumulator
-// in registers, and write P (bf16) to shared memory for the P V product.
+// S = Q K^T and O += P V run as tcgen05.mma into TMEM (two S buffers so the
+// next S overlaps the softmax, one O accumulator); four softmax warps own one
+// query row per thread, keep the running max and sum, rescale O in TMEM when
+// the reference max moves, and write P (bf16) to shared memory.
 //
 // Roles (256 threads): warps 0-2 load (TMA for prefix and Q, gathers for
 // block keys), warp 3 allocates TMEM and issues MMAs, warps 4-7 softmax
@@ -95,8 +95,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint64_t* s_full = bars + 5;    // [2]
   uint64_t* s_free = bars + 7;    // [2]
   uint64_t* p_full = bars + 9;
-  uint64_t* o_full = bars + 10;   // [2]
-  uint64_t* o_free = bars + 12;   // [2]
+  uint64_t* o_full = bars + 10;   // one completion per P V product
   uint64_t* drain = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -143,10 +142,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&kv_empty[i]), 1);
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 128);
-      mbar_init(smem_u32(&o_full[i]), 1);
-      mbar_init(smem_u32(&o_free[i]), 128);
+
     }
     mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(o_full), 1);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -231,6 +230,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax --
+    // One query row per thread.  S is read from TMEM once per key block; the
+    // output accumulates in TMEM (P V with accumulate) against a reference
+    // max m_ref that is raised -- and O rescaled in place -- only when a row's
+    // max grows by more than 2^8, so the probabilities stay below 2^8.
     const int qw = warp & 3;
     const int row = qw * 32 + lane;
     const int m = m0 + row;
@@ -239,10 +242,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const int hg = m - (m / g) * g;
     const int my_b = valid ? p.packed_idx[k] / L : -2;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    float o[HD];
-#pragma unroll
-    for (int e = 0; e < HD; ++e) o[e] = 0.f;
-    float m_run = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    const uint32_t to = tmem + lane_off + C::COL_O;
+    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < NT && ok; ++t) {
       const int j = jb + t;
@@ -279,50 +280,59 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           km[c] = mk;
         }
       }
-      // pass 1: row max of the visible scores
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(ts + c * 32, sv[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(ts + c * 32, r);
-        tmem_ld_wait(r);
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          mx = fmaxf(mx, ((km[c] >> e) & 1u) ? __uint_as_float(r[e]) : -INFINITY);
+          mx = fmaxf(mx, ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
+      const float m_new = fmaxf(m_ref, mx * p.sl2);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_ref == -INFINITY) {
+        m_ref = m_new;               // nothing accumulated yet (every earlier p was 0)
+      } else if (m_new > m_ref + 8.f) {
+        alpha = ex2(m_ref - m_new);
+        m_ref = m_new;
+        rescale = true;
       }
-      const float m_new = fmaxf(m_run, mx * p.sl2);
-      // fold the previous block's P V into the accumulator (also frees P)
+      l *= alpha;
       if (t >= 1) {
-        const int ob = (t - 1) & 1;
-        if (!mbar_wait(smem_u32(&o_full[ob]), ((t - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        // P V of the previous block must be done: it frees the P tile, and O
+        // may only be rescaled once it holds that block's contribution
+        if (!mbar_wait(smem_u32(&o_full[0]), (t - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         __syncwarp();
         tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
-          tmem_ld_wait(r);
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(to + c * 32, r);
+            tmem_ld_wait(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(to + c * 32, r);
+          }
+          tmem_st_wait();
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&o_free[ob]));
       }
-      const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m_run - m_new);
-      l *= alpha;
-      // pass 2: probabilities -> bf16 P tile (K-major, 128-byte swizzle)
+      // probabilities -> bf16 P tile (K-major, 128-byte swizzle)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(ts + c * 32, r);
-        tmem_ld_wait(r);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float pv[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const float x = ex2(fmaf(__uint_as_float(r[e + u]), p.sl2, -m_new));
+            const float x = ex2(fmaf(__uint_as_float(sv[c][e + u]), p.sl2, -m_ref));
             pv[u] = ((km[c] >> (e + u)) & 1u) ? x : 0.f;
             l += pv[u];
           }
@@ -336,42 +346,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&s_free[sb]));
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(p_full));
-      m_run = m_new;
-      alpha_prev = alpha;
     }
-    if (ok) {
-      const int ob = (NT - 1) & 1;
-      if (mbar_wait(smem_u32(&o_full[ob]), ((NT - 1) >> 1) & 1, abort_flag, p.status)) {
-        __syncwarp();
-        tc_fence_after();
+    if (ok && mbar_wait(smem_u32(&o_full[0]), (NT - 1) & 1, abort_flag, p.status)) {
+      __syncwarp();
+      tc_fence_after();
+      if (SP > 1) {
+        float* po = p.part_o + (pslot * 128 + row) * HD;
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + C::COL_O + ob * HD + c * 32, r);
+          tmem_ld32(to + c * 32, r);
           tmem_ld_wait(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha_prev, __uint_as_float(r[e]));
+          for (int q4 = 0; q4 < 8; ++q4)
+            reinterpret_cast<float4*>(po + c * 32)[q4] =
+                make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                            __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
         }
-        if (SP > 1) {
-          float* po = p.part_o + (pslot * 128 + row) * HD;
+        p.part_ml[(pslot * 128 + row) * 2] = m_ref;
+        p.part_ml[(pslot * 128 + row) * 2 + 1] = l;
+      } else {
+        const float inv = 1.f / l;
+        uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
+                                              static_cast<size_t>(h * g + hg) * HD);
 #pragma unroll
-          for (int q4 = 0; q4 < HD / 4; ++q4)
-            reinterpret_cast<float4*>(po)[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-          p.part_ml[(pslot * 128 + row) * 2] = m_run;
-          p.part_ml[(pslot * 128 + row) * 2 + 1] = l;
-        } else if (valid) {
-          const float inv = 1.f / l;
-          uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
-                                                static_cast<size_t>(h * g + hg) * HD);
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(to + c * 32, r);
+          tmem_ld_wait(r);
+          if (valid) {
 #pragma unroll
-          for (int q8 = 0; q8 < HD / 8; ++q8)
-            dst[q8] = make_uint4(pack_bf16x2(o[8 * q8] * inv, o[8 * q8 + 1] * inv),
-                                 pack_bf16x2(o[8 * q8 + 2] * inv, o[8 * q8 + 3] * inv),
-                                 pack_bf16x2(o[8 * q8 + 4] * inv, o[8 * q8 + 5] * inv),
-                                 pack_bf16x2(o[8 * q8 + 6] * inv, o[8 * q8 + 7] * inv));
+            for (int q8 = 0; q8 < 4; ++q8)
+              dst[c * 4 + q8] = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * q8]) * inv, __uint_as_float(r[8 * q8 + 1]) * inv),
+                  pack_bf16x2(__uint_as_float(r[8 * q8 + 2]) * inv, __uint_as_float(r[8 * q8 + 3]) * inv),
+                  pack_bf16x2(__uint_as_float(r[8 * q8 + 4]) * inv, __uint_as_float(r[8 * q8 + 5]) * inv),
+                  pack_bf16x2(__uint_as_float(r[8 * q8 + 6]) * inv, __uint_as_float(r[8 * q8 + 7]) * inv));
+          }
         }
       }
     }
@@ -385,17 +398,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint32_t aP = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {  // i: local block index
         if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
-        const int ob = i & 1;
-        if (!mbar_wait(smem_u32(&o_free[ob]), ((i >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (i & 1) + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16(tmem + C::COL_O + ob * HD,
-                     sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, kk > 0 ? 1u : 0u);
+          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&o_full[ob]));
+        tc_commit(smem_u32(&o_full[0]));
         tc_commit(smem_u32(&kv_empty[i & 1]));
         return true;
       };

@@ -165,6 +165,22 @@ SF_DEV void epi_elem(const GemmParams& p, int k, int c, float x, float u) {
   }
 }
 
+// EPI_QKV element with the destination row r = row_idx[k] already known.
+SF_DEV void epi_qkv_elem(const GemmParams& p, int k, int r, int c, float x) {
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+  const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+  if (c < nq) {
+    const int head = c / p.hd, j = c - head * p.hd;
+    const int hk = head / p.g, hg = head - hk * p.g;
+    Y[((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j] = __float2bfloat16_rn(x);
+  } else {
+    const bool is_k = c < nq + nkv;
+    const int cc = is_k ? c - nq : c - nq - nkv;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
+    dst[static_cast<size_t>(r) * nkv + cc] = __float2bfloat16_rn(x);
+  }
+}
+
 struct Unit {
   int m, s, nt, kb0, kb1, tile;
 };
@@ -342,6 +358,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       float* stg = epi_stage + q * (32 * 33);
       const int row0 = w.m * kBM + q * 32;          // first packed row of this warp
       const int rows_here = min(32, n - row0);      // valid rows (may be <= 0)
+      // lane j holds the row index of the warp's row j (broadcast by shuffle)
+      int ridx = 0;
+      if constexpr (EPI == EPI_QKV || EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER)
+        if (S == 1 && lane < rows_here) ridx = p.row_idx[row0 + lane];
       float* prow = p.partial + (static_cast<size_t>(w.tile) * S + w.s) * kBM * BN + static_cast<size_t>(q * 32) * BN;
       constexpr int NCH = EPI == EPI_SWIGLU ? BN / 64 : BN / 32;
       for (int ch = 0; ch < NCH; ++ch) {
@@ -366,14 +386,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         __syncwarp();
         if (S == 1) {
           const int cbase = EPI == EPI_SWIGLU ? w.nt * (BN / 2) + ch * 32 : w.nt * BN + ch * 32;
+          const int c = cbase + lane;
+          __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+          const __nv_bfloat16* Rz = static_cast<const __nv_bfloat16*>(p.resid);
+          if constexpr (EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
+            // all 32 residual loads of the chunk are in flight before any store
+            float rv[32];
 #pragma unroll
-          for (int rr = 0; rr < 32; ++rr) {
-            if (rr < rows_here) {
-              const float x = stg[rr * 33 + lane];
-              if constexpr (EPI == EPI_SWIGLU)
-                epi_elem<EPI>(p, row0 + rr, cbase + lane, gt[rr], x);
-              else
-                epi_elem<EPI>(p, row0 + rr, cbase + lane, x, 0.f);
+            for (int rr = 0; rr < 32; ++rr) {
+              const int rres = EPI == EPI_RESID_PACKED ? __shfl_sync(0xffffffffu, ridx, rr) : row0 + rr;
+              rv[rr] = rr < rows_here ? __bfloat162float(Rz[static_cast<size_t>(rres) * p.ldr + c]) : 0.f;
+            }
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+              const int rdst = EPI == EPI_RESID_PACKED ? row0 + rr : __shfl_sync(0xffffffffu, ridx, rr);
+              if (rr < rows_here)
+                Y[static_cast<size_t>(rdst) * p.ldy + c] = __float2bfloat16_rn(stg[rr * 33 + lane] + rv[rr]);
+            }
+          } else if constexpr (EPI == EPI_QKV) {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+              const int r = __shfl_sync(0xffffffffu, ridx, rr);
+              if (rr < rows_here) epi_qkv_elem(p, row0 + rr, r, c, stg[rr * 33 + lane]);
+            }
+          } else {
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+              if (rr < rows_here) {
+                const float x = stg[rr * 33 + lane];
+                if constexpr (EPI == EPI_SWIGLU)
+                  epi_elem<EPI>(p, row0 + rr, c, gt[rr], x);
+                else
+                  epi_elem<EPI>(p, row0 + rr, c, x, 0.f);
+              }
             }
           }
         } else {
