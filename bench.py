@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stress", action="store_true", help="skip the stress-workload recompute-fraction sweep")
+    ap.add_argument("--no-budget", action="store_true", help="skip the draft-budget sweep")
     return ap.parse_args()
 
 
@@ -375,13 +376,71 @@ def run_ours(args, rank, world):
         dense = next(s for s in sweep if s["tau"] == 0.0)["us_per_step"]
         for s in sweep:
             s["time_vs_dense"] = round(s["us_per_step"] / dense, 4)
+    budget = [] if (args.no_budget or args.workload != "7b_layer") else budget_sweep(args, lay.dims, W, pk, pv, flush,
+                                                                                       barrier)
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
     return {
+        "budget_sweep": budget,
         "stress_sweep": stress,
         "value": value, "ms_per_step": total_ms_max / args.steps, "n_packed": n, "R": R, "w": w,
         "stages": stages, "roofline": rf, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
         "sweep": sweep, "inp": inp,
     }
+
+
+# Draft graphs of growing budget for the 7B-like layer (level sizes; node 0 is
+# the main branch).
+BUDGET_LEVELS = {4: ((1, 1, 2), None), 8: ((1, 2, 3, 2), None), 16: ((1, 4, 11), 4),
+                 32: ((1, 4, 6, 6, 6, 5, 4), None), 64: ((1, 8, 55), 8)}
+
+
+def budget_sweep(args, dims, W, pk, pv, flush, barrier):
+    """µs per verify step against the draft budget B (the explainer's Fig. 3
+    question): the same 7B-like layer (prefix 512, L 32) over B branches,
+    dense (tau = 0, every branch fully recomputed) and folded (tau = 0.05)."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+    base = synth.WORKLOADS["7b_layer"]
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    steps = max(20, min(args.steps, 200))
+    rows = []
+    for B, (levels, fanout) in BUDGET_LEVELS.items():
+        w = synth.Workload(f"7b_budget{B}", base.dims, P=base.P, L=base.L, levels=levels, max_fanout=fanout,
+                           second_parent=True, reveals=base.reveals, ripple_len=base.ripple_len, taus=(0.05,),
+                           dtype="bf16")
+        br = synth.make_branches(w, np.random.default_rng(args.seed + B))
+        H = to(br.H)
+        parent = torch.from_numpy(br.graph.parent.astype(np.int32)).cuda()
+        out = torch.empty_like(H)
+        lay = binding.FoldedLayer(dims, W, B, base.L, pk, pv)
+        row = {"B": B}
+        for tau, key in ((0.0, "dense"), (0.05, "folded")):
+            g = lay.graph(H, parent, tau, out)
+            for _ in range(3):
+                flush()
+                g.launch()
+            torch.cuda.synchronize()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for _ in range(steps):
+                flush()
+                a.record(stream)
+                g.launch()
+                b.record(stream)
+                b.synchronize()
+                tot += a.elapsed_time(b)
+            g.close()
+            row[f"{key}_us"] = round(tot / steps * 1e3, 2)
+            if key == "folded":
+                row["n_packed"] = lay.n_packed()
+                row["rho"] = round(row["n_packed"] / (B * base.L), 4)
+        row["folded_vs_dense"] = round(row["folded_us"] / row["dense_us"], 4)
+        rows.append(row)
+        del lay
+    return rows
 
 
 def stress_sweep(args, flush, barrier):
@@ -522,6 +581,7 @@ def main():
             "stages_us": {k: round(v, 2) for k, v in r["stages"].items()},
             "sweep": r["sweep"],
             "stress_sweep": r["stress_sweep"],
+            "budget_sweep": r["budget_sweep"],
         }
         print(json.dumps(line))
     if world > 1:

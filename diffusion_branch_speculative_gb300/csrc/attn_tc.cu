@@ -492,6 +492,9 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
         acc[6] = fmaf(ob[z].z, wz, acc[6]); acc[7] = fmaf(ob[z].w, wz, acc[7]);
       }
     }
+    // four consecutive threads consumed one 128-byte line of every split's o
+    __syncwarp(__activemask());
+    for (int z = dg & 3; z < SP; z += 4) l2_discard_line(p.part_o + ((pb + z) * 128 + row) * HD + (dg & ~3) * 8);
     const float inv = 1.f / l;
     const int k = m / p.g, hg = m - k * p.g;
     uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +

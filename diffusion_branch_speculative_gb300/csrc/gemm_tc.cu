@@ -503,6 +503,16 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
         }
       }
     }
+    // four consecutive threads consumed one 128-byte line of every split
+    // (each lane of the quad drops every fourth split's line)
+    __syncwarp(__activemask());
+    {
+      const float* line = base - (threadIdx.x & 3) * 8;
+      for (int s = threadIdx.x & 3; s < S; s += 4) {
+        l2_discard_line(line + static_cast<size_t>(s) * kBM * BN);
+        if constexpr (EPI == EPI_SWIGLU) l2_discard_line(line + static_cast<size_t>(s) * kBM * BN + BN / 2);
+      }
+    }
     epi_chunk<EPI, 8>(p, k, nt * TW + tc, v, u);
   }
 }

@@ -104,6 +104,14 @@ SF_DEV void issue_l2_prefetch(const L2Prefetch& pf, int lane) {
 SF_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 SF_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Drop a consumed 128-byte scratch line from L2 without writing it back (the
+// next call rewrites the scratch before reading it).  Dead split-K and
+// split-KV partials would otherwise be written back to HBM while a later,
+// bandwidth-bound kernel of the layer runs.
+SF_DEV void l2_discard_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 SF_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
