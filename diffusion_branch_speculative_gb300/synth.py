@@ -333,3 +333,88 @@ def small_workload(d=256, n_q=4, n_kv=2, hd=64, F=512, P=64, L=16, levels=(1, 2,
     return Workload(name, LayerDims(d=d, n_q=n_q, n_kv=n_kv, hd=hd, F=F), P=P, L=L,
                     levels=tuple(levels), max_fanout=max_fanout, second_parent=second_parent,
                     reveals=tuple(reveals), ripple_len=ripple_len, taus=(0.05,), dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# stacks of layers
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class StackInputs:
+    """Inputs of an n-layer stack: the branch states entering layer 0 and,
+    per layer, its own weights and prefix cache.  The draft deltas are drawn
+    at layer 0 only; deeper layers see whatever the stack propagates."""
+    workload: Workload
+    dims: LayerDims
+    branches: BranchInputs
+    weights: List[dict]
+    prefixes: List[PrefixCache]
+    dtype: str
+
+    @property
+    def H(self) -> np.ndarray:
+        return self.branches.H
+
+    @property
+    def parent(self) -> np.ndarray:
+        return self.branches.graph.parent
+
+    @property
+    def n_layers(self) -> int:
+        return len(self.weights)
+
+    def layer(self, l: int) -> LayerInputs:
+        """Layer l's weights and prefix with the layer-0 branch states."""
+        return LayerInputs(workload=self.workload, dims=self.dims, branches=self.branches,
+                           weights=self.weights[l], prefix=self.prefixes[l], dtype=self.dtype)
+
+
+def make_stack_inputs(name_or_workload, seed: int = 0, n_layers: Optional[int] = None,
+                      dtype: Optional[str] = None, P: Optional[int] = None, **branch_kw) -> StackInputs:
+    """A seeded stack: branches, then (weights, prefix) of layer 0, 1, ... from
+    one numpy generator, so a one-layer stack draws exactly the inputs of
+    make_layer_inputs with the same seed."""
+    w = WORKLOADS[name_or_workload] if isinstance(name_or_workload, str) else name_or_workload
+    dtype = dtype or w.dtype
+    n_layers = w.n_layers if n_layers is None else int(n_layers)
+    if n_layers < 1:
+        raise ValueError("a stack needs at least one layer")
+    rng = np.random.default_rng(seed)
+    br = make_branches(w, rng, dtype=dtype, **branch_kw)
+    weights, prefixes = [], []
+    for _ in range(n_layers):
+        weights.append(make_weights(w.dims, rng, dtype=dtype))
+        prefixes.append(make_prefix(w.dims, w.P if P is None else P, rng, dtype=dtype))
+    return StackInputs(workload=w, dims=w.dims, branches=br, weights=weights, prefixes=prefixes, dtype=dtype)
+
+
+def torch_stack_params(dims: LayerDims, n_layers: int, P: int, seed: int, device="cuda"):
+    """Per-layer bf16 weights and fused prefix caches drawn with torch's own
+    seeded generator on ``device`` (same distributions as make_weights /
+    make_prefix, nn.Linear layout).  Used where a full-size stack is only timed
+    or compared with itself: drawing 28 layers of 7B-class weights with numpy
+    takes minutes.  Returns (list of weight dicts, list of caches
+    [P + offset + slack, 2, n_kv, hd])."""
+    import torch  # local: the numpy generators above do not need torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    d, hq, hkv, F = dims.d, dims.n_q * dims.hd, dims.n_kv * dims.hd, dims.F
+
+    def lin(o, i):
+        t = torch.randn((o, i), generator=gen, device=device, dtype=torch.float32)
+        return t.mul_(WEIGHT_STD).to(torch.bfloat16)
+
+    ws, caches = [], []
+    T = P + PREFIX_OFFSET + PREFIX_SLACK
+    s = WEIGHT_STD * math.sqrt(d)
+    for _ in range(n_layers):
+        ws.append({
+            "g1": torch.ones(d, device=device, dtype=torch.bfloat16),
+            "w_q": lin(hq, d), "w_k": lin(hkv, d), "w_v": lin(hkv, d), "w_o": lin(d, hq),
+            "g2": torch.ones(d, device=device, dtype=torch.bfloat16),
+            "w_gate": lin(F, d), "w_up": lin(F, d), "w_down": lin(d, F),
+        })
+        c = torch.randn((T, 2, dims.n_kv, dims.hd), generator=gen, device=device, dtype=torch.float32)
+        caches.append(c.mul_(s).to(torch.bfloat16))
+    return ws, caches

@@ -338,3 +338,38 @@ def near_tau_rows(rel: np.ndarray, tau: float, frac: float = 1e-4) -> np.ndarray
     m = np.abs(r - tau) <= frac * tau
     m[0, :] = False
     return m
+
+
+# ---------------------------------------------------------------------------
+# stack of layers (SpecFold explainer page, "mechanism" paragraph: automatic
+# release; appendix D: how the recompute fraction evolves with depth)
+# ---------------------------------------------------------------------------
+
+def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None) -> dict:
+    """A stack of folded layers: layer l's output is layer l+1's input.
+
+    ``layers`` is a sequence of (W, prefK, prefV), one per layer.  Each layer
+    runs the gate again on its own input (the reading of "automatic release":
+    a row folded at layer l is recomputed at layer l+1 once its difference to
+    the parent's layer-(l+1) input is no longer below tau).  ``store``, when
+    given, is applied to each layer's output before the next layer reads it
+    (the storage precision of the hidden states between layers); without it
+    the stack runs in float64 throughout.
+
+    Returns the input of every layer ("inputs", [n_layers] arrays [B, L, d]),
+    the final output "out", and per layer the gate decisions "fold", the
+    relative differences "rel" and the packed-row count "n".
+    """
+    X = np.asarray(H, F64)
+    B, L, d = X.shape
+    inputs, folds, rels, ns = [], [], [], []
+    for (W, pk, pv) in layers:
+        inputs.append(X)
+        res = layer_forward(X, parent, W, pk, pv, tau, eps, n_kv, hd)
+        folds.append(res["fold"])
+        rels.append(res["rel"])
+        ns.append(int(res["n"]))
+        X = res["out"].reshape(B, L, d)
+        if store is not None:
+            X = np.asarray(store(X), F64)
+    return {"inputs": inputs, "out": X, "fold": folds, "rel": rels, "n": ns}
