@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stress", action="store_true", help="skip the stress-workload recompute-fraction sweep")
     ap.add_argument("--no-budget", action="store_true", help="skip the draft-budget sweep")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer stack tau sweep")
     return ap.parse_args()
 
 
@@ -379,7 +380,11 @@ def run_ours(args, rank, world):
     budget = [] if (args.no_budget or args.workload != "7b_layer") else budget_sweep(args, lay.dims, W, pk, pv, flush,
                                                                                        barrier)
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
+    del lay
+    torch.cuda.empty_cache()
+    stack = [] if args.no_stack else stack_sweep(args, flush, barrier)
     return {
+        "stack_sweep": stack,
         "budget_sweep": budget,
         "stress_sweep": stress,
         "value": value, "ms_per_step": total_ms_max / args.steps, "n_packed": n, "R": R, "w": w,
@@ -498,6 +503,63 @@ def stress_sweep(args, flush, barrier):
     return rows
 
 
+def stack_sweep(args, flush, barrier):
+    """The 28-layer 7B-like stack (prefix 2048, 16 branches in a fanout-4
+    tree): one verify step runs every layer, each re-gating on its own input.
+    Per tau: µs per step, branch-tokens/s per layer and the recompute fraction
+    of every layer (the explainer's appendix D question).  Weights are drawn
+    on the device by torch's seeded generator (28 x 466 MB)."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+    w = synth.WORKLOADS["7b_stack"]
+    d = w.dims
+    dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+    weights, caches = synth.torch_stack_params(d, w.n_layers, w.P, seed=args.seed + 101)
+    o = synth.PREFIX_OFFSET
+    pk = [c[o:o + w.P, 0] for c in caches]
+    pv = [c[o:o + w.P, 1] for c in caches]
+    br = synth.make_branches(w, np.random.default_rng(args.seed + 29))
+    H = torch.from_numpy(np.ascontiguousarray(br.H, np.float32)).cuda().to(torch.bfloat16)
+    parent = torch.from_numpy(br.graph.parent.astype(np.int32)).cuda()
+    out = torch.empty_like(H)
+    stack = binding.FoldedStack(dims, weights, w.B, w.L, pk, pv)
+    stream = torch.cuda.current_stream()
+    steps = max(10, min(args.steps, 30))
+    R = w.B * w.L
+    rows = []
+    for tau in w.taus:
+        g = stack.graph(H, parent, tau, out)
+        for _ in range(3):
+            flush()
+            g.launch()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(steps):
+            flush()
+            a.record(stream)
+            g.launch()
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        g.close()
+        ns = stack.n_packed.cpu().tolist()
+        us = tot / steps * 1e3
+        rows.append({"tau": tau, "us_per_step": round(us, 1), "us_per_layer": round(us / w.n_layers, 2),
+                     "tokens_per_s_per_layer": round(R * w.n_layers / (us * 1e-6), 1),
+                     "rho_mean": round(sum(ns) / (R * w.n_layers), 4),
+                     "rho_per_layer": [round(n / R, 4) for n in ns]})
+    assert stack.status() == 0, "device status set"
+    dense = rows[0]["us_per_step"] if rows and rows[0]["tau"] == 0.0 else None
+    for r in rows:
+        r["time_vs_dense"] = round(r["us_per_step"] / dense, 4) if dense else None
+    del stack, weights, caches
+    torch.cuda.empty_cache()
+    return rows
+
+
 # -------------------------------------------------------- oracle on CPU ----
 def oracle_sample(inp, tau, rows_per_step, steps, budget_s=None):
     """Time the CPU oracle producing `rows_per_step` output rows per step."""
@@ -582,6 +644,7 @@ def main():
             "sweep": r["sweep"],
             "stress_sweep": r["stress_sweep"],
             "budget_sweep": r["budget_sweep"],
+            "stack_sweep": r["stack_sweep"],
         }
         print(json.dumps(line))
     if world > 1:

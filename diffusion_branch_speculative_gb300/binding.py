@@ -52,6 +52,10 @@ class specfold_ws_layout(ctypes.Structure):
                  "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "attn_scratch", "total")]
 
 
+class specfold_stack_trace(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_void_p), ("fold", ctypes.c_void_p), ("n_packed", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIG = {
@@ -77,6 +81,11 @@ _SIG = {
     "specfold_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
     "specfold_layer_graph_create": (_I, [_P, _P, _P, _P, _I, _I, specfold_kv_view, specfold_kv_view, _I,
                                          ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
+    "specfold_stack_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
+    "specfold_stack_forward": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P, _P, _P,
+                                    ctypes.c_size_t, _P]),
+    "specfold_stack_graph_create": (_I, [_P, _I, _P, _P, _P, _I, _I, _P, _P, _I, ctypes.c_float, _P, _P, _P,
+                                         ctypes.c_size_t, _P]),
     "specfold_graph_launch": (_I, [_P, _P]),
     "specfold_graph_destroy": (_I, [_P]),
 }
@@ -227,6 +236,41 @@ def specfold_layer_forward(dims, weights, H_in, parent, prefK, prefV, P, tau, H_
                                         ws.numel(), ev, _stream(stream)), "specfold_layer_forward")
 
 
+def stack_workspace_size(dims: specfold_dims, B: int, L: int) -> int:
+    return int(lib().specfold_stack_workspace_size(ctypes.byref(dims), B, L))
+
+
+def _stack_args(weights: Sequence[specfold_weights], prefK: Sequence, prefV: Sequence):
+    n = len(weights)
+    if len(prefK) != n or len(prefV) != n:
+        raise ValueError("one weight set and one prefix view per layer")
+    W = (specfold_weights * n)(*weights)
+    K = (specfold_kv_view * n)(*[kv_view(t) for t in prefK])
+    V = (specfold_kv_view * n)(*[kv_view(t) for t in prefV])
+    return n, W, K, V
+
+
+def _trace_arg(hidden=None, fold=None, n_packed=None):
+    if hidden is None and fold is None and n_packed is None:
+        return None
+    return specfold_stack_trace(None if hidden is None else hidden.data_ptr(),
+                                None if fold is None else fold.data_ptr(),
+                                None if n_packed is None else n_packed.data_ptr())
+
+
+def specfold_stack_forward(dims, weights: Sequence[specfold_weights], H_in, parent, prefK: Sequence,
+                           prefV: Sequence, P, tau, H_out, ws, hidden=None, fold=None, n_packed=None, stream=None):
+    """weights / prefK / prefV: one entry per layer (specfold_weights structs,
+    [P, n_kv, hd] views or None).  hidden / fold / n_packed: optional
+    per-layer records (see specfold_stack_trace)."""
+    B, L, _ = H_in.shape
+    n, W, K, V = _stack_args(weights, prefK, prefV)
+    tr = _trace_arg(hidden, fold, n_packed)
+    _check(lib().specfold_stack_forward(ctypes.byref(dims), n, W, _ptr(H_in), _ptr(parent), B, L, K, V, P,
+                                        float(tau), _ptr(H_out), None if tr is None else ctypes.byref(tr), _ptr(ws),
+                                        ws.numel(), _stream(stream)), "specfold_stack_forward")
+
+
 def specfold_linear(X: torch.Tensor, W: torch.Tensor, Y: torch.Tensor, ws: torch.Tensor, stream=None):
     M, K = X.shape
     N = W.shape[0]
@@ -262,10 +306,31 @@ def specfold_selftest_timeout(status: torch.Tensor, wait_ns: int, stream=None):
     _check(lib().specfold_selftest_timeout(_ptr(status), int(wait_ns), _stream(stream)), "specfold_selftest_timeout")
 
 
-class LayerGraph:
-    """A captured specfold_layer_forward call (specfold_layer_graph_create):
-    launch() replays all of its kernels with one graph launch.  Inputs are read
-    from, and outputs written to, the buffers given at capture."""
+class _Graph:
+    """A captured call: launch() replays all of its kernels with one graph
+    launch.  Inputs are read from, and outputs written to, the buffers given
+    at capture."""
+
+    _h = None
+
+    def launch(self, stream=None):
+        _check(lib().specfold_graph_launch(self._h, _stream(stream)), "specfold_graph_launch")
+
+    def close(self):
+        if self._h:
+            torch.cuda.synchronize()
+            lib().specfold_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class LayerGraph(_Graph):
+    """A captured specfold_layer_forward call (specfold_layer_graph_create)."""
 
     def __init__(self, dims, weights, H_in, parent, prefK, prefV, P, tau, H_out, ws,
                  events: Optional[Sequence] = None):
@@ -287,20 +352,23 @@ class LayerGraph:
                "specfold_layer_graph_create")
         self._h = h
 
-    def launch(self, stream=None):
-        _check(lib().specfold_graph_launch(self._h, _stream(stream)), "specfold_graph_launch")
 
-    def close(self):
-        if self._h:
-            torch.cuda.synchronize()
-            lib().specfold_graph_destroy(self._h)
-            self._h = None
+class StackGraph(_Graph):
+    """A captured specfold_stack_forward call (specfold_stack_graph_create)."""
 
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
+    def __init__(self, dims, weights: Sequence[specfold_weights], H_in, parent, prefK: Sequence, prefV: Sequence,
+                 P, tau, H_out, ws, hidden=None, fold=None, n_packed=None):
+        B, L, _ = H_in.shape
+        n, W, K, V = _stack_args(weights, prefK, prefV)
+        tr = _trace_arg(hidden, fold, n_packed)
+        self._keep = (dims, weights, H_in, parent, prefK, prefV, H_out, ws, hidden, fold, n_packed)
+        h = ctypes.c_void_p()
+        torch.cuda.synchronize()
+        _check(lib().specfold_stack_graph_create(ctypes.byref(dims), n, W, _ptr(H_in), _ptr(parent), B, L, K, V, P,
+                                                 float(tau), _ptr(H_out), None if tr is None else ctypes.byref(tr),
+                                                 _ptr(ws), ws.numel(), ctypes.byref(h)),
+               "specfold_stack_graph_create")
+        self._h = h
 
 
 # ------------------------------------------------------------ convenience --
@@ -352,6 +420,62 @@ class FoldedLayer:
 
     def n_packed(self) -> int:
         return int(self.view("n_packed", torch.int32)[0].item())
+
+    def status(self) -> int:
+        return specfold_get_status(self.ws)
+
+
+class FoldedStack:
+    """A stack of folded layers: per-layer device weights and prefix views
+    plus one workspace.  forward(H_in, parent, tau) runs every layer through
+    specfold_stack_forward; with ``record=True`` the per-layer input states,
+    decisions and packed counts are kept (self.hidden / self.fold /
+    self.n_packed)."""
+
+    def __init__(self, dims: specfold_dims, weights: Sequence[dict], B: int, L: int,
+                 prefK: Sequence = None, prefV: Sequence = None, device="cuda"):
+        self.dims = dims
+        self.w = list(weights)
+        self.cw = [make_weights(w) for w in self.w]
+        self.n_layers = len(self.w)
+        self.B, self.L = B, L
+        self.prefK = list(prefK) if prefK is not None else [None] * self.n_layers
+        self.prefV = list(prefV) if prefV is not None else [None] * self.n_layers
+        Ps = {0 if k is None else k.shape[0] for k in self.prefK}
+        if len(Ps) != 1:
+            raise ValueError("every layer's prefix has the same length")
+        self.P = Ps.pop()
+        self.lo = workspace_layout(dims, B, L)
+        self.ws = alloc_workspace(stack_workspace_size(dims, B, L), device)
+        R = B * L
+        self.fold = torch.zeros((self.n_layers, B, L), dtype=torch.uint8, device=device)
+        self.n_packed = torch.zeros(self.n_layers, dtype=torch.int32, device=device)
+        self.hidden = None
+        self._device = device
+
+    def _hidden(self, H_in):
+        if self.hidden is None or self.hidden.dtype != H_in.dtype:
+            self.hidden = torch.empty((max(self.n_layers - 1, 1),) + tuple(H_in.shape), dtype=H_in.dtype,
+                                      device=self._device)
+        return self.hidden
+
+    def forward(self, H_in, parent, tau, H_out=None, record=False, stream=None):
+        if H_out is None:
+            H_out = torch.empty_like(H_in)
+        hidden = self._hidden(H_in) if (record and self.n_layers > 1) else None
+        specfold_stack_forward(self.dims, self.cw, H_in, parent, self.prefK, self.prefV, self.P, tau, H_out,
+                               self.ws, hidden=hidden, fold=self.fold, n_packed=self.n_packed, stream=stream)
+        return H_out
+
+    def graph(self, H_in, parent, tau, H_out, record=False) -> StackGraph:
+        """Capture forward(H_in, parent, tau, H_out) as one replayable graph."""
+        hidden = self._hidden(H_in) if (record and self.n_layers > 1) else None
+        return StackGraph(self.dims, self.cw, H_in, parent, self.prefK, self.prefV, self.P, tau, H_out, self.ws,
+                          hidden=hidden, fold=self.fold, n_packed=self.n_packed)
+
+    def layer_inputs(self, H_in) -> list:
+        """Inputs of layers 0..n-1 of the last recorded forward."""
+        return [H_in] + ([self.hidden[l] for l in range(self.n_layers - 1)] if self.n_layers > 1 else [])
 
     def status(self) -> int:
         return specfold_get_status(self.ws)

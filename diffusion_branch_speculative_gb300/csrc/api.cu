@@ -356,6 +356,76 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   return SPECFOLD_OK;
 }
 
+// Host-side checks of one layer call (everything but the workspace size).
+static int check_layer_call(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                            const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV,
+                            int P, float tau, const void* H_out, const void* ws) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  SF_TRY(check_weights(w));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!H_in || !parent || !H_out || !ws || P < 0) return SPECFOLD_EINVAL;
+  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
+  SF_TRY(check_view(prefK, P));
+  SF_TRY(check_view(prefV, P));
+  if (!a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
+  return SPECFOLD_OK;
+}
+
+// A stack's workspace: one layer workspace, then the [B, L, d] state buffer.
+static size_t stack_ws_bytes(const specfold_dims* d, int B, int L, const specfold_ws_layout& lo) {
+  return lo.total + up256(static_cast<size_t>(B) * L * d->d_model * esize(d->dtype));
+}
+
+// S1..S10 of one layer on `st` (arguments already checked).  fold_hist and
+// n_hist, when given, receive copies of the layer's decisions and n.
+static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                         const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV, int P,
+                         float tau, void* H_out, void* ws, const specfold_ws_layout& lo,
+                         void* const* stage_events, uint8_t* fold_hist, int32_t* n_hist, cudaStream_t st) {
+  const int R = B * L;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  uint32_t* status = at<uint32_t>(ws, lo.status);
+  uint8_t* fold = at<uint8_t>(ws, lo.fold);
+  int32_t* src = at<int32_t>(ws, lo.src);
+  int32_t* pidx = at<int32_t>(ws, lo.packed_idx);
+  int32_t* n_dev = at<int32_t>(ws, lo.n_packed);
+  auto mark = [&](int i) {
+    if (stage_events) record_stage_event(stage_events[i], st);
+  };
+  // L2 prefetch plan: the attention projections are pulled in while the
+  // (latency-bound) gate and pack run, the head of the SwiGLU weights while
+  // attention runs.  The layer still reads every weight byte from HBM once.
+  const size_t e = esize(dims->dtype);
+  const size_t d_ = dims->d_model;
+  const size_t nq = static_cast<size_t>(dims->n_q_heads) * dims->head_dim;
+  const size_t nkv = static_cast<size_t>(dims->n_kv_heads) * dims->head_dim;
+  const size_t ffn_head = std::min(static_cast<size_t>(dims->ffn_dim) * d_ * e, kPrefetchFfnBytes / 2);
+  L2Prefetch pf_gate = {{w->w_q, w->w_k, w->w_v, w->w_o},
+                        {nq * d_ * e, nkv * d_ * e, nkv * d_ * e, d_ * nq * e}};
+  L2Prefetch pf_attn = {{w->w_gate, w->w_up, nullptr, nullptr}, {ffn_head, ffn_head, 0, 0}};
+  mark(0);
+  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
+                     l2pf_enabled() ? &pf_gate : nullptr, fold_hist));
+  mark(1);
+  SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
+                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist));
+  mark(2);
+  SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
+                   at<void>(ws, lo.block_v), s, status, st));
+  mark(3);
+  SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
+                         at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st,
+                         l2pf_enabled() ? &pf_attn : nullptr));
+  mark(4);
+  SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
+                        at<void>(ws, lo.x2)));
+  mark(5);
+  return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true);
+}
+
 }  // namespace sf
 
 using namespace sf;
@@ -490,60 +560,67 @@ int specfold_layer_forward(const specfold_dims* dims, const specfold_weights* w,
                            const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV, int P,
                            float tau, void* H_out, void* ws, size_t ws_bytes, void* const* stage_events,
                            void* stream) {
-  SF_TRY(check_dims(dims));
-  SF_TRY(check_rows(B, L));
-  SF_TRY(check_weights(w));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
-  if (!H_in || !parent || !H_out || !ws || P < 0) return SPECFOLD_EINVAL;
-  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
-  SF_TRY(check_view(prefK, P));
-  SF_TRY(check_view(prefV, P));
-  if (!a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
+  SF_TRY(check_layer_call(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws));
   specfold_ws_layout lo;
   layout(dims, B, L, &lo);
   if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  return enqueue_layer(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, lo, stage_events, nullptr,
+                       nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t specfold_stack_workspace_size(const specfold_dims* dims, int B, int L) {
+  if (check_dims(dims) || check_rows(B, L)) return 0;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  return stack_ws_bytes(dims, B, L, lo);
+}
+
+int specfold_stack_forward(const specfold_dims* dims, int n_layers, const specfold_weights* w, const void* H_in,
+                           const int32_t* parent, int B, int L, const specfold_kv_view* prefK,
+                           const specfold_kv_view* prefV, int P, float tau, void* H_out,
+                           const specfold_stack_trace* trace, void* ws, size_t ws_bytes, void* stream) {
+  if (n_layers < 1 || !w || !prefK || !prefV) return SPECFOLD_EINVAL;
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  // every layer is checked before anything is launched
+  for (int l = 0; l < n_layers; ++l)
+    SF_TRY(check_layer_call(dims, &w[l], H_in, parent, B, L, prefK[l], prefV[l], P, tau, H_out, ws));
+  if (H_out == H_in) return SPECFOLD_EINVAL;
+  const specfold_stack_trace tr = trace ? *trace : specfold_stack_trace{nullptr, nullptr, nullptr};
+  if (tr.hidden && !a16(tr.hidden)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < stack_ws_bytes(dims, B, L, lo)) return SPECFOLD_ECAPACITY;
+  const size_t R = static_cast<size_t>(B) * L;
+  const size_t state_bytes = R * dims->d_model * esize(dims->dtype);
+  if (tr.hidden) {
+    // the caller's record of the states must not overlap H_in or H_out
+    const uintptr_t h0 = reinterpret_cast<uintptr_t>(tr.hidden);
+    const uintptr_t h1 = h0 + state_bytes * static_cast<size_t>(n_layers - 1);
+    for (const void* p : {H_in, static_cast<const void*>(H_out)}) {
+      const uintptr_t p0 = reinterpret_cast<uintptr_t>(p), p1 = p0 + state_bytes;
+      if (p0 < h1 && h0 < p1) return SPECFOLD_EINVAL;
+    }
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int R = B * L;
-  const Scratch s = layer_scratch(ws, dims, B, L, lo);
-  uint32_t* status = at<uint32_t>(ws, lo.status);
-  uint8_t* fold = at<uint8_t>(ws, lo.fold);
-  int32_t* src = at<int32_t>(ws, lo.src);
-  int32_t* pidx = at<int32_t>(ws, lo.packed_idx);
-  int32_t* n_dev = at<int32_t>(ws, lo.n_packed);
-  auto mark = [&](int i) {
-    if (stage_events) record_stage_event(stage_events[i], st);
-  };
-  // L2 prefetch plan: the attention projections are pulled in while the
-  // (latency-bound) gate and pack run, the head of the SwiGLU weights while
-  // attention runs.  The layer still reads every weight byte from HBM once.
-  const size_t e = esize(dims->dtype);
-  const size_t d_ = dims->d_model;
-  const size_t nq = static_cast<size_t>(dims->n_q_heads) * dims->head_dim;
-  const size_t nkv = static_cast<size_t>(dims->n_kv_heads) * dims->head_dim;
-  const size_t ffn_head = std::min(static_cast<size_t>(dims->ffn_dim) * d_ * e, kPrefetchFfnBytes / 2);
-  L2Prefetch pf_gate = {{w->w_q, w->w_k, w->w_v, w->w_o},
-                        {nq * d_ * e, nkv * d_ * e, nkv * d_ * e, d_ * nq * e}};
-  L2Prefetch pf_attn = {{w->w_gate, w->w_up, nullptr, nullptr}, {ffn_head, ffn_head, 0, 0}};
-  mark(0);
-  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
-                     l2pf_enabled() ? &pf_gate : nullptr));
-  mark(1);
-  SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
-                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st));
-  mark(2);
-  SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
-                   at<void>(ws, lo.block_v), s, status, st));
-  mark(3);
-  SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
-                         at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
-                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st,
-                         l2pf_enabled() ? &pf_attn : nullptr));
-  mark(4);
-  SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
-                        at<void>(ws, lo.x2)));
-  mark(5);
-  return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
-                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true);
+  // Layer outputs alternate between H_out and the workspace's state buffer so
+  // that the last layer writes H_out and no layer writes the state it reads.
+  uint8_t* spare = at<uint8_t>(ws, lo.total);
+  const void* x = H_in;
+  for (int l = 0; l < n_layers; ++l) {
+    void* y;
+    if (l == n_layers - 1)
+      y = H_out;
+    else if (tr.hidden)
+      y = static_cast<uint8_t*>(tr.hidden) + state_bytes * static_cast<size_t>(l);
+    else
+      y = ((n_layers - 1 - l) & 1) ? static_cast<void*>(spare) : H_out;
+    SF_TRY(enqueue_layer(dims, &w[l], x, parent, B, L, prefK[l], prefV[l], P, tau, y, ws, lo, nullptr,
+                         tr.fold ? tr.fold + R * static_cast<size_t>(l) : nullptr,
+                         tr.n_packed ? tr.n_packed + l : nullptr, st));
+    x = y;
+  }
+  return SPECFOLD_OK;
 }
 
 int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y, void* ws, size_t ws_bytes,
@@ -578,17 +655,18 @@ struct specfold_graph_s {
   uint64_t kernels;  // kernels per replay
 };
 
-int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
-                                const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV,
-                                int P, float tau, void* H_out, void* ws, size_t ws_bytes, void* const* stage_events,
-                                specfold_graph* graph) {
+}  // extern "C"
+
+// Captures enqueue(stream, capturing) into a graph: one eager call first
+// (kernel attributes are set and arguments checked outside the capture), then
+// the same call under a thread-local capture on a private stream.
+template <typename F>
+static int capture_graph(F enqueue, specfold_graph* graph) {
   if (!graph) return SPECFOLD_EINVAL;
   *graph = nullptr;
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return SPECFOLD_ECUDA;
-  // one eager call first: kernel attributes are set and arguments checked
-  // outside the capture
-  int rc = specfold_layer_forward(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, ws_bytes, nullptr, s);
+  int rc = enqueue(s, false);
   if (rc == SPECFOLD_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = SPECFOLD_ECUDA;
   if (rc != SPECFOLD_OK) {
     cudaStreamDestroy(s);
@@ -600,8 +678,7 @@ int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weight
     cudaStreamDestroy(s);
     return SPECFOLD_ECUDA;
   }
-  rc = specfold_layer_forward(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, ws_bytes, stage_events,
-                              s);
+  rc = enqueue(s, true);
   const cudaError_t ce = cudaStreamEndCapture(s, &g);
   const uint64_t kernels = g_launches.load() - k0;
   g_launches.fetch_sub(kernels);  // captured, not launched
@@ -623,6 +700,33 @@ int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weight
   }
   *graph = h;
   return SPECFOLD_OK;
+}
+
+extern "C" {
+
+int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                                const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV,
+                                int P, float tau, void* H_out, void* ws, size_t ws_bytes, void* const* stage_events,
+                                specfold_graph* graph) {
+  return capture_graph(
+      [&](cudaStream_t s, bool capturing) {
+        return specfold_layer_forward(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, ws_bytes,
+                                      capturing ? stage_events : nullptr, s);
+      },
+      graph);
+}
+
+int specfold_stack_graph_create(const specfold_dims* dims, int n_layers, const specfold_weights* w,
+                                const void* H_in, const int32_t* parent, int B, int L,
+                                const specfold_kv_view* prefK, const specfold_kv_view* prefV, int P, float tau,
+                                void* H_out, const specfold_stack_trace* trace, void* ws, size_t ws_bytes,
+                                specfold_graph* graph) {
+  return capture_graph(
+      [&](cudaStream_t s, bool) {
+        return specfold_stack_forward(dims, n_layers, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, trace, ws,
+                                      ws_bytes, s);
+      },
+      graph);
 }
 
 int specfold_graph_launch(specfold_graph graph, void* stream) {

@@ -49,7 +49,8 @@ constexpr int kRowWarps = 8;  // warps (rows) per block of the row kernels
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(kRowWarps * 32)
 gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d,
-            float tau, uint8_t* __restrict__ fold, float* __restrict__ rel, const L2Prefetch pf) {
+            float tau, uint8_t* __restrict__ fold, float* __restrict__ rel, const L2Prefetch pf,
+            uint8_t* __restrict__ fold_hist) {
   using V = VecT<T>;
   // weights of the next kernels start streaming into L2 while this
   // latency-bound kernel and the pack run
@@ -65,6 +66,7 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
     if (lane == 0) {
       fold[row] = 0;
       if (rel) rel[row] = -1.f;
+      if (fold_hist) fold_hist[row] = 0;
     }
     return;
   }
@@ -104,6 +106,7 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
   if (lane == 0) {
     const bool f = (num < tau * tau * den) || (num == 0.f && tau > 0.f);
     fold[row] = f ? 1 : 0;
+    if (fold_hist) fold_hist[row] = f ? 1 : 0;
     if (rel) rel[row] = den > 0.f ? sqrtf(num / den) : (num == 0.f ? 0.f : __int_as_float(0x7f800000));
   }
 }
@@ -190,7 +193,8 @@ __global__ void __launch_bounds__(kPackThreads)
 select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ parent, int B, int L,
                    int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
                    int32_t* __restrict__ src, int32_t* __restrict__ packed_idx, int32_t* __restrict__ slot,
-                   int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status) {
+                   int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status,
+                   int32_t* __restrict__ n_hist) {
   extern __shared__ int smem_i[];
   __shared__ int s_warp[kPackThreads / 32];
   __shared__ int s_bad;
@@ -260,6 +264,7 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
   }
   if (blockIdx.x == 0 && tid == 0) {
     if (n_dev) n_dev[0] = n;
+    if (n_hist) n_hist[0] = n;
     if (s_bad && status) atomicOr(status, SPECFOLD_DEV_BAD_PARENT);
   }
   // RMSNorm1 gather of this block's packed rows
@@ -355,7 +360,7 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
 }  // namespace
 
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
-                uint8_t* fold, float* rel, cudaStream_t st, const L2Prefetch* prefetch) {
+                uint8_t* fold, float* rel, cudaStream_t st, const L2Prefetch* prefetch, uint8_t* fold_hist) {
   L2Prefetch pf = {};
   if (prefetch) pf = *prefetch;
   const int R = B * L;
@@ -364,15 +369,15 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
   if (dtype == SPECFOLD_BF16) {
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
     if (per_lane <= 8)
-      launch_k(gate_kernel<__nv_bfloat16, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf);
+      launch_k(gate_kernel<__nv_bfloat16, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
     else
-      launch_k(gate_kernel<__nv_bfloat16, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf);
+      launch_k(gate_kernel<__nv_bfloat16, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
   } else {
     const float* h = static_cast<const float*>(H);
     if (per_lane <= 8)
-      launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf);
+      launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
     else
-      launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf);
+      launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
   }
   count_launch();
   return check_launch();
@@ -381,7 +386,7 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
 template <typename T, int MAXV>
 static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                               const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st) {
+                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
   const int R = B * L;
   const size_t smem = static_cast<size_t>(3) * R * sizeof(int);
   static int attr_done[64] = {0};
@@ -396,7 +401,7 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
   launch_k(select_pack_kernel<T, MAXV>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
-                                                          n_dev, static_cast<T*>(X1), status);
+                                                          n_dev, static_cast<T*>(X1), status, n_hist);
   count_launch();
   return check_launch();
 }
@@ -404,27 +409,27 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
 template <typename T>
 static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                                 const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st) {
+                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
   const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
   if (per_lane <= 4)
-    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
   if (per_lane <= 8)
-    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
   if (per_lane <= 16)
-    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
   if (per_lane <= 32)
-    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st);
+    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
   return SPECFOLD_EUNSUPPORTED;
 }
 
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                        const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot, int32_t* n_dev,
-                       void* X1, uint32_t* status, cudaStream_t st) {
+                       void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
   if (dtype == SPECFOLD_BF16)
     return select_pack_dispatch<__nv_bfloat16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1,
-                                               status, st);
+                                               status, st, n_hist);
   return select_pack_dispatch<float>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status,
-                                     st);
+                                     st, n_hist);
 }
 
 template <typename T>

@@ -17,14 +17,18 @@ int num_sms();                        // SMs of the current device (cached per d
 int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a launch
 
 // ---- row-wise kernels (rowwise.cu) ----
-// gate: fold/rel per row; dtype bf16 or f32.
+// gate: fold/rel per row; dtype bf16 or f32.  fold_hist (optional) receives
+// a second copy of the decisions.
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
-                uint8_t* fold, float* rel, cudaStream_t st, const struct L2Prefetch* prefetch = nullptr);
+                uint8_t* fold, float* rel, cudaStream_t st, const struct L2Prefetch* prefetch = nullptr,
+                uint8_t* fold_hist = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
-// given); parent may be null (pack alone); any output may be null.
+// given); parent may be null (pack alone); any output may be null.  n_hist
+// (optional) receives a second copy of the packed-row count.
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
                        const void* H, const void* g1, float eps, int32_t* src, int32_t* packed_idx,
-                       int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st);
+                       int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st,
+                       int32_t* n_hist = nullptr);
 // Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
                         int R, int d, const void* g, float eps, void* Y, cudaStream_t st);

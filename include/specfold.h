@@ -227,6 +227,52 @@ int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weight
                                 specfold_kv_view prefK, specfold_kv_view prefV, int P, float tau,
                                 void* H_out, void* ws, size_t ws_bytes,
                                 void* const* stage_events, specfold_graph* graph);
+/* ---- stack of layers ---------------------------------------------- */
+/* Optional per-layer records of a stack call (all device pointers, each may
+ * be NULL):
+ *   hidden    [n_layers - 1, B, L, d] dims.dtype: the input of layers
+ *             1 .. n_layers-1 (= the output of layers 0 .. n_layers-2).
+ *             When NULL those states live in the workspace and are
+ *             overwritten as the stack proceeds.
+ *   fold      uint8 [n_layers, B*L]: each layer's gate decisions.
+ *   n_packed  int32 [n_layers]: each layer's packed-row count n (the
+ *             recompute fraction of layer l is n_packed[l] / (B*L)). */
+typedef struct specfold_stack_trace {
+  void* hidden;
+  uint8_t* fold;
+  int32_t* n_packed;
+} specfold_stack_trace;
+
+/* Workspace bytes for a stack of layers of this shape: a layer workspace
+ * plus one [B, L, d] buffer for the states between layers.  0 if invalid. */
+size_t specfold_stack_workspace_size(const specfold_dims* dims, int B, int L);
+
+/* A stack of n_layers folded layers: layer l reads layer l-1's output
+ * (layer 0 reads H_in) and the last layer writes H_out.  Explainer,
+ * "mechanism" paragraph (automatic release of a fold) and appendix D (how
+ * the recompute fraction changes with depth): the gate runs again at every
+ * layer on that layer's own input, so a row folded at layer l is recomputed
+ * at layer l+1 when its difference to the parent's new input reaches tau.
+ * w, prefK and prefV are HOST arrays of n_layers entries (each layer's own
+ * weights and prefix view; the pointers inside are device pointers).  Same
+ * shape for every layer, same parent table and tau.  trace may be NULL.
+ * ws: specfold_stack_workspace_size bytes.  H_out must not alias H_in or
+ * trace->hidden.  Errors as for specfold_layer_forward; an invalid layer
+ * makes the call return before anything is launched. */
+int specfold_stack_forward(const specfold_dims* dims, int n_layers, const specfold_weights* w,
+                           const void* H_in, const int32_t* parent, int B, int L,
+                           const specfold_kv_view* prefK, const specfold_kv_view* prefV, int P,
+                           float tau, void* H_out, const specfold_stack_trace* trace,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* CUDA graph of one specfold_stack_forward call (same rules as
+ * specfold_layer_graph_create; the host arrays are read at creation only). */
+int specfold_stack_graph_create(const specfold_dims* dims, int n_layers, const specfold_weights* w,
+                                const void* H_in, const int32_t* parent, int B, int L,
+                                const specfold_kv_view* prefK, const specfold_kv_view* prefV, int P,
+                                float tau, void* H_out, const specfold_stack_trace* trace,
+                                void* ws, size_t ws_bytes, specfold_graph* graph);
+
 /* Enqueue one replay on `stream`. */
 int specfold_graph_launch(specfold_graph graph, void* stream);
 /* Release the graph (after its launches have completed). */

@@ -91,3 +91,52 @@ def oracle_with_gpu_decisions(inp: synth.LayerInputs, tau: float, gpu_fold: np.n
     res = orc.layer_forward(inp.H, inp.parent, inp.weights, inp.prefix.K, inp.prefix.V, float(np.float32(tau)),
                             d.eps, d.n_kv, d.hd, force=force, rows=rows)
     return res, int(near.sum()), int(bad.sum())
+
+
+def check_layer(inp, tau, rows=None, inter=True):
+    dev = DeviceInputs(inp)
+    lay, out = run_layer(dev, tau)
+    assert lay.status() == 0
+    gi = read_intermediates(lay, dev)
+    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows)
+    assert n_bad == 0, f"{n_bad} gate decisions differ away from tau"
+    B, L, D = inp.H.shape
+    R = B * L
+    # S1: relative differences (fp32 on the GPU) and decisions
+    nonroot = np.arange(R) >= L
+    rg, ro = gi["rel"][nonroot], res["rel"].reshape(-1)[nonroot]
+    fin = np.isfinite(ro)
+    np.testing.assert_allclose(rg[fin], ro[fin], rtol=1e-4, atol=1e-6)
+    assert np.array_equal(gi["fold"], res["fold"].reshape(-1))
+    # S2/S3: provenance and packed list, bit-exact
+    assert np.array_equal(gi["src"], res["src"])
+    assert gi["n"] == res["n"]
+    assert np.array_equal(gi["packed_idx"], res["packed_idx"])
+    assert np.array_equal(gi["slot"], res["slot"])
+    m = {"n": gi["n"], "near_tau": n_near}
+    if inter:
+        act = res["act_rows"]
+        k = gi["slot"][act]
+        m["X1"] = rel_l2(gi["X1"][k], res["X1"])
+        m["Q"] = rel_l2(gi["Q"][k], res["Q"])
+        m["K"] = rel_l2(gi["bK"][act], np.stack([res["K_rows"][r] for r in act]))
+        m["V"] = rel_l2(gi["bV"][act], np.stack([res["V_rows"][r] for r in act]))
+        m["attnO"] = rel_l2(gi["attnO"][k], res["attnO"])
+        m["A"] = rel_l2(gi["A"][k], res["A"])
+        m["X2"] = rel_l2(gi["X2"][k], res["X2"])
+        m["G"] = rel_l2(gi["G"][k], res["G"])
+    Hg = to_np(out).reshape(R, D)
+    Hin = inp.H.reshape(R, D).astype(np.float64)
+    rr = res["out_rows"]
+    m["H_out"] = rel_l2(Hg[rr], res["out"])
+    m["delta"] = rel_l2(Hg[rr] - Hin[rr], res["out"] - Hin[rr])
+    # The layer's own contribution (H_out - H_in) can be small next to H, so
+    # the bf16 rounding of H_out alone may exceed 2e-2 of it: bound the error
+    # by 2e-2 of the contribution plus twice that rounding floor.
+    err = np.linalg.norm(Hg[rr] - res["out"])
+    floor = np.linalg.norm(synth.round_bf16(res["out"].astype(np.float32)) - res["out"])
+    assert err <= TOL * np.linalg.norm(res["out"] - Hin[rr]) + 2.0 * floor, m
+    for key, val in m.items():
+        if key not in ("n", "near_tau", "delta"):
+            assert val < TOL, (key, val, m)
+    return m, lay, out

@@ -116,6 +116,41 @@ def test_host_argument_errors_launch_nothing(L):
     assert L.specfold_launch_count() == before
 
 
+def test_stack_host_checks_launch_nothing(L):
+    """Stack entry point: sizes and every host-side rejection, with no GPU."""
+    from diffusion_branch_speculative_gb300 import binding
+    before = L.specfold_launch_count()
+    P = ctypes.c_void_p
+    f32 = ctypes.c_float
+    d = _dims()
+    layer = binding.workspace_size(d, 16, 32)
+    stack = binding.stack_workspace_size(d, 16, 32)
+    assert stack == layer + 16 * 32 * 3584 * 2          # one bf16 state buffer, already 256-byte multiple
+    assert binding.stack_workspace_size(_dims(hd=96), 16, 32) == 0
+    good_w = binding.specfold_weights(*([0x20000] * 9))
+    bad_w = binding.specfold_weights(*([0x20000] * 8 + [0x20004]))
+    view = binding.specfold_kv_view(0x30000, 2 * 4 * 128, 128)
+    W = (binding.specfold_weights * 3)(good_w, good_w, bad_w)
+    V = (binding.specfold_kv_view * 3)(view, view, view)
+    H, par, out, ws = P(0x100000), P(0x10000), P(0x200000), P(0x400000)
+
+    def call(n=3, w=W, h=H, o=out, wsb=stack, tau=0.05, trace=None):
+        return L.specfold_stack_forward(ctypes.byref(d), n, w, h, par, 16, 32, V, V, 2048, f32(tau), o, trace, ws,
+                                        wsb, None)
+    assert call(n=0) == binding.EINVAL
+    assert call(w=None) == binding.EINVAL
+    assert call() == binding.EALIGN                     # layer 2's w_down is misaligned
+    assert call(n=2, wsb=stack - 1) == binding.ECAPACITY
+    assert call(n=2, wsb=layer) == binding.ECAPACITY    # no room for the state buffer
+    assert call(n=2, o=H) == binding.EINVAL             # H_out aliasing H_in
+    assert call(n=2, tau=float("nan")) == binding.EINVAL
+    overlap = binding.specfold_stack_trace(0x100000 - 64, None, None)
+    assert call(n=2, trace=ctypes.byref(overlap)) == binding.EINVAL
+    odd = binding.specfold_stack_trace(0x800008, None, None)
+    assert call(n=2, trace=ctypes.byref(odd)) == binding.EALIGN
+    assert L.specfold_launch_count() == before
+
+
 def test_product_path_has_no_oracle_import():
     """The package never imports the oracle (it is test infrastructure)."""
     pkg = os.path.join(ROOT, "diffusion_branch_speculative_gb300")
