@@ -382,7 +382,7 @@ def run_ours(args, rank, world):
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
     del lay
     torch.cuda.empty_cache()
-    stack = [] if args.no_stack else stack_sweep(args, flush, barrier)
+    stack = None if args.no_stack else stack_sweep(args, flush, barrier)
     return {
         "stack_sweep": stack,
         "budget_sweep": budget,
@@ -552,12 +552,34 @@ def stack_sweep(args, flush, barrier):
                      "rho_mean": round(sum(ns) / (R * w.n_layers), 4),
                      "rho_per_layer": [round(n / R, 4) for n in ns]})
     assert stack.status() == 0, "device status set"
+    # depth profile at the command-line tau (one recorded, untimed step): how
+    # far the state and the child/parent differences move with depth, and how
+    # many rows change decision against layer 0 (released or newly folded)
+    stack.forward(H, parent, args.tau, out, record=True)
+    torch.cuda.synchronize()
+    states = [H] + [stack.hidden[l] for l in range(w.n_layers - 1)]
+    par = br.graph.parent
+    root_rms, r_med, r_p10, r_p90 = [], [], [], []
+    for x in states:
+        xf = x.float()
+        root_rms.append(round(float(xf[0].pow(2).mean().sqrt()), 3))
+        diff = (xf[1:] - xf[torch.from_numpy(par[1:].astype(np.int64)).cuda()]).norm(dim=-1)
+        base = xf[torch.from_numpy(par[1:].astype(np.int64)).cuda()].norm(dim=-1)
+        r = (diff / base).flatten()
+        q = torch.quantile(r, torch.tensor([0.1, 0.5, 0.9], device=r.device))
+        r_p10.append(round(float(q[0]), 4))
+        r_med.append(round(float(q[1]), 4))
+        r_p90.append(round(float(q[2]), 4))
+    f0 = stack.fold[0]
+    changed = [int((stack.fold[l] != f0).sum()) for l in range(w.n_layers)]
+    profile = {"tau": args.tau, "root_rms": root_rms, "r_p10": r_p10, "r_median": r_med, "r_p90": r_p90,
+               "rows_changed_vs_layer0": changed}
     dense = rows[0]["us_per_step"] if rows and rows[0]["tau"] == 0.0 else None
     for r in rows:
         r["time_vs_dense"] = round(r["us_per_step"] / dense, 4) if dense else None
     del stack, weights, caches
     torch.cuda.empty_cache()
-    return rows
+    return {"taus": rows, "depth_profile": profile}
 
 
 # -------------------------------------------------------- oracle on CPU ----
