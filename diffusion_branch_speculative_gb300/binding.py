@@ -48,7 +48,7 @@ class specfold_kv_view(ctypes.Structure):
 
 class specfold_ws_layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in
-                ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "x1", "q",
+                ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "dep_off", "dep_rows", "x1", "q",
                  "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "attn_scratch", "total")]
 
 

@@ -171,6 +171,8 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->src = take(R * 4);
   o->packed_idx = take(R * 4);
   o->slot_of_row = take(R * 4);
+  o->dep_off = take((R + 1) * 4);
+  o->dep_rows = take(R * 4);
   o->x1 = take(R * d->d_model * e);
   o->q = take(R * nq * e);
   o->block_k = take(R * nkv * e);
@@ -307,10 +309,14 @@ static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, con
   return launch_gemm(c, st);
 }
 
+// dep_off / dep_rows (the folded rows grouped by source slot, from the pack
+// step) move the fold-fill into the down projection's finish kernel; without
+// them a separate fold-fill kernel walks fold / src.
 static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const void* A, const int32_t* packed_idx,
                      const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int R,
                      void* H_out, void* X2, void* G, const Scratch& s, uint32_t* status, cudaStream_t st,
-                     void* const* ev, int ev0, bool x2_ready) {
+                     void* const* ev, int ev0, bool x2_ready, const int32_t* dep_off = nullptr,
+                     const int32_t* dep_rows = nullptr) {
   auto mark = [&](int i) {
     if (ev) record_stage_event(ev[i], st);
   };
@@ -349,9 +355,14 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.ldr = d->d_model;
   c.row_idx = packed_idx;
   fill_scratch(c, s, status);
+  if (dep_off) {
+    c.dep_off = dep_off;
+    c.dep_rows = dep_rows;
+    c.hin = H_in;
+  }
   SF_TRY(launch_gemm(c, st));
   mark(ev0 + 2);
-  SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
+  if (!dep_off) SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
   mark(ev0 + 3);
   return SPECFOLD_OK;
 }
@@ -409,7 +420,8 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
                      l2pf_enabled() ? &pf_gate : nullptr, fold_hist));
   mark(1);
   SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
-                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist));
+                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,
+                            at<int32_t>(ws, lo.dep_off), at<int32_t>(ws, lo.dep_rows)));
   mark(2);
   SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
                    at<void>(ws, lo.block_v), s, status, st));
@@ -423,7 +435,8 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
                         at<void>(ws, lo.x2)));
   mark(5);
   return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
-                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true);
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_off),
+                   at<int32_t>(ws, lo.dep_rows));
 }
 
 }  // namespace sf

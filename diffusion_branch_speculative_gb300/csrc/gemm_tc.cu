@@ -7,9 +7,15 @@
 // One CTA per SM loops over work units (m-tile, k-split, n-tile).  The number
 // of packed rows n is read on the device, so the decomposition adapts to the
 // recompute fraction without a host round trip: when the m x n tiles cannot
-// fill the SMs, the K loop is split across CTAs, each writes its fp32 partial
-// tile, and a second, fully parallel kernel sums the partials in a fixed
-// order (deterministic) and runs the fused epilogue.
+// fill the SMs, the K loop is split across CTAs.  Two ways to sum the splits:
+//   * clustered launch (when the host knows every n leaves SMs idle): the S
+//     CTAs of one tile sit in one thread-block cluster; each stages its fp32
+//     partial tile in its own shared memory, and after a cluster barrier each
+//     sums a 1/S column share of the tile from all S stages through
+//     distributed shared memory, in split order, and runs the epilogue;
+//   * otherwise each CTA writes its fp32 partial tile to global memory and a
+//     second, fully parallel kernel sums them in split order.
+// Both orders are fixed, so results are deterministic.
 //
 // Roles (192 threads): warp 0 issues TMA loads into a multi-stage ring of
 // 128-byte-swizzled tiles; warp 1 allocates TMEM and issues tcgen05.mma
@@ -20,6 +26,7 @@
 #include "sf_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -32,6 +39,7 @@ constexpr int kGemmThreads = 192;
 constexpr int kMaxGrid = 160;        // persistent CTAs (>= SMs of one GB300)
 constexpr int kMaxSplits = 16;
 constexpr int kMinKbPerSplit = 4;
+constexpr int kMaxClusterSplit = 8;  // largest cluster (portable size)
 
 template <int BN>
 struct Cfg {
@@ -43,6 +51,10 @@ struct Cfg {
   static constexpr int BAR_BYTES = 256;
   static constexpr int EPI_STAGE_BYTES = 4 * 32 * 33 * 4;  // per epilogue warp: 32 x 32 fp32, padded
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EPI_STAGE_BYTES + 1024;
+  // clustered split: the fp32 partial tile, rows padded by 16 bytes, staged
+  // over the operand ring once the CTA's only unit has consumed it
+  static constexpr int SROW = BN + 4;
+  static_assert(kBM * SROW * 4 + kBM * 4 <= STAGES * STAGE_BYTES, "partial tile and row indices must fit the ring");
 };
 
 struct GemmParams {
@@ -62,6 +74,10 @@ struct GemmParams {
   int n_q, n_kv, hd, g, R;
   float* partial;
   uint32_t* status;
+  int cs;               // cluster size of a clustered launch (0: plain launch)
+  const int32_t* dep_off;   // RESID_SCATTER: fold-fill of dependents in the finish kernel
+  const int32_t* dep_rows;
+  const __nv_bfloat16* hin;
 };
 
 SF_DEV float silu(float x) { return __fdividef(x, 1.f + ex2(-x * 1.4426950408889634f)); }
@@ -181,23 +197,123 @@ SF_DEV void epi_qkv_elem(const GemmParams& p, int k, int r, int c, float x) {
   }
 }
 
+// Split factor under clusters of cs CTAs: the largest divisor of cs that keeps
+// tiles * S within the grid and kMinKbPerSplit k-blocks per split.
+SF_DEV int split_factor_cl(int tiles, int grid, int KB, int cs) {
+  for (int S = cs; S > 1; --S)
+    if (cs % S == 0 && tiles * S <= grid && KB / S >= kMinKbPerSplit) return S;
+  return 1;
+}
+
 struct Unit {
   int m, s, nt, kb0, kb1, tile;
 };
 
-SF_DEV Unit decode(int u, int Mt, int S, int Nt, int KB) {
+// Work unit u.  Plain: m fastest, then split, then n-tile.  Clustered split
+// (dsm): the S consecutive CTAs u = tile * S + s share one tile, so they sit
+// in one cluster (S divides the cluster size).
+SF_DEV Unit decode(int u, int Mt, int S, int Nt, int KB, bool dsm) {
   Unit w;
-  w.m = u % Mt;
-  const int rest = u / Mt;
-  w.s = rest % S;
-  w.nt = rest / S;
+  if (dsm) {
+    w.s = u % S;
+    const int tile = u / S;
+    w.m = tile % Mt;
+    w.nt = tile / Mt;
+  } else {
+    w.m = u % Mt;
+    const int rest = u / Mt;
+    w.s = rest % S;
+    w.nt = rest / S;
+  }
   w.kb0 = (w.s * KB) / S;
   w.kb1 = ((w.s + 1) * KB) / S;
   w.tile = w.m * Nt + w.nt;
   return w;
 }
 
+// Clustered split-K finish: this CTA (split s of its tile) sums output
+// columns [s, s + 1) * TW / S of every valid row over the S partial tiles
+// staged in the group's shared memories, in split order, and runs the
+// epilogue on groups of 8 columns.  The row indices were staged next to the
+// partial tile, so every global load of an item (residual row) is issued
+// before its distributed-shared-memory loads and the two latencies overlap.
 template <int BN, int EPI>
+SF_DEV void dsm_reduce(const GemmParams& p, const uint8_t* smem, int n, int Mt, int S) {
+  constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
+  constexpr int SROW = Cfg<BN>::SROW;
+  const int* s_ridx = reinterpret_cast<const int*>(smem + kBM * SROW * 4);
+  const int s = static_cast<int>(blockIdx.x) % S;
+  const uint32_t rank0 = cluster_ctarank() - static_cast<uint32_t>(s);
+  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int m = tile % Mt, nt = tile / Mt;
+  const int rows = min(kBM, n - m * kBM);
+  const int share = TW / S;
+  const int groups = share / 8;
+  const uint32_t sbase = smem_u32(smem);
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+  const __nv_bfloat16* Rz = static_cast<const __nv_bfloat16*>(p.resid);
+  for (int idx = threadIdx.x; idx < rows * groups; idx += kGemmThreads) {
+    const int r = idx / groups;
+    const int tc = s * share + (idx - r * groups) * 8;
+    const int k = m * kBM + r;
+    const int c = nt * TW + tc;
+    uint4 res = make_uint4(0, 0, 0, 0);
+    if constexpr (EPI == EPI_RESID_PACKED)
+      res = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(s_ridx[r]) * p.ldr + c));
+    if constexpr (EPI == EPI_RESID_SCATTER)
+      res = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(k) * p.ldr + c));
+    const uint32_t off = sbase + static_cast<uint32_t>((r * SROW + tc) * 4);
+    float4 a[kMaxClusterSplit][2], b[kMaxClusterSplit][2];
+#pragma unroll
+    for (int j = 0; j < kMaxClusterSplit; ++j) {
+      if (j < S) {
+        const uint32_t ra = dsmem_addr(off, rank0 + j);
+        a[j][0] = ld_dsmem_f4(ra);
+        a[j][1] = ld_dsmem_f4(ra + 16);
+        if constexpr (EPI == EPI_SWIGLU) {
+          b[j][0] = ld_dsmem_f4(ra + (BN / 2) * 4);
+          b[j][1] = ld_dsmem_f4(ra + (BN / 2) * 4 + 16);
+        }
+      }
+    }
+    float v[8], u[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = u[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxClusterSplit; ++j) {
+      if (j < S) {
+        v[0] += a[j][0].x; v[1] += a[j][0].y; v[2] += a[j][0].z; v[3] += a[j][0].w;
+        v[4] += a[j][1].x; v[5] += a[j][1].y; v[6] += a[j][1].z; v[7] += a[j][1].w;
+        if constexpr (EPI == EPI_SWIGLU) {
+          u[0] += b[j][0].x; u[1] += b[j][0].y; u[2] += b[j][0].z; u[3] += b[j][0].w;
+          u[4] += b[j][1].x; u[5] += b[j][1].y; u[6] += b[j][1].z; u[7] += b[j][1].w;
+        }
+      }
+    }
+    if constexpr (EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
+      v[0] += bf16lo(res.x); v[1] += bf16hi(res.x); v[2] += bf16lo(res.y); v[3] += bf16hi(res.y);
+      v[4] += bf16lo(res.z); v[5] += bf16hi(res.z); v[6] += bf16lo(res.w); v[7] += bf16hi(res.w);
+      const int rdst = EPI == EPI_RESID_PACKED ? k : s_ridx[r];
+      store_bf16<8>(Y + static_cast<size_t>(rdst) * p.ldy + c, v);
+    } else if constexpr (EPI == EPI_QKV) {
+      const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+      if (c < nq) {
+        const int head = c / p.hd, j = c - head * p.hd;
+        const int hk = head / p.g, hg = head - hk * p.g;
+        store_bf16<8>(Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j, v);
+      } else {
+        const bool is_k = c < nq + nkv;
+        const int cc = is_k ? c - nq : c - nq - nkv;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
+        store_bf16<8>(dst + static_cast<size_t>(s_ridx[r]) * nkv + cc, v);
+      }
+    } else {
+      epi_chunk<EPI, 8>(p, k, c, v, u);
+    }
+  }
+}
+
+template <int BN, int EPI, bool CL>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -221,9 +337,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
   const int KB = p.K / kBK;
-  const int S = split_factor(tiles, static_cast<int>(gridDim.x), KB);
+  const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs)
+                  : split_factor(tiles, static_cast<int>(gridDim.x), KB);
+  const bool dsm = CL && S > 1;  // splits summed through distributed shared memory
   const int U = tiles * S;
-  if (static_cast<int>(blockIdx.x) >= U) return;
+  if (static_cast<int>(blockIdx.x) >= U) {
+    if constexpr (CL) {
+      if (dsm) {  // an idle CTA still takes part in its cluster's two barriers
+        cluster_sync_all();
+        cluster_sync_all();
+      }
+    }
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
@@ -257,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit w = decode(u, Mt, S, p.Nt, KB);
+        const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
         const CUtensorMap* mlo;
         const CUtensorMap* mhi;
         int ylo, yhi;
@@ -305,7 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t it = 0, t = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++t) {
-        const Unit w = decode(u, Mt, S, p.Nt, KB);
+        const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
         const int ab = t & 1;
         if (!mbar_wait(smem_u32(&acce[ab]), ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -342,7 +468,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const int et = threadIdx.x - 64;    // 0..127
     uint32_t t = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++t) {
-      const Unit w = decode(u, Mt, S, p.Nt, KB);
+      const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
       const int ab = t & 1;
       if (et == 0) *s_ok = mbar_wait(smem_u32(&accf[ab]), (t >> 1) & 1, abort_flag, p.status) ? 1 : 0;
       named_bar_sync(1, 128);
@@ -352,6 +478,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       __syncwarp();
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + ab * BN;
+      if (dsm) {
+        // this CTA's only unit: stage its fp32 partial tile (one row per
+        // thread) over the operand ring, whose loads have all been consumed
+        float* dst = reinterpret_cast<float*>(smem) + (q * 32 + lane) * C::SROW;
+        if constexpr (EPI == EPI_QKV || EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
+          const int row = w.m * kBM + q * 32 + lane;
+          reinterpret_cast<int*>(smem + kBM * C::SROW * 4)[q * 32 + lane] = row < n ? p.row_idx[row] : 0;
+        }
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tb + ch * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4)
+            reinterpret_cast<float4*>(dst + ch * 32)[e4] =
+                make_float4(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1]),
+                            __uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3]));
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&acce[ab]));
+        continue;
+      }
       // Each 32-column chunk of the warp's 32 rows goes through a padded smem
       // transpose so that lane j then handles column j of one row at a time:
       // every store (and residual load) of the warp is one contiguous segment.
@@ -447,12 +596,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if constexpr (CL) {
+    if (dsm) {
+      cluster_sync_all();  // every split of the cluster is staged
+      dsm_reduce<BN, EPI>(p, smem, n, Mt, S);
+      cluster_sync_all();  // no CTA leaves while its stage may still be read
+    }
+  }
 }
 
 // Sums the S fp32 partial tiles of a split-K GEMM in split order and runs the
 // epilogue.  One thread per (packed row, 8 output columns); all partial loads
 // of a thread are issued before the adds.  Returns at once when the GEMM ran
 // unsplit (S recomputed from the same n and grid).
+// With fold-fill (RESID_SCATTER and p.dep_off set) the kernel also writes,
+// for every folded row r that resolves to packed row k, Y[r] = Y[s] +
+// (hin[r] - hin[s]) with s = row_idx[k] and Y[s] as stored in bf16; when the
+// GEMM ran unsplit it reads Y[s] back and does only the fill.
+template <int BN, int EPI>
+SF_DEV void fill_dependents(const GemmParams& p, int k, int c, const float (&yb)[8]) {
+  const int d0 = p.dep_off[k], d1 = p.dep_off[k + 1];
+  if (d1 <= d0) return;
+  const int s = p.row_idx[k];
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+  float hs[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) hs[e] = 0.f;
+  add_bf16<8>(p.hin + static_cast<size_t>(s) * p.ldy + c, hs);
+  for (int j0 = d0; j0 < d1; j0 += 4) {
+    uint4 hr[4];
+    int rr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      rr[q] = j0 + q < d1 ? p.dep_rows[j0 + q] : -1;
+      if (rr[q] >= 0) hr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(rr[q]) * p.ldy + c));
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (rr[q] < 0) continue;
+      float o[8];
+      o[0] = yb[0] + (bf16lo(hr[q].x) - hs[0]); o[1] = yb[1] + (bf16hi(hr[q].x) - hs[1]);
+      o[2] = yb[2] + (bf16lo(hr[q].y) - hs[2]); o[3] = yb[3] + (bf16hi(hr[q].y) - hs[3]);
+      o[4] = yb[4] + (bf16lo(hr[q].z) - hs[4]); o[5] = yb[5] + (bf16hi(hr[q].z) - hs[5]);
+      o[6] = yb[6] + (bf16lo(hr[q].w) - hs[6]); o[7] = yb[7] + (bf16hi(hr[q].w) - hs[7]);
+      store_bf16<8>(Y + static_cast<size_t>(rr[q]) * p.ldy + c, o);
+    }
+  }
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
   pdl_wait();
@@ -460,6 +651,25 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int Mt = (n + kBM - 1) / kBM;
   const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
+  if constexpr (EPI == EPI_RESID_SCATTER) {
+    if (S <= 1 && p.dep_off) {
+      // unsplit GEMM: its epilogue wrote Y[s]; fill the dependents only
+      const int groups = p.N / 8;
+      const long long total = static_cast<long long>(n) * groups;
+      for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+           idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int k = static_cast<int>(idx / groups);
+        const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
+        if (p.dep_off[k + 1] <= p.dep_off[k]) continue;
+        float yb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) yb[e] = 0.f;
+        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, yb);
+        fill_dependents<BN, EPI>(p, k, c, yb);
+      }
+      return;
+    }
+  }
   if (S <= 1) return;
   constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;   // output columns per tile
   const int groups = (p.Nt * TW) / 8;
@@ -511,6 +721,19 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
       for (int s = threadIdx.x & 3; s < S; s += 4) {
         l2_discard_line(line + static_cast<size_t>(s) * kBM * BN);
         if constexpr (EPI == EPI_SWIGLU) l2_discard_line(line + static_cast<size_t>(s) * kBM * BN + BN / 2);
+      }
+    }
+    if constexpr (EPI == EPI_RESID_SCATTER) {
+      if (p.dep_off) {
+        // the residual add and the bf16 rounding of the stored row, then the fill
+        const int c = nt * TW + tc;
+        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + c, v);
+        store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, v);
+        float yb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) yb[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+        fill_dependents<BN, EPI>(p, k, c, yb);
+        continue;
       }
     }
     epi_chunk<EPI, 8>(p, k, nt * TW + tc, v, u);
@@ -602,8 +825,40 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
   }
 }
 
+// Clusters of cs CTAs of the GEMM (one CTA per SM) that can be resident at
+// once on the current device, for cs = 2, 4, 8 (queried once per device).
+int cluster_capacity(int cs) {
+  static int cache[64][kMaxClusterSplit + 1];
+  static bool done[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || cs < 2 || cs > kMaxClusterSplit) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    using Cf = Cfg<256>;
+    if (cudaFuncSetAttribute(gemm_kernel<256, EPI_STORE, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cf::SMEM_BYTES) == cudaSuccess) {
+      for (int c = 2; c <= kMaxClusterSplit; c *= 2)
+        cache[dev][c] = max_active_clusters(gemm_kernel<256, EPI_STORE, true>, dim3(kGemmThreads), Cf::SMEM_BYTES, c);
+    } else {
+      cudaGetLastError();
+    }
+    done[dev] = true;
+  }
+  return cache[dev][cs];
+}
+
+// SPECFOLD_CLUSTER=0 in the environment turns the clustered split-K off.
+bool cluster_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("SPECFOLD_CLUSTER");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 template <int BN, int EPI>
-int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
+int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, int cgrid = 0) {
   using Cf = Cfg<BN>;
   GemmParams p;
   memset(&p, 0, sizeof(p));
@@ -637,18 +892,40 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   if (c.partial_len < gemm_partial_floats()) return SPECFOLD_ECAPACITY;
   p.partial = c.partial;
   p.status = c.status;
+  if constexpr (EPI == EPI_RESID_SCATTER) {
+    if (c.dep_off) {
+      if (!c.dep_rows || !c.hin || c.ldy != c.N) return SPECFOLD_EINVAL;
+      p.dep_off = c.dep_off;
+      p.dep_rows = c.dep_rows;
+      p.hin = static_cast<const __nv_bfloat16*>(c.hin);
+    }
+  }
 
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cf::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_kernel<BN, EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cf::SMEM_BYTES) != cudaSuccess)
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
+  if (cs > 1) {
+    // clustered: the splits are summed inside the GEMM
+    p.cs = cs;
+    launch_kc(gemm_kernel<BN, EPI, true>, dim3(cgrid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, cs, p);
+    count_launch();
+    if (check_launch()) return SPECFOLD_ECUDA;
+    if constexpr (EPI == EPI_RESID_PACKED) {
+      if (rn) return launch_rmsnorm_rows(SPECFOLD_BF16, c.Y, nullptr, c.n_dev, c.Mcap, c.N, rn->gain, rn->eps,
+                                         rn->out, st);
+    }
+    return SPECFOLD_OK;
+  }
   const int grid = min(num_sms(), kMaxGrid);
-  launch_k(gemm_kernel<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
+  launch_k(gemm_kernel<BN, EPI, false>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
   if constexpr (EPI == EPI_RESID_PACKED) {
@@ -668,8 +945,9 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
       return check_launch();
     }
   }
-  // a split is possible only if even one m-tile leaves SMs idle
-  if (grid / p.Nt >= 2 && p.K / kBK >= 2 * kMinKbPerSplit) {
+  // a split is possible only if even one m-tile leaves SMs idle; the fold-fill
+  // of the down projection runs in this kernel in any case
+  if ((grid / p.Nt >= 2 && p.K / kBK >= 2 * kMinKbPerSplit) || p.dep_off) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
@@ -680,9 +958,55 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   return SPECFOLD_OK;
 }
 
+struct Plan {
+  int BN;
+  int cs;     // cluster size, 0 = plain launch
+  int grid;   // grid of a clustered launch
+};
+
+// Tile width and launch shape.  A clustered split-K launch is planned when
+// every n up to Mcap leaves SMs idle (so a split always happens) and its
+// clusters cover at least 70 % of the CTAs the plain split would use at one
+// m-tile; among those, the plan with most CTAs wins (ties: wider tile).
+Plan plan_gemm(int Mcap, int N, int K, bool swiglu, bool ok128, bool ok256) {
+  const int grid_nc = min(num_sms(), kMaxGrid);
+  Plan plain = {ok256 ? 256 : 128, 0, 0};
+  if (!cluster_enabled()) return plain;
+  const int Mt_max = (Mcap + kBM - 1) / kBM;
+  const int KB = K / kBK;
+  const int Nt_plain = swiglu ? N / (plain.BN / 2) : N / plain.BN;
+  int S_plain = 1;
+  if (Nt_plain < grid_nc) S_plain = std::max(1, std::min({grid_nc / Nt_plain, KB / kMinKbPerSplit, kMaxSplits}));
+  const int ctas_plain = Nt_plain * S_plain;
+  Plan best = plain;
+  int best_ctas = 0;
+  for (int BN : {256, 128}) {
+    if ((BN == 256 && !ok256) || (BN == 128 && !ok128)) continue;
+    const int Nt = swiglu ? N / (BN / 2) : N / BN;
+    if (Nt <= 0 || static_cast<long long>(Mt_max) * Nt >= grid_nc) continue;
+    for (int cs = kMaxClusterSplit; cs >= 2; cs /= 2) {
+      const int G = std::min(cluster_capacity(cs), kMaxGrid / cs) * cs;
+      if (G < cs) continue;
+      int S = 1;
+      for (int d = cs; d > 1; --d)
+        if (cs % d == 0 && Nt * d <= G && KB / d >= kMinKbPerSplit) {
+          S = d;
+          break;
+        }
+      if (S < 2) continue;
+      if (Nt * S > best_ctas) {
+        best = {BN, cs, G};
+        best_ctas = Nt * S;
+      }
+    }
+  }
+  if (best_ctas * 10 < ctas_plain * 7) return plain;
+  return best;
+}
+
 template <int EPI>
-int run_epi(const GemmCall& c, int BN, cudaStream_t st, const RowNorm* rn = nullptr) {
-  return BN == 256 ? run_gemm<256, EPI>(c, st, rn) : run_gemm<128, EPI>(c, st, rn);
+int run_epi(const GemmCall& c, const Plan& pl, cudaStream_t st, const RowNorm* rn = nullptr) {
+  return pl.BN == 256 ? run_gemm<256, EPI>(c, st, rn, pl.cs, pl.grid) : run_gemm<128, EPI>(c, st, rn, pl.cs, pl.grid);
 }
 
 }  // namespace
@@ -693,12 +1017,11 @@ size_t gemm_partial_floats() { return static_cast<size_t>(kMaxGrid) * kBM * 256;
 
 int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   if (c.K <= 0 || c.K % kBK || c.Mcap <= 0 || c.N <= 0) return SPECFOLD_EUNSUPPORTED;
-  int BN = 128;
   switch (c.epi) {
-    case EPI_SWIGLU:
+    case EPI_SWIGLU: {
       if (c.N % 64) return SPECFOLD_EUNSUPPORTED;
-      BN = c.N % 128 == 0 ? 256 : 128;
-      return run_epi<EPI_SWIGLU>(c, BN, st);
+      return run_epi<EPI_SWIGLU>(c, plan_gemm(c.Mcap, c.N, c.K, true, true, c.N % 128 == 0), st);
+    }
     case EPI_QKV: {
       bool all256 = true;
       for (int j = 0; j < c.nb; ++j) {
@@ -706,17 +1029,21 @@ int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
         all256 = all256 && (c.b_rows[j] % 256 == 0);
       }
       if (c.hd % 32) return SPECFOLD_EUNSUPPORTED;
-      return run_epi<EPI_QKV>(c, all256 ? 256 : 128, st);
+      return run_epi<EPI_QKV>(c, plan_gemm(c.Mcap, c.N, c.K, false, true, all256), st);
     }
     default:
       break;
   }
   if (c.N % 128) return SPECFOLD_EUNSUPPORTED;
-  BN = c.N % 256 == 0 ? 256 : 128;
+  // The residual epilogues keep the plain launch: their split finish is a
+  // separate row-parallel kernel that also runs the fused RMSNorm (output
+  // projection) or the fold-fill (down projection), and measured faster than
+  // the clustered finish, whose whole clusters fit on fewer SMs.
+  const Plan plain = {c.N % 256 == 0 ? 256 : 128, 0, 0};
   switch (c.epi) {
-    case EPI_STORE: return run_epi<EPI_STORE>(c, BN, st);
-    case EPI_RESID_PACKED: return run_epi<EPI_RESID_PACKED>(c, BN, st, rn);
-    case EPI_RESID_SCATTER: return run_epi<EPI_RESID_SCATTER>(c, BN, st);
+    case EPI_STORE: return run_epi<EPI_STORE>(c, plan_gemm(c.Mcap, c.N, c.K, false, true, c.N % 256 == 0), st);
+    case EPI_RESID_PACKED: return run_epi<EPI_RESID_PACKED>(c, plain, st, rn);
+    case EPI_RESID_SCATTER: return run_epi<EPI_RESID_SCATTER>(c, plain, st);
     default: return SPECFOLD_EINVAL;
   }
 }
@@ -785,12 +1112,12 @@ int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI_STORE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cf::SMEM_BYTES) != cudaSuccess)
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
-  launch_k(gemm_kernel<BN, EPI_STORE>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
+  launch_k(gemm_kernel<BN, EPI_STORE, false>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
   if (grid / p.Nt >= 2 && K / kBK >= 2 * kMinKbPerSplit) {

@@ -194,14 +194,14 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
                    int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
                    int32_t* __restrict__ src, int32_t* __restrict__ packed_idx, int32_t* __restrict__ slot,
                    int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status,
-                   int32_t* __restrict__ n_hist) {
+                   int32_t* __restrict__ n_hist, int32_t* __restrict__ dep_off, int32_t* __restrict__ dep_rows) {
   extern __shared__ int smem_i[];
   __shared__ int s_warp[kPackThreads / 32];
   __shared__ int s_bad;
   const int R = B * L;
   int* s_src = smem_i;          // [R] source row (-1: not recomputed, no source)
   int* s_slot = smem_i + R;     // [R] packed slot or -1
-  int* s_inv = smem_i + 2 * R;  // [R] row of packed slot k
+  int* s_inv = smem_i + 2 * R;  // [R + 1] row of packed slot k; block 0 reuses it for the dependents
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   uint4 gw[MAXV];
   if (X1) load_gains<T, MAXV>(g1, d, lane, gw);   // weights: independent of earlier kernels
@@ -267,11 +267,61 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
     if (n_hist) n_hist[0] = n;
     if (s_bad && status) atomicOr(status, SPECFOLD_DEV_BAD_PARENT);
   }
-  // RMSNorm1 gather of this block's packed rows
-  if (X1) {
-    const int k = blockIdx.x * kRowWarps + w;
-    if (k < n) norm_row<T, MAXV>(H + static_cast<size_t>(s_inv[k]) * d, gw, d, eps, X1 + static_cast<size_t>(k) * d, lane);
+  const int k_norm = blockIdx.x * kRowWarps + w;
+  const int r_norm = k_norm < n ? s_inv[k_norm] : -1;
+  if (blockIdx.x == 0 && dep_off) {
+    // Block 0 groups the folded rows by the packed slot of their source
+    // (counting sort in shared memory): dep_rows[dep_off[k] .. dep_off[k+1])
+    // are the rows that take packed row k's output plus their own difference.
+    int* cnt = s_inv;  // [n + 1]
+    __syncthreads();   // every read of s_inv above is done
+    for (int k = tid; k <= n; k += kPackThreads) cnt[k] = 0;
+    __syncthreads();
+    for (int r = tid; r < R; r += kPackThreads) {
+      const int sr = s_src[r];
+      if (sr >= 0 && sr != r) atomicAdd(&cnt[s_slot[sr]], 1);
+    }
+    __syncthreads();
+    // exclusive scan of cnt[0 .. n] (n + 1 entries) in place
+    const int per = (n + 1 + kPackThreads - 1) / kPackThreads;
+    const int c0 = min(n + 1, tid * per), c1 = min(n + 1, c0 + per);
+    int loc = 0;
+    for (int k = c0; k < c1; ++k) loc += cnt[k];
+    int inc = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t;
+    }
+    __syncthreads();  // s_warp is free again
+    if (lane == 31) s_warp[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+      int v = lane < kPackThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
+      }
+      if (lane < kPackThreads / 32) s_warp[lane] = v;
+    }
+    __syncthreads();
+    int run = (w > 0 ? s_warp[w - 1] : 0) + inc - loc;
+    for (int k = c0; k < c1; ++k) {
+      const int c = cnt[k];
+      cnt[k] = run;
+      dep_off[k] = run;
+      run += c;
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += kPackThreads) {
+      const int sr = s_src[r];
+      if (sr >= 0 && sr != r) dep_rows[atomicAdd(&cnt[s_slot[sr]], 1)] = r;
+    }
   }
+  // RMSNorm1 gather of this block's packed rows
+  if (X1 && r_norm >= 0)
+    norm_row<T, MAXV>(H + static_cast<size_t>(r_norm) * d, gw, d, eps, X1 + static_cast<size_t>(k_norm) * d, lane);
 }
 
 // ------------------------------------------------------- RMSNorm rows --
@@ -386,22 +436,23 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
 template <typename T, int MAXV>
 static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                               const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
+                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                              int32_t* dep_rows) {
   const int R = B * L;
-  const size_t smem = static_cast<size_t>(3) * R * sizeof(int);
+  const size_t smem = (static_cast<size_t>(3) * R + 1) * sizeof(int);
   static int attr_done[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_done[dev]) {
     if (cudaFuncSetAttribute(select_pack_kernel<T, MAXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             3 * SPECFOLD_MAX_ROWS * static_cast<int>(sizeof(int))) != cudaSuccess)
+                             (3 * SPECFOLD_MAX_ROWS + 1) * static_cast<int>(sizeof(int))) != cudaSuccess)
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
   launch_k(select_pack_kernel<T, MAXV>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
-                                                          n_dev, static_cast<T*>(X1), status, n_hist);
+                                                          n_dev, static_cast<T*>(X1), status, n_hist, dep_off, dep_rows);
   count_launch();
   return check_launch();
 }
@@ -409,27 +460,29 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
 template <typename T>
 static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                                 const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
+                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                              int32_t* dep_rows) {
   const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
   if (per_lane <= 4)
-    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
+    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
   if (per_lane <= 8)
-    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
+    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
   if (per_lane <= 16)
-    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
+    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
   if (per_lane <= 32)
-    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist);
+    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
   return SPECFOLD_EUNSUPPORTED;
 }
 
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                        const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot, int32_t* n_dev,
-                       void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist) {
+                       void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                       int32_t* dep_rows) {
   if (dtype == SPECFOLD_BF16)
     return select_pack_dispatch<__nv_bfloat16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1,
-                                               status, st, n_hist);
+                                               status, st, n_hist, dep_off, dep_rows);
   return select_pack_dispatch<float>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status,
-                                     st, n_hist);
+                                     st, n_hist, dep_off, dep_rows);
 }
 
 template <typename T>

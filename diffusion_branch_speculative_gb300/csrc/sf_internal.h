@@ -24,11 +24,13 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
                 uint8_t* fold_hist = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
 // given); parent may be null (pack alone); any output may be null.  n_hist
-// (optional) receives a second copy of the packed-row count.
+// (optional) receives a second copy of the packed-row count; dep_off [R+1] /
+// dep_rows [R] (optional) receive the folded rows grouped by the packed slot
+// of their source.
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
                        const void* H, const void* g1, float eps, int32_t* src, int32_t* packed_idx,
                        int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st,
-                       int32_t* n_hist = nullptr);
+                       int32_t* n_hist = nullptr, int32_t* dep_off = nullptr, int32_t* dep_rows = nullptr);
 // Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
                         int R, int d, const void* g, float eps, void* Y, cudaStream_t st);
@@ -70,6 +72,12 @@ struct GemmCall {
   float* partial;
   size_t partial_len;     // floats, >= gemm_partial_floats()
   uint32_t* status;
+  // RESID_SCATTER only, optional: fold-fill of the dependents of each packed
+  // row (dep_rows[dep_off[k] .. dep_off[k+1]) take Y[row_idx[k]] + hin[r] -
+  // hin[row_idx[k]]), run by the split finish kernel
+  const int32_t* dep_off;
+  const int32_t* dep_rows;
+  const void* hin;
 };
 size_t gemm_partial_floats();
 // Optional RMSNorm of the finished rows of an EPI_RESID_PACKED GEMM (the

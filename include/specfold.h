@@ -110,6 +110,8 @@ typedef struct {
   size_t src;          /* int32  [R] */
   size_t packed_idx;   /* int32  [R] (first n valid) */
   size_t slot_of_row;  /* int32  [R] (-1 for folded rows) */
+  size_t dep_off;      /* int32  [R+1] folded rows grouped by source slot: */
+  size_t dep_rows;     /* int32  [R]   dep_rows[dep_off[k] .. dep_off[k+1]) resolve to packed row k */
   size_t x1;           /* [R, d]        RMSNorm1 of packed rows */
   size_t q;            /* [n_kv, R*g, hd]  queries, head-group major */
   size_t block_k;      /* [R, n_kv, hd]  keys of recomputed rows (row r) */
