@@ -31,15 +31,6 @@ int num_sms() {
   return cached[dev];
 }
 
-// SPECFOLD_L2PF=0 in the environment turns the layer's L2 weight prefetch off.
-static bool l2pf_enabled() {
-  static const bool on = [] {
-    const char* e = std::getenv("SPECFOLD_L2PF");
-    return !(e && e[0] == '0');
-  }();
-  return on;
-}
-
 bool pdl_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("SPECFOLD_PDL");
@@ -147,8 +138,6 @@ static int check_view(const specfold_kv_view& v, int P) {
     if (_rc) return _rc;       \
   } while (0)
 
-// Bytes of the SwiGLU weights (gate + up) pulled into L2 during attention.
-static constexpr size_t kPrefetchFfnBytes = static_cast<size_t>(64) << 20;
 
 // ------------------------------------------------------ workspace layout --
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
@@ -257,7 +246,7 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
                            const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
                            const int32_t* n_dev, int B, int L, void* O, uint32_t* status, void* part,
-                           size_t part_bytes, cudaStream_t st, const L2Prefetch* prefetch = nullptr) {
+                           size_t part_bytes, cudaStream_t st) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
   a.Q = Q;
@@ -278,7 +267,6 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
   a.status = status;
   a.part = part;
   a.part_bytes = part_bytes;
-  if (prefetch) a.prefetch = *prefetch;
   return launch_attention(a, st);
 }
 
@@ -404,20 +392,9 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   auto mark = [&](int i) {
     if (stage_events) record_stage_event(stage_events[i], st);
   };
-  // L2 prefetch plan: the attention projections are pulled in while the
-  // (latency-bound) gate and pack run, the head of the SwiGLU weights while
-  // attention runs.  The layer still reads every weight byte from HBM once.
-  const size_t e = esize(dims->dtype);
-  const size_t d_ = dims->d_model;
-  const size_t nq = static_cast<size_t>(dims->n_q_heads) * dims->head_dim;
-  const size_t nkv = static_cast<size_t>(dims->n_kv_heads) * dims->head_dim;
-  const size_t ffn_head = std::min(static_cast<size_t>(dims->ffn_dim) * d_ * e, kPrefetchFfnBytes / 2);
-  L2Prefetch pf_gate = {{w->w_q, w->w_k, w->w_v, w->w_o},
-                        {nq * d_ * e, nkv * d_ * e, nkv * d_ * e, d_ * nq * e}};
-  L2Prefetch pf_attn = {{w->w_gate, w->w_up, nullptr, nullptr}, {ffn_head, ffn_head, 0, 0}};
   mark(0);
   SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
-                     l2pf_enabled() ? &pf_gate : nullptr, fold_hist));
+                     fold_hist));
   mark(1);
   SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
                             at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,
@@ -428,8 +405,7 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
-                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st,
-                         l2pf_enabled() ? &pf_attn : nullptr));
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
   mark(4);
   SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
                         at<void>(ws, lo.x2)));

@@ -53,7 +53,6 @@ struct AttnParams {
   int num_sms;
   float* part_o;    // [tiles_x * n_kv * sp_max][128][hd]
   float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
-  L2Prefetch pf;    // weights of the FFN, streamed into L2 during attention
 };
 
 // Number of key-range splits for n packed rows: enough CTAs to cover the SMs.
@@ -102,7 +101,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   volatile int* okflag = abort_flag + 1;  // [2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && warp == 0) issue_l2_prefetch(p.pf, lane);
   pdl_wait();
   pdl_trigger();
   const int h = blockIdx.y;
@@ -536,7 +534,6 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   const int tiles_x = (R * g + 127) / 128;
   p.sp_max = attn_sp_max(R, g, c.n_kv);
   p.num_sms = num_sms();
-  p.pf = c.prefetch;
   if (p.sp_max > 1) {
     if (!c.part || c.part_bytes < attn_partial_bytes(R, g, c.n_kv, HD)) return SPECFOLD_ECAPACITY;
     p.part_o = static_cast<float*>(c.part);

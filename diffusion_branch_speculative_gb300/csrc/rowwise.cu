@@ -49,12 +49,8 @@ constexpr int kRowWarps = 8;  // warps (rows) per block of the row kernels
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(kRowWarps * 32)
 gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d,
-            float tau, uint8_t* __restrict__ fold, float* __restrict__ rel, const L2Prefetch pf,
-            uint8_t* __restrict__ fold_hist) {
+            float tau, uint8_t* __restrict__ fold, float* __restrict__ rel, uint8_t* __restrict__ fold_hist) {
   using V = VecT<T>;
-  // weights of the next kernels start streaming into L2 while this
-  // latency-bound kernel and the pack run
-  if (blockIdx.x == 0 && threadIdx.x < 32) issue_l2_prefetch(pf, threadIdx.x);
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -410,24 +406,22 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
 }  // namespace
 
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
-                uint8_t* fold, float* rel, cudaStream_t st, const L2Prefetch* prefetch, uint8_t* fold_hist) {
-  L2Prefetch pf = {};
-  if (prefetch) pf = *prefetch;
+                uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist) {
   const int R = B * L;
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
   const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
   if (dtype == SPECFOLD_BF16) {
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
     if (per_lane <= 8)
-      launch_k(gate_kernel<__nv_bfloat16, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
+      launch_k(gate_kernel<__nv_bfloat16, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
     else
-      launch_k(gate_kernel<__nv_bfloat16, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
+      launch_k(gate_kernel<__nv_bfloat16, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
   } else {
     const float* h = static_cast<const float*>(H);
     if (per_lane <= 8)
-      launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
+      launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
     else
-      launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, pf, fold_hist);
+      launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
   }
   count_launch();
   return check_launch();

@@ -73,29 +73,6 @@ SF_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32
   }
 }
 
-// L2 prefetch of up to four byte ranges (weights a later kernel of the layer
-// will stream), issued by one warp as bulk prefetches of at most 1 MiB each.
-// It only moves data into L2 early: nothing waits for it.
-struct L2Prefetch {
-  const void* ptr[4];
-  unsigned long long bytes[4];
-};
-SF_DEV void issue_l2_prefetch(const L2Prefetch& pf, int lane) {
-  constexpr unsigned long long kChunk = 1ull << 20;
-#pragma unroll 1
-  for (int r = 0; r < 4; ++r) {
-    const char* base = static_cast<const char*>(pf.ptr[r]);
-    const unsigned long long bytes = pf.bytes[r];
-    if (!base || bytes < 16) continue;
-    const unsigned long long chunks = (bytes + kChunk - 1) / kChunk;
-    for (unsigned long long c = lane; c < chunks; c += 32) {
-      const unsigned long long off = c * kChunk;
-      const unsigned long long left = bytes - off;
-      const uint32_t sz = static_cast<uint32_t>((left < kChunk ? left : kChunk) & ~15ull);
-      if (sz) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(sz) : "memory");
-    }
-  }
-}
 
 // Programmatic dependent launch: every kernel of the library waits for the
 // grids it depends on before touching their outputs (griddepcontrol.wait is a

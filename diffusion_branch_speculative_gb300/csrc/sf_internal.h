@@ -20,8 +20,7 @@ int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a l
 // gate: fold/rel per row; dtype bf16 or f32.  fold_hist (optional) receives
 // a second copy of the decisions.
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
-                uint8_t* fold, float* rel, cudaStream_t st, const struct L2Prefetch* prefetch = nullptr,
-                uint8_t* fold_hist = nullptr);
+                uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
 // given); parent may be null (pack alone); any output may be null.  n_hist
 // (optional) receives a second copy of the packed-row count; dep_off [R+1] /
@@ -104,7 +103,6 @@ struct AttnCall {
   uint32_t* status;
   void* part;             // split-KV partials (attn_partial_bytes)
   size_t part_bytes;
-  L2Prefetch prefetch;    // optional: weights to pull into L2 meanwhile
 };
 int attn_sp_max(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);
