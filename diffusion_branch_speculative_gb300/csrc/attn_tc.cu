@@ -55,11 +55,12 @@ struct AttnParams {
   float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
 };
 
-// Number of key-range splits for n packed rows: enough CTAs to cover the SMs.
+// Number of key-range splits for n packed rows: as many CTAs as fit on the
+// SMs in one wave (one CTA per SM: a second wave would double the time).
 SF_DEV int attn_splits(int rows_total, int n_kv, int sp_max, int num_sms) {
   const int tiles = ((rows_total + 127) / 128) * n_kv;
   if (tiles <= 0) return 1;
-  return max(1, min(sp_max, (num_sms + tiles - 1) / tiles));
+  return max(1, min(sp_max, num_sms / tiles));
 }
 
 template <int HD>
