@@ -74,6 +74,21 @@ def softmax_rows(s: np.ndarray) -> np.ndarray:
 # S1 gate
 # ---------------------------------------------------------------------------
 
+def rope(x: np.ndarray, pos, theta: float) -> np.ndarray:
+    """Rotary position embedding in the rotate-half convention (the one of the
+    Qwen/Llama model families): for j < hd/2 the pair (x[j], x[j + hd/2]) is
+    rotated by the angle pos * theta^(-2j/hd).  x [..., hd] (last axis one
+    head); pos broadcasts against x[..., 0]."""
+    x = np.asarray(x, F64)
+    hd = x.shape[-1]
+    half = hd // 2
+    freq = float(theta) ** (-2.0 * np.arange(half) / hd)
+    ang = np.asarray(pos, F64)[..., None] * freq
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
 def gate(H: np.ndarray, parent: np.ndarray, tau: float,
          force: Optional[np.ndarray] = None):
     """Per (branch b, position i): fold flag and relative difference.
@@ -193,7 +208,7 @@ def attention_rows(q_rows: np.ndarray, branch_of_row: np.ndarray, kv_src: np.nda
 
 
 def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
-                  force=None, rows: Optional[Iterable[int]] = None) -> dict:
+                  force=None, rows: Optional[Iterable[int]] = None, rope_theta: float = 0.0) -> dict:
     """Folded layer over all branches, in the packed order.
 
     With ``rows`` given, only those output rows are produced (plus what they
@@ -204,6 +219,10 @@ def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
     computed rows (increasing row id, listed in "act_rows"): X1, Q, attnO, A,
     X2, G, out_act; K/V per source row; and "out" for the requested rows
     (in "out_rows" order).
+
+    rope_theta > 0 rotates the queries and the block keys (``rope``, position
+    P + i for block position i); the prefix keys are taken as already
+    rotated, as a KV cache stores them.  Values are never rotated.
     """
     H = np.asarray(H, F64)
     B, L, d = H.shape
@@ -224,11 +243,17 @@ def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
     Xk = np.stack([X1[r] for r in kv_need])
     Kp = Xk @ wk.T
     Vp = Xk @ wv.T
+    P = np.asarray(prefK).shape[0]
     K_rows = {r: Kp[t].reshape(n_kv, hd) for t, r in enumerate(kv_need)}
+    if rope_theta > 0:
+        K_rows = {r: rope(k, P + r % L, rope_theta) for r, k in K_rows.items()}
     V_rows = {r: Vp[t].reshape(n_kv, hd) for t, r in enumerate(kv_need)}
     Xa = np.stack([X1[r] for r in act])
     Q = Xa @ wq.T
     n_q = Q.shape[1] // hd
+    if rope_theta > 0:
+        pos = np.array([P + r % L for r in act], F64)[:, None]
+        Q = rope(Q.reshape(len(act), n_q, hd), pos, rope_theta).reshape(len(act), n_q * hd)
     # S5: attention over prefix + own branch block
     attnO = attention_rows(Q.reshape(len(act), n_q, hd), np.array([r // L for r in act]),
                            kv_src, K_rows, V_rows, prefK, prefV, n_kv)
@@ -257,13 +282,17 @@ def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
 # modes used as cross-checks
 # ---------------------------------------------------------------------------
 
-def dense_branch_forward(Hb, W, prefK, prefV, eps, n_kv, hd) -> np.ndarray:
+def dense_branch_forward(Hb, W, prefK, prefV, eps, n_kv, hd, rope_theta: float = 0.0) -> np.ndarray:
     """Plain pre-norm layer over one branch's L rows with no folding."""
     Hb = np.asarray(Hb, F64)
     L, d = Hb.shape
     x = rmsnorm(Hb, W["g1"], eps)
     q = (x @ _w(W, "w_q").T).reshape(L, -1, hd)
     k = (x @ _w(W, "w_k").T).reshape(L, n_kv, hd)
+    if rope_theta > 0:
+        pos = np.asarray(prefK).shape[0] + np.arange(L, dtype=F64)[:, None]
+        q = rope(q, pos, rope_theta)
+        k = rope(k, pos, rope_theta)
     v = (x @ _w(W, "w_v").T).reshape(L, n_kv, hd)
     keys = np.concatenate([np.asarray(prefK, F64), k], axis=0)
     vals = np.concatenate([np.asarray(prefV, F64), v], axis=0)
@@ -279,7 +308,8 @@ def dense_branch_forward(Hb, W, prefK, prefV, eps, n_kv, hd) -> np.ndarray:
     return A + G @ _w(W, "w_down").T
 
 
-def layer_serialized(H, parent, W, prefK, prefV, tau, eps, n_kv, hd, force=None) -> np.ndarray:
+def layer_serialized(H, parent, W, prefK, prefV, tau, eps, n_kv, hd, force=None,
+                     rope_theta: float = 0.0) -> np.ndarray:
     """Serialized evaluation: one row at a time, straight from the definition,
     with no packed batch and no scan (the check the SpecFold authors describe
     in their appendix C).  Small inputs only.  Returns out [B, L, d]."""
@@ -289,9 +319,14 @@ def layer_serialized(H, parent, W, prefK, prefV, tau, eps, n_kv, hd, force=None)
     g1 = W["g1"]
     cache: Dict[int, np.ndarray] = {}
 
+    P = np.asarray(prefK).shape[0]
+
     def kv_of(r):
         x = rmsnorm(H.reshape(B * L, d)[r], g1, eps)
-        return ((x @ _w(W, "w_k").T).reshape(n_kv, hd), (x @ _w(W, "w_v").T).reshape(n_kv, hd))
+        k = (x @ _w(W, "w_k").T).reshape(n_kv, hd)
+        if rope_theta > 0:
+            k = rope(k, P + r % L, rope_theta)
+        return (k, (x @ _w(W, "w_v").T).reshape(n_kv, hd))
 
     def computed_out(b, i):
         r = b * L + i
@@ -300,6 +335,8 @@ def layer_serialized(H, parent, W, prefK, prefV, tau, eps, n_kv, hd, force=None)
         h = H[b, i]
         x = rmsnorm(h, g1, eps)
         q = (x @ _w(W, "w_q").T).reshape(-1, hd)
+        if rope_theta > 0:
+            q = rope(q, P + i, rope_theta)
         n_q = q.shape[0]
         g = n_q // n_kv
         ks, vs = [], []
@@ -345,7 +382,7 @@ def near_tau_rows(rel: np.ndarray, tau: float, frac: float = 1e-4) -> np.ndarray
 # release; appendix D: how the recompute fraction evolves with depth)
 # ---------------------------------------------------------------------------
 
-def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None) -> dict:
+def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None, rope_theta: float = 0.0) -> dict:
     """A stack of folded layers: layer l's output is layer l+1's input.
 
     ``layers`` is a sequence of (W, prefK, prefV), one per layer.  Each layer
@@ -365,7 +402,7 @@ def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None) -> dict:
     inputs, folds, rels, ns = [], [], [], []
     for (W, pk, pv) in layers:
         inputs.append(X)
-        res = layer_forward(X, parent, W, pk, pv, tau, eps, n_kv, hd)
+        res = layer_forward(X, parent, W, pk, pv, tau, eps, n_kv, hd, rope_theta=rope_theta)
         folds.append(res["fold"])
         rels.append(res["rel"])
         ns.append(int(res["n"]))
