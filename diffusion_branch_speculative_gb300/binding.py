@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libspecfold.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "specfold.h")
 
 OK, EINVAL, EALIGN, ECAPACITY, EUNSUPPORTED, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6
-DEV_TIMEOUT, DEV_BAD_PARENT = 1, 2
+DEV_TIMEOUT, DEV_BAD_PARENT, DEV_BAD_PAGE = 1, 2, 4
 BF16, F32 = 0, 1
 STAGE_EVENTS = 9
 STAGE_NAMES = ("gate", "select_pack", "qkv", "attention", "out_proj_norm", "gate_up", "down", "fold_fill")
@@ -34,7 +34,7 @@ class SpecfoldError(RuntimeError):
 class specfold_dims(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("rope_theta", ctypes.c_float)]
 
 
 class specfold_weights(ctypes.Structure):
@@ -43,7 +43,8 @@ class specfold_weights(ctypes.Structure):
 
 
 class specfold_kv_view(ctypes.Structure):
-    _fields_ = [("ptr", ctypes.c_void_p), ("token_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64)]
+    _fields_ = [("ptr", ctypes.c_void_p), ("token_stride", ctypes.c_int64), ("head_stride", ctypes.c_int64),
+                ("block_table", ctypes.c_void_p), ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
 class specfold_ws_layout(ctypes.Structure):
@@ -63,6 +64,7 @@ _SIG = {
     "specfold_resolve": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "specfold_pack": (_I, [_I, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _P]),
     "specfold_qkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "specfold_rope": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P]),
     "specfold_attention": (_I, [_P, _P, specfold_kv_view, specfold_kv_view, _I, _P, _P, _P, _P, _P, _I, _I,
                                 _P, _P, ctypes.c_size_t, _P]),
     "specfold_out_proj": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
@@ -143,8 +145,8 @@ def dtype_code(t: torch.dtype) -> int:
     raise ValueError(f"unsupported dtype {t}")
 
 
-def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16) -> specfold_dims:
-    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype)
+def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16, rope_theta=0.0) -> specfold_dims:
+    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype, rope_theta)
 
 
 def make_weights(w: dict) -> specfold_weights:
@@ -152,12 +154,33 @@ def make_weights(w: dict) -> specfold_weights:
                               ("g1", "w_q", "w_k", "w_v", "w_o", "g2", "w_gate", "w_up", "w_down")])
 
 
-def kv_view(t: Optional[torch.Tensor]) -> specfold_kv_view:
-    """A [P, n_kv, hd] strided view (last dim contiguous), passed without copy."""
+class PagedPrefix:
+    """A paged prefix K or V: `pool` is [num_pages * page_size, n_kv, hd]
+    (unit last stride), `block_table` int32 on the device, P the prefix
+    length (the attention reads prefix token t from pool token
+    block_table[t // page_size] * page_size + t % page_size)."""
+
+    def __init__(self, pool: torch.Tensor, block_table: torch.Tensor, page_size: int, P: int):
+        assert pool.dim() == 3 and pool.stride(2) == 1
+        assert pool.shape[0] % page_size == 0
+        self.pool, self.block_table, self.page_size, self.P = pool, block_table, int(page_size), int(P)
+        self.shape = (self.P,) + tuple(pool.shape[1:])
+
+    def view(self) -> "specfold_kv_view":
+        p = self.pool
+        return specfold_kv_view(p.data_ptr(), p.stride(0), p.stride(1), self.block_table.data_ptr(), self.page_size,
+                                p.shape[0] // self.page_size)
+
+
+def kv_view(t) -> specfold_kv_view:
+    """A [P, n_kv, hd] strided view (last dim contiguous), passed without
+    copy, or a PagedPrefix."""
+    if isinstance(t, PagedPrefix):
+        return t.view()
     if t is None or t.numel() == 0:
-        return specfold_kv_view(None, 8, 8)
+        return specfold_kv_view(None, 8, 8, None, 0, 0)
     assert t.dim() == 3 and t.stride(2) == 1, "prefix view must be [P, n_kv, hd] with unit last stride"
-    return specfold_kv_view(t.data_ptr(), t.stride(0), t.stride(1))
+    return specfold_kv_view(t.data_ptr(), t.stride(0), t.stride(1), None, 0, 0)
 
 
 def workspace_size(dims: specfold_dims, B: int, L: int) -> int:
@@ -201,6 +224,11 @@ def specfold_qkv(dims, weights, X1, packed_idx, n_dev, B, L, Q, blockK, blockV, 
     _check(lib().specfold_qkv(ctypes.byref(dims), ctypes.byref(weights), _ptr(X1), _ptr(packed_idx), _ptr(n_dev),
                               B, L, _ptr(Q), _ptr(blockK), _ptr(blockV), _ptr(ws), ws.numel(), _stream(stream)),
            "specfold_qkv")
+
+
+def specfold_rope(dims, Q, blockK, packed_idx, n_dev, B, L, P, stream=None):
+    _check(lib().specfold_rope(ctypes.byref(dims), _ptr(Q), _ptr(blockK), _ptr(packed_idx), _ptr(n_dev), B, L, P,
+                               _stream(stream)), "specfold_rope")
 
 
 def specfold_attention(dims, Q, prefK, prefV, P, blockK, blockV, src, packed_idx, n_dev, B, L, O, ws, stream=None):

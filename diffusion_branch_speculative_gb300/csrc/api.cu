@@ -89,6 +89,12 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t dim, uint64_t heads
 }
 
 // ------------------------------------------------------------- checks --
+#define SF_TRY(x)              \
+  do {                         \
+    const int _rc = (x);       \
+    if (_rc) return _rc;       \
+  } while (0)
+
 static bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static int esize(int dtype) { return dtype == SPECFOLD_BF16 ? 2 : 4; }
 static bool dtype_ok(int dtype) { return dtype == SPECFOLD_BF16 || dtype == SPECFOLD_F32; }
@@ -105,6 +111,7 @@ static int check_dims(const specfold_dims* d) {
   if (d->d_model <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 || d->ffn_dim <= 0)
     return SPECFOLD_EINVAL;
   if (!(d->rms_eps >= 0.f) || std::isinf(d->rms_eps)) return SPECFOLD_EINVAL;
+  if (!(d->rope_theta >= 0.f) || std::isinf(d->rope_theta)) return SPECFOLD_EINVAL;
   if (d->head_dim != 64 && d->head_dim != 128) return SPECFOLD_EUNSUPPORTED;
   if (d->n_q_heads % d->n_kv_heads) return SPECFOLD_EUNSUPPORTED;
   if (d->d_model % 256) return SPECFOLD_EUNSUPPORTED;
@@ -129,14 +136,22 @@ static int check_view(const specfold_kv_view& v, int P) {
   if (!a16(v.ptr)) return SPECFOLD_EALIGN;
   if (v.token_stride <= 0 || v.head_stride <= 0) return SPECFOLD_EINVAL;
   if (v.token_stride % 8 || v.head_stride % 8) return SPECFOLD_EALIGN;
+  if (v.block_table) {
+    if (v.page_size <= 0 || v.num_pages <= 0) return SPECFOLD_EINVAL;
+    if (v.page_size % 8) return SPECFOLD_EUNSUPPORTED;
+  }
   return SPECFOLD_OK;
 }
 
-#define SF_TRY(x)              \
-  do {                         \
-    const int _rc = (x);       \
-    if (_rc) return _rc;       \
-  } while (0)
+// K and V of one call are both contiguous or both paged over one table.
+static int check_views(const specfold_kv_view& k, const specfold_kv_view& v, int P) {
+  SF_TRY(check_view(k, P));
+  SF_TRY(check_view(v, P));
+  if (P > 0 && (k.block_table != v.block_table || (k.block_table && k.page_size != v.page_size)))
+    return SPECFOLD_EINVAL;
+  return SPECFOLD_OK;
+}
+
 
 
 // ------------------------------------------------------ workspace layout --
@@ -365,8 +380,7 @@ static int check_layer_call(const specfold_dims* dims, const specfold_weights* w
   if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!H_in || !parent || !H_out || !ws || P < 0) return SPECFOLD_EINVAL;
   if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
-  SF_TRY(check_view(prefK, P));
-  SF_TRY(check_view(prefV, P));
+  SF_TRY(check_views(prefK, prefV, P));
   if (!a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
   return SPECFOLD_OK;
 }
@@ -402,6 +416,9 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   mark(2);
   SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
                    at<void>(ws, lo.block_v), s, status, st));
+  if (dims->rope_theta > 0.f)
+    SF_TRY(launch_rope(at<void>(ws, lo.q), at<void>(ws, lo.block_k), pidx, n_dev, R, L, P, dims->n_q_heads,
+                       dims->n_kv_heads, dims->head_dim, dims->rope_theta, st));
   mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
@@ -492,6 +509,18 @@ int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const voi
                    static_cast<cudaStream_t>(stream));
 }
 
+int specfold_rope(const specfold_dims* dims, void* Q, void* blockK, const int32_t* packed_idx, const int32_t* n_dev,
+                  int B, int L, int P, void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
+  if (!Q || !blockK || !packed_idx || !n_dev || P < 0) return SPECFOLD_EINVAL;
+  if (!a16(Q) || !a16(blockK)) return SPECFOLD_EALIGN;
+  if (dims->rope_theta == 0.f) return SPECFOLD_OK;
+  return launch_rope(Q, blockK, packed_idx, n_dev, B * L, L, P, dims->n_q_heads, dims->n_kv_heads, dims->head_dim,
+                     dims->rope_theta, static_cast<cudaStream_t>(stream));
+}
+
 int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_view prefK, specfold_kv_view prefV,
                        int P, const void* blockK, const void* blockV, const int32_t* src, const int32_t* packed_idx,
                        const int32_t* n_dev, int B, int L, void* O, void* ws, size_t ws_bytes, void* stream) {
@@ -499,8 +528,7 @@ int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_vie
   SF_TRY(check_rows(B, L));
   if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (P < 0 || !Q || !blockK || !blockV || !src || !packed_idx || !n_dev || !O || !ws) return SPECFOLD_EINVAL;
-  SF_TRY(check_view(prefK, P));
-  SF_TRY(check_view(prefV, P));
+  SF_TRY(check_views(prefK, prefV, P));
   if (!a16(Q) || !a16(blockK) || !a16(blockV) || !a16(O)) return SPECFOLD_EALIGN;
   specfold_ws_layout lo;
   layout(dims, B, L, &lo);

@@ -51,6 +51,13 @@ struct AttnParams {
   // an unnormalised partial (o, running max m in log2 units, sum l)
   int sp_max;
   int num_sms;
+  // paged prefix (table != null): whole 128-key blocks inside one page go
+  // through TMA over the pool, the rest through plain gathers
+  const int32_t* table;
+  int page_size, num_pages, page_tma;
+  const __nv_bfloat16* pkp;  // prefix K / V base (pool or contiguous view)
+  const __nv_bfloat16* pvp;
+  long long k_ts, k_hs, v_ts, v_hs;  // token and head strides, elements
   float* part_o;    // [tiles_x * n_kv * sp_max][128][hd]
   float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
 };
@@ -182,33 +189,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       if (!okflag[st]) break;
       uint8_t* sK = smem + C::OFF_KV + (2 * st) * C::KV_BYTES;
       uint8_t* sV = sK + C::KV_BYTES;
-      if (j < NBP) {
+      // prefix blocks go through TMA unless paged with the block not inside
+      // one page or not whole (pool tokens past P may hold anything)
+      const bool use_tma = j < NBP && (!p.table || (p.page_tma && (j + 1) * 128 <= p.P));
+      if (use_tma) {
         if (lt == 0) {
+          int z = j * 128;
+          if (p.table) {
+            const int page = p.table[(j * 128) / p.page_size];
+            if (page >= 0 && page < p.num_pages) {
+              z = page * p.page_size + (j * 128) % p.page_size;
+            } else {
+              z = p.num_pages * p.page_size;  // wholly past the pool: the box reads zeros
+              atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
+            }
+          }
           const uint32_t fb = smem_u32(&kv_full[st]);
           mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
           for (int a = 0; a < C::NATOM; ++a) {
-            tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, j * 128);
-            tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, j * 128);
+            tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, z);
+            tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, z);
           }
           issued_tma = t;
         }
       } else {
         for (int kr = lt; kr < 128; kr += kLoaders) {
-          const int e = (j - NBP) * 128 + kr;
           int bb = -1;
           const uint4* krow = nullptr;
           const uint4* vrow = nullptr;
-          if (e < keys_blk) {
-            const int b = b_lo + e / L;
-            const int s = p.src[b * L + (e - (e / L) * L)];
-            if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
-              bb = b;
-              const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
-              krow = reinterpret_cast<const uint4*>(p.bK + off);
-              vrow = reinterpret_cast<const uint4*>(p.bV + off);
+          if (j < NBP) {  // paged prefix token
+            const int tk = j * 128 + kr;
+            if (tk < p.P) {
+              const int page = p.table[tk / p.page_size];
+              if (page >= 0 && page < p.num_pages) {
+                const size_t tok = static_cast<size_t>(page) * p.page_size + tk % p.page_size;
+                krow = reinterpret_cast<const uint4*>(p.pkp + tok * p.k_ts + static_cast<size_t>(h) * p.k_hs);
+                vrow = reinterpret_cast<const uint4*>(p.pvp + tok * p.v_ts + static_cast<size_t>(h) * p.v_hs);
+              } else {
+                atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
+              }
             }
+          } else {
+            const int e = (j - NBP) * 128 + kr;
+            if (e < keys_blk) {
+              const int b = b_lo + e / L;
+              const int s = p.src[b * L + (e - (e / L) * L)];
+              if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
+                bb = b;
+                const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
+                krow = reinterpret_cast<const uint4*>(p.bK + off);
+                vrow = reinterpret_cast<const uint4*>(p.bV + off);
+              }
+            }
+            meta[st * 128 + kr] = bb;
           }
-          meta[st * 128 + kr] = bb;
 #pragma unroll
           for (int c16 = 0; c16 < HD / 8; ++c16) {
             const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
@@ -513,10 +547,25 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   int rc = make_map_2d(&p.mapQ, c.Q, static_cast<uint64_t>(c.n_kv) * R * g, HD, HD, 128);
   if (rc) return rc;
   if (c.P > 0) {
-    rc = make_map_3d(&p.mapK, c.pk.ptr, HD, c.n_kv, c.P, c.pk.head_stride, c.pk.token_stride, 128);
+    // contiguous: the map spans the P prefix tokens; paged: the whole pool
+    const uint64_t tokens = c.pk.block_table ? static_cast<uint64_t>(c.pk.num_pages) * c.pk.page_size : c.P;
+    const uint64_t vtokens = c.pv.block_table ? static_cast<uint64_t>(c.pv.num_pages) * c.pv.page_size : c.P;
+    rc = make_map_3d(&p.mapK, c.pk.ptr, HD, c.n_kv, tokens, c.pk.head_stride, c.pk.token_stride, 128);
     if (rc) return rc;
-    rc = make_map_3d(&p.mapV, c.pv.ptr, HD, c.n_kv, c.P, c.pv.head_stride, c.pv.token_stride, 128);
+    rc = make_map_3d(&p.mapV, c.pv.ptr, HD, c.n_kv, vtokens, c.pv.head_stride, c.pv.token_stride, 128);
     if (rc) return rc;
+    if (c.pk.block_table) {
+      p.table = c.pk.block_table;
+      p.page_size = c.pk.page_size;
+      p.num_pages = std::min(c.pk.num_pages, c.pv.num_pages);
+      p.page_tma = c.pk.page_size % 128 == 0 ? 1 : 0;
+    }
+    p.pkp = static_cast<const __nv_bfloat16*>(c.pk.ptr);
+    p.pvp = static_cast<const __nv_bfloat16*>(c.pv.ptr);
+    p.k_ts = c.pk.token_stride;
+    p.k_hs = c.pk.head_stride;
+    p.v_ts = c.pv.token_stride;
+    p.v_hs = c.pv.head_stride;
   }
   p.bK = static_cast<const __nv_bfloat16*>(c.blockK);
   p.bV = static_cast<const __nv_bfloat16*>(c.blockV);

@@ -2,6 +2,8 @@
 // resolve + pack scan (S2, S3), the RMSNorm gathers (S3, S7) and the fold-fill
 // of folded rows (S10).  All are HBM-bound: one warp per row, 16-byte
 // vectorised coalesced loads, fp32 warp-shuffle reductions.
+#include <algorithm>
+
 #include "sf_device.cuh"
 #include "sf_internal.h"
 
@@ -386,6 +388,64 @@ fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ s
   }
 }
 
+// ------------------------------------------------------------- S4b rope --
+// One thread per (packed row, head, 8 rotation pairs).  Q: [n_kv][R*g][hd]
+// (row k*g + j of KV head h holds query head h*g + j of packed row k);
+// block keys: [R][n_kv][hd] at row packed_idx[k].  Frequencies are computed
+// once per block in double and rounded to float; angles and sincosf in fp32.
+__global__ void __launch_bounds__(256)
+rope_kernel(__nv_bfloat16* __restrict__ Q, __nv_bfloat16* __restrict__ Kb, const int32_t* __restrict__ packed_idx,
+            const int32_t* __restrict__ n_dev, int R, int L, int P, int n_q, int n_kv, int hd, float theta) {
+  __shared__ float s_freq[64];
+  pdl_wait();
+  pdl_trigger();
+  const int half = hd / 2;
+  for (int j = threadIdx.x; j < half; j += blockDim.x)
+    s_freq[j] = static_cast<float>(pow(static_cast<double>(theta), -2.0 * j / hd));
+  __syncthreads();
+  const int n = min(max(n_dev[0], 0), R);
+  const int g = n_q / n_kv;
+  const int heads = n_q + n_kv;
+  const int G8 = half / 8;
+  const long long total = static_cast<long long>(n) * heads * G8;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(idx / (heads * G8));
+    const int rem = static_cast<int>(idx - static_cast<long long>(k) * heads * G8);
+    const int h = rem / G8;
+    const int j0 = (rem - h * G8) * 8;
+    const int r = packed_idx[k];
+    if (r < 0 || r >= R) continue;
+    const float pos = static_cast<float>(P + r % L);
+    __nv_bfloat16* row;
+    if (h < n_q) {
+      const int hk = h / g, hg = h - hk * g;
+      row = Q + ((static_cast<size_t>(hk) * R + k) * g + hg) * hd;
+    } else {
+      row = Kb + (static_cast<size_t>(r) * n_kv + (h - n_q)) * hd;
+    }
+    uint4* p1 = reinterpret_cast<uint4*>(row + j0);
+    uint4* p2 = reinterpret_cast<uint4*>(row + half + j0);
+    const uint4 a = *p1, b = *p2;
+    float x1[8], x2[8], y1[8], y2[8];
+    x1[0] = bf16lo(a.x); x1[1] = bf16hi(a.x); x1[2] = bf16lo(a.y); x1[3] = bf16hi(a.y);
+    x1[4] = bf16lo(a.z); x1[5] = bf16hi(a.z); x1[6] = bf16lo(a.w); x1[7] = bf16hi(a.w);
+    x2[0] = bf16lo(b.x); x2[1] = bf16hi(b.x); x2[2] = bf16lo(b.y); x2[3] = bf16hi(b.y);
+    x2[4] = bf16lo(b.z); x2[5] = bf16hi(b.z); x2[6] = bf16lo(b.w); x2[7] = bf16hi(b.w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float sn, cs;
+      sincosf(pos * s_freq[j0 + e], &sn, &cs);
+      y1[e] = x1[e] * cs - x2[e] * sn;
+      y2[e] = x2[e] * cs + x1[e] * sn;
+    }
+    *p1 = make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]), pack_bf16x2(y1[4], y1[5]),
+                     pack_bf16x2(y1[6], y1[7]));
+    *p2 = make_uint4(pack_bf16x2(y2[0], y2[1]), pack_bf16x2(y2[2], y2[3]), pack_bf16x2(y2[4], y2[5]),
+                     pack_bf16x2(y2[6], y2[7]));
+  }
+}
+
 // ------------------------------------------------------ bounded-wait probe --
 __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -404,6 +464,16 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
 }
 
 }  // namespace
+
+int launch_rope(void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P, int n_q,
+                int n_kv, int hd, float theta, cudaStream_t st) {
+  const long long total = static_cast<long long>(R) * (n_q + n_kv) * (hd / 16);
+  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * num_sms()));
+  launch_k(rope_kernel, dim3(std::max(grid, 1)), dim3(256), 0, st, static_cast<__nv_bfloat16*>(Q),
+           static_cast<__nv_bfloat16*>(Kb), packed_idx, n_dev, R, L, P, n_q, n_kv, hd, theta);
+  count_launch();
+  return check_launch();
+}
 
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
                 uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist) {

@@ -37,6 +37,9 @@ int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int3
 int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const void* H_in,
                      void* H_out, int R, int d, cudaStream_t st);
 int launch_timeout_probe(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
+// Rotary embedding of the packed rows' queries and block keys in place (bf16).
+int launch_rope(void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P, int n_q,
+                int n_kv, int hd, float theta, cudaStream_t st);
 
 // ---- tcgen05 GEMM (gemm_tc.cu) ----
 enum GemmEpi : int {

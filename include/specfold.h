@@ -59,6 +59,7 @@ extern "C" {
 /* ---- device status bits (specfold_get_status) ---- */
 #define SPECFOLD_DEV_TIMEOUT    1u  /* a bounded wait inside a kernel ran out; outputs invalid */
 #define SPECFOLD_DEV_BAD_PARENT 2u  /* parent[b] outside [0, b) for b > 0, or parent[0] != -1 */
+#define SPECFOLD_DEV_BAD_PAGE   4u  /* a paged prefix view's block table names a page outside the pool */
 
 #define SPECFOLD_MAX_ROWS 16384     /* largest B*L */
 
@@ -76,6 +77,7 @@ typedef struct {
   int ffn_dim;      /* SwiGLU inner width F */
   float rms_eps;    /* RMSNorm epsilon (>= 0) */
   int dtype;        /* specfold_dtype */
+  float rope_theta; /* rotary embedding base; 0 = no positional rotation inside the layer */
 } specfold_dims;
 
 /* Layer weights (device, [out, in] row-major, dims.dtype). */
@@ -91,13 +93,26 @@ typedef struct {
   const void* w_down;  /* [d, F] */
 } specfold_weights;
 
-/* Zero-copy strided view of the shared prefix K (or V): element
- * (token t, kv head h, dim j) is ptr[t*token_stride + h*head_stride + j].
- * Any slice of a larger (e.g. fused K/V) cache can be passed without a copy. */
+/* Zero-copy view of the shared prefix K (or V).
+ * Contiguous (block_table == NULL): element (token t, kv head h, dim j) is
+ * ptr[t*token_stride + h*head_stride + j].  Any slice of a larger (e.g.
+ * fused K/V) cache can be passed without a copy.
+ * Paged (block_table != NULL): ptr is a pool of num_pages pages of page_size
+ * tokens; prefix token t lives in pool token
+ * block_table[t / page_size] * page_size + t % page_size, i.e. at
+ * ptr[(that pool token)*token_stride + h*head_stride + j].  The table
+ * (device int32, ceil(P / page_size) entries) is shared by K and V: both
+ * views of a call must give the same table and page size.  page_size is a
+ * multiple of 8; a page id outside [0, num_pages) reads as zeros and sets
+ * SPECFOLD_DEV_BAD_PAGE.  Pool tokens past P are never used, whatever they
+ * hold. */
 typedef struct {
   const void* ptr;
   int64_t token_stride;   /* elements, multiple of 8 */
   int64_t head_stride;    /* elements, multiple of 8 */
+  const int32_t* block_table;  /* NULL: contiguous view */
+  int32_t page_size;      /* tokens per page (paged only) */
+  int32_t num_pages;      /* pages in the pool (paged only) */
 } specfold_kv_view;
 
 /* Byte offsets of the intermediates inside a layer workspace (for
@@ -172,6 +187,19 @@ int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1,
 int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const void* X1,
                  const int32_t* packed_idx, const int32_t* n_dev, int B, int L,
                  void* Q, void* blockK, void* blockV, void* ws, size_t ws_bytes, void* stream);
+
+/* S4b rotary position embedding (rotate-half convention of the Qwen/Llama
+ * families; the pages put no positional encoding inside the layer, so this
+ * is the real-model follow-on).  Only when dims->rope_theta > 0: the queries
+ * of every packed row k < n and the block keys of its row r = packed_idx[k]
+ * are rotated in place, block position i = r % L sitting at absolute
+ * position P + i: for j < hd/2 the pair (x[j], x[j + hd/2]) turns by the
+ * angle (P + i) * rope_theta^(-2j/hd).  The prefix keys are taken as already
+ * rotated (a KV cache stores them so); values are never rotated.  Q and
+ * blockK use the layouts of specfold_qkv.  Returns SPECFOLD_OK without
+ * launching anything when rope_theta == 0. */
+int specfold_rope(const specfold_dims* dims, void* Q, void* blockK, const int32_t* packed_idx,
+                  const int32_t* n_dev, int B, int L, int P, void* stream);
 
 /* S5 folded attention.  Explainer, implementation note: FlashAttention-style
  * streaming with GQA; the shared prefix K/V is read through the strided view

@@ -29,10 +29,10 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 class DeviceInputs:
-    def __init__(self, inp: synth.LayerInputs, device="cuda"):
+    def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0):
         self.inp = inp
         d = inp.dims
-        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, rope_theta)
         self.H = bf16(inp.H, device)
         self.parent = torch.from_numpy(inp.parent.astype(np.int32)).to(device)
         self.W = {k: bf16(v, device) for k, v in inp.weights.items()}
@@ -76,7 +76,8 @@ def read_intermediates(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
     return res
 
 
-def oracle_with_gpu_decisions(inp: synth.LayerInputs, tau: float, gpu_fold: np.ndarray, rows=None):
+def oracle_with_gpu_decisions(inp: synth.LayerInputs, tau: float, gpu_fold: np.ndarray, rows=None,
+                              rope_theta: float = 0.0):
     """Run the oracle; rows within NEAR_TAU of tau take the GPU's decision
     (spec rule: such rows are reported and excluded from decision
     parity).  Returns (oracle result, number of near-tau rows, mismatches
@@ -89,16 +90,16 @@ def oracle_with_gpu_decisions(inp: synth.LayerInputs, tau: float, gpu_fold: np.n
     bad = (gf != f0) & ~near
     force = np.where(near, gf.astype(np.int8), np.int8(-1)).astype(np.int8)
     res = orc.layer_forward(inp.H, inp.parent, inp.weights, inp.prefix.K, inp.prefix.V, float(np.float32(tau)),
-                            d.eps, d.n_kv, d.hd, force=force, rows=rows)
+                            d.eps, d.n_kv, d.hd, force=force, rows=rows, rope_theta=rope_theta)
     return res, int(near.sum()), int(bad.sum())
 
 
-def check_layer(inp, tau, rows=None, inter=True):
-    dev = DeviceInputs(inp)
+def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0):
+    dev = DeviceInputs(inp, rope_theta=rope_theta)
     lay, out = run_layer(dev, tau)
     assert lay.status() == 0
     gi = read_intermediates(lay, dev)
-    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows)
+    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows, rope_theta=rope_theta)
     assert n_bad == 0, f"{n_bad} gate decisions differ away from tau"
     B, L, D = inp.H.shape
     R = B * L

@@ -252,3 +252,113 @@ def test_graph_with_stage_events():
         assert all(t >= 0 for t in times) and sum(times) > 0
     g.close()
     assert torch.equal(out, lay.forward(dev.H, dev.parent, 0.05))
+
+
+# ------------------------------------------------------------ rotary embedding --
+
+@pytest.mark.parametrize("tau,theta", [(0.05, 10000.0), (0.0, 500.0)])
+def test_layer_rope_small(tau, theta):
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=512, P=72, L=24, levels=(1, 2, 3))
+    m, _, _ = check_layer(synth.make_layer_inputs(w, seed=21), tau, rope_theta=theta)
+    print(m)
+
+
+def test_layer_rope_7b_sampled():
+    """7B layer with the Qwen2.5 rope base (1e6), sampled rows."""
+    inp = synth.make_layer_inputs("7b_layer", seed=2)
+    B, L, _ = inp.H.shape
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([np.arange(L), rng.choice(np.arange(L, B * L), 24, replace=False)]))
+    check_layer(inp, 0.05, rows=rows, inter=False, rope_theta=1.0e6)
+
+
+def test_rope_standalone_matches_oracle():
+    """specfold_rope on given Q / block-K layouts against the oracle's rope,
+    at positions up to the stress prefix (P 8192)."""
+    R, L, P, n_q, n_kv, hd = 96, 32, 8192, 8, 2, 128
+    g = n_q // n_kv
+    rng = np.random.default_rng(5)
+    Q = synth.round_bf16(rng.standard_normal((n_kv, R * g, hd)).astype(np.float32))
+    K = synth.round_bf16(rng.standard_normal((R, n_kv, hd)).astype(np.float32))
+    n = 70
+    pidx = np.sort(rng.choice(R, size=n, replace=False)).astype(np.int32)
+    dims = binding.make_dims(256, n_q, n_kv, hd, 512, 1e-6, binding.BF16, 1.0e6)
+    Qd, Kd = bf16(Q), bf16(K)
+    pid = torch.from_numpy(np.concatenate([pidx, np.full(R - n, -1, np.int32)])).cuda()
+    n_dev = torch.tensor([n], dtype=torch.int32, device="cuda")
+    binding.specfold_rope(dims, Qd, Kd, pid, n_dev, R // L, L, P)
+    torch.cuda.synchronize()
+    Qg, Kg = to_np(Qd), to_np(Kd)
+    for k in range(n):
+        r = int(pidx[k])
+        pos = P + r % L
+        q_ref = orc.rope(Q[:, k * g:(k + 1) * g, :], pos, 1.0e6)
+        assert rel_l2(Qg[:, k * g:(k + 1) * g, :], q_ref) < 1e-2
+        assert rel_l2(Kg[r], orc.rope(K[r], pos, 1.0e6)) < 1e-2
+    # rows beyond n and keys of unpacked rows are untouched
+    assert np.array_equal(Qg[:, n * g:, :], Q[:, n * g:, :])
+    untouched = np.setdiff1d(np.arange(R), pidx)
+    assert np.array_equal(Kg[untouched], K[untouched])
+
+
+# ------------------------------------------------------------ paged prefix --
+
+def _paged(inp, page_size, spare_pages=3, seed=0, poison=True):
+    """Scatter the seeded prefix K/V into a fused page pool
+    [pages * page_size, 2, n_kv, hd] in shuffled page order; unused pool
+    tokens hold NaN (they must never be read)."""
+    P = inp.prefix.P
+    d = inp.dims
+    need = (P + page_size - 1) // page_size
+    pages = need + spare_pages
+    rng = np.random.default_rng(seed)
+    table = rng.permutation(pages)[:need].astype(np.int32)
+    pool = np.full((pages * page_size, 2, d.n_kv, d.hd), np.nan if poison else 0.0, np.float32)
+    for t in range(P):
+        tok = table[t // page_size] * page_size + t % page_size
+        pool[tok, 0] = inp.prefix.K[t]
+        pool[tok, 1] = inp.prefix.V[t]
+    pool_d = bf16(pool)
+    table_d = torch.from_numpy(table).cuda()
+    return (binding.PagedPrefix(pool_d[:, 0], table_d, page_size, P),
+            binding.PagedPrefix(pool_d[:, 1], table_d, page_size, P), pool_d, table_d)
+
+
+@pytest.mark.parametrize("P,page_size", [(200, 16), (512, 128), (300, 256), (72, 8)])
+def test_layer_paged_prefix(P, page_size):
+    """The layer on a paged prefix (shuffled pages, NaN in every unused pool
+    token) against the oracle on the logical prefix."""
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=128, F=512, P=P, L=16, levels=(1, 2, 2))
+    inp = synth.make_layer_inputs(w, seed=31)
+    pk, pv, _pool, _table = _paged(inp, page_size)
+    dev = DeviceInputs(inp)
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, pk, pv)
+    out = lay.forward(dev.H, dev.parent, 0.05)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    gi = read_intermediates(lay, dev)
+    res, _, bad = oracle_with_gpu_decisions(inp, 0.05, gi["fold"])
+    assert bad == 0
+    k = gi["slot"][res["act_rows"]]
+    assert rel_l2(gi["attnO"][k], res["attnO"]) < TOL
+    # the same layer on the contiguous view gives the same bits
+    lay2 = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, dev.pk, dev.pv)
+    out2 = lay2.forward(dev.H, dev.parent, 0.05)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+
+
+def test_paged_prefix_bad_page_sets_status():
+    """A block-table entry outside the pool reads as zeros and sets
+    SPECFOLD_DEV_BAD_PAGE; the context stays usable."""
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=512, P=96, L=16, levels=(1, 2))
+    inp = synth.make_layer_inputs(w, seed=32)
+    pk, pv, pool, table = _paged(inp, 16, poison=False)
+    table[2] = 10_000
+    dev = DeviceInputs(inp)
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, pk, pv)
+    out = lay.forward(dev.H, dev.parent, 0.05)
+    torch.cuda.synchronize()
+    assert lay.status() & binding.DEV_BAD_PAGE
+    assert torch.isfinite(out.float()).all()
+    assert lay.status() == 0   # cleared by the read
