@@ -125,6 +125,41 @@ def gate(H: np.ndarray, parent: np.ndarray, tau: float,
     return fold, rel
 
 
+def gate_source(H: np.ndarray, parent: np.ndarray, tau: float,
+                force: Optional[np.ndarray] = None):
+    """Variant gate: compare child row (b, i) with the row its parent's
+    output at position i actually comes from, s = src(parent[b], i), instead
+    of the parent's own input: r = |H_b[i] - H_s[i]| / |H_s[i]|, same fold
+    rule as ``gate``.  A fold then never reuses an output whose input is more
+    than tau away, however long the chain.  Branches are visited in
+    topological order, so src of every parent is known; a forced decision
+    (``force``) feeds the later sources too.  Returns (fold, rel) like
+    ``gate``."""
+    H = np.asarray(H, F64)
+    B, L, _ = H.shape
+    tau = float(tau)
+    fold = np.zeros((B, L), dtype=bool)
+    rel = np.full((B, L), -1.0)
+    srcb = np.zeros((B, L), dtype=np.int64)   # branch whose row is reused
+    frc = None if force is None else np.asarray(force)
+    if frc is not None and np.any(frc[0] >= 0):
+        raise ValueError("root rows cannot be forced")
+    for b in range(1, B):
+        p = int(parent[b])
+        for i in range(L):
+            s = int(srcb[p, i])
+            delta = H[b, i] - H[s, i]
+            num = float(np.sum(delta * delta))
+            den = float(np.sum(H[s, i] * H[s, i]))
+            f = (num < (tau * tau) * den) or (num == 0.0 and tau > 0.0)
+            if frc is not None and frc[b, i] >= 0:
+                f = bool(frc[b, i] == 1)
+            fold[b, i] = f
+            rel[b, i] = math.sqrt(num / den) if den > 0 else (0.0 if num == 0 else math.inf)
+            srcb[b, i] = s if f else b
+    return fold, rel
+
+
 # ---------------------------------------------------------------------------
 # S2 resolve
 # ---------------------------------------------------------------------------
@@ -208,7 +243,8 @@ def attention_rows(q_rows: np.ndarray, branch_of_row: np.ndarray, kv_src: np.nda
 
 
 def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
-                  force=None, rows: Optional[Iterable[int]] = None, rope_theta: float = 0.0) -> dict:
+                  force=None, rows: Optional[Iterable[int]] = None, rope_theta: float = 0.0,
+                  gate_ref: str = "parent") -> dict:
     """Folded layer over all branches, in the packed order.
 
     With ``rows`` given, only those output rows are produced (plus what they
@@ -223,10 +259,12 @@ def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
     rope_theta > 0 rotates the queries and the block keys (``rope``, position
     P + i for block position i); the prefix keys are taken as already
     rotated, as a KV cache stores them.  Values are never rotated.
+
+    gate_ref "source" runs the variant gate (``gate_source``) instead.
     """
     H = np.asarray(H, F64)
     B, L, d = H.shape
-    fold, rel = gate(H, parent, tau, force)
+    fold, rel = (gate_source if gate_ref == "source" else gate)(H, parent, tau, force)
     src = resolve(fold, parent)
     packed_idx, slot, n = pack(fold)
     H2 = H.reshape(B * L, d)
@@ -309,13 +347,13 @@ def dense_branch_forward(Hb, W, prefK, prefV, eps, n_kv, hd, rope_theta: float =
 
 
 def layer_serialized(H, parent, W, prefK, prefV, tau, eps, n_kv, hd, force=None,
-                     rope_theta: float = 0.0) -> np.ndarray:
+                     rope_theta: float = 0.0, gate_ref: str = "parent") -> np.ndarray:
     """Serialized evaluation: one row at a time, straight from the definition,
     with no packed batch and no scan (the check the SpecFold authors describe
     in their appendix C).  Small inputs only.  Returns out [B, L, d]."""
     H = np.asarray(H, F64)
     B, L, d = H.shape
-    fold, _ = gate(H, parent, tau, force)
+    fold, _ = (gate_source if gate_ref == "source" else gate)(H, parent, tau, force)
     g1 = W["g1"]
     cache: Dict[int, np.ndarray] = {}
 
@@ -382,7 +420,8 @@ def near_tau_rows(rel: np.ndarray, tau: float, frac: float = 1e-4) -> np.ndarray
 # release; appendix D: how the recompute fraction evolves with depth)
 # ---------------------------------------------------------------------------
 
-def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None, rope_theta: float = 0.0) -> dict:
+def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None, rope_theta: float = 0.0,
+                  gate_ref: str = "parent") -> dict:
     """A stack of folded layers: layer l's output is layer l+1's input.
 
     ``layers`` is a sequence of (W, prefK, prefV), one per layer.  Each layer
@@ -402,7 +441,7 @@ def stack_forward(H, parent, layers, tau, eps, n_kv, hd, store=None, rope_theta:
     inputs, folds, rels, ns = [], [], [], []
     for (W, pk, pv) in layers:
         inputs.append(X)
-        res = layer_forward(X, parent, W, pk, pv, tau, eps, n_kv, hd, rope_theta=rope_theta)
+        res = layer_forward(X, parent, W, pk, pv, tau, eps, n_kv, hd, rope_theta=rope_theta, gate_ref=gate_ref)
         folds.append(res["fold"])
         rels.append(res["rel"])
         ns.append(int(res["n"]))
