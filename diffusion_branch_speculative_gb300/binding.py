@@ -34,7 +34,7 @@ class SpecfoldError(RuntimeError):
 class specfold_dims(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("dtype", ctypes.c_int), ("rope_theta", ctypes.c_float)]
+                ("dtype", ctypes.c_int), ("rope_theta", ctypes.c_float), ("gate_ref", ctypes.c_int)]
 
 
 class specfold_weights(ctypes.Structure):
@@ -61,6 +61,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIG = {
     "specfold_gate": (_I, [_I, _P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P]),
+    "specfold_gate_source": (_I, [_I, _P, _P, _I, _I, _I, ctypes.c_float, _P, _P, _P]),
     "specfold_resolve": (_I, [_P, _P, _I, _I, _P, _P, _P]),
     "specfold_pack": (_I, [_I, _P, _P, _P, ctypes.c_float, _I, _I, _I, _P, _P, _P, _P, _P]),
     "specfold_qkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -145,8 +146,9 @@ def dtype_code(t: torch.dtype) -> int:
     raise ValueError(f"unsupported dtype {t}")
 
 
-def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16, rope_theta=0.0) -> specfold_dims:
-    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype, rope_theta)
+def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16, rope_theta=0.0, gate_ref=0) -> specfold_dims:
+    """gate_ref 0: the gate compares with the parent; 1: with the parent's computed source."""
+    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype, rope_theta, gate_ref)
 
 
 def make_weights(w: dict) -> specfold_weights:
@@ -205,6 +207,13 @@ def specfold_gate(H: torch.Tensor, parent: torch.Tensor, tau: float, fold: torch
     B, L, d = H.shape
     _check(lib().specfold_gate(dtype_code(H.dtype), _ptr(H), _ptr(parent), B, L, d, float(tau), _ptr(fold),
                                _ptr(rel), _stream(stream)), "specfold_gate")
+
+
+def specfold_gate_source(H: torch.Tensor, parent: torch.Tensor, tau: float, fold: torch.Tensor,
+                         rel: Optional[torch.Tensor] = None, stream=None):
+    B, L, d = H.shape
+    _check(lib().specfold_gate_source(dtype_code(H.dtype), _ptr(H), _ptr(parent), B, L, d, float(tau), _ptr(fold),
+                                      _ptr(rel), _stream(stream)), "specfold_gate_source")
 
 
 def specfold_resolve(fold: torch.Tensor, parent: torch.Tensor, B: int, L: int, src: torch.Tensor,

@@ -112,6 +112,7 @@ static int check_dims(const specfold_dims* d) {
     return SPECFOLD_EINVAL;
   if (!(d->rms_eps >= 0.f) || std::isinf(d->rms_eps)) return SPECFOLD_EINVAL;
   if (!(d->rope_theta >= 0.f) || std::isinf(d->rope_theta)) return SPECFOLD_EINVAL;
+  if (d->gate_ref != 0 && d->gate_ref != 1) return SPECFOLD_EINVAL;
   if (d->head_dim != 64 && d->head_dim != 128) return SPECFOLD_EUNSUPPORTED;
   if (d->n_q_heads % d->n_kv_heads) return SPECFOLD_EUNSUPPORTED;
   if (d->d_model % 256) return SPECFOLD_EUNSUPPORTED;
@@ -407,8 +408,12 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
     if (stage_events) record_stage_event(stage_events[i], st);
   };
   mark(0);
-  SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
-                     fold_hist));
+  if (dims->gate_ref == 1)
+    SF_TRY(launch_gate_source(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
+                              fold_hist));
+  else
+    SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
+                       fold_hist));
   mark(1);
   SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
                             at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,
@@ -468,6 +473,17 @@ int specfold_gate(int dtype, const void* H, const int32_t* parent, int B, int L,
   if (d % 256) return SPECFOLD_EUNSUPPORTED;
   if (!a16(H)) return SPECFOLD_EALIGN;
   return launch_gate(dtype, H, parent, B, L, d, tau, fold, rel_opt, static_cast<cudaStream_t>(stream));
+}
+
+int specfold_gate_source(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                         uint8_t* fold, float* rel_opt, void* stream) {
+  if (!dtype_ok(dtype) || !H || !parent || !fold) return SPECFOLD_EINVAL;
+  SF_TRY(check_rows(B, L));
+  if (d <= 0) return SPECFOLD_EINVAL;
+  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
+  if (d % 256) return SPECFOLD_EUNSUPPORTED;
+  if (!a16(H)) return SPECFOLD_EALIGN;
+  return launch_gate_source(dtype, H, parent, B, L, d, tau, fold, rel_opt, static_cast<cudaStream_t>(stream));
 }
 
 int specfold_resolve(const uint8_t* fold, const int32_t* parent, int B, int L, int32_t* src, uint32_t* status_opt,

@@ -109,6 +109,105 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
   }
 }
 
+// ------------------------------------------- S1 variant: gate vs source --
+// One CTA per block position i.  Child (b, i) is compared with the row its
+// parent's output at i comes from, s = src(parent[b], i), which depends on
+// the parent's own decision: branches are processed level by level (a
+// node's level is its number of hops to the root), each level's nodes in
+// parallel, one warp per node, and the source branch of every decided node
+// is kept in shared memory.  A parent outside [0, b) makes the row
+// recompute (level 1), as in the parent gate.
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(kRowWarps * 32)
+gate_source_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, int L, int d, float tau,
+                   uint8_t* __restrict__ fold, float* __restrict__ rel, uint8_t* __restrict__ fold_hist) {
+  using V = VecT<T>;
+  extern __shared__ int sgs[];
+  int* s_src = sgs;        // [B] branch whose row (., i) is reused
+  int* s_lvl = sgs + B;    // [B]
+  __shared__ int s_maxlvl;
+  pdl_wait();
+  pdl_trigger();
+  const int i = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid == 0) s_maxlvl = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += blockDim.x) {
+    int lv = 0, x = b;
+    while (x > 0) {
+      const int p = parent[x];
+      ++lv;
+      if (p < 0 || p >= x) break;
+      x = p;
+    }
+    s_lvl[b] = lv;
+    s_src[b] = b;
+    atomicMax(&s_maxlvl, lv);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    fold[i] = 0;
+    if (rel) rel[i] = -1.f;
+    if (fold_hist) fold_hist[i] = 0;
+  }
+  const int nv = d / V::N;
+  for (int lv = 1; lv <= s_maxlvl; ++lv) {
+    for (int b = w; b < B; b += kRowWarps) {
+      if (s_lvl[b] != lv) continue;
+      const int row = b * L + i;
+      const int p = parent[b];
+      if (p < 0 || p >= b) {
+        if (lane == 0) {
+          fold[row] = 0;
+          if (rel) rel[row] = -1.f;
+          if (fold_hist) fold_hist[row] = 0;
+        }
+        continue;  // s_src[b] stays b
+      }
+      const int sb = s_src[p];
+      const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(row) * d);
+      const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(sb) * L + i) * d);
+      float num = 0.f, den = 0.f;
+      for (int v0 = 0; v0 < nv; v0 += 32 * MAXV) {
+        uint4 cv[MAXV], pv[MAXV];
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+          const int v = v0 + lane + u * 32;
+          if (v < nv) {
+            cv[u] = __ldg(c + v);
+            pv[u] = __ldg(q + v);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u) {
+          const int v = v0 + lane + u * 32;
+          if (v < nv) {
+            float fc[V::N], fp[V::N];
+            V::unpack(cv[u], fc);
+            V::unpack(pv[u], fp);
+#pragma unroll
+            for (int e = 0; e < V::N; ++e) {
+              const float df = fc[e] - fp[e];
+              num = fmaf(df, df, num);
+              den = fmaf(fp[e], fp[e], den);
+            }
+          }
+        }
+      }
+      num = warp_sum(num);
+      den = warp_sum(den);
+      const bool f = (num < tau * tau * den) || (num == 0.f && tau > 0.f);
+      if (lane == 0) {
+        fold[row] = f ? 1 : 0;
+        if (fold_hist) fold_hist[row] = f ? 1 : 0;
+        if (rel) rel[row] = den > 0.f ? sqrtf(num / den) : (num == 0.f ? 0.f : __int_as_float(0x7f800000));
+        s_src[b] = f ? sb : b;
+      }
+    }
+    __syncthreads();  // this level's sources are visible to the next
+  }
+}
+
 // ------------------------------------------------------- RMSNorm of a row --
 // Loads the gains (independent of the packed list) into registers.
 template <typename T, int MAXV>
@@ -492,6 +591,47 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
       launch_k(gate_kernel<float, 8>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
     else
       launch_k(gate_kernel<float, 16>, dim3(grid), dim3(block), 0, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
+  }
+  count_launch();
+  return check_launch();
+}
+
+int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                       uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist) {
+  const size_t smem = static_cast<size_t>(2) * B * sizeof(int);
+  const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
+  static int attr_done[64][4] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto prep = [&](auto kern, int slot) -> bool {
+    if (smem <= 48 * 1024 || dev < 0 || dev >= 64 || attr_done[dev][slot]) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             2 * SPECFOLD_MAX_ROWS * static_cast<int>(sizeof(int))) != cudaSuccess)
+      return false;
+    attr_done[dev][slot] = 1;
+    return true;
+  };
+  const dim3 grid(L), block(kRowWarps * 32);
+  if (dtype == SPECFOLD_BF16) {
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
+    if (per_lane <= 8) {
+      if (!prep(gate_source_kernel<__nv_bfloat16, 8>, 0)) return SPECFOLD_ECUDA;
+      launch_k(gate_source_kernel<__nv_bfloat16, 8>, grid, block, smem, st, h, parent, B, L, d, tau, fold, rel,
+               fold_hist);
+    } else {
+      if (!prep(gate_source_kernel<__nv_bfloat16, 16>, 1)) return SPECFOLD_ECUDA;
+      launch_k(gate_source_kernel<__nv_bfloat16, 16>, grid, block, smem, st, h, parent, B, L, d, tau, fold, rel,
+               fold_hist);
+    }
+  } else {
+    const float* h = static_cast<const float*>(H);
+    if (per_lane <= 8) {
+      if (!prep(gate_source_kernel<float, 8>, 2)) return SPECFOLD_ECUDA;
+      launch_k(gate_source_kernel<float, 8>, grid, block, smem, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
+    } else {
+      if (!prep(gate_source_kernel<float, 16>, 3)) return SPECFOLD_ECUDA;
+      launch_k(gate_source_kernel<float, 16>, grid, block, smem, st, h, parent, B, L, d, tau, fold, rel, fold_hist);
+    }
   }
   count_launch();
   return check_launch();

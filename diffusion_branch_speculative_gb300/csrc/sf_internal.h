@@ -21,6 +21,10 @@ int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a l
 // a second copy of the decisions.
 int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
                 uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist = nullptr);
+// variant gate: compare with the computed source of the parent's row
+// (level-by-level over the draft graph, one CTA per block position).
+int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                       uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
 // given); parent may be null (pack alone); any output may be null.  n_hist
 // (optional) receives a second copy of the packed-row count; dep_off [R+1] /

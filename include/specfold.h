@@ -78,6 +78,9 @@ typedef struct {
   float rms_eps;    /* RMSNorm epsilon (>= 0) */
   int dtype;        /* specfold_dtype */
   float rope_theta; /* rotary embedding base; 0 = no positional rotation inside the layer */
+  int gate_ref;     /* 0: the gate compares a child with its parent's input (specfold_gate);
+                       1: with the input of the row its parent's output comes from
+                       (specfold_gate_source) */
 } specfold_dims;
 
 /* Layer weights (device, [out, in] row-major, dims.dtype). */
@@ -157,6 +160,16 @@ typedef struct {
  * d % 256 == 0. */
 int specfold_gate(int dtype, const void* H, const int32_t* parent, int B, int L, int d,
                   float tau, uint8_t* fold, float* rel_opt, void* stream);
+
+/* S1 variant: the gate against the computed source.  As specfold_gate, but
+ * child row (b, i) is compared with row (s, i), s the branch whose row the
+ * parent's output at position i comes from (the parent itself if it was
+ * recomputed, else the parent's source): r = |H_b[i] - H_s[i]| / |H_s[i]|.
+ * A chain of folds then never reuses an output whose input is more than
+ * tau away.  Decisions follow the draft graph level by level (one CTA per
+ * position i).  Same arguments and outputs as specfold_gate. */
+int specfold_gate_source(int dtype, const void* H, const int32_t* parent, int B, int L, int d,
+                         float tau, uint8_t* fold, float* rel_opt, void* stream);
 
 /* S2 resolve.  Explainer, implementation note (provenance kernel): src[r] = r
  * for a recomputed row, else src of the same position in the parent branch,

@@ -29,10 +29,10 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 class DeviceInputs:
-    def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0):
+    def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0, gate_ref: int = 0):
         self.inp = inp
         d = inp.dims
-        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, rope_theta)
+        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, rope_theta, gate_ref)
         self.H = bf16(inp.H, device)
         self.parent = torch.from_numpy(inp.parent.astype(np.int32)).to(device)
         self.W = {k: bf16(v, device) for k, v in inp.weights.items()}
@@ -77,29 +77,42 @@ def read_intermediates(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
 
 
 def oracle_with_gpu_decisions(inp: synth.LayerInputs, tau: float, gpu_fold: np.ndarray, rows=None,
-                              rope_theta: float = 0.0):
+                              rope_theta: float = 0.0, gate_ref: int = 0):
     """Run the oracle; rows within NEAR_TAU of tau take the GPU's decision
     (spec rule: such rows are reported and excluded from decision
     parity).  Returns (oracle result, number of near-tau rows, mismatches
-    outside the near-tau band)."""
+    outside the near-tau band).  With the variant gate (gate_ref 1) a forced
+    decision changes the sources later rows compare with, so the near-tau
+    set is found again after forcing (twice)."""
     d = inp.dims
     B, L, _ = inp.H.shape
-    f0, rel = orc.gate(inp.H, inp.parent, np.float32(tau))
-    near = orc.near_tau_rows(rel, float(np.float32(tau)), NEAR_TAU)
+    t32 = np.float32(tau)
     gf = gpu_fold.reshape(B, L)
+    if gate_ref == 1:
+        f0, rel = orc.gate_source(inp.H, inp.parent, t32)
+        for _ in range(2):
+            near = orc.near_tau_rows(rel, float(t32), NEAR_TAU)
+            force = np.where(near, gf.astype(np.int8), np.int8(-1)).astype(np.int8)
+            f0, rel = orc.gate_source(inp.H, inp.parent, t32, force)
+        near = orc.near_tau_rows(rel, float(t32), NEAR_TAU)
+    else:
+        f0, rel = orc.gate(inp.H, inp.parent, t32)
+        near = orc.near_tau_rows(rel, float(t32), NEAR_TAU)
     bad = (gf != f0) & ~near
     force = np.where(near, gf.astype(np.int8), np.int8(-1)).astype(np.int8)
-    res = orc.layer_forward(inp.H, inp.parent, inp.weights, inp.prefix.K, inp.prefix.V, float(np.float32(tau)),
-                            d.eps, d.n_kv, d.hd, force=force, rows=rows, rope_theta=rope_theta)
+    res = orc.layer_forward(inp.H, inp.parent, inp.weights, inp.prefix.K, inp.prefix.V, float(t32),
+                            d.eps, d.n_kv, d.hd, force=force, rows=rows, rope_theta=rope_theta,
+                            gate_ref="source" if gate_ref == 1 else "parent")
     return res, int(near.sum()), int(bad.sum())
 
 
-def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0):
-    dev = DeviceInputs(inp, rope_theta=rope_theta)
+def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0, gate_ref: int = 0):
+    dev = DeviceInputs(inp, rope_theta=rope_theta, gate_ref=gate_ref)
     lay, out = run_layer(dev, tau)
     assert lay.status() == 0
     gi = read_intermediates(lay, dev)
-    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows, rope_theta=rope_theta)
+    res, n_near, n_bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rows, rope_theta=rope_theta,
+                                                   gate_ref=gate_ref)
     assert n_bad == 0, f"{n_bad} gate decisions differ away from tau"
     B, L, D = inp.H.shape
     R = B * L

@@ -362,3 +362,51 @@ def test_paged_prefix_bad_page_sets_status():
     assert lay.status() & binding.DEV_BAD_PAGE
     assert torch.isfinite(out.float()).all()
     assert lay.status() == 0   # cleared by the read
+
+
+# ------------------------------------------------- variant: gate vs source --
+
+@pytest.mark.parametrize("name,tau", [("7b_layer", 0.05), ("3b_layer", 0.05), ("tiny", 0.1), ("stress", 0.05)])
+def test_gate_source_standalone(name, tau):
+    """Decisions of the variant gate bit-exact against the oracle (rows
+    within 1e-4 of tau take the GPU's decision), r within fp32 rounding."""
+    inp = synth.make_layer_inputs(name, seed=4, dtype="bf16")
+    dev = DeviceInputs(inp)
+    B, L, _ = inp.H.shape
+    R = B * L
+    fold = torch.empty(R, dtype=torch.uint8, device="cuda")
+    rel = torch.empty(R, dtype=torch.float32, device="cuda")
+    binding.specfold_gate_source(dev.H, dev.parent, tau, fold, rel)
+    torch.cuda.synchronize()
+    fg = fold.cpu().numpy().astype(bool)
+    t32 = np.float32(tau)
+    f0, r0 = orc.gate_source(inp.H, inp.parent, t32)
+    for _ in range(2):
+        near = orc.near_tau_rows(r0, float(t32))
+        force = np.where(near, fg.reshape(B, L).astype(np.int8), np.int8(-1)).astype(np.int8)
+        f0, r0 = orc.gate_source(inp.H, inp.parent, t32, force)
+    near = orc.near_tau_rows(r0, float(t32))
+    assert np.array_equal(fg.reshape(B, L)[~near], f0[~near])
+    rg = rel.cpu().numpy().reshape(B, L)
+    fin = np.isfinite(r0) & (r0 >= 0)
+    np.testing.assert_allclose(rg[fin], r0[fin], rtol=1e-4, atol=1e-6)
+    # it differs from the parent gate somewhere on deep graphs (or equals it)
+    fp = np.zeros(R, np.uint8)
+    fpd = torch.empty(R, dtype=torch.uint8, device="cuda")
+    binding.specfold_gate(dev.H, dev.parent, tau, fpd)
+    print(name, "rows folded: source", int(fg.sum()), "parent", int(fpd.sum().item()))
+
+
+@pytest.mark.parametrize("tau", [0.05, 0.1])
+def test_layer_gate_source_small(tau):
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=512, P=64, L=16, levels=(1, 2, 3, 2, 1))
+    m, _, _ = check_layer(synth.make_layer_inputs(w, seed=41), tau, gate_ref=1)
+    print(m)
+
+
+def test_layer_gate_source_3b_sampled():
+    inp = synth.make_layer_inputs("3b_layer", seed=1)
+    B, L, _ = inp.H.shape
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([np.arange(L), rng.choice(np.arange(L, B * L), 24, replace=False)]))
+    check_layer(inp, 0.05, rows=rows, inter=False, gate_ref=1)
