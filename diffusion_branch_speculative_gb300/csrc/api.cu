@@ -231,6 +231,11 @@ static void record_stage_event(void* ev, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------- stage bodies --
+// bf16: the tcgen05 engine; fp32: the CUDA-core fp32 path.
+static int gemm_call(int dtype, const GemmCall& c, cudaStream_t st, const RowNorm* rn = nullptr) {
+  return dtype == SPECFOLD_F32 ? launch_gemm_f32(c, st, rn) : launch_gemm(c, st, rn);
+}
+
 static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const void* X1, const int32_t* packed_idx,
                      const int32_t* n_dev, int R, void* Q, void* bK, void* bV, const Scratch& s, uint32_t* status,
                      cudaStream_t st) {
@@ -256,7 +261,7 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
   c.n_kv = d->n_kv_heads;
   c.hd = d->head_dim;
   fill_scratch(c, s, status);
-  return launch_gemm(c, st);
+  return gemm_call(d->dtype, c, st);
 }
 
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
@@ -283,7 +288,7 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
   a.status = status;
   a.part = part;
   a.part_bytes = part_bytes;
-  return launch_attention(a, st);
+  return d->dtype == SPECFOLD_F32 ? launch_attention_f32(a, st) : launch_attention(a, st);
 }
 
 static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, const void* O,
@@ -308,9 +313,9 @@ static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, con
   fill_scratch(c, s, status);
   if (X2_fused) {
     const RowNorm rn{w->g2, d->rms_eps, X2_fused};
-    return launch_gemm(c, st, &rn);
+    return gemm_call(d->dtype, c, st, &rn);
   }
-  return launch_gemm(c, st);
+  return gemm_call(d->dtype, c, st);
 }
 
 // dep_off / dep_rows (the folded rows grouped by source slot, from the pack
@@ -341,7 +346,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.Y = G;
   c.ldy = d->ffn_dim;
   fill_scratch(c, s, status);
-  SF_TRY(launch_gemm(c, st));
+  SF_TRY(gemm_call(d->dtype, c, st));
   mark(ev0 + 1);
   memset(&c, 0, sizeof(c));
   c.epi = EPI_RESID_SCATTER;
@@ -359,12 +364,14 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.ldr = d->d_model;
   c.row_idx = packed_idx;
   fill_scratch(c, s, status);
-  if (dep_off) {
+  if (dep_off && d->dtype == SPECFOLD_BF16) {  // the fp32 path fills with the fold-fill kernel
     c.dep_off = dep_off;
     c.dep_rows = dep_rows;
     c.hin = H_in;
+  } else {
+    dep_off = nullptr;
   }
-  SF_TRY(launch_gemm(c, st));
+  SF_TRY(gemm_call(d->dtype, c, st));
   mark(ev0 + 2);
   if (!dep_off) SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
   mark(ev0 + 3);
@@ -378,7 +385,6 @@ static int check_layer_call(const specfold_dims* dims, const specfold_weights* w
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
   SF_TRY(check_weights(w));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!H_in || !parent || !H_out || !ws || P < 0) return SPECFOLD_EINVAL;
   if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
   SF_TRY(check_views(prefK, prefV, P));
@@ -422,8 +428,8 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
                    at<void>(ws, lo.block_v), s, status, st));
   if (dims->rope_theta > 0.f)
-    SF_TRY(launch_rope(at<void>(ws, lo.q), at<void>(ws, lo.block_k), pidx, n_dev, R, L, P, dims->n_q_heads,
-                       dims->n_kv_heads, dims->head_dim, dims->rope_theta, st));
+    SF_TRY(launch_rope(dims->dtype, at<void>(ws, lo.q), at<void>(ws, lo.block_k), pidx, n_dev, R, L, P,
+                       dims->n_q_heads, dims->n_kv_heads, dims->head_dim, dims->rope_theta, st));
   mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
@@ -514,7 +520,6 @@ int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const voi
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
   SF_TRY(check_weights(w));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!X1 || !packed_idx || !n_dev || !Q || !blockK || !blockV || !ws) return SPECFOLD_EINVAL;
   if (!a16(X1) || !a16(Q) || !a16(blockK) || !a16(blockV) || !a16(ws)) return SPECFOLD_EALIGN;
   specfold_ws_layout lo;
@@ -529,12 +534,11 @@ int specfold_rope(const specfold_dims* dims, void* Q, void* blockK, const int32_
                   int B, int L, int P, void* stream) {
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!Q || !blockK || !packed_idx || !n_dev || P < 0) return SPECFOLD_EINVAL;
   if (!a16(Q) || !a16(blockK)) return SPECFOLD_EALIGN;
   if (dims->rope_theta == 0.f) return SPECFOLD_OK;
-  return launch_rope(Q, blockK, packed_idx, n_dev, B * L, L, P, dims->n_q_heads, dims->n_kv_heads, dims->head_dim,
-                     dims->rope_theta, static_cast<cudaStream_t>(stream));
+  return launch_rope(dims->dtype, Q, blockK, packed_idx, n_dev, B * L, L, P, dims->n_q_heads, dims->n_kv_heads,
+                     dims->head_dim, dims->rope_theta, static_cast<cudaStream_t>(stream));
 }
 
 int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_view prefK, specfold_kv_view prefV,
@@ -542,7 +546,6 @@ int specfold_attention(const specfold_dims* dims, const void* Q, specfold_kv_vie
                        const int32_t* n_dev, int B, int L, void* O, void* ws, size_t ws_bytes, void* stream) {
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (P < 0 || !Q || !blockK || !blockV || !src || !packed_idx || !n_dev || !O || !ws) return SPECFOLD_EINVAL;
   SF_TRY(check_views(prefK, prefV, P));
   if (!a16(Q) || !a16(blockK) || !a16(blockV) || !a16(O)) return SPECFOLD_EALIGN;
@@ -560,7 +563,6 @@ int specfold_out_proj(const specfold_dims* dims, const specfold_weights* w, cons
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
   SF_TRY(check_weights(w));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!O || !packed_idx || !n_dev || !H_in || !A || !ws) return SPECFOLD_EINVAL;
   if (!a16(O) || !a16(H_in) || !a16(A)) return SPECFOLD_EALIGN;
   specfold_ws_layout lo;
@@ -577,7 +579,6 @@ int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const voi
   SF_TRY(check_dims(dims));
   SF_TRY(check_rows(B, L));
   SF_TRY(check_weights(w));
-  if (dims->dtype != SPECFOLD_BF16) return SPECFOLD_EUNSUPPORTED;
   if (!A || !packed_idx || !n_dev || !H_in || !src || !fold || !H_out || !ws) return SPECFOLD_EINVAL;
   if (!a16(A) || !a16(H_in) || !a16(H_out) || !a16(ws)) return SPECFOLD_EALIGN;
   specfold_ws_layout lo;
@@ -658,9 +659,9 @@ int specfold_stack_forward(const specfold_dims* dims, int n_layers, const specfo
 
 int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K, void* Y, void* ws, size_t ws_bytes,
                     void* stream) {
-  if (dtype != SPECFOLD_BF16) return dtype_ok(dtype) ? SPECFOLD_EUNSUPPORTED : SPECFOLD_EINVAL;
+  if (!dtype_ok(dtype)) return SPECFOLD_EINVAL;
   if (!X || !W || !Y || !ws || M <= 0 || N <= 0 || K <= 0) return SPECFOLD_EINVAL;
-  if (K % 64 || N % 128) return SPECFOLD_EUNSUPPORTED;
+  if (dtype == SPECFOLD_F32 ? (K % 32 || N % 32) : (K % 64 || N % 128)) return SPECFOLD_EUNSUPPORTED;
   if (!a16(X) || !a16(W) || !a16(Y) || !a16(ws)) return SPECFOLD_EALIGN;
   if (ws_bytes < specfold_linear_workspace_size(M, N)) return SPECFOLD_ECAPACITY;
   GemmCall c;
@@ -679,7 +680,7 @@ int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K
   c.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
   c.partial_len = gemm_partial_floats();
   c.status = static_cast<uint32_t*>(ws);
-  return launch_gemm(c, static_cast<cudaStream_t>(stream));
+  return gemm_call(dtype, c, static_cast<cudaStream_t>(stream));
 }
 
 struct specfold_graph_s {

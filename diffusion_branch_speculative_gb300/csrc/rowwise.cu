@@ -492,8 +492,27 @@ fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ s
 // (row k*g + j of KV head h holds query head h*g + j of packed row k);
 // block keys: [R][n_kv][hd] at row packed_idx[k].  Frequencies are computed
 // once per block in double and rounded to float; angles and sincosf in fp32.
+SF_DEV void load8(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  x[0] = bf16lo(a.x); x[1] = bf16hi(a.x); x[2] = bf16lo(a.y); x[3] = bf16hi(a.y);
+  x[4] = bf16lo(a.z); x[5] = bf16hi(a.z); x[6] = bf16lo(a.w); x[7] = bf16hi(a.w);
+}
+SF_DEV void load8(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+SF_DEV void store8(__nv_bfloat16* p, const float (&y)[8]) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                            pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+}
+SF_DEV void store8(float* p, const float (&y)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+}
+
+template <typename T>
 __global__ void __launch_bounds__(256)
-rope_kernel(__nv_bfloat16* __restrict__ Q, __nv_bfloat16* __restrict__ Kb, const int32_t* __restrict__ packed_idx,
+rope_kernel(T* __restrict__ Q, T* __restrict__ Kb, const int32_t* __restrict__ packed_idx,
             const int32_t* __restrict__ n_dev, int R, int L, int P, int n_q, int n_kv, int hd, float theta) {
   __shared__ float s_freq[64];
   pdl_wait();
@@ -516,21 +535,16 @@ rope_kernel(__nv_bfloat16* __restrict__ Q, __nv_bfloat16* __restrict__ Kb, const
     const int r = packed_idx[k];
     if (r < 0 || r >= R) continue;
     const float pos = static_cast<float>(P + r % L);
-    __nv_bfloat16* row;
+    T* row;
     if (h < n_q) {
       const int hk = h / g, hg = h - hk * g;
       row = Q + ((static_cast<size_t>(hk) * R + k) * g + hg) * hd;
     } else {
       row = Kb + (static_cast<size_t>(r) * n_kv + (h - n_q)) * hd;
     }
-    uint4* p1 = reinterpret_cast<uint4*>(row + j0);
-    uint4* p2 = reinterpret_cast<uint4*>(row + half + j0);
-    const uint4 a = *p1, b = *p2;
     float x1[8], x2[8], y1[8], y2[8];
-    x1[0] = bf16lo(a.x); x1[1] = bf16hi(a.x); x1[2] = bf16lo(a.y); x1[3] = bf16hi(a.y);
-    x1[4] = bf16lo(a.z); x1[5] = bf16hi(a.z); x1[6] = bf16lo(a.w); x1[7] = bf16hi(a.w);
-    x2[0] = bf16lo(b.x); x2[1] = bf16hi(b.x); x2[2] = bf16lo(b.y); x2[3] = bf16hi(b.y);
-    x2[4] = bf16lo(b.z); x2[5] = bf16hi(b.z); x2[6] = bf16lo(b.w); x2[7] = bf16hi(b.w);
+    load8(row + j0, x1);
+    load8(row + half + j0, x2);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       float sn, cs;
@@ -538,10 +552,8 @@ rope_kernel(__nv_bfloat16* __restrict__ Q, __nv_bfloat16* __restrict__ Kb, const
       y1[e] = x1[e] * cs - x2[e] * sn;
       y2[e] = x2[e] * cs + x1[e] * sn;
     }
-    *p1 = make_uint4(pack_bf16x2(y1[0], y1[1]), pack_bf16x2(y1[2], y1[3]), pack_bf16x2(y1[4], y1[5]),
-                     pack_bf16x2(y1[6], y1[7]));
-    *p2 = make_uint4(pack_bf16x2(y2[0], y2[1]), pack_bf16x2(y2[2], y2[3]), pack_bf16x2(y2[4], y2[5]),
-                     pack_bf16x2(y2[6], y2[7]));
+    store8(row + j0, y1);
+    store8(row + half + j0, y2);
   }
 }
 
@@ -564,12 +576,16 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
 
 }  // namespace
 
-int launch_rope(void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P, int n_q,
-                int n_kv, int hd, float theta, cudaStream_t st) {
+int launch_rope(int dtype, void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P,
+                int n_q, int n_kv, int hd, float theta, cudaStream_t st) {
   const long long total = static_cast<long long>(R) * (n_q + n_kv) * (hd / 16);
-  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * num_sms()));
-  launch_k(rope_kernel, dim3(std::max(grid, 1)), dim3(256), 0, st, static_cast<__nv_bfloat16*>(Q),
-           static_cast<__nv_bfloat16*>(Kb), packed_idx, n_dev, R, L, P, n_q, n_kv, hd, theta);
+  const int grid = std::max(static_cast<int>(std::min<long long>((total + 255) / 256, 8LL * num_sms())), 1);
+  if (dtype == SPECFOLD_BF16)
+    launch_k(rope_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, static_cast<__nv_bfloat16*>(Q),
+             static_cast<__nv_bfloat16*>(Kb), packed_idx, n_dev, R, L, P, n_q, n_kv, hd, theta);
+  else
+    launch_k(rope_kernel<float>, dim3(grid), dim3(256), 0, st, static_cast<float*>(Q), static_cast<float*>(Kb),
+             packed_idx, n_dev, R, L, P, n_q, n_kv, hd, theta);
   count_launch();
   return check_launch();
 }

@@ -41,9 +41,9 @@ int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int3
 int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const void* H_in,
                      void* H_out, int R, int d, cudaStream_t st);
 int launch_timeout_probe(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
-// Rotary embedding of the packed rows' queries and block keys in place (bf16).
-int launch_rope(void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P, int n_q,
-                int n_kv, int hd, float theta, cudaStream_t st);
+// Rotary embedding of the packed rows' queries and block keys in place.
+int launch_rope(int dtype, void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P,
+                int n_q, int n_kv, int hd, float theta, cudaStream_t st);
 
 // ---- tcgen05 GEMM (gemm_tc.cu) ----
 enum GemmEpi : int {
@@ -94,6 +94,8 @@ struct RowNorm {
   void* out;
 };
 int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn = nullptr);
+// The same call for fp32 operands (simt_f32.cu): CUDA-core FMA, fp32 throughout.
+int launch_gemm_f32(const GemmCall& c, cudaStream_t st, const RowNorm* rn = nullptr);
 
 // ---- tcgen05 attention (attn_tc.cu) ----
 struct AttnCall {
@@ -114,6 +116,7 @@ struct AttnCall {
 int attn_sp_max(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);
 int launch_attention(const AttnCall& c, cudaStream_t st);
+int launch_attention_f32(const AttnCall& c, cudaStream_t st);  // fp32 Q/K/V/O (simt_f32.cu)
 
 // ---- TMA descriptors (api.cu) ----
 // 2-D bf16 map over a row-major [rows, cols] matrix with a {64, box_rows}

@@ -28,15 +28,26 @@ def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
+def f32(x: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
+
+
 class DeviceInputs:
+    """Seeded inputs on the device, in the workload's dtype (bf16, or fp32
+    for the tiny fp32 configuration)."""
+
     def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0, gate_ref: int = 0):
         self.inp = inp
         d = inp.dims
-        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, rope_theta, gate_ref)
-        self.H = bf16(inp.H, device)
+        self.fp32 = inp.dtype == "f32"
+        conv = f32 if self.fp32 else bf16
+        self.tdtype = torch.float32 if self.fp32 else torch.bfloat16
+        self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.F32 if self.fp32 else binding.BF16,
+                                      rope_theta, gate_ref)
+        self.H = conv(inp.H, device)
         self.parent = torch.from_numpy(inp.parent.astype(np.int32)).to(device)
-        self.W = {k: bf16(v, device) for k, v in inp.weights.items()}
-        self.cache = bf16(inp.prefix.cache, device)
+        self.W = {k: conv(v, device) for k, v in inp.weights.items()}
+        self.cache = conv(inp.prefix.cache, device)
         pre = inp.prefix
         self.P = pre.P
         self.pk = self.cache[pre.offset:pre.offset + pre.P, 0] if pre.P > 0 else None
@@ -57,6 +68,7 @@ def read_intermediates(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
     n = lay.n_packed()
     g = d.n_q // d.n_kv
     v = lay.view
+    et = dev.tdtype
     res = {
         "n": n,
         "fold": v("fold", torch.uint8, (R,)).cpu().numpy().astype(bool),
@@ -64,14 +76,14 @@ def read_intermediates(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
         "src": v("src", torch.int32, (R,)).cpu().numpy(),
         "packed_idx": v("packed_idx", torch.int32, (R,)).cpu().numpy()[:n],
         "slot": v("slot_of_row", torch.int32, (R,)).cpu().numpy(),
-        "X1": to_np(v("x1", torch.bfloat16, (R, d.d))[:n]),
-        "Q": to_np(v("q", torch.bfloat16, (d.n_kv, R, g, d.hd))[:, :n].permute(1, 0, 2, 3).reshape(n, -1)),
-        "bK": to_np(v("block_k", torch.bfloat16, (R, d.n_kv, d.hd))),
-        "bV": to_np(v("block_v", torch.bfloat16, (R, d.n_kv, d.hd))),
-        "attnO": to_np(v("attn_o", torch.bfloat16, (R, d.n_q * d.hd))[:n]),
-        "A": to_np(v("a", torch.bfloat16, (R, d.d))[:n]),
-        "X2": to_np(v("x2", torch.bfloat16, (R, d.d))[:n]),
-        "G": to_np(v("g", torch.bfloat16, (R, d.F))[:n]),
+        "X1": to_np(v("x1", et, (R, d.d))[:n]),
+        "Q": to_np(v("q", et, (d.n_kv, R, g, d.hd))[:, :n].permute(1, 0, 2, 3).reshape(n, -1)),
+        "bK": to_np(v("block_k", et, (R, d.n_kv, d.hd))),
+        "bV": to_np(v("block_v", et, (R, d.n_kv, d.hd))),
+        "attnO": to_np(v("attn_o", et, (R, d.n_q * d.hd))[:n]),
+        "A": to_np(v("a", et, (R, d.d))[:n]),
+        "X2": to_np(v("x2", et, (R, d.d))[:n]),
+        "G": to_np(v("g", et, (R, d.F))[:n]),
     }
     return res
 

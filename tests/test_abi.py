@@ -111,7 +111,8 @@ def test_host_argument_errors_launch_nothing(L):
     # linear: unsupported shapes
     assert L.specfold_linear(0, good, good, 128, 100, 64, good, good, 1 << 30, None) == binding.EUNSUPPORTED
     assert L.specfold_linear(0, good, good, 128, 128, 60, good, good, 1 << 30, None) == binding.EUNSUPPORTED
-    assert L.specfold_linear(1, good, good, 128, 128, 64, good, good, 1 << 30, None) == binding.EUNSUPPORTED
+    assert L.specfold_linear(1, good, good, 128, 100, 64, good, good, 1 << 30, None) == binding.EUNSUPPORTED
+    assert L.specfold_linear(7, good, good, 128, 128, 64, good, good, 1 << 30, None) == binding.EINVAL
     assert L.specfold_selftest_timeout(None, 1000, None) == binding.EINVAL
     assert L.specfold_launch_count() == before
 

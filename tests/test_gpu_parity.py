@@ -10,8 +10,8 @@ import torch
 
 from diffusion_branch_speculative_gb300 import binding, synth
 from oracle import specfold_oracle as orc
-from tests.gpu_cases import (TOL, DeviceInputs, bf16, check_layer, oracle_with_gpu_decisions, read_intermediates,
-                             rel_l2, run_layer, to_np)
+from tests.gpu_cases import (TOL, DeviceInputs, bf16, check_layer, f32, oracle_with_gpu_decisions,
+                             read_intermediates, rel_l2, run_layer, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -115,6 +115,64 @@ def test_layer_ragged_hd128():
 def test_layer_no_prefix():
     w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=256, P=0, L=8, levels=(1, 2))
     check_layer(synth.make_layer_inputs(w, seed=2), 0.05)
+
+
+TOL_F32 = 1e-4   # relative L2 for the fp32 path (fp32 storage and accumulation)
+
+
+def check_layer_f32(inp, tau, rope_theta=0.0, gate_ref=0, prefix=None):
+    """The fp32 path against the oracle: decisions, provenance and packed
+    lists bit-exact; every fp32 intermediate and the output within 1e-4."""
+    dev = DeviceInputs(inp, rope_theta=rope_theta, gate_ref=gate_ref)
+    pk, pv = (dev.pk, dev.pv) if prefix is None else prefix
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, pk, pv)
+    out = lay.forward(dev.H, dev.parent, tau)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    gi = read_intermediates(lay, dev)
+    res, _, bad = oracle_with_gpu_decisions(inp, tau, gi["fold"], rope_theta=rope_theta, gate_ref=gate_ref)
+    assert bad == 0
+    assert np.array_equal(gi["src"], res["src"]) and gi["n"] == res["n"]
+    assert np.array_equal(gi["packed_idx"], res["packed_idx"])
+    act = res["act_rows"]
+    k = gi["slot"][act]
+    m = {"X1": rel_l2(gi["X1"][k], res["X1"]), "Q": rel_l2(gi["Q"][k], res["Q"]),
+         "K": rel_l2(gi["bK"][act], np.stack([res["K_rows"][r] for r in act])),
+         "attnO": rel_l2(gi["attnO"][k], res["attnO"]), "A": rel_l2(gi["A"][k], res["A"]),
+         "X2": rel_l2(gi["X2"][k], res["X2"]), "G": rel_l2(gi["G"][k], res["G"])}
+    B, L, D = inp.H.shape
+    Hg = to_np(out).reshape(B * L, D)
+    Hin = inp.H.reshape(B * L, D).astype(np.float64)
+    m["H_out"] = rel_l2(Hg, res["out"])
+    m["delta"] = rel_l2(Hg - Hin, res["out"] - Hin)
+    for key, val in m.items():
+        assert val < TOL_F32, (key, val, m)
+    return m
+
+
+@pytest.mark.parametrize("tau", [0.05, 0.0, 0.2])
+def test_layer_tiny_fp32(tau):
+    """The tiny fp32 configuration (d 256, 4/2 x 64, F 1024, P 64, L 16, a
+    4-branch chain) through the fp32 path."""
+    m = check_layer_f32(synth.make_layer_inputs("tiny", seed=0), tau)
+    print(m)
+
+
+def test_layer_tiny_fp32_rope_paged_variant():
+    inp = synth.make_layer_inputs("tiny", seed=1)
+    pk, pv, _pool, _table = _paged(inp, 16, poison=True, as_f32=True)
+    check_layer_f32(inp, 0.05, rope_theta=10000.0, gate_ref=1, prefix=(pk, pv))
+
+
+def test_linear_fp32_matches_fp64():
+    rng = np.random.default_rng(8)
+    M, N, K = 70, 96, 256
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    Y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    ws = binding.alloc_workspace(binding.linear_workspace_size(M, N))
+    binding.specfold_linear(f32(X), f32(W), Y, ws)
+    assert rel_l2(to_np(Y), X.astype(np.float64) @ W.astype(np.float64).T) < 1e-5
 
 
 def test_layer_tiny_workload_bf16():
@@ -303,7 +361,7 @@ def test_rope_standalone_matches_oracle():
 
 # ------------------------------------------------------------ paged prefix --
 
-def _paged(inp, page_size, spare_pages=3, seed=0, poison=True):
+def _paged(inp, page_size, spare_pages=3, seed=0, poison=True, as_f32=False):
     """Scatter the seeded prefix K/V into a fused page pool
     [pages * page_size, 2, n_kv, hd] in shuffled page order; unused pool
     tokens hold NaN (they must never be read)."""
@@ -318,7 +376,7 @@ def _paged(inp, page_size, spare_pages=3, seed=0, poison=True):
         tok = table[t // page_size] * page_size + t % page_size
         pool[tok, 0] = inp.prefix.K[t]
         pool[tok, 1] = inp.prefix.V[t]
-    pool_d = bf16(pool)
+    pool_d = f32(pool) if as_f32 else bf16(pool)
     table_d = torch.from_numpy(table).cuda()
     return (binding.PagedPrefix(pool_d[:, 0], table_d, page_size, P),
             binding.PagedPrefix(pool_d[:, 1], table_d, page_size, P), pool_d, table_d)
