@@ -30,9 +30,11 @@
  *     position i.  R = B*L is the row capacity.  The number of packed rows n
  *     stays on the device (n_dev) and kernels are sized for n = R, so a call
  *     never synchronises with the host.
- *   - Element type: dims.dtype.  SPECFOLD_BF16 is supported by every entry
- *     point.  All activations, weights and the prefix view use that type;
- *     accumulation is fp32.
+ *   - Element type: dims.dtype.  SPECFOLD_BF16 runs the contractions on the
+ *     tcgen05 tensor cores (fp32 accumulation); SPECFOLD_F32 keeps fp32
+ *     throughout (CUDA-core fp32 FMA for the projections and attention, the
+ *     tiny fp32 configuration).  All activations, weights and the prefix view
+ *     use that type.
  *   - Matrices are row-major.  Weights use the [out, in] layout.
  *   - Alignment: every pointer is 16-byte aligned; the prefix view strides are
  *     multiples of 8 elements (SPECFOLD_EALIGN otherwise).
