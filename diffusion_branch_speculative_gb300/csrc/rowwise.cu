@@ -59,7 +59,17 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
   const int lane = threadIdx.x & 31;
   if (row >= B * L) return;
   const int b = row / L, i = row - b * L;
+  const int nv = d / V::N;
+  const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(row) * d);
   const int p = b > 0 ? parent[b] : -1;
+  uint4 cv[MAXV], pv[MAXV];
+  // the child row's first vectors do not depend on the parent index: they
+  // are in flight while it arrives
+  if (b > 0) {
+#pragma unroll
+    for (int u = 0; u < MAXV; ++u)
+      if (lane + u * 32 < nv) cv[u] = __ldg(c + lane + u * 32);
+  }
   if (b == 0 || p < 0 || p >= b) {  // root, or a parent the resolver will reject
     if (lane == 0) {
       fold[row] = 0;
@@ -68,18 +78,14 @@ gate_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, int B, 
     }
     return;
   }
-  const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(row) * d);
   const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(p) * L + i) * d);
-  const int nv = d / V::N;
   float num = 0.f, den = 0.f;
-  // the whole row is in flight at once (the kernel is latency-bound otherwise)
   for (int v0 = 0; v0 < nv; v0 += 32 * MAXV) {
-    uint4 cv[MAXV], pv[MAXV];
 #pragma unroll
     for (int u = 0; u < MAXV; ++u) {
       const int v = v0 + lane + u * 32;
       if (v < nv) {
-        cv[u] = __ldg(c + v);
+        if (v0 > 0) cv[u] = __ldg(c + v);
         pv[u] = __ldg(q + v);
       }
     }
@@ -209,21 +215,33 @@ gate_source_kernel(const T* __restrict__ H, const int32_t* __restrict__ parent, 
 }
 
 // ------------------------------------------------------- RMSNorm of a row --
-// Loads the gains (independent of the packed list) into registers.
-template <typename T, int MAXV>
-SF_DEV void load_gains(const T* g, int d, int lane, uint4 (&gw)[MAXV]) {
-  using V = VecT<T>;
-  const uint4* gv = reinterpret_cast<const uint4*>(g);
-  const int nv = d / V::N;
+// Gains of one row, for the norm: held in registers (GREG, loaded before the
+// programmatic wait, overlapping the previous kernel) when the grid fits in
+// one wave at one block per SM; otherwise read through L1 at the scaled
+// store (every warp reads the same g), which keeps two or more blocks per SM.
+template <typename T, int MAXV, bool GREG>
+struct Gains {
+  uint4 r[GREG ? MAXV : 1];
+  const uint4* g;
+  SF_DEV void load(const T* gp, int d, int lane) {
+    g = reinterpret_cast<const uint4*>(gp);
+    if constexpr (GREG) {
+      const int nv = d / VecT<T>::N;
 #pragma unroll
-  for (int j = 0; j < MAXV; ++j)
-    if (lane + 32 * j < nv) gw[j] = __ldg(gv + lane + 32 * j);
-}
+      for (int j = 0; j < MAXV; ++j)
+        if (lane + 32 * j < nv) r[j] = __ldg(g + lane + 32 * j);
+    }
+  }
+  SF_DEV uint4 at(int j, int vi) const {
+    if constexpr (GREG) return r[j];
+    return __ldg(g + vi);
+  }
+};
 
 // y = x * g / sqrt(mean(x^2) + eps) for one row, one warp; the whole row is
 // loaded before the reduction and held in registers until the scaled store.
-template <typename T, int MAXV>
-SF_DEV void norm_row(const T* __restrict__ xrow, const uint4 (&gw)[MAXV], int d, float eps,
+template <typename T, int MAXV, bool GREG>
+SF_DEV void norm_row(const T* __restrict__ xrow, const Gains<T, MAXV, GREG>& gn, int d, float eps,
                      T* __restrict__ yrow, int lane) {
   using V = VecT<T>;
   const uint4* x = reinterpret_cast<const uint4*>(xrow);
@@ -251,7 +269,7 @@ SF_DEV void norm_row(const T* __restrict__ xrow, const uint4 (&gw)[MAXV], int d,
     if (vi < nv) {
       float f[V::N], gf[V::N];
       V::unpack(v[j], f);
-      V::unpack(gw[j], gf);
+      V::unpack(gn.at(j, vi), gf);
 #pragma unroll
       for (int e = 0; e < V::N; ++e) f[e] = f[e] * inv * gf[e];
       y[vi] = V::pack(f);
@@ -285,7 +303,7 @@ SF_DEV int chain_end(const uint8_t* fold, const int32_t* parent, int b, int i, i
   return s;
 }
 
-template <typename T, int MAXV>
+template <typename T, int MAXV, bool GREG>
 __global__ void __launch_bounds__(kPackThreads)
 select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ parent, int B, int L,
                    int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
@@ -300,8 +318,8 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
   int* s_slot = smem_i + R;     // [R] packed slot or -1
   int* s_inv = smem_i + 2 * R;  // [R + 1] row of packed slot k; block 0 reuses it for the dependents
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  uint4 gw[MAXV];
-  if (X1) load_gains<T, MAXV>(g1, d, lane, gw);   // weights: independent of earlier kernels
+  Gains<T, MAXV, GREG> gn;
+  if (X1) gn.load(g1, d, lane);  // weights: independent of earlier kernels
   pdl_wait();
   pdl_trigger();
   if (tid == 0) s_bad = 0;
@@ -313,10 +331,31 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
     }
   const int ipt = (R + kPackThreads - 1) / kPackThreads;
   const int r0 = min(R, tid * ipt), r1 = min(R, r0 + ipt);
+  // The chain walks are dependent loads: copy fold and parent into the
+  // (not yet used) packed-slot array first, one coalesced pass, when they fit.
+  const int fold_words = (R + 3) / 4;
+  const bool staged = fold_words + (parent ? B : 0) <= R + 1;
+  const uint8_t* fsrc = fold;
+  const int32_t* psrc = parent;
+  if (staged) {
+    uint32_t* sf = reinterpret_cast<uint32_t*>(s_inv);
+    for (int j = tid; j < fold_words; j += kPackThreads) {
+      uint32_t wv = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * j + e < R) wv |= static_cast<uint32_t>(fold[4 * j + e]) << (8 * e);
+      sf[j] = wv;
+    }
+    if (parent)
+      for (int b = tid; b < B; b += kPackThreads) s_inv[fold_words + b] = parent[b];
+    __syncthreads();
+    fsrc = reinterpret_cast<const uint8_t*>(s_inv);
+    psrc = parent ? s_inv + fold_words : nullptr;
+  }
   int cnt = 0;
   for (int r = r0; r < r1; ++r) {
     const int b = r / L, i = r - b * L;
-    const int sb = chain_end(fold, parent, b, i, L);
+    const int sb = chain_end(fsrc, psrc, b, i, L);
     const int sr = sb < 0 ? -1 : sb * L + i;
     s_src[r] = sr;
     cnt += (sr == r);
@@ -418,27 +457,28 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
   }
   // RMSNorm1 gather of this block's packed rows
   if (X1 && r_norm >= 0)
-    norm_row<T, MAXV>(H + static_cast<size_t>(r_norm) * d, gw, d, eps, X1 + static_cast<size_t>(k_norm) * d, lane);
+    norm_row<T, MAXV, GREG>(H + static_cast<size_t>(r_norm) * d, gn, d, eps, X1 + static_cast<size_t>(k_norm) * d,
+                            lane);
 }
 
 // ------------------------------------------------------- RMSNorm rows --
 // Y[k] = X[idx ? idx[k] : k] * g / sqrt(mean(X^2) + eps) for k < n.
-template <typename T, int MAXV>
+template <typename T, int MAXV, bool GREG>
 __global__ void __launch_bounds__(kRowWarps * 32)
 rmsnorm_rows_kernel(const T* __restrict__ X, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ n_dev, int R, int d, const T* __restrict__ g,
                     float eps, T* __restrict__ Y) {
   const int k = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  uint4 gw[MAXV];
-  if (k < R) load_gains<T, MAXV>(g, d, lane, gw);   // weights: independent of earlier kernels
+  Gains<T, MAXV, GREG> gn;
+  if (k < R) gn.load(g, d, lane);  // weights: independent of earlier kernels
   pdl_wait();
   pdl_trigger();
   if (k >= R) return;
   const int n = n_dev ? min(max(n_dev[0], 0), R) : R;
   if (k >= n) return;
   const int r = idx ? idx[k] : k;
-  norm_row<T, MAXV>(X + static_cast<size_t>(r) * d, gw, d, eps, Y + static_cast<size_t>(k) * d, lane);
+  norm_row<T, MAXV, GREG>(X + static_cast<size_t>(r) * d, gn, d, eps, Y + static_cast<size_t>(k) * d, lane);
 }
 
 // -------------------------------------------------------------- S10 fill --
@@ -594,7 +634,11 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
                 uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist) {
   const int R = B * L;
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
-  const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
+  // A whole row in flight per lane (one pass) needs one block per SM; when
+  // the grid would then take more than one wave, two passes of eight
+  // vectors keep two blocks per SM instead.
+  int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
+  if (static_cast<int>(grid.x) > num_sms()) per_lane = std::min(per_lane, 8);
   if (dtype == SPECFOLD_BF16) {
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(H);
     if (per_lane <= 8)
@@ -653,7 +697,7 @@ int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, i
   return check_launch();
 }
 
-template <typename T, int MAXV>
+template <typename T, int MAXV, bool GREG>
 static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                               const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
                               int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
@@ -664,13 +708,13 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(select_pack_kernel<T, MAXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(select_pack_kernel<T, MAXV, GREG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (3 * SPECFOLD_MAX_ROWS + 1) * static_cast<int>(sizeof(int))) != cudaSuccess)
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
-  launch_k(select_pack_kernel<T, MAXV>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
+  launch_k(select_pack_kernel<T, MAXV, GREG>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
                                                           n_dev, static_cast<T*>(X1), status, n_hist, dep_off, dep_rows);
   count_launch();
@@ -683,14 +727,18 @@ static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int 
                                 int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
                               int32_t* dep_rows) {
   const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
-  if (per_lane <= 4)
-    return select_pack_launch<T, 4>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
-  if (per_lane <= 8)
-    return select_pack_launch<T, 8>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
-  if (per_lane <= 16)
-    return select_pack_launch<T, 16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
-  if (per_lane <= 32)
-    return select_pack_launch<T, 32>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status, st, n_hist, dep_off, dep_rows);
+  // gains in registers when the grid fits one wave at one block per SM
+  const bool greg = (B * L + kRowWarps - 1) / kRowWarps <= num_sms();
+#define SF_SP(MV)                                                                                                 \
+  return greg ? select_pack_launch<T, MV, true>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev,  \
+                                                X1, status, st, n_hist, dep_off, dep_rows)                        \
+              : select_pack_launch<T, MV, false>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, \
+                                                 X1, status, st, n_hist, dep_off, dep_rows)
+  if (per_lane <= 4) SF_SP(4);
+  if (per_lane <= 8) SF_SP(8);
+  if (per_lane <= 16) SF_SP(16);
+  if (per_lane <= 32) SF_SP(32);
+#undef SF_SP
   return SPECFOLD_EUNSUPPORTED;
 }
 
@@ -713,14 +761,21 @@ static void rmsnorm_dispatch(const void* X, const int32_t* idx, const int32_t* n
   const T* x = static_cast<const T*>(X);
   const T* gg = static_cast<const T*>(g);
   T* y = static_cast<T*>(Y);
+  const bool greg = static_cast<int>(grid.x) <= num_sms();
+#define SF_RN(MV)                                                                                         \
+  (greg ? launch_k(rmsnorm_rows_kernel<T, MV, true>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d,  \
+                   gg, eps, y)                                                                           \
+        : launch_k(rmsnorm_rows_kernel<T, MV, false>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, \
+                   gg, eps, y))
   if (per_lane <= 4)
-    launch_k(rmsnorm_rows_kernel<T, 4>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
+    SF_RN(4);
   else if (per_lane <= 8)
-    launch_k(rmsnorm_rows_kernel<T, 8>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
+    SF_RN(8);
   else if (per_lane <= 16)
-    launch_k(rmsnorm_rows_kernel<T, 16>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
+    SF_RN(16);
   else
-    launch_k(rmsnorm_rows_kernel<T, 32>, dim3(grid), dim3(block), 0, st, x, idx, n_dev, R, d, gg, eps, y);
+    SF_RN(32);
+#undef SF_RN
 }
 
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
