@@ -181,22 +181,6 @@ SF_DEV void epi_elem(const GemmParams& p, int k, int c, float x, float u) {
   }
 }
 
-// EPI_QKV element with the destination row r = row_idx[k] already known.
-SF_DEV void epi_qkv_elem(const GemmParams& p, int k, int r, int c, float x) {
-  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
-  const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
-  if (c < nq) {
-    const int head = c / p.hd, j = c - head * p.hd;
-    const int hk = head / p.g, hg = head - hk * p.g;
-    Y[((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j] = __float2bfloat16_rn(x);
-  } else {
-    const bool is_k = c < nq + nkv;
-    const int cc = is_k ? c - nq : c - nq - nkv;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
-    dst[static_cast<size_t>(r) * nkv + cc] = __float2bfloat16_rn(x);
-  }
-}
-
 // Split factor under clusters of cs CTAs: the largest divisor of cs that keeps
 // tiles * S within the grid and kMinKbPerSplit k-blocks per split.
 SF_DEV int split_factor_cl(int tiles, int grid, int KB, int cs) {
@@ -207,7 +191,103 @@ SF_DEV int split_factor_cl(int tiles, int grid, int KB, int cs) {
 
 struct Unit {
   int m, s, nt, kb0, kb1, tile;
+  int slot;    // fp32 partial tile written by a split unit
+  bool split;  // the unit covers part of its tile's K range
 };
+
+// Work decomposition of a plain launch for n packed rows on G CTAs.  When
+// the tiles cannot fill the grid, every tile's K loop is split S ways.  When
+// they can, the last partial wave would leave SMs idle: if it holds at most
+// half a wave (r tiles), those r tiles are split St ways instead, so the
+// last wave is full and each of its units is St times shorter.
+struct Sched {
+  int Mt, tiles, KB;
+  int S;         // split of every tile (tiles < G), else 1
+  int full;      // units [0, full) are whole tiles
+  int r, St;     // the last r tiles split St ways (St >= 2), else r = 0, St = 1
+  int U;         // units
+};
+
+SF_DEV Sched make_sched(int n, int Nt, int G, int KB) {
+  Sched c;
+  c.Mt = (n + kBM - 1) / kBM;
+  c.tiles = c.Mt * Nt;
+  c.KB = KB;
+  c.S = 1;
+  c.full = c.tiles;
+  c.r = 0;
+  c.St = 1;
+  if (c.tiles < G) {
+    c.S = split_factor(c.tiles, G, KB);
+  } else {
+    const int r = c.tiles % G;
+    if (r > 0 && 2 * r <= G) {
+      const int St = min(min(G / r, KB / kMinKbPerSplit), kMaxSplits);
+      if (St >= 2) {
+        c.r = r;
+        c.St = St;
+        c.full = c.tiles - r;
+      }
+    }
+  }
+  c.U = c.S > 1 ? c.tiles * c.S : c.full + c.r * c.St;
+  return c;
+}
+
+SF_DEV Unit decode_plain(int u, const Sched& c, int Nt) {
+  Unit w;
+  if (c.S > 1) {
+    w.m = u % c.Mt;
+    const int rest = u / c.Mt;
+    w.s = rest % c.S;
+    w.nt = rest / c.S;
+    w.kb0 = (w.s * c.KB) / c.S;
+    w.kb1 = ((w.s + 1) * c.KB) / c.S;
+    w.tile = w.m * Nt + w.nt;
+    w.slot = w.tile * c.S + w.s;
+    w.split = true;
+  } else if (u < c.full) {
+    w.m = u % c.Mt;
+    w.nt = u / c.Mt;
+    w.s = 0;
+    w.kb0 = 0;
+    w.kb1 = c.KB;
+    w.tile = w.m * Nt + w.nt;
+    w.slot = 0;
+    w.split = false;
+  } else {
+    const int v = u - c.full;
+    const int q = v / c.St;
+    w.s = v - q * c.St;
+    const int t = c.full + q;  // whole-tile unit index of this tail tile
+    w.m = t % c.Mt;
+    w.nt = t / c.Mt;
+    w.kb0 = (w.s * c.KB) / c.St;
+    w.kb1 = ((w.s + 1) * c.KB) / c.St;
+    w.tile = w.m * Nt + w.nt;
+    w.slot = q * c.St + w.s;
+    w.split = true;
+  }
+  return w;
+}
+
+// Whether tile (m, nt) was split, by how many, and its first partial slot.
+SF_DEV bool tile_split(const Sched& c, int m, int nt, int Nt, int& nsplit, int& slot0) {
+  if (c.S > 1) {
+    nsplit = c.S;
+    slot0 = (m * Nt + nt) * c.S;
+    return true;
+  }
+  if (c.St > 1) {
+    const int u = m + c.Mt * nt;
+    if (u >= c.full) {
+      nsplit = c.St;
+      slot0 = (u - c.full) * c.St;
+      return true;
+    }
+  }
+  return false;
+}
 
 // Work unit u.  Plain: m fastest, then split, then n-tile.  Clustered split
 // (dsm): the S consecutive CTAs u = tile * S + s share one tile, so they sit
@@ -228,6 +308,8 @@ SF_DEV Unit decode(int u, int Mt, int S, int Nt, int KB, bool dsm) {
   w.kb0 = (w.s * KB) / S;
   w.kb1 = ((w.s + 1) * KB) / S;
   w.tile = w.m * Nt + w.nt;
+  w.slot = w.tile * S + w.s;
+  w.split = S > 1;
   return w;
 }
 
@@ -337,10 +419,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
   const int KB = p.K / kBK;
-  const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs)
-                  : split_factor(tiles, static_cast<int>(gridDim.x), KB);
+  const Sched sc = make_sched(n, p.Nt, static_cast<int>(gridDim.x), KB);
+  const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs) : sc.S;
   const bool dsm = CL && S > 1;  // splits summed through distributed shared memory
-  const int U = tiles * S;
+  const int U = CL ? tiles * S : sc.U;
+  auto unit = [&](int u) { return CL ? decode(u, Mt, S, p.Nt, KB, dsm) : decode_plain(u, sc, p.Nt); };
   if (static_cast<int>(blockIdx.x) >= U) {
     if constexpr (CL) {
       if (dsm) {  // an idle CTA still takes part in its cluster's two barriers
@@ -383,7 +466,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
+        const Unit w = unit(u);
         const CUtensorMap* mlo;
         const CUtensorMap* mhi;
         int ylo, yhi;
@@ -431,7 +514,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t it = 0, t = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++t) {
-        const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
+        const Unit w = unit(u);
         const int ab = t & 1;
         if (!mbar_wait(smem_u32(&acce[ab]), ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -468,7 +551,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const int et = threadIdx.x - 64;    // 0..127
     uint32_t t = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++t) {
-      const Unit w = decode(u, Mt, S, p.Nt, KB, dsm);
+      const Unit w = unit(u);
       const int ab = t & 1;
       if (et == 0) *s_ok = mbar_wait(smem_u32(&accf[ab]), (t >> 1) & 1, abort_flag, p.status) ? 1 : 0;
       named_bar_sync(1, 128);
@@ -510,8 +593,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       // lane j holds the row index of the warp's row j (broadcast by shuffle)
       int ridx = 0;
       if constexpr (EPI == EPI_QKV || EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER)
-        if (S == 1 && lane < rows_here) ridx = p.row_idx[row0 + lane];
-      float* prow = p.partial + (static_cast<size_t>(w.tile) * S + w.s) * kBM * BN + static_cast<size_t>(q * 32) * BN;
+        if (!w.split && lane < rows_here) ridx = p.row_idx[row0 + lane];
+      float* prow = p.partial + static_cast<size_t>(w.slot) * kBM * BN + static_cast<size_t>(q * 32) * BN;
       constexpr int NCH = EPI == EPI_SWIGLU ? BN / 64 : BN / 32;
       for (int ch = 0; ch < NCH; ++ch) {
         uint32_t r[32];
@@ -533,7 +616,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           for (int e = 0; e < 32; ++e) stg[lane * 33 + e] = __uint_as_float(r2[e]);
         }
         __syncwarp();
-        if (S == 1) {
+        if (!w.split) {
           const int cbase = EPI == EPI_SWIGLU ? w.nt * (BN / 2) + ch * 32 : w.nt * BN + ch * 32;
           const int c = cbase + lane;
           __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
@@ -553,10 +636,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 Y[static_cast<size_t>(rdst) * p.ldy + c] = __float2bfloat16_rn(stg[rr * 33 + lane] + rv[rr]);
             }
           } else if constexpr (EPI == EPI_QKV) {
+            // the 32 columns of a chunk lie in one head (hd % 32 == 0): the
+            // destination is decomposed once per chunk, not per element
+            const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+            if (cbase < nq) {
+              const int head = cbase / p.hd;
+              const int hk = head / p.g, hg = head - hk * p.g;
+              const size_t rstride = static_cast<size_t>(p.g) * p.hd;
+              __nv_bfloat16* qb = Y + (static_cast<size_t>(hk) * p.R * p.g + hg) * p.hd + (cbase - head * p.hd) + lane;
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-              const int r = __shfl_sync(0xffffffffu, ridx, rr);
-              if (rr < rows_here) epi_qkv_elem(p, row0 + rr, r, c, stg[rr * 33 + lane]);
+              for (int rr = 0; rr < 32; ++rr)
+                if (rr < rows_here) qb[static_cast<size_t>(row0 + rr) * rstride] = __float2bfloat16_rn(stg[rr * 33 + lane]);
+            } else {
+              const bool is_k = cbase < nq + nkv;
+              __nv_bfloat16* kb = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv) +
+                                  (is_k ? cbase - nq : cbase - nq - nkv) + lane;
+#pragma unroll
+              for (int rr = 0; rr < 32; ++rr) {
+                const int r = __shfl_sync(0xffffffffu, ridx, rr);
+                if (rr < rows_here) kb[static_cast<size_t>(r) * nkv] = __float2bfloat16_rn(stg[rr * 33 + lane]);
+              }
             }
           } else {
 #pragma unroll
@@ -649,28 +748,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const int Mt = (n + kBM - 1) / kBM;
-  const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
-  if constexpr (EPI == EPI_RESID_SCATTER) {
-    if (S <= 1 && p.dep_off) {
-      // unsplit GEMM: its epilogue wrote Y[s]; fill the dependents only
-      const int groups = p.N / 8;
-      const long long total = static_cast<long long>(n) * groups;
-      for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-           idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int k = static_cast<int>(idx / groups);
-        const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
-        if (p.dep_off[k + 1] <= p.dep_off[k]) continue;
-        float yb[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) yb[e] = 0.f;
-        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, yb);
-        fill_dependents<BN, EPI>(p, k, c, yb);
-      }
-      return;
-    }
-  }
-  if (S <= 1) return;
+  const Sched sc = make_sched(n, p.Nt, gemm_grid, p.K / kBK);
+  bool fill = false;
+  if constexpr (EPI == EPI_RESID_SCATTER) fill = p.dep_off != nullptr;
+  if (sc.S <= 1 && sc.St <= 1 && !fill) return;  // nothing split, nothing to fill
   constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;   // output columns per tile
   const int groups = (p.Nt * TW) / 8;
   const long long total = static_cast<long long>(n) * groups;
@@ -680,8 +761,21 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
     const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
     const int nt = c / TW, tc = c - nt * TW;
     const int m = k / kBM, row = k - m * kBM;
-    const float* base = p.partial + (static_cast<size_t>(m * p.Nt + nt) * S) * kBM * BN +
-                        static_cast<size_t>(row) * BN + tc;
+    int S = 1, slot0 = 0;
+    if (!tile_split(sc, m, nt, p.Nt, S, slot0)) {
+      if constexpr (EPI == EPI_RESID_SCATTER) {
+        // unsplit tile: the GEMM epilogue wrote Y[s]; fill the dependents only
+        if (fill && p.dep_off[k + 1] > p.dep_off[k]) {
+          float yb[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) yb[e] = 0.f;
+          add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, yb);
+          fill_dependents<BN, EPI>(p, k, c, yb);
+        }
+      }
+      continue;
+    }
+    const float* base = p.partial + static_cast<size_t>(slot0) * kBM * BN + static_cast<size_t>(row) * BN + tc;
     float v[8], u[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] = u[e] = 0.f;
@@ -724,15 +818,15 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
       }
     }
     if constexpr (EPI == EPI_RESID_SCATTER) {
-      if (p.dep_off) {
+      if (fill) {
         // the residual add and the bf16 rounding of the stored row, then the fill
-        const int c = nt * TW + tc;
-        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + c, v);
-        store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, v);
+        const int cc = nt * TW + tc;
+        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + cc, v);
+        store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + cc, v);
         float yb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) yb[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-        fill_dependents<BN, EPI>(p, k, c, yb);
+        fill_dependents<BN, EPI>(p, k, cc, yb);
         continue;
       }
     }
@@ -755,8 +849,7 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int k = blockIdx.x;
   if (k >= n) return;
-  const int Mt = (n + kBM - 1) / kBM;
-  const int S = split_factor(Mt * p.Nt, gemm_grid, p.K / kBK);
+  const Sched sc = make_sched(n, p.Nt, gemm_grid, p.K / kBK);
   const int groups = p.N / 8;
   const int m = k / kBM, row = k - m * kBM;
   __nv_bfloat16* Arow = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(k) * p.ldy;
@@ -767,10 +860,10 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
     const int gi = threadIdx.x + 256 * j;
     if (gi >= groups) break;
     const int c = gi * 8;
-    if (S > 1) {
-      const int nt = c / BN, tc = c - nt * BN;
-      const float* base = p.partial + (static_cast<size_t>(m * p.Nt + nt) * S) * kBM * BN +
-                          static_cast<size_t>(row) * BN + tc;
+    const int nt = c / BN, tc = c - nt * BN;
+    int S = 1, slot0 = 0;
+    if (tile_split(sc, m, nt, p.Nt, S, slot0)) {
+      const float* base = p.partial + static_cast<size_t>(slot0) * kBM * BN + static_cast<size_t>(row) * BN + tc;
       float acc[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -945,9 +1038,16 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
       return check_launch();
     }
   }
-  // a split is possible only if even one m-tile leaves SMs idle; the fold-fill
-  // of the down projection runs in this kernel in any case
-  if ((grid / p.Nt >= 2 && p.K / kBK >= 2 * kMinKbPerSplit) || p.dep_off) {
+  // a split is possible only if even one m-tile leaves SMs idle, or if some
+  // n <= Mcap leaves a partial last wave of at most half the grid (tail
+  // split); the fold-fill of the down projection runs in this kernel anyway
+  bool tail = false;
+  const int KB = p.K / kBK;
+  for (int mt = 1; !tail && mt <= (c.Mcap + kBM - 1) / kBM; ++mt) {
+    const int tiles = mt * p.Nt, r = tiles % grid;
+    tail = tiles >= grid && r > 0 && 2 * r <= grid && std::min(grid / r, KB / kMinKbPerSplit) >= 2;
+  }
+  if ((grid / p.Nt >= 2 && KB >= 2 * kMinKbPerSplit) || tail || p.dep_off) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
