@@ -62,12 +62,25 @@ struct AttnParams {
   float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
 };
 
-// Number of key-range splits for n packed rows: as many CTAs as fit on the
-// SMs in one wave (one CTA per SM: a second wave would double the time).
-SF_DEV int attn_splits(int rows_total, int n_kv, int sp_max, int num_sms) {
+// Number of key-range splits for n packed rows.  With one CTA per SM, S
+// splits cost about ceil(tiles * S / SMs) waves, each CTA paying a fixed
+// cost (setup, first loads, write-out: about two key blocks) plus its share
+// NB / S of the key blocks; take the S with the least cost (the smallest on a
+// near tie, since a split adds the combine step).
+SF_DEV int attn_splits(int rows_total, int n_kv, int sp_max, int num_sms, int P) {
   const int tiles = ((rows_total + 127) / 128) * n_kv;
   if (tiles <= 0) return 1;
-  return max(1, min(sp_max, num_sms / tiles));
+  const float nb = static_cast<float>((P + 127) / 128 + 1);
+  int best = 1;
+  float best_t = static_cast<float>((tiles + num_sms - 1) / num_sms) * (2.f + nb);
+  for (int sp = 2; sp <= sp_max && sp <= nb + 1; ++sp) {  // the block keys may span two blocks
+    const float t = static_cast<float>((tiles * sp + num_sms - 1) / num_sms) * (2.f + nb / sp);
+    if (t < best_t * 0.97f) {
+      best = sp;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 template <int HD>
@@ -79,7 +92,7 @@ struct ACfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;          // stage s: K at +2s*KV, V at +(2s+1)*KV
   static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
-  static constexpr int OFF_META = OFF_P + P_BYTES;          // int [2][128]
+  static constexpr int OFF_META = OFF_P + 2 * P_BYTES;      // two P tiles, then int [2][128]
   static constexpr int OFF_BAR = OFF_META + 2 * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -101,8 +114,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint64_t* kv_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;    // [2]
   uint64_t* s_free = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_full = bars + 10;   // one completion per P V product
+  uint64_t* p_full = bars + 9;    // [2]: P tile t & 1 written
+  uint64_t* o_full = bars + 11;   // [2]: P V of block t done (block t commits to [t & 1])
   uint64_t* drain = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int NBP = (p.P + 127) / 128;
   const int NB = NBP + (keys_blk + 127) / 128;
   // this CTA's share of the key blocks
-  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms);
+  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms, p.P);
   const int z = blockIdx.z;
   if (z >= SP) return;
   const int jb = (z * NB) / SP;
@@ -150,8 +163,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&s_free[i]), 128);
 
     }
-    mbar_init(smem_u32(p_full), 128);
-    mbar_init(smem_u32(o_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&p_full[i]), 128);
+      mbar_init(smem_u32(&o_full[i]), 1);
+    }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -320,12 +335,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
       tc_fence_before();
       mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
-      float mx = -INFINITY;
+      // a whole prefix block needs no mask; eight independent max chains
+      // (one warp per SM sub-partition: a single 128-deep chain would stall)
+      const bool allv = prefix && p.P - key0 >= 128;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+      if (allv) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx = fmaxf(mx, ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx8[e & 7] = fmaxf(mx8[e & 7], ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_ref, mx * p.sl2);
       float alpha = 1.f;
       bool rescale = false;
@@ -337,13 +366,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         rescale = true;
       }
       l *= alpha;
-      if (t >= 1) {
-        // P V of the previous block must be done: it frees the P tile, and O
-        // may only be rescaled once it holds that block's contribution
-        if (!mbar_wait(smem_u32(&o_full[0]), (t - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      // two P tiles: P V of block t - 2 must be done before tile t & 1 is
+      // rewritten; O may only be rescaled once it holds block t - 1
+      if (t >= 2) {
+        if (!mbar_wait(smem_u32(&o_full[t & 1]), ((t >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        __syncwarp();
+      }
+      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+        if (!mbar_wait(smem_u32(&o_full[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
         __syncwarp();
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        {
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t r[32];
@@ -356,33 +392,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           tmem_st_wait();
         }
       }
-      // probabilities -> bf16 P tile (K-major, 128-byte swizzle)
+      // probabilities -> bf16 P tile (K-major, 128-byte swizzle); the row sum
+      // in four independent partial sums
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
+        if (allv) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float x = ex2(fmaf(__uint_as_float(sv[c][e + u]), p.sl2, -m_ref));
-            pv[u] = ((km[c] >> (e + u)) & 1u) ? x : 0.f;
-            l += pv[u];
+          for (int e = 0; e < 32; e += 2) {
+            const float x0 = ex2(fmaf(__uint_as_float(sv[c][e]), p.sl2, -m_ref));
+            const float x1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), p.sl2, -m_ref));
+            ls[(e >> 1) & 3] += x0 + x1;
+            pk[e / 2] = pack_bf16x2(x0, x1);
           }
-          pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float x = ex2(fmaf(__uint_as_float(sv[c][e + u]), p.sl2, -m_ref));
+              pv[u] = ((km[c] >> (e + u)) & 1u) ? x : 0.f;
+            }
+            ls[(e >> 1) & 3] += pv[0] + pv[1];
+            pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+          }
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
-          const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+          const int off = (t & 1) * C::P_BYTES + (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
           *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
         }
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(p_full));
+      mbar_arrive(smem_u32(&p_full[t & 1]));
     }
-    if (ok && mbar_wait(smem_u32(&o_full[0]), (NT - 1) & 1, abort_flag, p.status)) {
+    if (ok && mbar_wait(smem_u32(&o_full[(NT - 1) & 1]), ((NT - 1) >> 1) & 1, abort_flag, p.status)) {
       __syncwarp();
       tc_fence_after();
       if (SP > 1) {
@@ -430,15 +479,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aP = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {  // i: local block index
-        if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(smem_u32(&p_full[i & 1]), (i >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
+        const uint32_t aPi = aP + (i & 1) * C::P_BYTES;
         const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (i & 1) + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aPi + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
                      sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&o_full[0]));
+        tc_commit(smem_u32(&o_full[i & 1]));
         tc_commit(smem_u32(&kv_empty[i & 1]));
         return true;
       };
@@ -481,7 +531,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   pdl_trigger();
   const int n = min(max(p.n_dev[0], 0), p.R);
   const int rows_total = n * p.g;
-  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms);
+  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms, p.P);
   if (SP <= 1) return;
   constexpr int DG = HD / 8;
   const long long total = static_cast<long long>(rows_total) * p.n_kv * DG;
