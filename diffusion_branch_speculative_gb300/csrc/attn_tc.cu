@@ -58,29 +58,19 @@ struct AttnParams {
   const __nv_bfloat16* pkp;  // prefix K / V base (pool or contiguous view)
   const __nv_bfloat16* pvp;
   long long k_ts, k_hs, v_ts, v_hs;  // token and head strides, elements
+  uint8_t sp_table[1024];            // key-range splits by tile count (see plan_splits)
   float* part_o;    // [tiles_x * n_kv * sp_max][128][hd]
   float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
 };
 
-// Number of key-range splits for n packed rows.  With one CTA per SM, S
-// splits cost about ceil(tiles * S / SMs) waves, each CTA paying a fixed
-// cost (setup, first loads, write-out: about two key blocks) plus its share
-// NB / S of the key blocks; take the S with the least cost (the smallest on a
-// near tie, since a split adds the combine step).
-SF_DEV int attn_splits(int rows_total, int n_kv, int sp_max, int num_sms, int P) {
-  const int tiles = ((rows_total + 127) / 128) * n_kv;
-  if (tiles <= 0) return 1;
-  const float nb = static_cast<float>((P + 127) / 128 + 1);
-  int best = 1;
-  float best_t = static_cast<float>((tiles + num_sms - 1) / num_sms) * (2.f + nb);
-  for (int sp = 2; sp <= sp_max && sp <= nb + 1; ++sp) {  // the block keys may span two blocks
-    const float t = static_cast<float>((tiles * sp + num_sms - 1) / num_sms) * (2.f + nb / sp);
-    if (t < best_t * 0.97f) {
-      best = sp;
-      best_t = t;
-    }
-  }
-  return best;
+// Number of key-range splits for n packed rows, looked up from a table the
+// host fills per launch (sp_table[tiles - 1]; beyond it, no split).  See
+// plan_splits for the rule.
+constexpr int kSpTable = 1024;
+SF_DEV int attn_splits(const AttnParams& p, int rows_total) {
+  const int tiles = ((rows_total + 127) / 128) * p.n_kv;
+  if (tiles <= 0 || tiles > kSpTable) return 1;
+  return p.sp_table[tiles - 1];
 }
 
 template <int HD>
@@ -92,7 +82,7 @@ struct ACfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;          // stage s: K at +2s*KV, V at +(2s+1)*KV
   static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
-  static constexpr int OFF_META = OFF_P + 2 * P_BYTES;      // two P tiles, then int [2][128]
+  static constexpr int OFF_META = OFF_P + P_BYTES;          // int [2][128]
   static constexpr int OFF_BAR = OFF_META + 2 * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -114,8 +104,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint64_t* kv_empty = bars + 3;  // [2]
   uint64_t* s_full = bars + 5;    // [2]
   uint64_t* s_free = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;    // [2]: P tile t & 1 written
-  uint64_t* o_full = bars + 11;   // [2]: P V of block t done (block t commits to [t & 1])
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_full = bars + 10;   // one completion per P V product
   uint64_t* drain = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -139,7 +129,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int NBP = (p.P + 127) / 128;
   const int NB = NBP + (keys_blk + 127) / 128;
   // this CTA's share of the key blocks
-  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms, p.P);
+  const int SP = attn_splits(p, rows_total);
   const int z = blockIdx.z;
   if (z >= SP) return;
   const int jb = (z * NB) / SP;
@@ -163,10 +153,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&s_free[i]), 128);
 
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&p_full[i]), 128);
-      mbar_init(smem_u32(&o_full[i]), 1);
-    }
+    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(o_full), 1);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -366,20 +354,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         rescale = true;
       }
       l *= alpha;
-      // two P tiles: P V of block t - 2 must be done before tile t & 1 is
-      // rewritten; O may only be rescaled once it holds block t - 1
-      if (t >= 2) {
-        if (!mbar_wait(smem_u32(&o_full[t & 1]), ((t >> 1) - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        __syncwarp();
-      }
-      if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
-        if (!mbar_wait(smem_u32(&o_full[(t - 1) & 1]), ((t - 1) >> 1) & 1, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
+      if (t >= 1) {
+        // P V of the previous block must be done: it frees the P tile, and O
+        // may only be rescaled once it holds that block's contribution
+        if (!mbar_wait(smem_u32(o_full), (t - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         __syncwarp();
         tc_fence_after();
-        {
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t r[32];
@@ -422,16 +403,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
-          const int off = (t & 1) * C::P_BYTES + (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+          const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
           *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
         }
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&p_full[t & 1]));
+      mbar_arrive(smem_u32(p_full));
     }
-    if (ok && mbar_wait(smem_u32(&o_full[(NT - 1) & 1]), ((NT - 1) >> 1) & 1, abort_flag, p.status)) {
+    if (ok && mbar_wait(smem_u32(o_full), (NT - 1) & 1, abort_flag, p.status)) {
       __syncwarp();
       tc_fence_after();
       if (SP > 1) {
@@ -479,16 +460,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aP = smem_u32(sP);
       auto issue_pv = [&](int i) -> bool {  // i: local block index
-        if (!mbar_wait(smem_u32(&p_full[i & 1]), (i >> 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t aPi = aP + (i & 1) * C::P_BYTES;
+        const uint32_t aPi = aP;
         const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (i & 1) + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aPi + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
                      sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&o_full[i & 1]));
+        tc_commit(smem_u32(o_full));
         tc_commit(smem_u32(&kv_empty[i & 1]));
         return true;
       };
@@ -531,7 +512,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   pdl_trigger();
   const int n = min(max(p.n_dev[0], 0), p.R);
   const int rows_total = n * p.g;
-  const int SP = attn_splits(rows_total, p.n_kv, p.sp_max, p.num_sms, p.P);
+  const int SP = attn_splits(p, rows_total);
   if (SP <= 1) return;
   constexpr int DG = HD / 8;
   const long long total = static_cast<long long>(rows_total) * p.n_kv * DG;
@@ -587,6 +568,26 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   }
 }
 
+// Split count for `tiles` (query tile, KV head) pairs: with one CTA per SM,
+// S splits cost about ceil(tiles * S / SMs) waves, each CTA paying a fixed
+// cost (setup, first loads, write-out: about two key blocks) plus its share
+// nb / S of the key blocks; the S with the least cost (the smallest on a near
+// tie, since a split adds the combine step), at most one more than the key
+// blocks (the block keys may span two).
+int plan_splits(int tiles, int sp_max, int num_sms, int P) {
+  const float nb = static_cast<float>((P + 127) / 128 + 1);
+  int best = 1;
+  float best_t = static_cast<float>((tiles + num_sms - 1) / num_sms) * (2.f + nb);
+  for (int sp = 2; sp <= sp_max && sp <= nb + 1; ++sp) {
+    const float t = static_cast<float>((tiles * sp + num_sms - 1) / num_sms) * (2.f + nb / sp);
+    if (t < best_t * 0.97f) {
+      best = sp;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
 template <int HD>
 int run_attn(const AttnCall& c, cudaStream_t st) {
   using C = ACfg<HD>;
@@ -634,6 +635,9 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   const int tiles_x = (R * g + 127) / 128;
   p.sp_max = attn_sp_max(R, g, c.n_kv);
   p.num_sms = num_sms();
+  const int tiles_max = std::min(((R * g + 127) / 128) * c.n_kv, kSpTable);  // n <= R
+  for (int t = 1; t <= tiles_max; ++t)
+    p.sp_table[t - 1] = static_cast<uint8_t>(plan_splits(t, p.sp_max, p.num_sms, c.P));
   if (p.sp_max > 1) {
     if (!c.part || c.part_bytes < attn_partial_bytes(R, g, c.n_kv, HD)) return SPECFOLD_ECAPACITY;
     p.part_o = static_cast<float*>(c.part);
