@@ -531,7 +531,7 @@ def stress_sweep(args, flush, barrier):
         H.copy_(to(br.H))
         parent.copy_(torch.from_numpy(br.graph.parent.astype(np.int32)))
         g = lay.graph(H, parent, tau, out)
-        for _ in range(3):
+        for _ in range(10):
             flush()
             g.launch()
         torch.cuda.synchronize()

@@ -40,6 +40,7 @@ constexpr int kMaxGrid = 160;        // persistent CTAs (>= SMs of one GB300)
 constexpr int kMaxSplits = 16;
 constexpr int kMinKbPerSplit = 4;
 constexpr int kMaxClusterSplit = 8;  // largest cluster (portable size)
+constexpr int kSchedRows = SPECFOLD_MAX_ROWS / 128;  // m-tile counts
 
 template <int BN>
 struct Cfg {
@@ -78,6 +79,9 @@ struct GemmParams {
   const int32_t* dep_off;   // RESID_SCATTER: fold-fill of dependents in the finish kernel
   const int32_t* dep_rows;
   const __nv_bfloat16* hin;
+  // work decomposition per m-tile count Mt (row Mt - 1): S, full, r, St, U
+  // (see Sched); filled by the host for this launch's grid
+  int sched[kSchedRows][5];
 };
 
 SF_DEV float silu(float x) { return __fdividef(x, 1.f + ex2(-x * 1.4426950408889634f)); }
@@ -140,11 +144,12 @@ SF_DEV void epi_chunk(const GemmParams& p, int k, int c, float (&v)[W], const fl
 
 // Split factor of the K loop for n packed rows: only when the m x n tiles
 // cannot fill the grid, and never below kMinKbPerSplit k-blocks per split.
-SF_DEV int split_factor(int tiles, int grid, int KB) {
+__host__ __device__ inline int split_factor(int tiles, int grid, int KB) {
   int S = 1;
   if (tiles > 0 && tiles < grid) {
-    S = min(grid / tiles, KB / kMinKbPerSplit);
-    S = max(1, min(S, kMaxSplits));
+    S = grid / tiles < KB / kMinKbPerSplit ? grid / tiles : KB / kMinKbPerSplit;
+    S = S < kMaxSplits ? S : kMaxSplits;
+    S = S > 1 ? S : 1;
   }
   return S;
 }
@@ -208,7 +213,7 @@ struct Sched {
   int U;         // units
 };
 
-SF_DEV Sched make_sched(int n, int Nt, int G, int KB) {
+__host__ __device__ inline Sched make_sched(int n, int Nt, int G, int KB) {
   Sched c;
   c.Mt = (n + kBM - 1) / kBM;
   c.tiles = c.Mt * Nt;
@@ -222,7 +227,8 @@ SF_DEV Sched make_sched(int n, int Nt, int G, int KB) {
   } else {
     const int r = c.tiles % G;
     if (r > 0 && 2 * r <= G) {
-      const int St = min(min(G / r, KB / kMinKbPerSplit), kMaxSplits);
+      int St = G / r < KB / kMinKbPerSplit ? G / r : KB / kMinKbPerSplit;
+      St = St < kMaxSplits ? St : kMaxSplits;
       if (St >= 2) {
         c.r = r;
         c.St = St;
@@ -231,6 +237,21 @@ SF_DEV Sched make_sched(int n, int Nt, int G, int KB) {
     }
   }
   c.U = c.S > 1 ? c.tiles * c.S : c.full + c.r * c.St;
+  return c;
+}
+
+// The launch's schedule for n rows, from the host-filled table.
+SF_DEV Sched get_sched(const int (&tab)[kSchedRows][5], int n, int Nt, int KB) {
+  Sched c;
+  c.Mt = (n + kBM - 1) / kBM;
+  c.tiles = c.Mt * Nt;
+  c.KB = KB;
+  if (c.Mt <= 0 || c.Mt > kSchedRows) {
+    c.S = 1, c.full = c.tiles, c.r = 0, c.St = 1, c.U = c.tiles;
+    return c;
+  }
+  const int* e = tab[c.Mt - 1];
+  c.S = e[0], c.full = e[1], c.r = e[2], c.St = e[3], c.U = e[4];
   return c;
 }
 
@@ -419,7 +440,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
   const int KB = p.K / kBK;
-  const Sched sc = make_sched(n, p.Nt, static_cast<int>(gridDim.x), KB);
+  const Sched sc = get_sched(p.sched, n, p.Nt, KB);
   const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs) : sc.S;
   const bool dsm = CL && S > 1;  // splits summed through distributed shared memory
   const int U = CL ? tiles * S : sc.U;
@@ -748,7 +769,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const Sched sc = make_sched(n, p.Nt, gemm_grid, p.K / kBK);
+  const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   bool fill = false;
   if constexpr (EPI == EPI_RESID_SCATTER) fill = p.dep_off != nullptr;
   if (sc.S <= 1 && sc.St <= 1 && !fill) return;  // nothing split, nothing to fill
@@ -849,7 +870,7 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int k = blockIdx.x;
   if (k >= n) return;
-  const Sched sc = make_sched(n, p.Nt, gemm_grid, p.K / kBK);
+  const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   const int groups = p.N / 8;
   const int m = k / kBM, row = k - m * kBM;
   __nv_bfloat16* Arow = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(k) * p.ldy;
@@ -916,6 +937,25 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
     o[6] = v[j][6] * inv * bf16lo(gu.w); o[7] = v[j][7] * inv * bf16hi(gu.w);
     store_bf16<8>(X2 + static_cast<size_t>(k) * p.N + c, o);
   }
+}
+
+// Fills the schedule table of a plain launch on `grid` CTAs (one row per
+// m-tile count up to Mcap) and returns whether some n <= Mcap splits a tile,
+// i.e. whether the finish kernel has partial tiles to sum.
+bool fill_sched(GemmParams& p, int Mcap, int grid) {
+  const int KB = p.K / kBK;
+  const int mt_max = std::min((Mcap + kBM - 1) / kBM, kSchedRows);
+  bool split = false;
+  for (int mt = 1; mt <= mt_max; ++mt) {
+    const Sched sc = make_sched(mt * kBM, p.Nt, grid, KB);
+    p.sched[mt - 1][0] = sc.S;
+    p.sched[mt - 1][1] = sc.full;
+    p.sched[mt - 1][2] = sc.r;
+    p.sched[mt - 1][3] = sc.St;
+    p.sched[mt - 1][4] = sc.U;
+    split = split || sc.S > 1 || sc.St > 1;
+  }
+  return split;
 }
 
 // Clusters of cs CTAs of the GEMM (one CTA per SM) that can be resident at
@@ -1005,6 +1045,9 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
+  // schedule table for the plain grid (a clustered launch computes its own
+  // split and sums it inside the GEMM)
+  const bool any_split = fill_sched(p, c.Mcap, min(num_sms(), kMaxGrid));
   if (cs > 1) {
     // clustered: the splits are summed inside the GEMM
     p.cs = cs;
@@ -1038,16 +1081,9 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
       return check_launch();
     }
   }
-  // a split is possible only if even one m-tile leaves SMs idle, or if some
-  // n <= Mcap leaves a partial last wave of at most half the grid (tail
-  // split); the fold-fill of the down projection runs in this kernel anyway
-  bool tail = false;
-  const int KB = p.K / kBK;
-  for (int mt = 1; !tail && mt <= (c.Mcap + kBM - 1) / kBM; ++mt) {
-    const int tiles = mt * p.Nt, r = tiles % grid;
-    tail = tiles >= grid && r > 0 && 2 * r <= grid && std::min(grid / r, KB / kMinKbPerSplit) >= 2;
-  }
-  if ((grid / p.Nt >= 2 && KB >= 2 * kMinKbPerSplit) || tail || p.dep_off) {
+  // the finish kernel sums split tiles; the fold-fill of the down projection
+  // runs in it in any case
+  if (any_split || p.dep_off) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
@@ -1217,10 +1253,11 @@ int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* 
       return SPECFOLD_ECUDA;
     attr_done[dev] = 1;
   }
+  const bool any_split = fill_sched(p, M, grid);
   launch_k(gemm_kernel<BN, EPI_STORE, false>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
-  if (grid / p.Nt >= 2 && K / kBK >= 2 * kMinKbPerSplit) {
+  if (any_split) {
     const long long work = static_cast<long long>(M) * (p.Nt * BN / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
     launch_k(splitk_reduce_kernel<BN, EPI_STORE>, dim3(std::max(rgrid, 1)), dim3(256), 0, st, p, grid);

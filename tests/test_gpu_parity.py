@@ -26,7 +26,8 @@ def _lib():
 # ------------------------------------------------------------ GEMM engine --
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (100, 256, 512), (300, 384, 1024), (129, 3584, 3584),
-                                   (64, 3584, 18944), (2048, 1024, 4096)])
+                                   (64, 3584, 18944), (2048, 1024, 4096),
+                                   (2560, 2048, 1024)])   # 160 tiles: the last 8 split along K
 def test_linear_matches_fp64(M, N, K):
     rng = np.random.default_rng(M + N + K)
     X = synth.round_bf16(rng.standard_normal((M, K)).astype(np.float32))

@@ -24,7 +24,8 @@ def _rel_l2(a, b):
     return float((a - b).norm() / b.norm())
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 3584, 18944), (95, 4608, 3584), (300, 384, 1024), (2048, 1024, 4096)])
+@pytest.mark.parametrize("M,N,K", [(64, 3584, 18944), (95, 4608, 3584), (300, 384, 1024), (2048, 1024, 4096),
+                                   (2176, 2048, 1024)])   # the last one splits the tiles of a partial last wave
 def test_linear_noalloc_matches_workspace_linear(M, N, K):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
