@@ -23,6 +23,10 @@ noted):
                  own diff" sentence; page 4 (iitog.ru, "SpecFold ...до 1,99x",
                  key facts): folded attention and FFN keep the residual hidden
                  states.  Folded rows take out = out_src + (H_in - H_in,src).
+  * variants  -- ``layer_forward_sublayers``: the implementation note's
+                 correction read literally (folded positions' attention
+                 matched again against their own branch's keys and values)
+                 and one gate per sublayer.
 
 Readings where the pages are silent or garbled (each listed in the design doc):
   fold iff r < tau (so tau = 0 folds nothing); the comparison is done squared
@@ -32,7 +36,7 @@ Readings where the pages are silent or garbled (each listed in the design doc):
   whole prefix and the branch's own block, never across branches; block keys
   and values of a folded position are those of its resolved source row.
 
-Parity pins: see tests/test_oracle_pins.py.  The outputs of folded rows are
+Parity pins: see tests/test_oracle_pins.py (and the *_pins.py files beside it).  The outputs of folded rows are
 pinned only by the invariants that define them (I2, I6); their quality against
 an unfolded model is an accuracy question the pages leave to task benchmarks,
 so that comparison is "parity unpinned" by design.
@@ -313,6 +317,110 @@ def layer_forward(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
         "X1": np.stack([X1[r] for r in act]), "Q": Q, "K_rows": K_rows, "V_rows": V_rows,
         "attnO": attnO, "A": A, "X2": X2, "G": G, "out_act": out_act,
         "out_rows": np.array(want, dtype=np.int64), "out": out,
+    }
+
+
+# ---------------------------------------------------------------------------
+# variant readings of the attention correction and of the gate's scope
+# ---------------------------------------------------------------------------
+
+def layer_forward_sublayers(H, parent, W, prefK, prefV, tau, eps, n_kv, hd,
+                            attn_rematch: bool = False, ffn_gate: bool = False,
+                            force=None, force_ffn=None, rope_theta: float = 0.0,
+                            gate_ref: str = "parent") -> dict:
+    """The folded layer under two variant readings, over all B*L rows.
+
+    attn_rematch -- the implementation note's correction taken literally:
+      "the attention output of a folded position is matched again against
+      its branch's own keys and values".  Every folded row (b, i) runs
+      attention: its query is its source's query (the row whose state it
+      reuses), its keys and values are the prefix plus branch b's own block
+      (block key j being the K/V of row src(b, j), as for every row).  Its
+      attention sublayer output A = H + attnO W_o^T is therefore its own, and a
+      change elsewhere in the branch reaches it (the "ripple" of the paper's
+      section 4.4).  Its FFN sublayer stays folded: out = A + (out_s - A_s).
+    ffn_gate -- one gate per sublayer: the FFN sublayer has a gate of its own
+      on the attention sublayer's output A (same rule, same tau, same
+      reference row: the parent, or the source with gate_ref "source"), with
+      its own sources and packed list.  Rows it folds take
+      out = out_s + (A - A_s), s their FFN source; the others run the FFN on
+      their own A.  Without attn_rematch an attention-folded row keeps its
+      residual difference through the attention sublayer:
+      A = A_s + (H - H_s), s its attention source.
+
+    With both flags off this is the layer of ``layer_forward``:
+    out = out_s + (A - A_s) = out_s + (H - H_s) there.  ``force_ffn`` overrides
+    FFN-gate decisions like ``force`` does the first gate's.
+
+    Returns the first gate's fold / rel / src / packed_idx / slot / n, its
+    computed rows "act_rows" with X1 and Q, K_rows / V_rows, attnO for the
+    rows in "attn_rows", A [B*L, d], the FFN gate's fold_ffn / rel_ffn /
+    src_ffn / packed_ffn / slot_ffn / n_ffn, X2 and G of the FFN's computed
+    rows ("ffn_rows"), and out [B*L, d].
+    """
+    H = np.asarray(H, F64)
+    B, L, d = H.shape
+    R = B * L
+    gate_fn = gate_source if gate_ref == "source" else gate
+    fold, rel = gate_fn(H, parent, tau, force)
+    src = resolve(fold, parent)
+    packed_idx, slot, n = pack(fold)
+    H2 = H.reshape(R, d)
+    act = [int(r) for r in packed_idx]
+    wq, wk, wv, wo = _w(W, "w_q"), _w(W, "w_k"), _w(W, "w_v"), _w(W, "w_o")
+    wg, wu, wd = _w(W, "w_gate"), _w(W, "w_up"), _w(W, "w_down")
+    P = np.asarray(prefK).shape[0]
+    # attention sublayer inputs of the computed rows
+    X1 = rmsnorm(H2[act], W["g1"], eps)
+    Q = X1 @ wq.T
+    n_q = Q.shape[1] // hd
+    Kp = (X1 @ wk.T).reshape(n, n_kv, hd)
+    Vp = (X1 @ wv.T).reshape(n, n_kv, hd)
+    if rope_theta > 0:
+        pos = np.array([P + r % L for r in act], F64)[:, None]
+        Q = rope(Q.reshape(n, n_q, hd), pos, rope_theta).reshape(n, n_q * hd)
+        Kp = rope(Kp, pos, rope_theta)
+    K_rows = {r: Kp[t] for t, r in enumerate(act)}
+    V_rows = {r: Vp[t] for t, r in enumerate(act)}
+    q_of = {r: Q[t] for t, r in enumerate(act)}
+    kv_src = {b: [int(src[b * L + j]) for j in range(L)] for b in range(B)}
+    if attn_rematch:
+        attn_rows = list(range(R))
+        q_rows = np.stack([q_of[int(src[r])] for r in attn_rows]).reshape(R, n_q, hd)
+        attnO = attention_rows(q_rows, np.arange(R) // L, kv_src, K_rows, V_rows, prefK, prefV, n_kv)
+        A = H2 + attnO @ wo.T
+    else:
+        attn_rows = act
+        attnO = attention_rows(Q.reshape(n, n_q, hd), np.array(act) // L, kv_src, K_rows, V_rows,
+                               prefK, prefV, n_kv)
+        A = np.zeros((R, d))
+        A[act] = H2[act] + attnO @ wo.T
+        for r in range(R):
+            s = int(src[r])
+            if s != r:
+                A[r] = A[s] + (H2[r] - H2[s])
+    # FFN sublayer
+    if ffn_gate:
+        fold_f, rel_f = gate_fn(A.reshape(B, L, d), parent, tau, force_ffn)
+        src_f = resolve(fold_f, parent)
+        packed_f, slot_f, n_f = pack(fold_f)
+    else:
+        fold_f, rel_f, src_f, packed_f, slot_f, n_f = fold, rel, src, packed_idx, slot, n
+    ffn_rows = [int(r) for r in packed_f]
+    X2 = rmsnorm(A[ffn_rows], W["g2"], eps)
+    G = silu(X2 @ wg.T) * (X2 @ wu.T)
+    out = np.zeros((R, d))
+    out[ffn_rows] = A[ffn_rows] + G @ wd.T
+    for r in range(R):
+        s = int(src_f[r])
+        if s != r:
+            out[r] = out[s] + (A[r] - A[s])
+    return {
+        "fold": fold, "rel": rel, "src": src, "packed_idx": packed_idx, "slot": slot, "n": n,
+        "act_rows": np.array(act, dtype=np.int64), "X1": X1, "Q": Q, "K_rows": K_rows, "V_rows": V_rows,
+        "attn_rows": np.array(attn_rows, dtype=np.int64), "attnO": attnO, "A": A,
+        "fold_ffn": fold_f, "rel_ffn": rel_f, "src_ffn": src_f, "packed_ffn": packed_f, "slot_ffn": slot_f,
+        "n_ffn": n_f, "ffn_rows": np.array(ffn_rows, dtype=np.int64), "X2": X2, "G": G, "out": out,
     }
 
 
