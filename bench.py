@@ -404,34 +404,43 @@ def run_ours(args, rank, world):
         dense = next(s for s in sweep if s["tau"] == 0.0)["us_per_step"]
         for s in sweep:
             s["time_vs_dense"] = round(s["us_per_step"] / dense, 4)
-        # the variant gate (compare with the parent's computed source) on the same layer
-        vdims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, 0.0, 1)
-        vlay = binding.FoldedLayer(vdims, W, B, L, pk, pv)
-        vout = torch.empty_like(H)
-        for tau in w.taus:
-            g = vlay.graph(H, parent, tau, vout)
-            for _ in range(3):
-                flush()
-                g.launch()
-            torch.cuda.synchronize()
-            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            steps_s = max(50, min(args.steps, 300))
-            tot = 0.0
-            for _ in range(steps_s):
-                flush()
-                ea.record(stream)
-                g.launch()
-                eb.record(stream)
-                eb.synchronize()
-                tot += ea.elapsed_time(eb)
-            g.close()
-            nn = vlay.n_packed()
-            sweep.append({"tau": tau, "gate_ref": "source", "n_packed": nn, "rho": round(nn / R, 4),
-                          "us_per_step": round(tot / steps_s * 1e3, 2),
-                          "tokens_per_s": round(R * steps_s / (tot * 1e-3), 1),
-                          "time_vs_dense": round(tot / steps_s * 1e3 / dense, 4)})
-        assert vlay.status() == 0, "device status set"
-        del vlay
+        # variant readings on the same layer: the gate against the parent's
+        # computed source; folded rows' attention matched again against their
+        # own branch; a gate of its own for the FFN sublayer
+        variants = [("source", 1, 0, 0), ("parent", 0, 1, 0), ("parent", 0, 0, 1), ("parent", 0, 1, 1)]
+        for ref, gref, rematch, fgate in variants:
+            vdims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16, 0.0, gref, rematch, fgate)
+            vlay = binding.FoldedLayer(vdims, W, B, L, pk, pv)
+            vout = torch.empty_like(H)
+            for tau in w.taus:
+                g = vlay.graph(H, parent, tau, vout)
+                for _ in range(3):
+                    flush()
+                    g.launch()
+                torch.cuda.synchronize()
+                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                steps_s = max(50, min(args.steps, 300))
+                tot = 0.0
+                for _ in range(steps_s):
+                    flush()
+                    ea.record(stream)
+                    g.launch()
+                    eb.record(stream)
+                    eb.synchronize()
+                    tot += ea.elapsed_time(eb)
+                g.close()
+                nn = vlay.n_packed()
+                row = {"tau": tau, "gate_ref": ref, "n_packed": nn, "rho": round(nn / R, 4),
+                       "us_per_step": round(tot / steps_s * 1e3, 2),
+                       "tokens_per_s": round(R * steps_s / (tot * 1e-3), 1),
+                       "time_vs_dense": round(tot / steps_s * 1e3 / dense, 4)}
+                if rematch or fgate:
+                    row["attn_rematch"] = rematch
+                    row["ffn_gate"] = fgate
+                    row["n_ffn"] = int(vlay.view("n_ffn", torch.int32)[0].item())
+                sweep.append(row)
+            assert vlay.status() == 0, "device status set"
+            del vlay
     budget = [] if (args.no_budget or args.workload != "7b_layer") else budget_sweep(args, lay.dims, W, pk, pv, flush,
                                                                                        barrier)
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)

@@ -34,7 +34,8 @@ class SpecfoldError(RuntimeError):
 class specfold_dims(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("ffn_dim", ctypes.c_int), ("rms_eps", ctypes.c_float),
-                ("dtype", ctypes.c_int), ("rope_theta", ctypes.c_float), ("gate_ref", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("rope_theta", ctypes.c_float), ("gate_ref", ctypes.c_int),
+                ("attn_rematch", ctypes.c_int), ("ffn_gate", ctypes.c_int)]
 
 
 class specfold_weights(ctypes.Structure):
@@ -50,7 +51,9 @@ class specfold_kv_view(ctypes.Structure):
 class specfold_ws_layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in
                 ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "dep_off", "dep_rows", "x1", "q",
-                 "block_k", "block_v", "attn_o", "a", "x2", "g", "gemm_scratch", "attn_scratch", "total")]
+                 "block_k", "block_v", "attn_o", "a", "x2", "g", "q_all", "all_idx", "n_all", "a_all", "fold_ffn",
+                 "rel_ffn", "src_ffn", "packed_ffn", "slot_ffn", "n_ffn", "dep_off_ffn", "dep_rows_ffn",
+                 "gemm_scratch", "attn_scratch", "total")]
 
 
 class specfold_stack_trace(ctypes.Structure):
@@ -146,9 +149,13 @@ def dtype_code(t: torch.dtype) -> int:
     raise ValueError(f"unsupported dtype {t}")
 
 
-def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16, rope_theta=0.0, gate_ref=0) -> specfold_dims:
-    """gate_ref 0: the gate compares with the parent; 1: with the parent's computed source."""
-    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype, rope_theta, gate_ref)
+def make_dims(d, n_q, n_kv, hd, F, eps=1e-6, dtype=BF16, rope_theta=0.0, gate_ref=0, attn_rematch=0,
+              ffn_gate=0) -> specfold_dims:
+    """gate_ref 0: the gate compares with the parent; 1: with the parent's
+    computed source.  attn_rematch 1: folded rows run attention again (their
+    source's query over their own branch's block).  ffn_gate 1: the FFN
+    sublayer has a gate of its own on the attention sublayer's output."""
+    return specfold_dims(d, n_q, n_kv, hd, F, eps, dtype, rope_theta, gate_ref, int(attn_rematch), int(ffn_gate))
 
 
 def make_weights(w: dict) -> specfold_weights:

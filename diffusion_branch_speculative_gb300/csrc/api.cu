@@ -113,6 +113,8 @@ static int check_dims(const specfold_dims* d) {
   if (!(d->rms_eps >= 0.f) || std::isinf(d->rms_eps)) return SPECFOLD_EINVAL;
   if (!(d->rope_theta >= 0.f) || std::isinf(d->rope_theta)) return SPECFOLD_EINVAL;
   if (d->gate_ref != 0 && d->gate_ref != 1) return SPECFOLD_EINVAL;
+  if ((d->attn_rematch != 0 && d->attn_rematch != 1) || (d->ffn_gate != 0 && d->ffn_gate != 1))
+    return SPECFOLD_EINVAL;
   if (d->head_dim != 64 && d->head_dim != 128) return SPECFOLD_EUNSUPPORTED;
   if (d->n_q_heads % d->n_kv_heads) return SPECFOLD_EUNSUPPORTED;
   if (d->d_model % 256) return SPECFOLD_EUNSUPPORTED;
@@ -186,6 +188,18 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->a = take(R * d->d_model * e);
   o->x2 = take(R * d->d_model * e);
   o->g = take(R * d->ffn_dim * e);
+  o->q_all = take(R * nq * e);
+  o->all_idx = take(R * 4);
+  o->n_all = take(4);
+  o->a_all = take(R * d->d_model * e);
+  o->fold_ffn = take(R);
+  o->rel_ffn = take(R * 4);
+  o->src_ffn = take(R * 4);
+  o->packed_ffn = take(R * 4);
+  o->slot_ffn = take(R * 4);
+  o->n_ffn = take(4);
+  o->dep_off_ffn = take((R + 1) * 4);
+  o->dep_rows_ffn = take(R * 4);
   o->gemm_scratch = take(gemm_partial_floats() * 4);
   o->attn_scratch = take(attn_partial_bytes(static_cast<int>(R), d->n_q_heads / d->n_kv_heads, d->n_kv_heads,
                                             d->head_dim));
@@ -397,12 +411,94 @@ static size_t stack_ws_bytes(const specfold_dims* d, int B, int L, const specfol
   return lo.total + up256(static_cast<size_t>(B) * L * d->d_model * esize(d->dtype));
 }
 
+static int launch_layer_gate(const specfold_dims* dims, const void* X, const int32_t* parent, int B, int L,
+                             float tau, uint8_t* fold, float* rel, uint8_t* fold_hist, cudaStream_t st) {
+  if (dims->gate_ref == 1)
+    return launch_gate_source(dims->dtype, X, parent, B, L, dims->d_model, tau, fold, rel, st, fold_hist);
+  return launch_gate(dims->dtype, X, parent, B, L, dims->d_model, tau, fold, rel, st, fold_hist);
+}
+
+// The layer as two sublayers (dims->attn_rematch or dims->ffn_gate): the
+// attention sublayer gives A for every row (a_all), then the FFN sublayer
+// packs its own rows of a_all (its own gate, or the first gate's decisions)
+// and fills the rest with their FFN source's output plus their own A
+// difference.
+static int enqueue_layer_sublayers(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
+                                   const int32_t* parent, int B, int L, specfold_kv_view prefK,
+                                   specfold_kv_view prefV, int P, float tau, void* H_out, void* ws,
+                                   const specfold_ws_layout& lo, void* const* stage_events, uint8_t* fold_hist,
+                                   int32_t* n_hist, cudaStream_t st) {
+  const int R = B * L;
+  const Scratch s = layer_scratch(ws, dims, B, L, lo);
+  uint32_t* status = at<uint32_t>(ws, lo.status);
+  uint8_t* fold = at<uint8_t>(ws, lo.fold);
+  int32_t* src = at<int32_t>(ws, lo.src);
+  int32_t* pidx = at<int32_t>(ws, lo.packed_idx);
+  int32_t* slot = at<int32_t>(ws, lo.slot_of_row);
+  int32_t* n_dev = at<int32_t>(ws, lo.n_packed);
+  void* a_all = at<void>(ws, lo.a_all);
+  auto mark = [&](int i) {
+    if (stage_events) record_stage_event(stage_events[i], st);
+  };
+  mark(0);
+  SF_TRY(launch_layer_gate(dims, H_in, parent, B, L, tau, fold, at<float>(ws, lo.rel), fold_hist, st));
+  mark(1);
+  SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
+                            slot, n_dev, at<void>(ws, lo.x1), status, st, n_hist));
+  mark(2);
+  SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
+                   at<void>(ws, lo.block_v), s, status, st));
+  if (dims->rope_theta > 0.f)
+    SF_TRY(launch_rope(dims->dtype, at<void>(ws, lo.q), at<void>(ws, lo.block_k), pidx, n_dev, R, L, P,
+                       dims->n_q_heads, dims->n_kv_heads, dims->head_dim, dims->rope_theta, st));
+  mark(3);
+  if (dims->attn_rematch) {
+    // every row's query is its source's; attention and W_o run on all rows
+    int32_t* all_idx = at<int32_t>(ws, lo.all_idx);
+    int32_t* n_all = at<int32_t>(ws, lo.n_all);
+    SF_TRY(launch_gather_query(dims->dtype, at<void>(ws, lo.q), src, slot, R, dims->n_kv_heads,
+                               dims->n_q_heads / dims->n_kv_heads * dims->head_dim, at<void>(ws, lo.q_all), all_idx,
+                               n_all, st));
+    SF_TRY(stage_attention(dims, at<void>(ws, lo.q_all), prefK, prefV, P, at<void>(ws, lo.block_k),
+                           at<void>(ws, lo.block_v), src, all_idx, n_all, B, L, at<void>(ws, lo.attn_o), status,
+                           at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
+    mark(4);
+    SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), all_idx, n_all, H_in, R, a_all, s, status, st));
+  } else {
+    SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
+                           at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
+                           at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
+    mark(4);
+    SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st));
+    SF_TRY(launch_unpack_fill(dims->dtype, at<void>(ws, lo.a), src, slot, H_in, a_all, R, dims->d_model, st));
+  }
+  // FFN sublayer
+  uint8_t* fold_f = fold;
+  if (dims->ffn_gate) {
+    fold_f = at<uint8_t>(ws, lo.fold_ffn);
+    SF_TRY(launch_layer_gate(dims, a_all, parent, B, L, tau, fold_f, at<float>(ws, lo.rel_ffn), nullptr, st));
+  }
+  int32_t* src_f = at<int32_t>(ws, lo.src_ffn);
+  int32_t* pidx_f = at<int32_t>(ws, lo.packed_ffn);
+  int32_t* n_f = at<int32_t>(ws, lo.n_ffn);
+  SF_TRY(launch_select_pack(dims->dtype, fold_f, parent, B, L, dims->d_model, a_all, w->g2, dims->rms_eps, src_f,
+                            pidx_f, at<int32_t>(ws, lo.slot_ffn), n_f, at<void>(ws, lo.x2), status, st, nullptr,
+                            at<int32_t>(ws, lo.dep_off_ffn), at<int32_t>(ws, lo.dep_rows_ffn), at<void>(ws, lo.a)));
+  mark(5);
+  return stage_ffn(dims, w, at<void>(ws, lo.a), pidx_f, n_f, a_all, src_f, fold_f, R, H_out, at<void>(ws, lo.x2),
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_off_ffn),
+                   at<int32_t>(ws, lo.dep_rows_ffn));
+}
+
 // S1..S10 of one layer on `st` (arguments already checked).  fold_hist and
 // n_hist, when given, receive copies of the layer's decisions and n.
 static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, const void* H_in,
                          const int32_t* parent, int B, int L, specfold_kv_view prefK, specfold_kv_view prefV, int P,
                          float tau, void* H_out, void* ws, const specfold_ws_layout& lo,
                          void* const* stage_events, uint8_t* fold_hist, int32_t* n_hist, cudaStream_t st) {
+  if (dims->attn_rematch || dims->ffn_gate)
+    return enqueue_layer_sublayers(dims, w, H_in, parent, B, L, prefK, prefV, P, tau, H_out, ws, lo, stage_events,
+                                   fold_hist, n_hist, st);
   const int R = B * L;
   const Scratch s = layer_scratch(ws, dims, B, L, lo);
   uint32_t* status = at<uint32_t>(ws, lo.status);
@@ -414,12 +510,7 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
     if (stage_events) record_stage_event(stage_events[i], st);
   };
   mark(0);
-  if (dims->gate_ref == 1)
-    SF_TRY(launch_gate_source(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
-                              fold_hist));
-  else
-    SF_TRY(launch_gate(dims->dtype, H_in, parent, B, L, dims->d_model, tau, fold, at<float>(ws, lo.rel), st,
-                       fold_hist));
+  SF_TRY(launch_layer_gate(dims, H_in, parent, B, L, tau, fold, at<float>(ws, lo.rel), fold_hist, st));
   mark(1);
   SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
                             at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,

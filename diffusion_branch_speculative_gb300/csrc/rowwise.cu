@@ -240,9 +240,10 @@ struct Gains {
 
 // y = x * g / sqrt(mean(x^2) + eps) for one row, one warp; the whole row is
 // loaded before the reduction and held in registers until the scaled store.
+// rawrow (optional) receives an unchanged copy of the row.
 template <typename T, int MAXV, bool GREG>
 SF_DEV void norm_row(const T* __restrict__ xrow, const Gains<T, MAXV, GREG>& gn, int d, float eps,
-                     T* __restrict__ yrow, int lane) {
+                     T* __restrict__ yrow, int lane, T* __restrict__ rawrow = nullptr) {
   using V = VecT<T>;
   const uint4* x = reinterpret_cast<const uint4*>(xrow);
   uint4* y = reinterpret_cast<uint4*>(yrow);
@@ -252,6 +253,12 @@ SF_DEV void norm_row(const T* __restrict__ xrow, const Gains<T, MAXV, GREG>& gn,
 #pragma unroll
   for (int j = 0; j < MAXV; ++j)
     if (lane + 32 * j < nv) v[j] = __ldg(x + lane + 32 * j);
+  if (rawrow) {
+    uint4* rw = reinterpret_cast<uint4*>(rawrow);
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j)
+      if (lane + 32 * j < nv) rw[lane + 32 * j] = v[j];
+  }
 #pragma unroll
   for (int j = 0; j < MAXV; ++j) {
     if (lane + 32 * j < nv) {
@@ -309,7 +316,8 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
                    int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
                    int32_t* __restrict__ src, int32_t* __restrict__ packed_idx, int32_t* __restrict__ slot,
                    int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status,
-                   int32_t* __restrict__ n_hist, int32_t* __restrict__ dep_off, int32_t* __restrict__ dep_rows) {
+                   int32_t* __restrict__ n_hist, int32_t* __restrict__ dep_off, int32_t* __restrict__ dep_rows,
+                   T* __restrict__ Xraw) {
   extern __shared__ int smem_i[];
   __shared__ int s_warp[kPackThreads / 32];
   __shared__ int s_bad;
@@ -455,10 +463,11 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
       if (sr >= 0 && sr != r) dep_rows[atomicAdd(&cnt[s_slot[sr]], 1)] = r;
     }
   }
-  // RMSNorm1 gather of this block's packed rows
+  // RMSNorm1 gather of this block's packed rows (and, when asked, the rows
+  // themselves)
   if (X1 && r_norm >= 0)
     norm_row<T, MAXV, GREG>(H + static_cast<size_t>(r_norm) * d, gn, d, eps, X1 + static_cast<size_t>(k_norm) * d,
-                            lane);
+                            lane, Xraw ? Xraw + static_cast<size_t>(k_norm) * d : nullptr);
 }
 
 // ------------------------------------------------------- RMSNorm rows --
@@ -507,6 +516,95 @@ fold_fill_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__ s
       const int v = v0 + 32 * u;
       if (v < nv) {
         a[u] = os[v];
+        b[u] = __ldg(ir + v);
+        c[u] = __ldg(is + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nv) {
+        float fa[V::N], fb[V::N], fc[V::N];
+        V::unpack(a[u], fa);
+        V::unpack(b[u], fb);
+        V::unpack(c[u], fc);
+#pragma unroll
+        for (int e = 0; e < V::N; ++e) fa[e] = fa[e] + (fb[e] - fc[e]);
+        orow[v] = V::pack(fa);
+      }
+    }
+  }
+}
+
+// ------------------------------------------- variant sublayer helpers --
+// Queries of every row for the literal attention correction: row r takes
+// the query of its source row src[r] (packed slot slot[src[r]]).  One warp
+// per (KV head, row) copies that row's g query heads (g*hd contiguous
+// elements of the head-group-major layout).  Also writes the all-rows list
+// (all_idx[r] = r, n_all = R) the attention and output projection then use.
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+gather_query_kernel(const T* __restrict__ Q, const int32_t* __restrict__ src, const int32_t* __restrict__ slot,
+                    int R, int n_kv, int ghd, T* __restrict__ Qall, int32_t* __restrict__ all_idx,
+                    int32_t* __restrict__ n_all) {
+  pdl_wait();
+  pdl_trigger();
+  const int wid = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) n_all[0] = R;
+  if (wid >= R * n_kv) return;
+  const int h = wid / R, r = wid - h * R;
+  if (h == 0 && lane == 0) all_idx[r] = r;
+  const int s = src[r];
+  const int k = (s >= 0 && s < R) ? slot[s] : -1;
+  uint4* dst = reinterpret_cast<uint4*>(Qall + (static_cast<size_t>(h) * R + r) * ghd);
+  const int nv = ghd * static_cast<int>(sizeof(T)) / 16;
+  if (k < 0 || k >= R) {
+    for (int v = lane; v < nv; v += 32) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* from = reinterpret_cast<const uint4*>(Q + (static_cast<size_t>(h) * R + k) * ghd);
+  for (int v = lane; v < nv; v += 32) dst[v] = from[v];
+}
+
+// Attention sublayer output of every row, in row order, from the packed
+// rows: a recomputed row copies its packed row, a folded row r takes its
+// source's plus its own input difference, Aall[r] = Ap[slot[s]] + (H[r] - H[s])
+// (one rounding).  One warp per row.
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32)
+unpack_fill_kernel(const T* __restrict__ Ap, const int32_t* __restrict__ src, const int32_t* __restrict__ slot,
+                   const T* __restrict__ H, T* __restrict__ Aall, int R, int d) {
+  using V = VecT<T>;
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  int s = src[r];
+  if (s < 0 || s >= R) s = r;
+  const int k = slot[s];
+  uint4* orow = reinterpret_cast<uint4*>(Aall + static_cast<size_t>(r) * d);
+  const int nv = d / V::N;
+  if (k < 0 || k >= R) {
+    for (int v = lane; v < nv; v += 32) orow[v] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* ap = reinterpret_cast<const uint4*>(Ap + static_cast<size_t>(k) * d);
+  if (s == r) {
+    for (int v = lane; v < nv; v += 32) orow[v] = ap[v];
+    return;
+  }
+  const uint4* ir = reinterpret_cast<const uint4*>(H + static_cast<size_t>(r) * d);
+  const uint4* is = reinterpret_cast<const uint4*>(H + static_cast<size_t>(s) * d);
+  constexpr int U = 8;
+  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+    uint4 a[U], b[U], c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nv) {
+        a[u] = ap[v];
         b[u] = __ldg(ir + v);
         c[u] = __ldg(is + v);
       }
@@ -701,7 +799,7 @@ template <typename T, int MAXV, bool GREG>
 static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                               const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
                               int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
-                              int32_t* dep_rows) {
+                              int32_t* dep_rows, void* Xraw) {
   const int R = B * L;
   const size_t smem = (static_cast<size_t>(3) * R + 1) * sizeof(int);
   static int attr_done[64] = {0};
@@ -716,7 +814,8 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
   launch_k(select_pack_kernel<T, MAXV, GREG>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
-                                                          n_dev, static_cast<T*>(X1), status, n_hist, dep_off, dep_rows);
+                                                          n_dev, static_cast<T*>(X1), status, n_hist, dep_off, dep_rows,
+                                                          static_cast<T*>(Xraw));
   count_launch();
   return check_launch();
 }
@@ -725,15 +824,15 @@ template <typename T>
 static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                                 const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
                                 int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
-                              int32_t* dep_rows) {
+                                int32_t* dep_rows, void* Xraw) {
   const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
   // gains in registers when the grid fits one wave at one block per SM
   const bool greg = (B * L + kRowWarps - 1) / kRowWarps <= num_sms();
 #define SF_SP(MV)                                                                                                 \
   return greg ? select_pack_launch<T, MV, true>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev,  \
-                                                X1, status, st, n_hist, dep_off, dep_rows)                        \
+                                                X1, status, st, n_hist, dep_off, dep_rows, Xraw)                  \
               : select_pack_launch<T, MV, false>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, \
-                                                 X1, status, st, n_hist, dep_off, dep_rows)
+                                                 X1, status, st, n_hist, dep_off, dep_rows, Xraw)
   if (per_lane <= 4) SF_SP(4);
   if (per_lane <= 8) SF_SP(8);
   if (per_lane <= 16) SF_SP(16);
@@ -745,12 +844,13 @@ static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int 
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                        const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot, int32_t* n_dev,
                        void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
-                       int32_t* dep_rows) {
+                       int32_t* dep_rows, void* Xraw) {
+  if (Xraw && !X1) return SPECFOLD_EINVAL;
   if (dtype == SPECFOLD_BF16)
     return select_pack_dispatch<__nv_bfloat16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1,
-                                               status, st, n_hist, dep_off, dep_rows);
+                                               status, st, n_hist, dep_off, dep_rows, Xraw);
   return select_pack_dispatch<float>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status,
-                                     st, n_hist, dep_off, dep_rows);
+                                     st, n_hist, dep_off, dep_rows, Xraw);
 }
 
 template <typename T>
@@ -800,6 +900,33 @@ int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const v
   else
     launch_k(fold_fill_kernel<float>, dim3(grid), dim3(block), 0, st, fold, src, static_cast<const float*>(H_in),
                                                     static_cast<float*>(H_out), R, d);
+  count_launch();
+  return check_launch();
+}
+
+int launch_gather_query(int dtype, const void* Q, const int32_t* src, const int32_t* slot, int R, int n_kv, int ghd,
+                        void* Qall, int32_t* all_idx, int32_t* n_all, cudaStream_t st) {
+  if ((ghd * (dtype == SPECFOLD_BF16 ? 2 : 4)) % 16) return SPECFOLD_EUNSUPPORTED;
+  const dim3 grid((R * n_kv + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
+  if (dtype == SPECFOLD_BF16)
+    launch_k(gather_query_kernel<__nv_bfloat16>, grid, block, 0, st, static_cast<const __nv_bfloat16*>(Q), src, slot,
+             R, n_kv, ghd, static_cast<__nv_bfloat16*>(Qall), all_idx, n_all);
+  else
+    launch_k(gather_query_kernel<float>, grid, block, 0, st, static_cast<const float*>(Q), src, slot, R, n_kv, ghd,
+             static_cast<float*>(Qall), all_idx, n_all);
+  count_launch();
+  return check_launch();
+}
+
+int launch_unpack_fill(int dtype, const void* Ap, const int32_t* src, const int32_t* slot, const void* H, void* Aall,
+                       int R, int d, cudaStream_t st) {
+  const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kRowWarps * 32);
+  if (dtype == SPECFOLD_BF16)
+    launch_k(unpack_fill_kernel<__nv_bfloat16>, grid, block, 0, st, static_cast<const __nv_bfloat16*>(Ap), src, slot,
+             static_cast<const __nv_bfloat16*>(H), static_cast<__nv_bfloat16*>(Aall), R, d);
+  else
+    launch_k(unpack_fill_kernel<float>, grid, block, 0, st, static_cast<const float*>(Ap), src, slot,
+             static_cast<const float*>(H), static_cast<float*>(Aall), R, d);
   count_launch();
   return check_launch();
 }

@@ -33,7 +33,8 @@ int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, i
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
                        const void* H, const void* g1, float eps, int32_t* src, int32_t* packed_idx,
                        int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st,
-                       int32_t* n_hist = nullptr, int32_t* dep_off = nullptr, int32_t* dep_rows = nullptr);
+                       int32_t* n_hist = nullptr, int32_t* dep_off = nullptr, int32_t* dep_rows = nullptr,
+                       void* Xraw = nullptr);  // Xraw [R, d]: the packed rows themselves (needs X1)
 // Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
                         int R, int d, const void* g, float eps, void* Y, cudaStream_t st);
@@ -41,6 +42,14 @@ int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int3
 int launch_fold_fill(int dtype, const uint8_t* fold, const int32_t* src, const void* H_in,
                      void* H_out, int R, int d, cudaStream_t st);
 int launch_timeout_probe(uint32_t* status, uint64_t wait_ns, cudaStream_t st);
+// Variant sublayer path: queries of every row from its source's packed row
+// (Q layout [n_kv][R*g][hd], ghd = g*hd), plus the all-rows list; and the
+// attention sublayer output of every row from the packed rows with the
+// folded rows' own input difference.
+int launch_gather_query(int dtype, const void* Q, const int32_t* src, const int32_t* slot, int R, int n_kv, int ghd,
+                        void* Qall, int32_t* all_idx, int32_t* n_all, cudaStream_t st);
+int launch_unpack_fill(int dtype, const void* Ap, const int32_t* src, const int32_t* slot, const void* H, void* Aall,
+                       int R, int d, cudaStream_t st);
 // Rotary embedding of the packed rows' queries and block keys in place.
 int launch_rope(int dtype, void* Q, void* Kb, const int32_t* packed_idx, const int32_t* n_dev, int R, int L, int P,
                 int n_q, int n_kv, int hd, float theta, cudaStream_t st);

@@ -83,6 +83,13 @@ typedef struct {
   int gate_ref;     /* 0: the gate compares a child with its parent's input (specfold_gate);
                        1: with the input of the row its parent's output comes from
                        (specfold_gate_source) */
+  int attn_rematch; /* 1: the implementation note's correction read literally: every folded
+                       row runs attention again (its source's query over its own branch's
+                       block keys/values and the prefix) and the output projection; only
+                       its FFN sublayer stays folded.  0: folded rows skip the whole layer. */
+  int ffn_gate;     /* 1: the FFN sublayer has a gate of its own on the attention sublayer's
+                       output A (same rule, tau and reference as the first gate) with its own
+                       sources and packed list.  0: one gate for the whole layer. */
 } specfold_dims;
 
 /* Layer weights (device, [out, in] row-major, dims.dtype). */
@@ -137,9 +144,23 @@ typedef struct {
   size_t block_k;      /* [R, n_kv, hd]  keys of recomputed rows (row r) */
   size_t block_v;      /* [R, n_kv, hd] */
   size_t attn_o;       /* [R, n_q*hd]   attention output, packed rows */
-  size_t a;            /* [R, d]        attention sublayer output, packed rows */
+  size_t a;            /* [R, d]        attention sublayer output, packed rows (variant
+                                        path: the FFN's packed rows of a_all) */
   size_t x2;           /* [R, d]        RMSNorm2 of a */
   size_t g;            /* [R, F]        silu(x2 Wg) * (x2 Wu) */
+  /* the variant sublayer path (dims.attn_rematch or dims.ffn_gate): */
+  size_t q_all;        /* [n_kv, R*g, hd]  queries of every row (row r: its source's) */
+  size_t all_idx;      /* int32 [R]     0 .. R-1, the all-rows list */
+  size_t n_all;        /* int32         R */
+  size_t a_all;        /* [R, d]        attention sublayer output of every row, row order */
+  size_t fold_ffn;     /* uint8 [R]     FFN-sublayer gate decisions */
+  size_t rel_ffn;      /* float [R] */
+  size_t src_ffn;      /* int32 [R]     FFN sources */
+  size_t packed_ffn;   /* int32 [R]     FFN packed list (first n_ffn valid) */
+  size_t slot_ffn;     /* int32 [R] */
+  size_t n_ffn;        /* int32 */
+  size_t dep_off_ffn;  /* int32 [R+1] */
+  size_t dep_rows_ffn; /* int32 [R] */
   size_t gemm_scratch; /* fp32 split-K partial sums */
   size_t attn_scratch; /* fp32 split-KV attention partials */
   size_t total;        /* total bytes */
@@ -250,6 +271,16 @@ int specfold_ffn(const specfold_dims* dims, const specfold_weights* w, const voi
  * parents, parent[0] = -1, parent[b] < b), prefix views of P tokens, tau >= 0
  * (0 = folding off: the dense multi-branch verify through the same kernels).
  * Writes H_out [B, L, d]; intermediates stay in ws (specfold_workspace_layout).
+ * With dims.attn_rematch or dims.ffn_gate the layer runs as two sublayers:
+ *   attention: gate, pack and QKV as above; with attn_rematch, attention and
+ *     the output projection run on every row (row r's query is its source's),
+ *     giving A for all rows; without it, on the packed rows, and a folded row
+ *     takes A[r] = A[s] + (H_in[r] - H_in[s]);
+ *   FFN: with ffn_gate a second gate on A (fold_ffn, src_ffn, packed_ffn);
+ *     without it the first gate's decisions; the FFN runs on its packed rows
+ *     and a folded row r with FFN source s takes
+ *     H_out[r] = H_out[s] + (A[r] - A[s]).
+ * With both 0 this is the layer above: H_out[r] = H_out[s] + (H_in[r] - H_in[s]).
  * stage_events: NULL, or SPECFOLD_STAGE_EVENTS cudaEvent_t handles recorded
  * on `stream` at the stage boundaries listed at SPECFOLD_STAGE_EVENTS; a NULL
  * entry skips that boundary. */

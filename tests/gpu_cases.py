@@ -36,14 +36,15 @@ class DeviceInputs:
     """Seeded inputs on the device, in the workload's dtype (bf16, or fp32
     for the tiny fp32 configuration)."""
 
-    def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0, gate_ref: int = 0):
+    def __init__(self, inp: synth.LayerInputs, device="cuda", rope_theta: float = 0.0, gate_ref: int = 0,
+                 attn_rematch: int = 0, ffn_gate: int = 0):
         self.inp = inp
         d = inp.dims
         self.fp32 = inp.dtype == "f32"
         conv = f32 if self.fp32 else bf16
         self.tdtype = torch.float32 if self.fp32 else torch.bfloat16
         self.dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.F32 if self.fp32 else binding.BF16,
-                                      rope_theta, gate_ref)
+                                      rope_theta, gate_ref, attn_rematch, ffn_gate)
         self.H = conv(inp.H, device)
         self.parent = torch.from_numpy(inp.parent.astype(np.int32)).to(device)
         self.W = {k: conv(v, device) for k, v in inp.weights.items()}
@@ -166,3 +167,138 @@ def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0, gate_r
         if key not in ("n", "near_tau", "delta"):
             assert val < TOL, (key, val, m)
     return m, lay, out
+
+
+# ---------------------------------------------------------------------------
+# the variant sublayer path (attn_rematch / ffn_gate)
+# ---------------------------------------------------------------------------
+
+# The FFN-sublayer gate decides on A, which the GPU stores in bf16 and the
+# oracle keeps in float64, so the two compare slightly different rows.  The
+# error of r = |A_b - A_p| / |A_p| is the projection of A's error on the
+# direction of A_b - A_p over |A_p|: about u / sqrt(d) with u the relative
+# per-element error of A (bf16 storage 2^-9 / sqrt(3) plus the projection's
+# own), 1e-4 at d = 256.  Rows with |r - tau| below these absolute bands take
+# the GPU's decision (reported, excluded from decision parity).
+FFN_NEAR_ABS = {"bf16": 2e-3, "f32": 1e-5}
+
+
+def read_sublayers(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
+    d = dev.inp.dims
+    R = dev.B * dev.L
+    v = lay.view
+    n_f = int(v("n_ffn", torch.int32)[0].item())
+    et = dev.tdtype
+    return {
+        "fold_ffn": v("fold_ffn", torch.uint8, (R,)).cpu().numpy().astype(bool),
+        "rel_ffn": v("rel_ffn", torch.float32, (R,)).cpu().numpy(),
+        "src_ffn": v("src_ffn", torch.int32, (R,)).cpu().numpy(),
+        "packed_ffn": v("packed_ffn", torch.int32, (R,)).cpu().numpy()[:n_f],
+        "n_ffn": n_f,
+        "A_all": to_np(v("a_all", et, (R, d.d))),
+        "X2": to_np(v("x2", et, (R, d.d))[:n_f]),
+        "G": to_np(v("g", et, (R, d.F))[:n_f]),
+    }
+
+
+def oracle_sublayers_with_gpu_decisions(inp, tau, gpu_fold, gpu_fold_ffn, attn_rematch, ffn_gate,
+                                        rope_theta=0.0, gate_ref=0, ffn_band=None):
+    """The variant oracle with the GPU's decisions on near-tau rows of both
+    gates.  Returns (result, near-tau rows of the first gate, mismatches
+    outside its band, near-tau rows of the FFN gate, mismatches outside
+    that band)."""
+    d = inp.dims
+    B, L, _ = inp.H.shape
+    t32 = float(np.float32(tau))
+    gf = gpu_fold.reshape(B, L)
+    gff = gpu_fold_ffn.reshape(B, L)
+    ref = "source" if gate_ref == 1 else "parent"
+    gate_fn = orc.gate_source if gate_ref == 1 else orc.gate
+    f0, rel = gate_fn(inp.H, inp.parent, t32)
+    for _ in range(2 if gate_ref == 1 else 0):
+        near = orc.near_tau_rows(rel, t32, NEAR_TAU)
+        f0, rel = gate_fn(inp.H, inp.parent, t32, np.where(near, gf.astype(np.int8), np.int8(-1)).astype(np.int8))
+    near = orc.near_tau_rows(rel, t32, NEAR_TAU)
+    bad = int(((gf != f0) & ~near).sum())
+    force = np.where(near, gf.astype(np.int8), np.int8(-1)).astype(np.int8)
+
+    def run(force_ffn):
+        return orc.layer_forward_sublayers(inp.H, inp.parent, inp.weights, inp.prefix.K, inp.prefix.V, t32, d.eps,
+                                           d.n_kv, d.hd, attn_rematch=bool(attn_rematch), ffn_gate=bool(ffn_gate),
+                                           force=force, force_ffn=force_ffn, rope_theta=rope_theta, gate_ref=ref)
+
+    res = run(None)
+    n_near_f, bad_f = 0, 0
+    if ffn_gate:
+        band = FFN_NEAR_ABS[inp.dtype] if ffn_band is None else ffn_band
+        band = band if t32 > 0 else 0.0   # tau = 0 folds nothing: no band
+        t_div = t32 if t32 > 0 else 1.0
+        for _ in range(2 if gate_ref == 1 else 1):
+            near_f = orc.near_tau_rows(res["rel_ffn"], t32, band / t_div)
+            res = run(np.where(near_f, gff.astype(np.int8), np.int8(-1)).astype(np.int8))
+        near_f = orc.near_tau_rows(res["rel_ffn"], t32, band / t_div)
+        n_near_f = int(near_f.sum())
+        bad_f = int(((gff != res["fold_ffn"]) & ~near_f).sum())
+    return res, int(near.sum()), bad, n_near_f, bad_f
+
+
+def check_layer_sublayers(inp, tau, attn_rematch, ffn_gate, rope_theta=0.0, gate_ref=0, prefix=None,
+                          ffn_band=None):
+    """The variant sublayer path against ``layer_forward_sublayers``: both
+    gates' decisions, sources and packed lists exact (near-tau rows aside);
+    A of every row, X2 and G of the FFN rows and H_out within tolerance."""
+    dev = DeviceInputs(inp, rope_theta=rope_theta, gate_ref=gate_ref, attn_rematch=attn_rematch,
+                       ffn_gate=ffn_gate)
+    pk, pv = (dev.pk, dev.pv) if prefix is None else prefix
+    lay = binding.FoldedLayer(dev.dims, dev.W, dev.B, dev.L, pk, pv)
+    out = lay.forward(dev.H, dev.parent, tau)
+    torch.cuda.synchronize()
+    assert lay.status() == 0
+    gi = read_intermediates(lay, dev)
+    gs = read_sublayers(lay, dev)
+    res, n_near, bad, n_near_f, bad_f = oracle_sublayers_with_gpu_decisions(
+        inp, tau, gi["fold"], gs["fold_ffn"] if ffn_gate else gi["fold"], attn_rematch, ffn_gate, rope_theta,
+        gate_ref, ffn_band)
+    assert bad == 0, f"{bad} first-gate decisions differ away from tau"
+    assert bad_f == 0, f"{bad_f} FFN-gate decisions differ away from tau"
+    d = inp.dims
+    B, L, D = inp.H.shape
+    R = B * L
+    assert np.array_equal(gi["fold"], res["fold"].reshape(-1))
+    assert np.array_equal(gi["src"], res["src"])
+    assert gi["n"] == res["n"] and np.array_equal(gi["packed_idx"], res["packed_idx"])
+    if ffn_gate:
+        assert np.array_equal(gs["fold_ffn"], res["fold_ffn"].reshape(-1))
+        nonroot = np.arange(R) >= L
+        ro = res["rel_ffn"].reshape(-1)[nonroot]
+        fin = np.isfinite(ro)
+        assert np.max(np.abs(gs["rel_ffn"][nonroot][fin] - ro[fin])) < 2e-3
+    assert np.array_equal(gs["src_ffn"], res["src_ffn"])
+    assert gs["n_ffn"] == res["n_ffn"] and np.array_equal(gs["packed_ffn"], res["packed_ffn"])
+    tol = 1e-4 if dev.fp32 else TOL
+    Hin = inp.H.reshape(R, D).astype(np.float64)
+    m = {"n": gi["n"], "n_ffn": gs["n_ffn"], "near_tau": n_near, "near_tau_ffn": n_near_f}
+    # attention output: every row with the correction, else the packed rows
+    if attn_rematch:
+        ao = to_np(lay.view("attn_o", dev.tdtype, (R, d.n_q * d.hd)))
+    else:
+        ao = gi["attnO"][gi["slot"][res["attn_rows"]]]
+    m["attnO"] = rel_l2(ao, res["attnO"])
+    m["X2"] = rel_l2(gs["X2"], res["X2"])
+    m["G"] = rel_l2(gs["G"], res["G"])
+    for key in ("attnO", "X2", "G"):
+        assert m[key] < tol, (key, m)
+    Hg = to_np(out).reshape(R, D)
+    m["A_delta"] = rel_l2(gs["A_all"] - Hin, res["A"] - Hin)
+    m["delta"] = rel_l2(Hg - Hin, res["out"] - Hin)
+    # A and H_out: the sublayers' own contributions (A - H_in, H_out - H_in)
+    # can be small next to the state, so the bf16 rounding of the stored rows
+    # alone may exceed 2e-2 of them: the bound is 2e-2 of the contribution plus
+    # twice that rounding floor
+    for got, ref, key in ((gs["A_all"], res["A"], "A_delta"), (Hg, res["out"], "delta")):
+        if dev.fp32:
+            assert m[key] < tol, (key, m)
+        else:
+            floor = np.linalg.norm(synth.round_bf16(ref.astype(np.float32)) - ref)
+            assert np.linalg.norm(got - ref) <= TOL * np.linalg.norm(ref - Hin) + 2.0 * floor, (key, m)
+    return m, res, lay, out

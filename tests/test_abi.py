@@ -58,7 +58,9 @@ def test_workspace_layout_host_only(L):
     assert lo.x1 - lo.slot_of_row >= R * 4
     assert lo.q - lo.x1 >= R * 3584 * 2
     assert lo.g - lo.x2 >= R * 3584 * 2
-    assert lo.total - lo.g >= R * 18944 * 2
+    assert lo.q_all - lo.g >= R * 18944 * 2
+    assert lo.a_all - lo.n_all >= 256 and lo.fold_ffn - lo.a_all >= R * 3584 * 2
+    assert lo.dep_rows_ffn - lo.dep_off_ffn >= (R + 1) * 4
     # invalid shapes give 0 / an error code
     assert binding.workspace_size(_dims(hd=96), 8, 32) == 0
     assert binding.workspace_size(_dims(n_q=27), 8, 32) == 0
@@ -100,6 +102,10 @@ def test_host_argument_errors_launch_nothing(L):
     assert call(tau=-1.0) == binding.EINVAL
     assert call(H=odd) == binding.EALIGN
     assert call(P=-1) == binding.EINVAL
+    for bad in ({"attn_rematch": 2}, {"ffn_gate": -1}, {"gate_ref": 3}):
+        db = binding.make_dims(3584, 28, 4, 128, 18944, **bad)
+        assert L.specfold_layer_forward(ctypes.byref(db), ctypes.byref(w), good, good, 8, 32, view, view, 512,
+                                        f32(0.05), good, good, size, None, None) == binding.EINVAL
     assert call(view=binding.specfold_kv_view(0x30000, 1028, 128)) == binding.EALIGN
     assert call(view=binding.specfold_kv_view(0x30008, 1024, 128)) == binding.EALIGN
     w_bad = binding.specfold_weights(*([0x20000] * 8 + [0x20004]))
