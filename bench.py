@@ -190,6 +190,25 @@ def stage_roofline(name, dims, n, R, us, peaks):
             "frac": round(a / peaks["bf16_tflops"], 4), "algorithmic_flops": flops}
 
 
+# ------------------------------------------------------ replica plumbing ----
+def reduce_max(value: float, world: int, device: str = "cuda") -> float:
+    """Max of one float over the ranks (one all-reduce); the value itself on
+    one rank.  device "cuda" for NCCL, "cpu" for gloo."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_step: int, steps: int, world: int, total_ms_max: float) -> float:
+    """Whole-job throughput of N replicas: every rank processed units_per_step
+    per step; the job took the slowest rank's time."""
+    return units_per_step * steps * world / (total_ms_max * 1e-3)
+
+
 # ------------------------------------------------------------- our arm ----
 def run_ours(args, rank, world):
     import torch
@@ -295,13 +314,8 @@ def run_ours(args, rank, world):
     _, _, _, stages, _ = timed_steps(args.tau, max(50, min(args.steps, 500)), 5, stage_events=True)
     assert lay.status() == 0, "device status set"
     n = lay.n_packed()
-    total_ms_max = total_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms_max = float(t.item())
-    value = B * L * args.steps * world / (total_ms_max * 1e-3)
+    total_ms_max = reduce_max(total_ms, world)
+    value = aggregate_rate(B * L, args.steps, world, total_ms_max)
 
     # dominant kernel of the step
     gemm_stages = ("qkv", "out_proj_norm", "gate_up", "down")
@@ -376,14 +390,10 @@ def run_ours(args, rank, world):
     e_total = e2e_run(e2e_steps)
     for g in graphs:
         g.close()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_total = float(t.item())
+    e_total = reduce_max(e_total, world)
     for j in range(NBUF):
         assert torch.equal(out_host[j].cuda(), Hout), "e2e output differs from the resident run"
-    e2e = {"value": round(B * L * e2e_steps * world / (e_total * 1e-3), 1), "unit": UNIT,
+    e2e = {"value": round(aggregate_rate(B * L, e2e_steps, world, e_total), 1), "unit": UNIT,
            "h2d_bytes_per_step": int(H.numel() * 2 + parent.numel() * 4),
            "d2h_bytes_per_step": int(Hout.numel() * 2), "steps": e2e_steps,
            "loop": f"{NBUF} buffer sets, input copy / layer / output copy on three streams, no L2 flush "
