@@ -522,6 +522,33 @@ def budget_sweep(args, dims, W, pk, pv, flush, barrier):
     return rows
 
 
+def stage_times(lay, H, parent, tau, out, flush, steps):
+    """Mean µs of every stage of one layer call: a graph of the call with an
+    event-record node at each stage boundary, replayed `steps` times after
+    an L2 flush each."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(binding.STAGE_EVENTS)]
+    for e in ev:  # torch creates the CUDA event at its first record
+        e.record(stream)
+    g = lay.graph(H, parent, tau, out, events=ev)
+    for _ in range(3):
+        flush()
+        g.launch()
+    torch.cuda.synchronize()
+    acc = [0.0] * (binding.STAGE_EVENTS - 1)
+    for _ in range(steps):
+        flush()
+        g.launch()
+        ev[-1].synchronize()
+        for si in range(binding.STAGE_EVENTS - 1):
+            acc[si] += ev[si].elapsed_time(ev[si + 1])
+    g.close()
+    return {nm: acc[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)}
+
+
 def stress_sweep(args, flush, barrier):
     """µs per verify step against the recompute fraction on the stress
     workload (prefix 8192, 64 branches): forced fractions of non-root rows
@@ -544,6 +571,7 @@ def stress_sweep(args, flush, barrier):
     out = torch.empty_like(H)
     stream = torch.cuda.current_stream()
     steps = max(20, min(args.steps, 100))
+    peaks = load_peaks()
     rows = []
     for frac, tau in [(0.0, 0.0)] + [(f, 0.05) for f in w.forced_fracs]:
         br = synth.make_branches(w, np.random.default_rng(args.seed + 17), forced_frac=frac)
@@ -566,9 +594,21 @@ def stress_sweep(args, flush, barrier):
             tot += a.elapsed_time(b)
         g.close()
         nn = lay.n_packed()
-        rows.append({"forced_frac": frac if tau > 0 else None, "tau": tau, "n_packed": nn,
-                     "rho": round(nn / (B * L), 4), "us_per_step": round(tot / steps * 1e3, 2),
-                     "tokens_per_s": round(B * L * steps / (tot * 1e-3), 1)})
+        stages = stage_times(lay, H, parent, tau, out, flush, max(10, steps // 2))
+        row = {"forced_frac": frac if tau > 0 else None, "tau": tau, "n_packed": nn,
+               "rho": round(nn / (B * L), 4), "us_per_step": round(tot / steps * 1e3, 2),
+               "tokens_per_s": round(B * L * steps / (tot * 1e-3), 1),
+               "stages_us": {k: round(v, 2) for k, v in stages.items()}}
+        # each GEMM stage and the attention against its bound (stage times come
+        # from event nodes in the graph, which add a few microseconds each)
+        row["stage_roofline"] = {nm: stage_roofline(nm, d, nn, B * L, stages[nm], peaks)
+                                 for nm in ("qkv", "out_proj_norm", "gate_up", "down")}
+        att_flops = 4.0 * nn * d.n_q * d.hd * (P + L)
+        row["stage_roofline"]["attention"] = {
+            "bound": "tensor", "achieved": round(att_flops / (stages["attention"] * 1e-6) / 1e12, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(att_flops / (stages["attention"] * 1e-6) / 1e12 / peaks["bf16_tflops"], 4)}
+        rows.append(row)
     dense = rows[0]["us_per_step"]
     for r in rows:
         r["time_vs_dense"] = round(r["us_per_step"] / dense, 4)

@@ -50,9 +50,9 @@ class specfold_kv_view(ctypes.Structure):
 
 class specfold_ws_layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in
-                ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "dep_off", "dep_rows", "x1", "q",
+                ("status", "n_packed", "fold", "rel", "src", "packed_idx", "slot_of_row", "dep_rng", "dep_rows", "sync", "x1", "q",
                  "block_k", "block_v", "attn_o", "a", "x2", "g", "q_all", "all_idx", "n_all", "a_all", "fold_ffn",
-                 "rel_ffn", "src_ffn", "packed_ffn", "slot_ffn", "n_ffn", "dep_off_ffn", "dep_rows_ffn",
+                 "rel_ffn", "src_ffn", "packed_ffn", "slot_ffn", "n_ffn", "dep_rng_ffn", "dep_rows_ffn",
                  "gemm_scratch", "attn_scratch", "total")]
 
 

@@ -9,6 +9,8 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <set>
+#include <utility>
 
 #include "sf_device.cuh"
 #include "sf_internal.h"
@@ -19,16 +21,30 @@ static std::atomic<uint64_t> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (dev < 0 || dev >= 64) return 1;
-  if (!cached[dev]) {
-    int v = 0;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (!v) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = v > 0 ? v : 1;
+    v = v > 0 ? v : 1;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return v;
+}
+
+int smem_limit_once(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPECFOLD_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, kernel})) return SPECFOLD_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return SPECFOLD_ECUDA;
+  done.insert({dev, kernel});
+  return SPECFOLD_OK;
 }
 
 bool pdl_enabled() {
@@ -171,6 +187,7 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
     off += up256(bytes);
     return at;
   };
+  memset(o, 0, sizeof(*o));
   o->status = take(4);
   o->n_packed = take(4);
   o->fold = take(R);
@@ -178,8 +195,9 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->src = take(R * 4);
   o->packed_idx = take(R * 4);
   o->slot_of_row = take(R * 4);
-  o->dep_off = take((R + 1) * 4);
+  o->dep_rng = take(R * 8);
   o->dep_rows = take(R * 4);
+  o->sync = take(gate_pack_sync_bytes());
   o->x1 = take(R * d->d_model * e);
   o->q = take(R * nq * e);
   o->block_k = take(R * nkv * e);
@@ -188,18 +206,20 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
   o->a = take(R * d->d_model * e);
   o->x2 = take(R * d->d_model * e);
   o->g = take(R * d->ffn_dim * e);
-  o->q_all = take(R * nq * e);
-  o->all_idx = take(R * 4);
-  o->n_all = take(4);
-  o->a_all = take(R * d->d_model * e);
-  o->fold_ffn = take(R);
-  o->rel_ffn = take(R * 4);
-  o->src_ffn = take(R * 4);
-  o->packed_ffn = take(R * 4);
-  o->slot_ffn = take(R * 4);
-  o->n_ffn = take(4);
-  o->dep_off_ffn = take((R + 1) * 4);
-  o->dep_rows_ffn = take(R * 4);
+  if (d->attn_rematch || d->ffn_gate) {  // the variant sublayer path only
+    o->q_all = take(R * nq * e);
+    o->all_idx = take(R * 4);
+    o->n_all = take(4);
+    o->a_all = take(R * d->d_model * e);
+    o->fold_ffn = take(R);
+    o->rel_ffn = take(R * 4);
+    o->src_ffn = take(R * 4);
+    o->packed_ffn = take(R * 4);
+    o->slot_ffn = take(R * 4);
+    o->n_ffn = take(4);
+    o->dep_rng_ffn = take(R * 8);
+    o->dep_rows_ffn = take(R * 4);
+  }
   o->gemm_scratch = take(gemm_partial_floats() * 4);
   o->attn_scratch = take(attn_partial_bytes(static_cast<int>(R), d->n_q_heads / d->n_kv_heads, d->n_kv_heads,
                                             d->head_dim));
@@ -332,13 +352,13 @@ static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, con
   return gemm_call(d->dtype, c, st);
 }
 
-// dep_off / dep_rows (the folded rows grouped by source slot, from the pack
+// dep_rng / dep_rows (the folded rows grouped by source row, from the pack
 // step) move the fold-fill into the down projection's finish kernel; without
 // them a separate fold-fill kernel walks fold / src.
 static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const void* A, const int32_t* packed_idx,
                      const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int R,
                      void* H_out, void* X2, void* G, const Scratch& s, uint32_t* status, cudaStream_t st,
-                     void* const* ev, int ev0, bool x2_ready, const int32_t* dep_off = nullptr,
+                     void* const* ev, int ev0, bool x2_ready, const int32_t* dep_rng = nullptr,
                      const int32_t* dep_rows = nullptr) {
   auto mark = [&](int i) {
     if (ev) record_stage_event(ev[i], st);
@@ -378,16 +398,16 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   c.ldr = d->d_model;
   c.row_idx = packed_idx;
   fill_scratch(c, s, status);
-  if (dep_off && d->dtype == SPECFOLD_BF16) {  // the fp32 path fills with the fold-fill kernel
-    c.dep_off = dep_off;
+  if (dep_rng && d->dtype == SPECFOLD_BF16) {  // the fp32 path fills with the fold-fill kernel
+    c.dep_rng = dep_rng;
     c.dep_rows = dep_rows;
     c.hin = H_in;
   } else {
-    dep_off = nullptr;
+    dep_rng = nullptr;
   }
   SF_TRY(gemm_call(d->dtype, c, st));
   mark(ev0 + 2);
-  if (!dep_off) SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
+  if (!dep_rng) SF_TRY(launch_fold_fill(d->dtype, fold, src, H_in, H_out, R, d->d_model, st));
   mark(ev0 + 3);
   return SPECFOLD_OK;
 }
@@ -483,10 +503,10 @@ static int enqueue_layer_sublayers(const specfold_dims* dims, const specfold_wei
   int32_t* n_f = at<int32_t>(ws, lo.n_ffn);
   SF_TRY(launch_select_pack(dims->dtype, fold_f, parent, B, L, dims->d_model, a_all, w->g2, dims->rms_eps, src_f,
                             pidx_f, at<int32_t>(ws, lo.slot_ffn), n_f, at<void>(ws, lo.x2), status, st, nullptr,
-                            at<int32_t>(ws, lo.dep_off_ffn), at<int32_t>(ws, lo.dep_rows_ffn), at<void>(ws, lo.a)));
+                            at<int32_t>(ws, lo.dep_rng_ffn), at<int32_t>(ws, lo.dep_rows_ffn), at<void>(ws, lo.a)));
   mark(5);
   return stage_ffn(dims, w, at<void>(ws, lo.a), pidx_f, n_f, a_all, src_f, fold_f, R, H_out, at<void>(ws, lo.x2),
-                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_off_ffn),
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_rng_ffn),
                    at<int32_t>(ws, lo.dep_rows_ffn));
 }
 
@@ -510,11 +530,24 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
     if (stage_events) record_stage_event(stage_events[i], st);
   };
   mark(0);
-  SF_TRY(launch_layer_gate(dims, H_in, parent, B, L, tau, fold, at<float>(ws, lo.rel), fold_hist, st));
-  mark(1);
-  SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
-                            at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,
-                            at<int32_t>(ws, lo.dep_off), at<int32_t>(ws, lo.dep_rows)));
+  // S1-S3 in one launch (parent gate); the two-kernel form where the fused
+  // kernel does not take the shape, or for the variant gate
+  int rc = SPECFOLD_EUNSUPPORTED;
+  if (dims->gate_ref == 0)
+    rc = launch_gate_pack(dims->dtype, H_in, parent, B, L, dims->d_model, tau, w->g1, dims->rms_eps, fold,
+                          at<float>(ws, lo.rel), src, pidx, at<int32_t>(ws, lo.slot_of_row), n_dev,
+                          at<void>(ws, lo.x1), at<int32_t>(ws, lo.dep_rng), at<int32_t>(ws, lo.dep_rows),
+                          at<void>(ws, lo.sync), status, st, fold_hist, n_hist);
+  if (rc == SPECFOLD_OK) {
+    mark(1);  // the fused launch is the "gate" stage; "select_pack" is empty
+  } else {
+    if (rc != SPECFOLD_EUNSUPPORTED) return rc;
+    SF_TRY(launch_layer_gate(dims, H_in, parent, B, L, tau, fold, at<float>(ws, lo.rel), fold_hist, st));
+    mark(1);
+    SF_TRY(launch_select_pack(dims->dtype, fold, parent, B, L, dims->d_model, H_in, w->g1, dims->rms_eps, src, pidx,
+                              at<int32_t>(ws, lo.slot_of_row), n_dev, at<void>(ws, lo.x1), status, st, n_hist,
+                              at<int32_t>(ws, lo.dep_rng), at<int32_t>(ws, lo.dep_rows)));
+  }
   mark(2);
   SF_TRY(stage_qkv(dims, w, at<void>(ws, lo.x1), pidx, n_dev, R, at<void>(ws, lo.q), at<void>(ws, lo.block_k),
                    at<void>(ws, lo.block_v), s, status, st));
@@ -530,7 +563,7 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
                         at<void>(ws, lo.x2)));
   mark(5);
   return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
-                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_off),
+                   at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_rng),
                    at<int32_t>(ws, lo.dep_rows));
 }
 

@@ -1,14 +1,18 @@
 // Folded attention (S5) on the 5th-generation tensor cores.
 //
-// One CTA takes 128 query rows of one KV head: row m = k*g + j is query head
-// (h*g + j) of packed row k, so a tile mixes the GQA group and consecutive
-// packed rows, which may belong to several branches.  Keys are streamed in
-// blocks of 128:
+// Work unit = (128 query rows of one KV head, one key range): row m = k*g + j
+// of the tile is query head (h*g + j) of packed row k, so a tile mixes the
+// GQA group and consecutive packed rows, which may belong to several
+// branches.  Keys are streamed in blocks of 128:
 //   * the shared prefix (all branches see it) through a 3-D TMA map over the
 //     caller's strided view -- never copied per branch;
 //   * then the L block keys of every branch present in the tile, gathered
 //     through the provenance table (key j of branch b is row src[b*L + j] of
 //     the block K/V), with scores of other branches' keys masked.
+// A key range is the whole key sequence or, split-KV, one of SP slices whose
+// partials a combine kernel merges.  The kernel is persistent: one CTA per SM
+// loops over the units of the packed-row count n read on the device, with
+// its pipeline running on across units.
 // S = Q K^T and O += P V run as tcgen05.mma into TMEM (two S buffers so the
 // next S overlaps the softmax, one O accumulator); four softmax warps own one
 // query row per thread, keep the running max and sum, rescale O in TMEM when
@@ -24,6 +28,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 namespace sf {
@@ -47,9 +52,9 @@ struct AttnParams {
   int P, L, R, n_kv, g, n_q;
   float sl2;  // log2(e) / sqrt(hd)
   uint32_t* status;
-  // split-KV: up to sp_max CTAs share one (query tile, kv head); each writes
-  // an unnormalised partial (o, running max m in log2 units, sum l)
-  int sp_max;
+  // split-KV: SP units share one (query tile, kv head); each writes an
+  // unnormalised partial (o, running max m in log2 units, sum l) to slot
+  // (h * tiles + x) * SP + z of the live tiles
   int num_sms;
   // paged prefix (table != null): whole 128-key blocks inside one page go
   // through TMA over the pool, the rest through plain gathers
@@ -59,8 +64,8 @@ struct AttnParams {
   const __nv_bfloat16* pvp;
   long long k_ts, k_hs, v_ts, v_hs;  // token and head strides, elements
   uint8_t sp_table[1024];            // key-range splits by tile count (see plan_splits)
-  float* part_o;    // [tiles_x * n_kv * sp_max][128][hd]
-  float* part_ml;   // [tiles_x * n_kv * sp_max][128][2]
+  float* part_o;    // [slot capacity][128][hd]
+  float* part_ml;   // [slot capacity][128][2]
 };
 
 // Number of key-range splits for n packed rows, looked up from a table the
@@ -89,6 +94,33 @@ struct ACfg {
   static constexpr uint32_t COL_O = 256;
 };
 
+// One unit of work (see the file comment) for the live packed-row count.
+struct AUnit {
+  int x, h, z, m0, b_lo, keys_blk, NB, jb, NT;
+  size_t pslot;
+};
+
+SF_DEV AUnit attn_unit(const AttnParams& p, int u, int n, int tiles_x, int SP) {
+  AUnit w;
+  w.x = u % tiles_x;
+  const int rest = u / tiles_x;
+  w.h = rest % p.n_kv;
+  w.z = rest / p.n_kv;
+  w.m0 = w.x * 128;
+  const int g = p.g, L = p.L, B = p.R / L;
+  const int k_lo = w.m0 / g;
+  const int k_hi = min(n - 1, (w.m0 + 127) / g);
+  w.b_lo = min(max(p.packed_idx[k_lo] / L, 0), B - 1);
+  const int b_hi = min(max(p.packed_idx[k_hi] / L, w.b_lo), B - 1);
+  w.keys_blk = (b_hi - w.b_lo + 1) * L;
+  const int NBP = (p.P + 127) / 128;
+  w.NB = NBP + (w.keys_blk + 127) / 128;
+  w.jb = (w.z * w.NB) / SP;
+  w.NT = ((w.z + 1) * w.NB) / SP - w.jb;
+  w.pslot = (static_cast<size_t>(w.h) * tiles_x + w.x) * SP + w.z;
+  return w;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_constant__ AttnParams p) {
   using C = ACfg<HD>;
@@ -106,6 +138,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint64_t* s_free = bars + 7;    // [2]
   uint64_t* p_full = bars + 9;
   uint64_t* o_full = bars + 10;   // one completion per P V product
+  uint64_t* q_empty = bars + 11;  // the S products of a unit are done: Q may be replaced
+  uint64_t* o_empty = bars + 12;  // the softmax warps have read a unit's output
   uint64_t* drain = bars + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -114,35 +148,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();
-  const int h = blockIdx.y;
-  const int m0 = blockIdx.x * 128;
   const int g = p.g, L = p.L;
   const int n = min(max(p.n_dev[0], 0), p.R);
   const int rows_total = n * g;
-  if (m0 >= rows_total) return;
-  const int k_lo = m0 / g;
-  const int k_hi = min(n - 1, (m0 + 127) / g);
-  const int B = p.R / L;
-  const int b_lo = min(max(p.packed_idx[k_lo] / L, 0), B - 1);
-  const int b_hi = min(max(p.packed_idx[k_hi] / L, b_lo), B - 1);
-  const int keys_blk = (b_hi - b_lo + 1) * L;
-  const int NBP = (p.P + 127) / 128;
-  const int NB = NBP + (keys_blk + 127) / 128;
-  // this CTA's share of the key blocks
+  const int tiles_x = (rows_total + 127) / 128;
   const int SP = attn_splits(p, rows_total);
-  const int z = blockIdx.z;
-  if (z >= SP) return;
-  const int jb = (z * NB) / SP;
-  const int NT = ((z + 1) * NB) / SP - jb;
-  const size_t pslot = (static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * p.sp_max + z;
-  if (NT == 0) {  // empty key range: a neutral partial
-    for (int i = threadIdx.x; i < 128 * HD; i += kAttnThreads) p.part_o[pslot * 128 * HD + i] = 0.f;
-    for (int i = threadIdx.x; i < 128; i += kAttnThreads) {
-      p.part_ml[(pslot * 128 + i) * 2] = -INFINITY;
-      p.part_ml[(pslot * 128 + i) * 2 + 1] = 0.f;
-    }
-    return;
-  }
+  const int U = tiles_x * p.n_kv * SP;
+  if (static_cast<int>(blockIdx.x) >= U) return;
+  const int NBP = (p.P + 127) / 128;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -151,10 +164,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&kv_empty[i]), 1);
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 128);
-
     }
     mbar_init(smem_u32(p_full), 128);
     mbar_init(smem_u32(o_full), 1);
+    mbar_init(smem_u32(q_empty), 1);
+    mbar_init(smem_u32(o_empty), 128);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -170,99 +184,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sP = smem + C::OFF_P;
 
+  // Every role walks the same units in the same order; gt counts this CTA's
+  // key blocks over all units so far (it sets the ring stage and the phase
+  // of every per-block barrier), j its units with keys (Q and O barriers).
   if (warp < 3) {
     // ------------------------------------------------------------ loaders --
     const int lt = threadIdx.x;
+    int gt = 0, j = 0;
+    int issued_tma = -1, issued_q = -1;
+    bool ok = true;
     if (lt == 0) {
       prefetch_tmap(&p.mapQ);
       if (NBP > 0) {
         prefetch_tmap(&p.mapK);
         prefetch_tmap(&p.mapV);
       }
-      mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
-      for (int a = 0; a < C::NATOM; ++a)
-        tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + m0);
     }
-    int issued_tma = -1;
-    for (int t = 0; t < NT; ++t) {
-      const int j = jb + t;
-      const int st = t & 1;
-      if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((t >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
-      named_bar_sync(1, kLoaders);
-      if (!okflag[st]) break;
-      uint8_t* sK = smem + C::OFF_KV + (2 * st) * C::KV_BYTES;
-      uint8_t* sV = sK + C::KV_BYTES;
-      // prefix blocks go through TMA unless paged with the block not inside
-      // one page or not whole (pool tokens past P may hold anything)
-      const bool use_tma = j < NBP && (!p.table || (p.page_tma && (j + 1) * 128 <= p.P));
-      if (use_tma) {
-        if (lt == 0) {
-          int z = j * 128;
-          if (p.table) {
-            const int page = p.table[(j * 128) / p.page_size];
-            if (page >= 0 && page < p.num_pages) {
-              z = page * p.page_size + (j * 128) % p.page_size;
-            } else {
-              z = p.num_pages * p.page_size;  // wholly past the pool: the box reads zeros
-              atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
-            }
-          }
-          const uint32_t fb = smem_u32(&kv_full[st]);
-          mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
-          for (int a = 0; a < C::NATOM; ++a) {
-            tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, z);
-            tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, z);
-          }
-          issued_tma = t;
+    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+      const AUnit w = attn_unit(p, u, n, tiles_x, SP);
+      if (w.NT == 0) continue;
+      const int h = w.h;
+      if (lt == 0) {
+        // the previous unit's S products must be done with the Q buffer
+        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status)) {
+          mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
+          for (int a = 0; a < C::NATOM; ++a)
+            tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + w.m0);
+          issued_q = j;
         }
-      } else {
-        for (int kr = lt; kr < 128; kr += kLoaders) {
-          int bb = -1;
-          const uint4* krow = nullptr;
-          const uint4* vrow = nullptr;
-          if (j < NBP) {  // paged prefix token
-            const int tk = j * 128 + kr;
-            if (tk < p.P) {
-              const int page = p.table[tk / p.page_size];
+      }
+      for (int t = 0; t < w.NT; ++t, ++gt) {
+        const int jblk = w.jb + t;
+        const int st = gt & 1;
+        if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+        named_bar_sync(1, kLoaders);
+        if (!okflag[st]) {
+          ok = false;
+          break;
+        }
+        uint8_t* sK = smem + C::OFF_KV + (2 * st) * C::KV_BYTES;
+        uint8_t* sV = sK + C::KV_BYTES;
+        // prefix blocks go through TMA unless paged with the block not inside
+        // one page or not whole (pool tokens past P may hold anything)
+        const bool use_tma = jblk < NBP && (!p.table || (p.page_tma && (jblk + 1) * 128 <= p.P));
+        if (use_tma) {
+          if (lt == 0) {
+            int z = jblk * 128;
+            if (p.table) {
+              const int page = p.table[(jblk * 128) / p.page_size];
               if (page >= 0 && page < p.num_pages) {
-                const size_t tok = static_cast<size_t>(page) * p.page_size + tk % p.page_size;
-                krow = reinterpret_cast<const uint4*>(p.pkp + tok * p.k_ts + static_cast<size_t>(h) * p.k_hs);
-                vrow = reinterpret_cast<const uint4*>(p.pvp + tok * p.v_ts + static_cast<size_t>(h) * p.v_hs);
+                z = page * p.page_size + (jblk * 128) % p.page_size;
               } else {
+                z = p.num_pages * p.page_size;  // wholly past the pool: the box reads zeros
                 atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
               }
             }
-          } else {
-            const int e = (j - NBP) * 128 + kr;
-            if (e < keys_blk) {
-              const int b = b_lo + e / L;
-              const int s = p.src[b * L + (e - (e / L) * L)];
-              if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
-                bb = b;
-                const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
-                krow = reinterpret_cast<const uint4*>(p.bK + off);
-                vrow = reinterpret_cast<const uint4*>(p.bV + off);
-              }
+            const uint32_t fb = smem_u32(&kv_full[st]);
+            mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+            for (int a = 0; a < C::NATOM; ++a) {
+              tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, z);
+              tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, z);
             }
-            meta[st * 128 + kr] = bb;
+            issued_tma = gt;
           }
+        } else {
+          for (int kr = lt; kr < 128; kr += kLoaders) {
+            int bb = -1;
+            const uint4* krow = nullptr;
+            const uint4* vrow = nullptr;
+            if (jblk < NBP) {  // paged prefix token
+              const int tk = jblk * 128 + kr;
+              if (tk < p.P) {
+                const int page = p.table[tk / p.page_size];
+                if (page >= 0 && page < p.num_pages) {
+                  const size_t tok = static_cast<size_t>(page) * p.page_size + tk % p.page_size;
+                  krow = reinterpret_cast<const uint4*>(p.pkp + tok * p.k_ts + static_cast<size_t>(h) * p.k_hs);
+                  vrow = reinterpret_cast<const uint4*>(p.pvp + tok * p.v_ts + static_cast<size_t>(h) * p.v_hs);
+                } else {
+                  atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
+                }
+              }
+            } else {
+              const int e = (jblk - NBP) * 128 + kr;
+              if (e < w.keys_blk) {
+                const int b = w.b_lo + e / L;
+                const int s = p.src[b * L + (e - (e / L) * L)];
+                if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
+                  bb = b;
+                  const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
+                  krow = reinterpret_cast<const uint4*>(p.bK + off);
+                  vrow = reinterpret_cast<const uint4*>(p.bV + off);
+                }
+              }
+              meta[st * 128 + kr] = bb;
+            }
 #pragma unroll
-          for (int c16 = 0; c16 < HD / 8; ++c16) {
-            const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
-            const uint4 vv = vrow ? __ldg(vrow + c16) : make_uint4(0, 0, 0, 0);
-            const int off = (c16 >> 3) * kAtom + kr * 128 + (((c16 & 7) ^ (kr & 7)) << 4);
-            *reinterpret_cast<uint4*>(sK + off) = kv;
-            *reinterpret_cast<uint4*>(sV + off) = vv;
+            for (int c16 = 0; c16 < HD / 8; ++c16) {
+              const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
+              const uint4 vv = vrow ? __ldg(vrow + c16) : make_uint4(0, 0, 0, 0);
+              const int off = (c16 >> 3) * kAtom + kr * 128 + (((c16 & 7) ^ (kr & 7)) << 4);
+              *reinterpret_cast<uint4*>(sK + off) = kv;
+              *reinterpret_cast<uint4*>(sV + off) = vv;
+            }
           }
+          fence_proxy_async_smem();
+          named_bar_sync(1, kLoaders);
+          if (lt == 0) mbar_arrive(smem_u32(&kv_full[st]));
         }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kLoaders);
-        if (lt == 0) mbar_arrive(smem_u32(&kv_full[st]));
       }
+      ++j;
     }
-    if (lt == 0 && *abort_flag && issued_tma >= 0) {
+    if (lt == 0 && *abort_flag) {
+      // let the copies already issued land before the CTA exits
       int never = 0;
-      mbar_wait(smem_u32(&kv_full[issued_tma & 1]), (issued_tma >> 1) & 1, &never, nullptr, 10000000ull);
+      if (issued_tma >= 0)
+        mbar_wait(smem_u32(&kv_full[issued_tma & 1]), (issued_tma >> 1) & 1, &never, nullptr, 10000000ull);
+      if (issued_q >= 0) mbar_wait(smem_u32(q_full), issued_q & 1, &never, nullptr, 10000000ull);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax --
@@ -272,151 +309,169 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     // max grows by more than 2^8, so the probabilities stay below 2^8.
     const int qw = warp & 3;
     const int row = qw * 32 + lane;
-    const int m = m0 + row;
-    const bool valid = m < rows_total;
-    const int k = valid ? m / g : 0;
-    const int hg = m - (m / g) * g;
-    const int my_b = valid ? p.packed_idx[k] / L : -2;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t to = tmem + lane_off + C::COL_O;
-    float m_ref = -INFINITY, l = 0.f;
+    int gt = 0, j = 0;
     bool ok = true;
-    for (int t = 0; t < NT && ok; ++t) {
-      const int j = jb + t;
-      const int sb = t & 1;
-      if (!mbar_wait(smem_u32(&s_full[sb]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      __syncwarp();
-      const bool prefix = j < NBP;
-      if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-      const int key0 = j * 128;
-      const uint32_t ts = tmem + lane_off + sb * 128;
-      // visibility of the 128 keys as four 32-bit masks (bit e of km[c]: key
-      // 32c + e): prefix keys below P, block keys of this row's own branch
-      uint32_t km[4];
-      if (prefix) {
-        const int lim = p.P - key0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int v = lim - c * 32;
-          km[c] = v >= 32 ? 0xffffffffu : (v <= 0 ? 0u : ((1u << v) - 1u));
-        }
-      } else {
-        const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t mk = 0;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int4 v = mb4[c * 8 + q];
-            mk |= (static_cast<uint32_t>(v.x == my_b) << (4 * q)) | (static_cast<uint32_t>(v.y == my_b) << (4 * q + 1)) |
-                  (static_cast<uint32_t>(v.z == my_b) << (4 * q + 2)) | (static_cast<uint32_t>(v.w == my_b) << (4 * q + 3));
-          }
-          km[c] = mk;
-        }
+    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+      const AUnit w = attn_unit(p, u, n, tiles_x, SP);
+      if (w.NT == 0) {  // empty key range: a neutral partial
+        float* po = p.part_o + (w.pslot * 128 + row) * HD;
+        for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.part_ml[(w.pslot * 128 + row) * 2] = -INFINITY;
+        p.part_ml[(w.pslot * 128 + row) * 2 + 1] = 0.f;
+        continue;
       }
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(ts + c * 32, sv[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
-      // a whole prefix block needs no mask; eight independent max chains
-      // (one warp per SM sub-partition: a single 128-deep chain would stall)
-      const bool allv = prefix && p.P - key0 >= 128;
-      float mx8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
-      if (allv) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mx8[e & 7] = fmaxf(mx8[e & 7], ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_ref, mx * p.sl2);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (m_ref == -INFINITY) {
-        m_ref = m_new;               // nothing accumulated yet (every earlier p was 0)
-      } else if (m_new > m_ref + 8.f) {
-        alpha = ex2(m_ref - m_new);
-        m_ref = m_new;
-        rescale = true;
-      }
-      l *= alpha;
-      if (t >= 1) {
-        // P V of the previous block must be done: it frees the P tile, and O
-        // may only be rescaled once it holds that block's contribution
-        if (!mbar_wait(smem_u32(o_full), (t - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      const int h = w.h;
+      const int m = w.m0 + row;
+      const bool valid = m < rows_total;
+      const int k = valid ? m / g : 0;
+      const int hg = m - (m / g) * g;
+      const int my_b = valid ? p.packed_idx[k] / L : -2;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int t = 0; t < w.NT; ++t) {
+        const int gi = gt + t;
+        const int jblk = w.jb + t;
+        const int sb = gi & 1;
+        if (!mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        __syncwarp();
+        const bool prefix = jblk < NBP;
+        if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         __syncwarp();
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
+        const int key0 = jblk * 128;
+        const uint32_t ts = tmem + lane_off + sb * 128;
+        // visibility of the 128 keys as four 32-bit masks (bit e of km[c]: key
+        // 32c + e): prefix keys below P, block keys of this row's own branch
+        uint32_t km[4];
+        if (prefix) {
+          const int lim = p.P - key0;
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(to + c * 32, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(to + c * 32, r);
-          }
-          tmem_st_wait();
-        }
-      }
-      // probabilities -> bf16 P tile (K-major, 128-byte swizzle); the row sum
-      // in four independent partial sums
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-        if (allv) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float x0 = ex2(fmaf(__uint_as_float(sv[c][e]), p.sl2, -m_ref));
-            const float x1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), p.sl2, -m_ref));
-            ls[(e >> 1) & 3] += x0 + x1;
-            pk[e / 2] = pack_bf16x2(x0, x1);
+          for (int c = 0; c < 4; ++c) {
+            const int v = lim - c * 32;
+            km[c] = v >= 32 ? 0xffffffffu : (v <= 0 ? 0u : ((1u << v) - 1u));
           }
         } else {
+          const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t mk = 0;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const float x = ex2(fmaf(__uint_as_float(sv[c][e + u]), p.sl2, -m_ref));
-              pv[u] = ((km[c] >> (e + u)) & 1u) ? x : 0.f;
+            for (int q = 0; q < 8; ++q) {
+              const int4 v = mb4[c * 8 + q];
+              mk |= (static_cast<uint32_t>(v.x == my_b) << (4 * q)) | (static_cast<uint32_t>(v.y == my_b) << (4 * q + 1)) |
+                    (static_cast<uint32_t>(v.z == my_b) << (4 * q + 2)) | (static_cast<uint32_t>(v.w == my_b) << (4 * q + 3));
             }
-            ls[(e >> 1) & 3] += pv[0] + pv[1];
-            pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
+            km[c] = mk;
           }
         }
+        uint32_t sv[4][32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
-          const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
-          *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        for (int c = 0; c < 4; ++c) tmem_ld32(ts + c * 32, sv[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
+        // a whole prefix block needs no mask; eight independent max chains
+        // (one warp per SM sub-partition: a single 128-deep chain would stall)
+        const bool allv = prefix && p.P - key0 >= 128;
+        float mx8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
+        if (allv) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              mx8[e & 7] = fmaxf(mx8[e & 7], ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float m_new = fmaxf(m_ref, mx * p.sl2);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_ref == -INFINITY) {
+          m_ref = m_new;               // nothing accumulated yet (every earlier p was 0)
+        } else if (m_new > m_ref + 8.f) {
+          alpha = ex2(m_ref - m_new);
+          m_ref = m_new;
+          rescale = true;
+        }
+        l *= alpha;
+        if (t >= 1) {
+          // P V of the previous block must be done: it frees the P tile, and O
+          // may only be rescaled once it holds that block's contribution
+          if (!mbar_wait(smem_u32(o_full), (gi - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          __syncwarp();
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(to + c * 32, r);
+              tmem_ld_wait(r);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(to + c * 32, r);
+            }
+            tmem_st_wait();
+          }
+        }
+        // probabilities -> bf16 P tile (K-major, 128-byte swizzle); the row sum
+        // in four independent partial sums, of the rounded values the P V
+        // product uses (so the output is an exactly normalised average of V
+        // rows, with no row-wide scale error from the rounding of P)
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+          if (allv) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float x0 = ex2(fmaf(__uint_as_float(sv[c][e]), p.sl2, -m_ref));
+              const float x1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), p.sl2, -m_ref));
+              const uint32_t pr = pack_bf16x2(x0, x1);
+              ls[(e >> 1) & 3] += bf16lo(pr) + bf16hi(pr);
+              pk[e / 2] = pr;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float pv[2];
+#pragma unroll
+              for (int uu = 0; uu < 2; ++uu) {
+                const float x = ex2(fmaf(__uint_as_float(sv[c][e + uu]), p.sl2, -m_ref));
+                pv[uu] = ((km[c] >> (e + uu)) & 1u) ? x : 0.f;
+              }
+              const uint32_t pr = pack_bf16x2(pv[0], pv[1]);
+              ls[(e >> 1) & 3] += bf16lo(pr) + bf16hi(pr);
+              pk[e / 2] = pr;
+            }
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
+            const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          }
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tc_fence_before();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(p_full));
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tc_fence_before();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(p_full));
-    }
-    if (ok && mbar_wait(smem_u32(o_full), (NT - 1) & 1, abort_flag, p.status)) {
+      if (!ok) break;
+      const int glast = gt + w.NT - 1;
+      if (!mbar_wait(smem_u32(o_full), glast & 1, abort_flag, p.status)) { ok = false; break; }
       __syncwarp();
       tc_fence_after();
       if (SP > 1) {
-        float* po = p.part_o + (pslot * 128 + row) * HD;
+        float* po = p.part_o + (w.pslot * 128 + row) * HD;
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t r[32];
@@ -428,8 +483,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
                             __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
         }
-        p.part_ml[(pslot * 128 + row) * 2] = m_ref;
-        p.part_ml[(pslot * 128 + row) * 2 + 1] = l;
+        p.part_ml[(w.pslot * 128 + row) * 2] = m_ref;
+        p.part_ml[(w.pslot * 128 + row) * 2 + 1] = l;
       } else {
         const float inv = 1.f / l;
         uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
@@ -450,45 +505,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
         }
       }
+      // the accumulator is free for the next unit's first P V product
+      tc_fence_before();
+      mbar_arrive(smem_u32(o_empty));
+      gt += w.NT;
+      ++j;
     }
   } else {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, HD, true);
-      bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, p.status);
       const uint32_t aQ = smem_u32(sQ);
       const uint32_t aP = smem_u32(sP);
-      auto issue_pv = [&](int i) -> bool {  // i: local block index
-        if (!mbar_wait(smem_u32(p_full), i & 1, abort_flag, p.status)) return false;
+      int gt = 0, j = 0;
+      bool ok = true;
+      // P V of key block gi (first: the unit's first block, which overwrites O
+      // once the softmax warps have read the previous unit's output)
+      auto issue_pv = [&](int gi, bool first) -> bool {
+        if (first && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(smem_u32(p_full), gi & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t aPi = aP;
-        const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (i & 1) + 1) * C::KV_BYTES);
+        const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (gi & 1) + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aPi + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (i > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(o_full));
-        tc_commit(smem_u32(&kv_empty[i & 1]));
+        tc_commit(smem_u32(&kv_empty[gi & 1]));
         return true;
       };
-      for (int t = 0; t < NT && ok; ++t) {
-        const int st = t & 1;
-        if (!mbar_wait(smem_u32(&kv_full[st]), (t >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&s_free[st]), ((t >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * st) * C::KV_BYTES);
+      for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+        const AUnit w = attn_unit(p, u, n, tiles_x, SP);
+        if (w.NT == 0) continue;
+        if (!mbar_wait(smem_u32(q_full), j & 1, abort_flag, p.status)) break;
+        for (int t = 0; t < w.NT && ok; ++t) {
+          const int gi = gt + t;
+          const int st = gi & 1;
+          if (!mbar_wait(smem_u32(&kv_full[st]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&s_free[st]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * st) * C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          tc_mma_f16(tmem + st * 128,
-                     sdesc_sw128(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(aK + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            tc_mma_f16(tmem + st * 128,
+                       sdesc_sw128(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                       sdesc_sw128(aK + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&s_full[st]));
+          if (t == w.NT - 1) tc_commit(smem_u32(q_empty));  // Q is read by no later product of this unit
+          if (t >= 1 && !issue_pv(gi - 1, t == 1)) { ok = false; break; }
         }
-        tc_commit(smem_u32(&s_full[st]));
-        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+        if (!ok) break;
+        if (!issue_pv(gt + w.NT - 1, w.NT == 1)) break;
+        gt += w.NT;
+        ++j;
       }
-      if (ok) issue_pv(NT - 1);
       tc_commit(smem_u32(drain));
       int never = 0;
       mbar_wait(smem_u32(drain), 0, &never, nullptr, 10000000ull);
@@ -507,13 +580,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 // Merges the split-KV partials: for each (query row, kv head, 8 dims),
 // O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s with M = max_s m_s.
 template <int HD>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p, int tiles_x) {
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   pdl_wait();
   pdl_trigger();
   const int n = min(max(p.n_dev[0], 0), p.R);
   const int rows_total = n * p.g;
   const int SP = attn_splits(p, rows_total);
   if (SP <= 1) return;
+  const int tiles_x = (rows_total + 127) / 128;
   constexpr int DG = HD / 8;
   const long long total = static_cast<long long>(rows_total) * p.n_kv * DG;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -523,7 +597,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     const int m = static_cast<int>(rest % rows_total);
     const int h = static_cast<int>(rest / rows_total);
     const int row = m & 127;
-    const size_t pb = (static_cast<size_t>(h) * tiles_x + (m >> 7)) * p.sp_max;
+    const size_t pb = (static_cast<size_t>(h) * tiles_x + (m >> 7)) * SP;
     // every load of the row is issued before any arithmetic
     float mz[16], lz[16];
     float4 oa[16], ob[16];
@@ -569,23 +643,37 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
 }
 
 // Split count for `tiles` (query tile, KV head) pairs: with one CTA per SM,
-// S splits cost about ceil(tiles * S / SMs) waves, each CTA paying a fixed
-// cost (setup, first loads, write-out: about two key blocks) plus its share
-// nb / S of the key blocks; the S with the least cost (the smallest on a near
-// tie, since a split adds the combine step), at most one more than the key
-// blocks (the block keys may span two).
-int plan_splits(int tiles, int sp_max, int num_sms, int P) {
+// S splits cost about ceil(tiles * S / SMs) waves, each unit paying a fixed
+// cost (first loads, the write-out of its output or partial, which the
+// softmax warps do in series with their next unit: about four key blocks)
+// plus its share
+// nb / S of the key blocks, and a split adds the combine launch (about
+// `combine` key blocks); the S with the least cost (the smallest on a near
+// tie), at most one more than the key blocks (the block keys may span two)
+// and at most sp_lim.
+int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
   const float nb = static_cast<float>((P + 127) / 128 + 1);
   int best = 1;
-  float best_t = static_cast<float>((tiles + num_sms - 1) / num_sms) * (2.f + nb);
-  for (int sp = 2; sp <= sp_max && sp <= nb + 1; ++sp) {
-    const float t = static_cast<float>((tiles * sp + num_sms - 1) / num_sms) * (2.f + nb / sp);
+  constexpr float kUnit = 4.f;
+  float best_t = static_cast<float>((tiles + num_sms - 1) / num_sms) * (kUnit + nb);
+  for (int sp = 2; sp <= sp_lim && sp <= nb + 1; ++sp) {
+    const float t = static_cast<float>((tiles * sp + num_sms - 1) / num_sms) * (kUnit + nb / sp) + combine;
     if (t < best_t * 0.97f) {
       best = sp;
       best_t = t;
     }
   }
   return best;
+}
+
+// Cost of the combine launch in key blocks (SPECFOLD_ATTN_COMBINE_COST
+// overrides it).
+float combine_cost() {
+  static const float c = [] {
+    const char* e = std::getenv("SPECFOLD_ATTN_COMBINE_COST");
+    return e ? static_cast<float>(std::atof(e)) : 3.f;
+  }();
+  return c;
 }
 
 template <int HD>
@@ -632,34 +720,32 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   p.n_q = c.n_q;
   p.sl2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   p.status = c.status;
-  const int tiles_x = (R * g + 127) / 128;
-  p.sp_max = attn_sp_max(R, g, c.n_kv);
   p.num_sms = num_sms();
+  // split counts per live tile count, within the partials' slot capacity
+  const int cap = attn_slot_cap(R, g, c.n_kv);
   const int tiles_max = std::min(((R * g + 127) / 128) * c.n_kv, kSpTable);  // n <= R
-  for (int t = 1; t <= tiles_max; ++t)
-    p.sp_table[t - 1] = static_cast<uint8_t>(plan_splits(t, p.sp_max, p.num_sms, c.P));
-  if (p.sp_max > 1) {
+  int units_max = ((R * g + 127) / 128) * c.n_kv;  // every tile, unsplit
+  for (int t = 1; t <= tiles_max; ++t) {
+    const int lim = std::min(16, cap / t);
+    const int sp = lim >= 2 ? plan_splits(t, lim, p.num_sms, c.P, combine_cost()) : 1;
+    p.sp_table[t - 1] = static_cast<uint8_t>(sp);
+    units_max = std::max(units_max, t * sp);
+  }
+  if (cap > 0) {
     if (!c.part || c.part_bytes < attn_partial_bytes(R, g, c.n_kv, HD)) return SPECFOLD_ECAPACITY;
     p.part_o = static_cast<float*>(c.part);
-    p.part_ml = p.part_o + static_cast<size_t>(tiles_x) * c.n_kv * p.sp_max * 128 * HD;
+    p.part_ml = p.part_o + static_cast<size_t>(cap) * 128 * HD;
   }
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-      return SPECFOLD_ECUDA;
-    attr_done[dev] = 1;
-  }
-  const dim3 grid(tiles_x, c.n_kv, p.sp_max);
+  if (smem_limit_once(attn_kernel<HD>, C::SMEM_BYTES)) return SPECFOLD_ECUDA;
+  // persistent: at most one CTA per SM, each looping over the live units
+  const dim3 grid(std::min(units_max, p.num_sms));
   launch_k(attn_kernel<HD>, dim3(grid), dim3(kAttnThreads), C::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
-  if (p.sp_max > 1) {
+  if (cap > 0) {
     const long long work = static_cast<long long>(R) * g * c.n_kv * (HD / 8);
     const int cg = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
-    launch_k(attn_combine_kernel<HD>, dim3(std::max(cg, 1)), dim3(256), 0, st, p, tiles_x);
+    launch_k(attn_combine_kernel<HD>, dim3(std::max(cg, 1)), dim3(256), 0, st, p);
     count_launch();
     return check_launch();
   }
@@ -668,19 +754,17 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
 
 }  // namespace
 
-// Largest split count for this shape: enough (query tile, head, split) CTAs
-// to cover about four waves of SMs when every row is packed, at most 16.
-int attn_sp_max(int R, int g, int n_kv) {
+// Partial slots of the split-KV path: enough for four waves of units on the
+// SMs the split sizing plans for, and at most 16 splits of every (query tile,
+// KV head) of R rows.  0 when no split is possible.
+int attn_slot_cap(int R, int g, int n_kv) {
   const int tiles = ((R * g + 127) / 128) * n_kv;
-  const int want = (4 * kSmBudget + tiles - 1) / tiles;
-  return std::max(1, std::min(16, want));
+  const int cap = std::min(16 * tiles, 4 * kSmBudget);
+  return cap >= 2 ? cap : 0;
 }
 
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd) {
-  const int sp = attn_sp_max(R, g, n_kv);
-  if (sp <= 1) return 0;
-  const size_t slots = static_cast<size_t>((R * g + 127) / 128) * n_kv * sp;
-  return slots * 128 * (hd + 2) * sizeof(float);
+  return static_cast<size_t>(attn_slot_cap(R, g, n_kv)) * 128 * (hd + 2) * sizeof(float);
 }
 
 int launch_attention(const AttnCall& c, cudaStream_t st) {

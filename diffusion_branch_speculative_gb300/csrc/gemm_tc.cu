@@ -76,7 +76,7 @@ struct GemmParams {
   float* partial;
   uint32_t* status;
   int cs;               // cluster size of a clustered launch (0: plain launch)
-  const int32_t* dep_off;   // RESID_SCATTER: fold-fill of dependents in the finish kernel
+  const int32_t* dep_rng;   // RESID_SCATTER: fold-fill of dependents in the finish kernel
   const int32_t* dep_rows;
   const __nv_bfloat16* hin;
   // work decomposition per m-tile count Mt (row Mt - 1): S, full, r, St, U
@@ -729,15 +729,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 // epilogue.  One thread per (packed row, 8 output columns); all partial loads
 // of a thread are issued before the adds.  Returns at once when the GEMM ran
 // unsplit (S recomputed from the same n and grid).
-// With fold-fill (RESID_SCATTER and p.dep_off set) the kernel also writes,
-// for every folded row r that resolves to packed row k, Y[r] = Y[s] +
+// With fold-fill (RESID_SCATTER and p.dep_rng set) the kernel also writes,
+// for every folded row r whose source is packed row k, Y[r] = Y[s] +
 // (hin[r] - hin[s]) with s = row_idx[k] and Y[s] as stored in bf16; when the
-// GEMM ran unsplit it reads Y[s] back and does only the fill.
+// GEMM ran unsplit it reads Y[s] back and does only the fill.  The folded
+// rows of source s are dep_rows[dep_rng[2s] .. dep_rng[2s + 1]).
+// Slice j of J of the dependents is filled (the dependents of a source are
+// split evenly between J threads when the folded rows far outnumber the
+// packed ones, so a few sources with many dependents do not serialise).
 template <int BN, int EPI>
-SF_DEV void fill_dependents(const GemmParams& p, int k, int c, const float (&yb)[8]) {
-  const int d0 = p.dep_off[k], d1 = p.dep_off[k + 1];
-  if (d1 <= d0) return;
+SF_DEV void fill_dependents(const GemmParams& p, int k, int c, const float (&yb)[8], int j = 0, int J = 1) {
   const int s = p.row_idx[k];
+  const int2 rg = reinterpret_cast<const int2*>(p.dep_rng)[s];
+  const int len = rg.y - rg.x;
+  const int d0 = rg.x + (len * j) / J, d1 = rg.x + (len * (j + 1)) / J;
+  if (d1 <= d0) return;
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
   float hs[8];
 #pragma unroll
@@ -771,27 +777,35 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   bool fill = false;
-  if constexpr (EPI == EPI_RESID_SCATTER) fill = p.dep_off != nullptr;
+  if constexpr (EPI == EPI_RESID_SCATTER) fill = p.dep_rng != nullptr;
   if (sc.S <= 1 && sc.St <= 1 && !fill) return;  // nothing split, nothing to fill
   constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;   // output columns per tile
   const int groups = (p.Nt * TW) / 8;
-  const long long total = static_cast<long long>(n) * groups;
+  // fold-fill slices: about eight dependents per thread when the folded rows
+  // (Mcap - n at most) far outnumber the packed ones
+  int J = 1;
+  if (fill && n > 0) J = min(16, max(1, (p.Mcap - n + 8 * n - 1) / (8 * n)));
+  const long long nk = static_cast<long long>(n) * groups;
+  const long long total = nk * J;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int k = static_cast<int>(idx / groups);
-    const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
+    const int jsl = static_cast<int>(idx / nk);
+    const long long kc = idx - static_cast<long long>(jsl) * nk;
+    const int k = static_cast<int>(kc / groups);
+    const int c = static_cast<int>(kc - static_cast<long long>(k) * groups) * 8;
     const int nt = c / TW, tc = c - nt * TW;
     const int m = k / kBM, row = k - m * kBM;
     int S = 1, slot0 = 0;
     if (!tile_split(sc, m, nt, p.Nt, S, slot0)) {
       if constexpr (EPI == EPI_RESID_SCATTER) {
         // unsplit tile: the GEMM epilogue wrote Y[s]; fill the dependents only
-        if (fill && p.dep_off[k + 1] > p.dep_off[k]) {
+        const int2 rg = fill ? reinterpret_cast<const int2*>(p.dep_rng)[p.row_idx[k]] : make_int2(0, 0);
+        if (rg.y > rg.x) {
           float yb[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) yb[e] = 0.f;
           add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, yb);
-          fill_dependents<BN, EPI>(p, k, c, yb);
+          fill_dependents<BN, EPI>(p, k, c, yb, jsl, J);
         }
       }
       continue;
@@ -829,9 +843,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
       }
     }
     // four consecutive threads consumed one 128-byte line of every split
-    // (each lane of the quad drops every fourth split's line)
+    // (each lane of the quad drops every fourth split's line); not when
+    // several fold-fill slices read the same partials
     __syncwarp(__activemask());
-    {
+    if (J == 1) {
       const float* line = base - (threadIdx.x & 3) * 8;
       for (int s = threadIdx.x & 3; s < S; s += 4) {
         l2_discard_line(line + static_cast<size_t>(s) * kBM * BN);
@@ -843,11 +858,11 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
         // the residual add and the bf16 rounding of the stored row, then the fill
         const int cc = nt * TW + tc;
         add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + cc, v);
-        store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + cc, v);
+        if (jsl == 0) store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + cc, v);
         float yb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) yb[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-        fill_dependents<BN, EPI>(p, k, cc, yb);
+        fill_dependents<BN, EPI>(p, k, cc, yb, jsl, J);
         continue;
       }
     }
@@ -1026,25 +1041,17 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
   p.partial = c.partial;
   p.status = c.status;
   if constexpr (EPI == EPI_RESID_SCATTER) {
-    if (c.dep_off) {
+    if (c.dep_rng) {
       if (!c.dep_rows || !c.hin || c.ldy != c.N) return SPECFOLD_EINVAL;
-      p.dep_off = c.dep_off;
+      p.dep_rng = c.dep_rng;
       p.dep_rows = c.dep_rows;
       p.hin = static_cast<const __nv_bfloat16*>(c.hin);
     }
   }
 
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cf::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_kernel<BN, EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cf::SMEM_BYTES) != cudaSuccess)
-      return SPECFOLD_ECUDA;
-    attr_done[dev] = 1;
-  }
+  if (smem_limit_once(gemm_kernel<BN, EPI, false>, Cf::SMEM_BYTES) ||
+      smem_limit_once(gemm_kernel<BN, EPI, true>, Cf::SMEM_BYTES))
+    return SPECFOLD_ECUDA;
   // schedule table for the plain grid (a clustered launch computes its own
   // split and sums it inside the GEMM)
   const bool any_split = fill_sched(p, c.Mcap, min(num_sms(), kMaxGrid));
@@ -1083,7 +1090,7 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
   }
   // the finish kernel sums split tiles; the fold-fill of the down projection
   // runs in it in any case
-  if (any_split || p.dep_off) {
+  if (any_split || p.dep_rng) {
     constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;
     const long long work = static_cast<long long>(c.Mcap) * (p.Nt * TW / 8);
     const int rgrid = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
@@ -1140,6 +1147,22 @@ Plan plan_gemm(int Mcap, int N, int K, bool swiglu, bool ok128, bool ok256) {
   return best;
 }
 
+// Tile width of the residual projections (output and down).  With few
+// packed rows the K loop is split to fill the SMs, and every split writes an
+// fp32 partial of its whole tile: 128-wide tiles give twice the n-tiles, so
+// half the splits and half the partial traffic.  With many rows the tiles
+// fill the SMs unsplit and 256-wide tiles keep the MMA wider.
+// SPECFOLD_RESID_BN=128 or 256 in the environment fixes the width.
+int resid_tile_width(int Mcap, int N) {
+  static const int forced = [] {
+    const char* e = std::getenv("SPECFOLD_RESID_BN");
+    return e ? std::atoi(e) : 0;
+  }();
+  if (N % 256) return 128;
+  if (forced == 128 || forced == 256) return forced;
+  return Mcap <= 4 * kBM ? 128 : 256;
+}
+
 template <int EPI>
 int run_epi(const GemmCall& c, const Plan& pl, cudaStream_t st, const RowNorm* rn = nullptr) {
   return pl.BN == 256 ? run_gemm<256, EPI>(c, st, rn, pl.cs, pl.grid) : run_gemm<128, EPI>(c, st, rn, pl.cs, pl.grid);
@@ -1175,7 +1198,7 @@ int launch_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn) {
   // separate row-parallel kernel that also runs the fused RMSNorm (output
   // projection) or the fold-fill (down projection), and measured faster than
   // the clustered finish, whose whole clusters fit on fewer SMs.
-  const Plan plain = {c.N % 256 == 0 ? 256 : 128, 0, 0};
+  const Plan plain = {resid_tile_width(c.Mcap, c.N), 0, 0};
   switch (c.epi) {
     case EPI_STORE: return run_epi<EPI_STORE>(c, plan_gemm(c.Mcap, c.N, c.K, false, true, c.N % 256 == 0), st);
     case EPI_RESID_PACKED: return run_epi<EPI_RESID_PACKED>(c, plain, st, rn);
@@ -1244,15 +1267,7 @@ int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* 
   p.g = 1;
   p.partial = static_cast<float*>(scratch);  // written in full before it is read: nothing to clear
   p.status = nullptr;
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN, EPI_STORE, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cf::SMEM_BYTES) != cudaSuccess)
-      return SPECFOLD_ECUDA;
-    attr_done[dev] = 1;
-  }
+  if (smem_limit_once(gemm_kernel<BN, EPI_STORE, false>, Cf::SMEM_BYTES)) return SPECFOLD_ECUDA;
   const bool any_split = fill_sched(p, M, grid);
   launch_k(gemm_kernel<BN, EPI_STORE, false>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();

@@ -3,6 +3,7 @@
 // of folded rows (S10).  All are HBM-bound: one warp per row, 16-byte
 // vectorised coalesced loads, fp32 warp-shuffle reductions.
 #include <algorithm>
+#include <cstring>
 
 #include "sf_device.cuh"
 #include "sf_internal.h"
@@ -316,7 +317,7 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
                    int d, const T* __restrict__ H, const T* __restrict__ g1, float eps,
                    int32_t* __restrict__ src, int32_t* __restrict__ packed_idx, int32_t* __restrict__ slot,
                    int32_t* __restrict__ n_dev, T* __restrict__ X1, uint32_t* status,
-                   int32_t* __restrict__ n_hist, int32_t* __restrict__ dep_off, int32_t* __restrict__ dep_rows,
+                   int32_t* __restrict__ n_hist, int32_t* __restrict__ dep_rng, int32_t* __restrict__ dep_rows,
                    T* __restrict__ Xraw) {
   extern __shared__ int smem_i[];
   __shared__ int s_warp[kPackThreads / 32];
@@ -413,10 +414,11 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
   }
   const int k_norm = blockIdx.x * kRowWarps + w;
   const int r_norm = k_norm < n ? s_inv[k_norm] : -1;
-  if (blockIdx.x == 0 && dep_off) {
+  if (blockIdx.x == 0 && dep_rng) {
     // Block 0 groups the folded rows by the packed slot of their source
-    // (counting sort in shared memory): dep_rows[dep_off[k] .. dep_off[k+1])
-    // are the rows that take packed row k's output plus their own difference.
+    // (counting sort in shared memory): for a recomputed row s,
+    // dep_rows[dep_rng[2s] .. dep_rng[2s+1]) are the rows that take its output
+    // plus their own difference.
     int* cnt = s_inv;  // [n + 1]
     __syncthreads();   // every read of s_inv above is done
     for (int k = tid; k <= n; k += kPackThreads) cnt[k] = 0;
@@ -454,8 +456,12 @@ select_pack_kernel(const uint8_t* __restrict__ fold, const int32_t* __restrict__
     for (int k = c0; k < c1; ++k) {
       const int c = cnt[k];
       cnt[k] = run;
-      dep_off[k] = run;
       run += c;
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += kPackThreads) {
+      const int k = s_slot[r];
+      if (k >= 0) reinterpret_cast<int2*>(dep_rng)[r] = make_int2(cnt[k], cnt[k + 1]);
     }
     __syncthreads();
     for (int r = tid; r < R; r += kPackThreads) {
@@ -695,6 +701,335 @@ rope_kernel(T* __restrict__ Q, T* __restrict__ Kb, const int32_t* __restrict__ p
   }
 }
 
+// ------------------------------------------------ S1 + S2 + S3 fused --
+// One launch for the gate, the resolve and the pack of the parent-gate
+// layer, on a grid of at most one CTA per SM (all resident at once).
+//
+// Phase 1 (gate): CTA j owns the contiguous rows [j*chunk, (j+1)*chunk), one
+// warp per row.  Each row streams its child and parent rows once, decides
+// fold (squared comparison, as the standalone gate) and, for RMSNorm1, sums
+// the squares of the child row; with HOLD (at most one row per warp) the row
+// stays in registers until its packed slot is known.  The CTA publishes its
+// count of recomputed rows.
+// Grid barrier (bounded, see grid_barrier).
+// Phase 2 (pack): every CTA stages all R decisions in shared memory; its
+// rows' packed slots follow from the counts of the CTAs before it and a
+// local scan (branch-major, position-ascending order); it writes src (fold
+// chains walked in shared memory), slot, packed_idx and X1 of its recomputed
+// rows.  A fold chain never leaves its block position, so the folded rows are
+// grouped by source per position: CTA j groups positions j, j + G, ...; the
+// folded rows of position i occupy dep_rows[i*B .. (i+1)*B).
+constexpr int kGPWarps = 16;
+constexpr int kGPThreads = kGPWarps * 32;
+constexpr int kGPMaxCtas = 256;
+constexpr int kGPPass = 8;  // vectors per lane per pass without HOLD
+
+struct GatePackArgs {
+  const void* H;
+  const int32_t* parent;
+  int B, L, d;
+  float tau;
+  const void* g1;
+  float eps;
+  uint8_t* fold;
+  float* rel;
+  uint8_t* fold_hist;
+  int32_t* src;
+  int32_t* packed_idx;
+  int32_t* slot;
+  int32_t* n_dev;
+  int32_t* n_hist;
+  void* X1;
+  int32_t* dep_rng;
+  int32_t* dep_rows;
+  uint32_t* bar;
+  int32_t* cta_cnt;
+  uint32_t* status;
+  int chunk;
+};
+
+// Exclusive prefix sums of v[0 .. N) into out (may alias v); returns the
+// total.  Called by every thread of the block; s_warp holds 32 ints.
+SF_DEV int block_scan_excl(const int* v, int* out, int N, int* s_warp) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
+  const int per = (N + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(N, tid * per), b1 = min(N, b0 + per);
+  int loc = 0;
+  for (int k = b0; k < b1; ++k) loc += v[k];
+  int inc = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) s_warp[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += t;
+    }
+    if (lane < nw) s_warp[lane] = x;
+  }
+  __syncthreads();
+  int run = (w > 0 ? s_warp[w - 1] : 0) + inc - loc;
+  const int total = s_warp[nw - 1];
+  for (int k = b0; k < b1; ++k) {
+    const int c = v[k];
+    out[k] = run;
+    run += c;
+  }
+  __syncthreads();
+  return total;
+}
+
+// Branch at the end of the fold chain that starts at (b, i), on staged
+// decisions: a folded row always has a valid parent.
+SF_DEV int chain_end_smem(const uint8_t* f, const int* par, int b, int i, int L, int B) {
+  int s = b;
+  for (int hop = 0; hop < B && s > 0 && f[s * L + i]; ++hop) s = par[s];
+  return s;
+}
+
+template <typename T>
+SF_DEV void accum_gate(const uint4& c, const uint4& q, float& num, float& den) {
+  using V = VecT<T>;
+  float fc[V::N], fp[V::N];
+  V::unpack(c, fc);
+  V::unpack(q, fp);
+#pragma unroll
+  for (int e = 0; e < V::N; ++e) {
+    const float df = fc[e] - fp[e];
+    num = fmaf(df, df, num);
+    den = fmaf(fp[e], fp[e], den);
+  }
+}
+
+template <typename T>
+SF_DEV void accum_sq(const uint4& c, float& ss) {
+  using V = VecT<T>;
+  float f[V::N];
+  V::unpack(c, f);
+#pragma unroll
+  for (int e = 0; e < V::N; ++e) ss = fmaf(f[e], f[e], ss);
+}
+
+template <typename T>
+SF_DEV uint4 scale_vec(const uint4& x, const uint4& g, float inv) {
+  using V = VecT<T>;
+  float f[V::N], gf[V::N];
+  V::unpack(x, f);
+  V::unpack(g, gf);
+#pragma unroll
+  for (int e = 0; e < V::N; ++e) f[e] = f[e] * inv * gf[e];
+  return V::pack(f);
+}
+
+// Gate decision of one row from its sums (the standalone gate's rule).
+SF_DEV void gate_write(const GatePackArgs& a, int row, bool valid, float num, float den) {
+  const bool f = valid && ((num < a.tau * a.tau * den) || (num == 0.f && a.tau > 0.f));
+  a.fold[row] = f ? 1 : 0;
+  if (a.fold_hist) a.fold_hist[row] = f ? 1 : 0;
+  if (a.rel)
+    a.rel[row] = !valid ? -1.f : (den > 0.f ? sqrtf(num / den) : (num == 0.f ? 0.f : __int_as_float(0x7f800000)));
+}
+
+template <typename T, int MAXV, bool HOLD>
+__global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_constant__ GatePackArgs a) {
+  using V = VecT<T>;
+  extern __shared__ __align__(16) uint8_t gp_smem[];
+  __shared__ int s_warp[32];
+  __shared__ int s_nb, s_n, s_bad;
+  __shared__ volatile int s_flag;
+  const int B = a.B, L = a.L, d = a.d, R = B * L;
+  const int nv = d / V::N;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  // shared memory: gains [nv] uint4 | parent [B] | decisions [R, 16-rounded] | three int arrays
+  uint4* s_g = reinterpret_cast<uint4*>(gp_smem);
+  int* s_par = reinterpret_cast<int*>(s_g + nv);
+  uint8_t* s_fold = reinterpret_cast<uint8_t*>(s_par + ((B + 3) & ~3));
+  int* s_c1 = reinterpret_cast<int*>(s_fold + ((R + 15) & ~15));  // [max(B, chunk)]
+  int* s_c2 = s_c1 + max(B, a.chunk);                              // [B]
+  int* s_c3 = s_c2 + B;                                            // [B]
+  // gains: weights, independent of earlier kernels
+  for (int v = tid; v < nv; v += kGPThreads) s_g[v] = __ldg(reinterpret_cast<const uint4*>(a.g1) + v);
+  pdl_wait();
+  if (tid == 0) s_bad = 0;
+  for (int b = tid; b < B; b += kGPThreads) {
+    const int p = a.parent[b];
+    s_par[b] = p;
+    if ((b == 0 && p != -1) || (b > 0 && (p < 0 || p >= b))) s_bad = 1;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------- phase 1: gate --
+  const int c0 = blockIdx.x * a.chunk, c1 = min(R, c0 + a.chunk);
+  const T* H = static_cast<const T*>(a.H);
+  uint4 cv[HOLD ? MAXV : 1];
+  float ss_hold = 0.f;
+  int act_here = 0;  // recomputed rows of this warp (lane 0)
+  for (int r = c0 + w; r < c1; r += kGPWarps) {
+    const int b = r / L, i = r - b * L;
+    const int p = b > 0 ? s_par[b] : -1;
+    const bool valid = b > 0 && p >= 0 && p < b;
+    const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(r) * d);
+    const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(valid ? p : 0) * L + i) * d);
+    float num = 0.f, den = 0.f, ss = 0.f;
+    if constexpr (HOLD) {
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u)
+        if (lane + 32 * u < nv) cv[u] = __ldg(c + lane + 32 * u);
+      if (valid) {
+#pragma unroll
+        for (int u0 = 0; u0 < MAXV; u0 += 8) {
+          uint4 pv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u0 + u < MAXV && lane + 32 * (u0 + u) < nv) pv[u] = __ldg(q + lane + 32 * (u0 + u));
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (u0 + u < MAXV && lane + 32 * (u0 + u) < nv) accum_gate<T>(cv[u0 + u], pv[u], num, den);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u)
+        if (lane + 32 * u < nv) accum_sq<T>(cv[u], ss);
+    } else {
+      for (int v0 = 0; v0 < nv; v0 += 32 * kGPPass) {
+        uint4 xv[kGPPass], pv[kGPPass];
+#pragma unroll
+        for (int u = 0; u < kGPPass; ++u) {
+          const int v = v0 + lane + 32 * u;
+          if (v < nv) {
+            xv[u] = __ldg(c + v);
+            if (valid) pv[u] = __ldg(q + v);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kGPPass; ++u) {
+          const int v = v0 + lane + 32 * u;
+          if (v < nv && valid) accum_gate<T>(xv[u], pv[u], num, den);
+        }
+      }
+    }
+    num = warp_sum(num);
+    den = warp_sum(den);
+    const bool f = valid && ((num < a.tau * a.tau * den) || (num == 0.f && a.tau > 0.f));
+    if (lane == 0) {
+      gate_write(a, r, valid, num, den);
+      act_here += f ? 0 : 1;
+    }
+    if constexpr (HOLD) ss_hold = warp_sum(ss);
+  }
+  // this CTA's count of recomputed rows
+  if (lane == 0) s_warp[w] = act_here;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+    for (int j = 0; j < kGPWarps; ++j) t += s_warp[j];
+    a.cta_cnt[blockIdx.x] = t;
+    if (blockIdx.x == 0 && s_bad && a.status) atomicOr(a.status, SPECFOLD_DEV_BAD_PARENT);
+  }
+  if (!grid_barrier(a.bar, a.status, &s_flag)) return;
+  pdl_trigger();
+
+  // ---------------------------------------------------- phase 2: pack --
+  {
+    const uint4* fg = reinterpret_cast<const uint4*>(a.fold);
+    uint4* fs = reinterpret_cast<uint4*>(s_fold);
+    for (int j = tid; j < (R + 15) / 16; j += kGPThreads) fs[j] = __ldcg(fg + j);
+  }
+  if (w == 0) {
+    int tot = 0, before = 0;
+    for (int j = lane; j < static_cast<int>(gridDim.x); j += 32) {
+      const int v = __ldcg(a.cta_cnt + j);
+      tot += v;
+      before += j < static_cast<int>(blockIdx.x) ? v : 0;
+    }
+    tot = __reduce_add_sync(0xffffffffu, tot);
+    before = __reduce_add_sync(0xffffffffu, before);
+    if (lane == 0) {
+      s_n = tot;
+      s_nb = before;
+    }
+  }
+  __syncthreads();
+  const int n = s_n, nb = s_nb;
+  const int nch = c1 - c0;
+  for (int t = tid; t < nch; t += kGPThreads) s_c1[t] = s_fold[c0 + t] ? 0 : 1;
+  __syncthreads();
+  block_scan_excl(s_c1, s_c1, max(nch, 0), s_warp);  // local rank of each recomputed row
+  for (int t = tid; t < nch; t += kGPThreads) {
+    const int r = c0 + t;
+    const int b = r / L, i = r - b * L;
+    const bool act = !s_fold[r];
+    const int k = nb + s_c1[t];
+    a.slot[r] = act ? k : -1;
+    if (act) a.packed_idx[k] = r;
+    a.src[r] = act ? r : chain_end_smem(s_fold, s_par, b, i, L, B) * L + i;
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    a.n_dev[0] = n;
+    if (a.n_hist) a.n_hist[0] = n;
+  }
+  // RMSNorm1 of this CTA's recomputed rows: X1[k] = H[r] * g1 / rms(H[r])
+  T* X1 = static_cast<T*>(a.X1);
+  if constexpr (HOLD) {
+    const int r = c0 + w;
+    if (r < c1 && !s_fold[r]) {
+      const float inv = rsqrtf(ss_hold / static_cast<float>(d) + a.eps);
+      uint4* y = reinterpret_cast<uint4*>(X1 + static_cast<size_t>(nb + s_c1[w]) * d);
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u) {
+        const int v = lane + 32 * u;
+        if (v < nv) y[v] = scale_vec<T>(cv[u], s_g[v], inv);
+      }
+    }
+  } else {
+    for (int t = w; t < nch; t += kGPWarps) {
+      const int r = c0 + t;
+      if (s_fold[r]) continue;
+      const uint4* x = reinterpret_cast<const uint4*>(H + static_cast<size_t>(r) * d);
+      float ss = 0.f;
+      for (int v0 = 0; v0 < nv; v0 += 32 * kGPPass) {
+        uint4 xv[kGPPass];
+#pragma unroll
+        for (int u = 0; u < kGPPass; ++u)
+          if (v0 + lane + 32 * u < nv) xv[u] = __ldg(x + v0 + lane + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kGPPass; ++u)
+          if (v0 + lane + 32 * u < nv) accum_sq<T>(xv[u], ss);
+      }
+      const float inv = rsqrtf(warp_sum(ss) / static_cast<float>(d) + a.eps);
+      uint4* y = reinterpret_cast<uint4*>(X1 + static_cast<size_t>(nb + s_c1[t]) * d);
+      for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(__ldg(x + v), s_g[v], inv);
+    }
+  }
+  // folded rows grouped by source, one block position at a time
+  for (int i = blockIdx.x; i < L; i += gridDim.x) {
+    __syncthreads();  // the arrays are free again
+    for (int b = tid; b < B; b += kGPThreads) s_c2[b] = 0;
+    __syncthreads();
+    for (int b = tid; b < B; b += kGPThreads) {
+      const int sb = s_fold[b * L + i] ? chain_end_smem(s_fold, s_par, b, i, L, B) : b;
+      s_c1[b] = sb;
+      if (sb != b) atomicAdd(&s_c2[sb], 1);
+    }
+    __syncthreads();
+    block_scan_excl(s_c2, s_c3, B, s_warp);  // s_c3: first slot of each source's group
+    for (int b = tid; b < B; b += kGPThreads)
+      if (s_c1[b] == b)
+        reinterpret_cast<int2*>(a.dep_rng)[b * L + i] = make_int2(i * B + s_c3[b], i * B + s_c3[b] + s_c2[b]);
+    __syncthreads();
+    for (int b = tid; b < B; b += kGPThreads) {
+      const int sb = s_c1[b];
+      if (sb != b) a.dep_rows[i * B + atomicAdd(&s_c3[sb], 1)] = b * L + i;
+    }
+  }
+}
+
 // ------------------------------------------------------ bounded-wait probe --
 __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -754,20 +1089,76 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
   return check_launch();
 }
 
+size_t gate_pack_sync_bytes() { return 128 + sizeof(int32_t) * kGPMaxCtas; }
+
+template <typename T, int MAXV, bool HOLD>
+static int gate_pack_go(const GatePackArgs& a, int grid, size_t smem, cudaStream_t st) {
+  if (smem > 48 * 1024 && smem_limit_once(gate_pack_kernel<T, MAXV, HOLD>, static_cast<int>(smem)))
+    return SPECFOLD_ECUDA;
+  launch_k(gate_pack_kernel<T, MAXV, HOLD>, dim3(grid), dim3(kGPThreads), smem, st, a);
+  count_launch();
+  return check_launch();
+}
+
+int launch_gate_pack(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                     const void* g1, float eps, uint8_t* fold, float* rel, int32_t* src, int32_t* packed_idx,
+                     int32_t* slot, int32_t* n_dev, void* X1, int32_t* dep_rng, int32_t* dep_rows, void* sync,
+                     uint32_t* status, cudaStream_t st, uint8_t* fold_hist, int32_t* n_hist) {
+  const int R = B * L;
+  const int es = dtype == SPECFOLD_BF16 ? 2 : 4;
+  const int nv = d * es / 16;
+  const int per_lane = (nv + 31) / 32;
+  const int sms = std::max(1, std::min(num_sms(), kGPMaxCtas));
+  const int chunk = (R + sms - 1) / sms;
+  const int grid = (R + chunk - 1) / chunk;
+  const size_t smem = static_cast<size_t>(nv) * 16 + 4 * static_cast<size_t>((B + 3) & ~3) + ((R + 15) & ~15) +
+                      4 * static_cast<size_t>(std::max(B, chunk)) + 8 * static_cast<size_t>(B);
+  if (per_lane > 32 || smem > 200 * 1024) return SPECFOLD_EUNSUPPORTED;
+  GatePackArgs a;
+  memset(&a, 0, sizeof(a));
+  a.H = H;
+  a.parent = parent;
+  a.B = B;
+  a.L = L;
+  a.d = d;
+  a.tau = tau;
+  a.g1 = g1;
+  a.eps = eps;
+  a.fold = fold;
+  a.rel = rel;
+  a.fold_hist = fold_hist;
+  a.src = src;
+  a.packed_idx = packed_idx;
+  a.slot = slot;
+  a.n_dev = n_dev;
+  a.n_hist = n_hist;
+  a.X1 = X1;
+  a.dep_rng = dep_rng;
+  a.dep_rows = dep_rows;
+  a.bar = static_cast<uint32_t*>(sync);
+  a.cta_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(sync) + 128);
+  a.status = status;
+  a.chunk = chunk;
+  const bool hold = chunk <= kGPWarps && per_lane <= 16;
+#define SF_GP(TT)                                                                   \
+  if (hold && per_lane <= 4) return gate_pack_go<TT, 4, true>(a, grid, smem, st);   \
+  if (hold && per_lane <= 8) return gate_pack_go<TT, 8, true>(a, grid, smem, st);   \
+  if (hold) return gate_pack_go<TT, 16, true>(a, grid, smem, st);                   \
+  return gate_pack_go<TT, 1, false>(a, grid, smem, st)
+  if (dtype == SPECFOLD_BF16) {
+    SF_GP(__nv_bfloat16);
+  }
+  SF_GP(float);
+#undef SF_GP
+}
+
 int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
                        uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist) {
   const size_t smem = static_cast<size_t>(2) * B * sizeof(int);
   const int per_lane = (d / (dtype == SPECFOLD_BF16 ? 8 : 4) + 31) / 32;
-  static int attr_done[64][4] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  auto prep = [&](auto kern, int slot) -> bool {
-    if (smem <= 48 * 1024 || dev < 0 || dev >= 64 || attr_done[dev][slot]) return true;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             2 * SPECFOLD_MAX_ROWS * static_cast<int>(sizeof(int))) != cudaSuccess)
-      return false;
-    attr_done[dev][slot] = 1;
-    return true;
+  auto prep = [&](auto kern, int) -> bool {
+    if (smem <= 48 * 1024) return true;
+    return smem_limit_once(kern, 2 * SPECFOLD_MAX_ROWS * static_cast<int>(sizeof(int))) == SPECFOLD_OK;
   };
   const dim3 grid(L), block(kRowWarps * 32);
   if (dtype == SPECFOLD_BF16) {
@@ -798,23 +1189,17 @@ int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, i
 template <typename T, int MAXV, bool GREG>
 static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                               const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                              int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_rng,
                               int32_t* dep_rows, void* Xraw) {
   const int R = B * L;
   const size_t smem = (static_cast<size_t>(3) * R + 1) * sizeof(int);
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_done[dev]) {
-    if (cudaFuncSetAttribute(select_pack_kernel<T, MAXV, GREG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (3 * SPECFOLD_MAX_ROWS + 1) * static_cast<int>(sizeof(int))) != cudaSuccess)
-      return SPECFOLD_ECUDA;
-    attr_done[dev] = 1;
-  }
+  if (smem > 48 * 1024 &&
+      smem_limit_once(select_pack_kernel<T, MAXV, GREG>, (3 * SPECFOLD_MAX_ROWS + 1) * static_cast<int>(sizeof(int))))
+    return SPECFOLD_ECUDA;
   const dim3 grid((R + kRowWarps - 1) / kRowWarps), block(kPackThreads);
   launch_k(select_pack_kernel<T, MAXV, GREG>, dim3(grid), dim3(block), smem, st, fold, parent, B, L, d, static_cast<const T*>(H),
                                                           static_cast<const T*>(g1), eps, src, packed_idx, slot,
-                                                          n_dev, static_cast<T*>(X1), status, n_hist, dep_off, dep_rows,
+                                                          n_dev, static_cast<T*>(X1), status, n_hist, dep_rng, dep_rows,
                                                           static_cast<T*>(Xraw));
   count_launch();
   return check_launch();
@@ -823,16 +1208,16 @@ static int select_pack_launch(const uint8_t* fold, const int32_t* parent, int B,
 template <typename T>
 static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                                 const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot,
-                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                                int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_rng,
                                 int32_t* dep_rows, void* Xraw) {
   const int per_lane = X1 ? (d / VecT<T>::N + 31) / 32 : 1;
   // gains in registers when the grid fits one wave at one block per SM
   const bool greg = (B * L + kRowWarps - 1) / kRowWarps <= num_sms();
 #define SF_SP(MV)                                                                                                 \
   return greg ? select_pack_launch<T, MV, true>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev,  \
-                                                X1, status, st, n_hist, dep_off, dep_rows, Xraw)                  \
+                                                X1, status, st, n_hist, dep_rng, dep_rows, Xraw)                  \
               : select_pack_launch<T, MV, false>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, \
-                                                 X1, status, st, n_hist, dep_off, dep_rows, Xraw)
+                                                 X1, status, st, n_hist, dep_rng, dep_rows, Xraw)
   if (per_lane <= 4) SF_SP(4);
   if (per_lane <= 8) SF_SP(8);
   if (per_lane <= 16) SF_SP(16);
@@ -843,14 +1228,14 @@ static int select_pack_dispatch(const uint8_t* fold, const int32_t* parent, int 
 
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d, const void* H,
                        const void* g1, float eps, int32_t* src, int32_t* packed_idx, int32_t* slot, int32_t* n_dev,
-                       void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_off,
+                       void* X1, uint32_t* status, cudaStream_t st, int32_t* n_hist, int32_t* dep_rng,
                        int32_t* dep_rows, void* Xraw) {
   if (Xraw && !X1) return SPECFOLD_EINVAL;
   if (dtype == SPECFOLD_BF16)
     return select_pack_dispatch<__nv_bfloat16>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1,
-                                               status, st, n_hist, dep_off, dep_rows, Xraw);
+                                               status, st, n_hist, dep_rng, dep_rows, Xraw);
   return select_pack_dispatch<float>(fold, parent, B, L, d, H, g1, eps, src, packed_idx, slot, n_dev, X1, status,
-                                     st, n_hist, dep_off, dep_rows, Xraw);
+                                     st, n_hist, dep_rng, dep_rows, Xraw);
 }
 
 template <typename T>

@@ -89,6 +89,43 @@ SF_DEV void l2_discard_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
+// Grid-wide barrier of a launch whose CTAs are all resident at once (grid no
+// larger than one CTA per SM).  *bar starts at 0 (or any multiple of 2^31):
+// the CTAs add 2^31 in total, so the top bit flips exactly when the last one
+// arrives and the low bits are back where they started, ready for the next
+// barrier or the next launch.  Writes before the barrier are visible to every
+// CTA after it.  The wait is bounded: when it runs out (a CTA that never
+// became resident) it sets SPECFOLD_DEV_TIMEOUT and returns false in every
+// thread of this CTA; the word is then left mid-count, and the workspace that
+// holds it must be zeroed again before its next use.
+SF_DEV bool grid_barrier(uint32_t* bar, uint32_t* status, volatile int* s_flag,
+                         uint64_t limit_ns = kWaitLimitNs) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t nb = gridDim.x * gridDim.y * gridDim.z;
+    const bool first = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+    __threadfence();
+    const uint32_t old = atomicAdd(bar, first ? 0x80000000u - (nb - 1u) : 1u);
+    int ok = 1;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      uint32_t cur;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(bar) : "memory");
+      if ((cur ^ old) & 0x80000000u) break;
+      if (globaltimer() - t0 > limit_ns) {
+        ok = 0;
+        if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT);
+        break;
+      }
+      __nanosleep(32);
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
 SF_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -15,6 +15,13 @@ namespace sf {
 void count_launch(int n = 1);
 int num_sms();                        // SMs of the current device (cached per device)
 int check_launch();                   // SPECFOLD_OK or SPECFOLD_ECUDA after a launch
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (device, kernel); safe to call from several host threads.
+int smem_limit_once(const void* kernel, int bytes);
+template <typename... KArgs>
+inline int smem_limit_once(void (*kernel)(KArgs...), int bytes) {
+  return smem_limit_once(reinterpret_cast<const void*>(kernel), bytes);
+}
 
 // ---- row-wise kernels (rowwise.cu) ----
 // gate: fold/rel per row; dtype bf16 or f32.  fold_hist (optional) receives
@@ -27,14 +34,25 @@ int launch_gate_source(int dtype, const void* H, const int32_t* parent, int B, i
                        uint8_t* fold, float* rel, cudaStream_t st, uint8_t* fold_hist = nullptr);
 // resolve + pack scan (+ RMSNorm1 gather of the packed rows when X1 is
 // given); parent may be null (pack alone); any output may be null.  n_hist
-// (optional) receives a second copy of the packed-row count; dep_off [R+1] /
-// dep_rows [R] (optional) receive the folded rows grouped by the packed slot
-// of their source.
+// (optional) receives a second copy of the packed-row count; dep_rng [R][2] /
+// dep_rows [R] (optional) receive the folded rows grouped by their source row
+// (for a recomputed row s, dep_rows[dep_rng[2s] .. dep_rng[2s+1])).
 int launch_select_pack(int dtype, const uint8_t* fold, const int32_t* parent, int B, int L, int d,
                        const void* H, const void* g1, float eps, int32_t* src, int32_t* packed_idx,
                        int32_t* slot, int32_t* n_dev, void* X1, uint32_t* status, cudaStream_t st,
-                       int32_t* n_hist = nullptr, int32_t* dep_off = nullptr, int32_t* dep_rows = nullptr,
+                       int32_t* n_hist = nullptr, int32_t* dep_rng = nullptr, int32_t* dep_rows = nullptr,
                        void* Xraw = nullptr);  // Xraw [R, d]: the packed rows themselves (needs X1)
+// S1 + S2 + S3 fused (parent gate, one launch): gate decisions and r, the
+// sources, the packed list, n, RMSNorm1 of the packed rows and the folded
+// rows grouped by source, with one bounded grid-wide barrier between the
+// gate and the pack.  sync: gate_pack_sync_bytes() of zero-initialised
+// workspace (it returns to its initial state after every complete call).
+// Returns SPECFOLD_EUNSUPPORTED for rows too wide for it.
+size_t gate_pack_sync_bytes();
+int launch_gate_pack(int dtype, const void* H, const int32_t* parent, int B, int L, int d, float tau,
+                     const void* g1, float eps, uint8_t* fold, float* rel, int32_t* src, int32_t* packed_idx,
+                     int32_t* slot, int32_t* n_dev, void* X1, int32_t* dep_rng, int32_t* dep_rows, void* sync,
+                     uint32_t* status, cudaStream_t st, uint8_t* fold_hist = nullptr, int32_t* n_hist = nullptr);
 // Y[k] = rmsnorm(X[idx ? idx[k] : k]) * g for k < n (n from n_dev, or R when null).
 int launch_rmsnorm_rows(int dtype, const void* X, const int32_t* idx, const int32_t* n_dev,
                         int R, int d, const void* g, float eps, void* Y, cudaStream_t st);
@@ -88,9 +106,9 @@ struct GemmCall {
   size_t partial_len;     // floats, >= gemm_partial_floats()
   uint32_t* status;
   // RESID_SCATTER only, optional: fold-fill of the dependents of each packed
-  // row (dep_rows[dep_off[k] .. dep_off[k+1]) take Y[row_idx[k]] + hin[r] -
-  // hin[row_idx[k]]), run by the split finish kernel
-  const int32_t* dep_off;
+  // row (with s = row_idx[k], the rows dep_rows[dep_rng[2s] .. dep_rng[2s+1])
+  // take Y[s] + hin[r] - hin[s]), run by the split finish kernel
+  const int32_t* dep_rng;
   const int32_t* dep_rows;
   const void* hin;
 };
@@ -122,7 +140,7 @@ struct AttnCall {
   void* part;             // split-KV partials (attn_partial_bytes)
   size_t part_bytes;
 };
-int attn_sp_max(int R, int g, int n_kv);
+int attn_slot_cap(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);
 int launch_attention(const AttnCall& c, cudaStream_t st);
 int launch_attention_f32(const AttnCall& c, cudaStream_t st);  // fp32 Q/K/V/O (simt_f32.cu)

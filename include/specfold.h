@@ -137,8 +137,9 @@ typedef struct {
   size_t src;          /* int32  [R] */
   size_t packed_idx;   /* int32  [R] (first n valid) */
   size_t slot_of_row;  /* int32  [R] (-1 for folded rows) */
-  size_t dep_off;      /* int32  [R+1] folded rows grouped by source slot: */
-  size_t dep_rows;     /* int32  [R]   dep_rows[dep_off[k] .. dep_off[k+1]) resolve to packed row k */
+  size_t dep_rng;      /* int32  [R][2] for a recomputed row s: {beg, end}, the folded rows */
+  size_t dep_rows;     /* int32  [R]    dep_rows[beg .. end) whose source is s */
+  size_t sync;         /* uint32 grid-barrier word, then int32 per-CTA counts (library use) */
   size_t x1;           /* [R, d]        RMSNorm1 of packed rows */
   size_t q;            /* [n_kv, R*g, hd]  queries, head-group major */
   size_t block_k;      /* [R, n_kv, hd]  keys of recomputed rows (row r) */
@@ -148,7 +149,8 @@ typedef struct {
                                         path: the FFN's packed rows of a_all) */
   size_t x2;           /* [R, d]        RMSNorm2 of a */
   size_t g;            /* [R, F]        silu(x2 Wg) * (x2 Wu) */
-  /* the variant sublayer path (dims.attn_rematch or dims.ffn_gate): */
+  /* the variant sublayer path (dims.attn_rematch or dims.ffn_gate); with
+   * both flags 0 these regions are not reserved and their offsets are 0: */
   size_t q_all;        /* [n_kv, R*g, hd]  queries of every row (row r: its source's) */
   size_t all_idx;      /* int32 [R]     0 .. R-1, the all-rows list */
   size_t n_all;        /* int32         R */
@@ -159,7 +161,7 @@ typedef struct {
   size_t packed_ffn;   /* int32 [R]     FFN packed list (first n_ffn valid) */
   size_t slot_ffn;     /* int32 [R] */
   size_t n_ffn;        /* int32 */
-  size_t dep_off_ffn;  /* int32 [R+1] */
+  size_t dep_rng_ffn;  /* int32 [R][2] */
   size_t dep_rows_ffn; /* int32 [R] */
   size_t gemm_scratch; /* fp32 split-K partial sums */
   size_t attn_scratch; /* fp32 split-KV attention partials */
@@ -312,7 +314,11 @@ int specfold_layer_graph_create(const specfold_dims* dims, const specfold_weight
  *             overwritten as the stack proceeds.
  *   fold      uint8 [n_layers, B*L]: each layer's gate decisions.
  *   n_packed  int32 [n_layers]: each layer's packed-row count n (the
- *             recompute fraction of layer l is n_packed[l] / (B*L)). */
+ *             recompute fraction of layer l is n_packed[l] / (B*L)).
+ * With dims.attn_rematch or dims.ffn_gate set, fold and n_packed record the
+ * layer's first gate only: attention and the output projection then run on
+ * every row (attn_rematch), and the FFN sublayer's own decisions and packed
+ * count (ffn_gate) are not recorded. */
 typedef struct specfold_stack_trace {
   void* hidden;
   uint8_t* fold;
@@ -361,22 +367,23 @@ int specfold_linear(int dtype, const void* X, const void* W, int M, int N, int K
 
 /* The plain GEMM of specfold_linear for callers that cannot allocate device
  * memory: a plain C caller that holds only its inputs and outputs and has no
- * allocator, or code running where cudaMalloc is not allowed (inside a CUDA
- * stream capture, or a runtime that forbids allocation after warm-up).  The
- * SpecFold pages have no counterpart; this is a library convenience.
- * Y[M, N] = X[M, K] W^T exactly as specfold_linear computes it, with no
- * workspace argument: the split-K scratch is a 16 MiB static device array
- * inside the library, held by every GPU that loads it until the process
- * exits.  Limits: M <= SPECFOLD_MAX_ROWS (larger M: SPECFOLD_ECAPACITY);
- * K % 64 == 0 and N % 128 == 0 (SPECFOLD_EUNSUPPORTED); at most 128 CTAs, so
- * it can be slower than specfold_linear on large problems.  The first call on
- * a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.
- * Every call shares the one array: calls that overlap on the GPU (other
- * streams, or other host threads) race and must be serialised by the caller.
- * The scratch is fully rewritten before it is read, so a call needs nothing
- * cleared from the previous one.  A bounded wait that runs out cannot be
- * reported (there is no status word). */
+ * device allocator of its own, or a serving runtime that owns all device
+ * memory and forbids allocation after warm-up.  The SpecFold pages have no
+ * counterpart; this is a library convenience.
+ * Y[M, N] = X[M, K] W^T, the same product as specfold_linear but with its own
+ * split-K schedule (a grid capped at 128 CTAs), so the two can differ in the
+ * last bits of a sum.  No workspace argument: the split-K scratch is a
+ * 16 MiB static device array inside the library, held by every GPU that
+ * loads it until the process exits.  Limits: M <= SPECFOLD_MAX_ROWS (larger
+ * M: SPECFOLD_ECAPACITY); K % 64 == 0 and N % 128 == 0
+ * (SPECFOLD_EUNSUPPORTED); at most 128 CTAs, so it can be slower than
+ * specfold_linear on large problems.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call shares the one
+ * array: calls that overlap on the GPU (other streams, or other host threads)
+ * race and must be serialised by the caller.  The scratch is fully rewritten
+ * before it is read, so a call needs nothing cleared from the previous one.
+ * A bounded wait that runs out cannot be reported (there is no status word). */
 int specfold_linear_noalloc(int dtype, const void* X, const void* W, int M, int N, int K, void* Y,
                             void* stream);
 

@@ -28,7 +28,7 @@ noted):
                  matched again against their own branch's keys and values)
                  and one gate per sublayer.
 
-Readings where the pages are silent or garbled (each listed in the design doc):
+Readings where the pages are silent or garbled:
   fold iff r < tau (so tau = 0 folds nothing); the comparison is done squared
   (|d|^2 < tau^2 |p|^2) and an all-zero parent row folds only an identical
   child; the gate compares against the first parent of a multi-parent node;

@@ -20,6 +20,33 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
 
 
+def rel_rows(a, b) -> np.ndarray:
+    """Relative L2 error of every row (axis 0), so that one wrong row (a bad
+    tile, split slot or gathered key) cannot hide in a whole-tensor norm."""
+    a = np.asarray(a, np.float64).reshape(len(a), -1)
+    b = np.asarray(b, np.float64).reshape(len(b), -1)
+    den = np.linalg.norm(b, axis=1)
+    return np.linalg.norm(a - b, axis=1) / np.where(den > 0, den, 1.0)
+
+
+def check_rows_out(Hg, ref, Hin, tol=TOL, floors=3.0):
+    """Per-row bound on a bf16 layer output: the error of row r is at most tol
+    of the layer's own contribution |ref_r - Hin_r| plus `floors` times the
+    bf16 rounding floor of the row (a folded row passes three roundings: its
+    source's A and output, and its own output).  Returns the worst ratio of
+    error to bound."""
+    Hg = np.asarray(Hg, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.linalg.norm(Hg - ref, axis=1)
+    contrib = np.linalg.norm(ref - Hin, axis=1)
+    floor = np.linalg.norm(synth.round_bf16(ref.astype(np.float32)).astype(np.float64) - ref, axis=1)
+    bound = tol * contrib + floors * floor
+    worst = int(np.argmax(err / np.maximum(bound, 1e-30)))
+    assert np.all(err <= bound), (worst, float(err[worst]), float(bound[worst]), float(contrib[worst]),
+                                  float(floor[worst]))
+    return float(np.max(err / np.maximum(bound, 1e-30)))
+
+
 def bf16(x: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device).to(torch.bfloat16)
 
@@ -141,17 +168,18 @@ def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0, gate_r
     assert np.array_equal(gi["packed_idx"], res["packed_idx"])
     assert np.array_equal(gi["slot"], res["slot"])
     m = {"n": gi["n"], "near_tau": n_near}
+    rows_max = {}
     if inter:
         act = res["act_rows"]
         k = gi["slot"][act]
-        m["X1"] = rel_l2(gi["X1"][k], res["X1"])
-        m["Q"] = rel_l2(gi["Q"][k], res["Q"])
-        m["K"] = rel_l2(gi["bK"][act], np.stack([res["K_rows"][r] for r in act]))
-        m["V"] = rel_l2(gi["bV"][act], np.stack([res["V_rows"][r] for r in act]))
-        m["attnO"] = rel_l2(gi["attnO"][k], res["attnO"])
-        m["A"] = rel_l2(gi["A"][k], res["A"])
-        m["X2"] = rel_l2(gi["X2"][k], res["X2"])
-        m["G"] = rel_l2(gi["G"][k], res["G"])
+        pairs = {"X1": (gi["X1"][k], res["X1"]), "Q": (gi["Q"][k], res["Q"]),
+                 "K": (gi["bK"][act], np.stack([res["K_rows"][r] for r in act])),
+                 "V": (gi["bV"][act], np.stack([res["V_rows"][r] for r in act])),
+                 "attnO": (gi["attnO"][k], res["attnO"]), "A": (gi["A"][k], res["A"]),
+                 "X2": (gi["X2"][k], res["X2"]), "G": (gi["G"][k], res["G"])}
+        for key, (g_, o_) in pairs.items():
+            m[key] = rel_l2(g_, o_)
+            rows_max[key] = float(rel_rows(g_, o_).max())
     Hg = to_np(out).reshape(R, D)
     Hin = inp.H.reshape(R, D).astype(np.float64)
     rr = res["out_rows"]
@@ -163,9 +191,14 @@ def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0, gate_r
     err = np.linalg.norm(Hg[rr] - res["out"])
     floor = np.linalg.norm(synth.round_bf16(res["out"].astype(np.float32)) - res["out"])
     assert err <= TOL * np.linalg.norm(res["out"] - Hin[rr]) + 2.0 * floor, m
+    # and row by row (every output row the oracle computed)
+    m["H_out_row_worst"] = check_rows_out(Hg[rr], res["out"], Hin[rr])
     for key, val in m.items():
-        if key not in ("n", "near_tau", "delta"):
+        if key not in ("n", "near_tau", "delta", "H_out_row_worst"):
             assert val < TOL, (key, val, m)
+    for key, val in rows_max.items():
+        assert val < TOL, ("per-row", key, val, rows_max)
+    m["rows_max"] = rows_max
     return m, lay, out
 
 
@@ -175,12 +208,17 @@ def check_layer(inp, tau, rows=None, inter=True, rope_theta: float = 0.0, gate_r
 
 # The FFN-sublayer gate decides on A, which the GPU stores in bf16 and the
 # oracle keeps in float64, so the two compare slightly different rows.  The
-# error of r = |A_b - A_p| / |A_p| is the projection of A's error on the
-# direction of A_b - A_p over |A_p|: about u / sqrt(d) with u the relative
-# per-element error of A (bf16 storage 2^-9 / sqrt(3) plus the projection's
-# own), 1e-4 at d = 256.  Rows with |r - tau| below these absolute bands take
-# the GPU's decision (reported, excluded from decision parity).
-FFN_NEAR_ABS = {"bf16": 2e-3, "f32": 1e-5}
+# error of r = |A_b - A_p| / |A_p| is the part of A's error along the
+# direction of A_b - A_p, over |A_p|.  Independent per-element errors give
+# about sqrt(2) u / sqrt(d) (u = 2^-9 / sqrt(3) for bf16 storage), 1e-4 at
+# d = 256; an error shared by a whole row (a scale error of the attention
+# output, which the strong-attention cases below amplify into most of A - H)
+# does not average out and gives about u itself.  Measured on GB300: up to
+# 1.6e-3.  Rows with |r - tau| below 2e-3 in bf16 (1e-5 in fp32) take the
+# GPU's decision (reported, excluded from decision parity), and the measured
+# error must stay inside that band.
+def ffn_near_abs(dtype: str, d: int) -> float:
+    return 2e-3 if dtype == "bf16" else 1e-5
 
 
 def read_sublayers(lay: binding.FoldedLayer, dev: DeviceInputs) -> dict:
@@ -230,7 +268,7 @@ def oracle_sublayers_with_gpu_decisions(inp, tau, gpu_fold, gpu_fold_ffn, attn_r
     res = run(None)
     n_near_f, bad_f = 0, 0
     if ffn_gate:
-        band = FFN_NEAR_ABS[inp.dtype] if ffn_band is None else ffn_band
+        band = ffn_near_abs(inp.dtype, d.d) if ffn_band is None else ffn_band
         band = band if t32 > 0 else 0.0   # tau = 0 folds nothing: no band
         t_div = t32 if t32 > 0 else 1.0
         for _ in range(2 if gate_ref == 1 else 1):
@@ -267,17 +305,23 @@ def check_layer_sublayers(inp, tau, attn_rematch, ffn_gate, rope_theta=0.0, gate
     assert np.array_equal(gi["fold"], res["fold"].reshape(-1))
     assert np.array_equal(gi["src"], res["src"])
     assert gi["n"] == res["n"] and np.array_equal(gi["packed_idx"], res["packed_idx"])
+    m0 = {}
     if ffn_gate:
         assert np.array_equal(gs["fold_ffn"], res["fold_ffn"].reshape(-1))
         nonroot = np.arange(R) >= L
         ro = res["rel_ffn"].reshape(-1)[nonroot]
         fin = np.isfinite(ro)
-        assert np.max(np.abs(gs["rel_ffn"][nonroot][fin] - ro[fin])) < 2e-3
+        m0["rel_ffn_err"] = float(np.max(np.abs(gs["rel_ffn"][nonroot][fin] - ro[fin])))
+        band = ffn_near_abs(inp.dtype, d.d) if ffn_band is None else ffn_band
+        print("FFN gate: max |r_gpu - r_oracle|", m0["rel_ffn_err"], "band", band, "near-tau rows", n_near_f, "of", R)
+        assert m0["rel_ffn_err"] < band, (m0["rel_ffn_err"], band)
+        # the band excuses few rows: at most 5 % of the rows (and 2 rows on tiny layers)
+        assert n_near_f <= max(2, R // 20), (n_near_f, R, m0["rel_ffn_err"], band)
     assert np.array_equal(gs["src_ffn"], res["src_ffn"])
     assert gs["n_ffn"] == res["n_ffn"] and np.array_equal(gs["packed_ffn"], res["packed_ffn"])
     tol = 1e-4 if dev.fp32 else TOL
     Hin = inp.H.reshape(R, D).astype(np.float64)
-    m = {"n": gi["n"], "n_ffn": gs["n_ffn"], "near_tau": n_near, "near_tau_ffn": n_near_f}
+    m = {"n": gi["n"], "n_ffn": gs["n_ffn"], "near_tau": n_near, "near_tau_ffn": n_near_f, **m0}
     # attention output: every row with the correction, else the packed rows
     if attn_rematch:
         ao = to_np(lay.view("attn_o", dev.tdtype, (R, d.n_q * d.hd)))
@@ -288,6 +332,11 @@ def check_layer_sublayers(inp, tau, attn_rematch, ffn_gate, rope_theta=0.0, gate
     m["G"] = rel_l2(gs["G"], res["G"])
     for key in ("attnO", "X2", "G"):
         assert m[key] < tol, (key, m)
+    # row by row as well
+    for key, (g_, o_) in (("attnO", (ao, res["attnO"])), ("X2", (gs["X2"], res["X2"])), ("G", (gs["G"], res["G"]))):
+        worst = float(rel_rows(g_, o_).max()) if len(o_) else 0.0
+        m[key + "_row_max"] = worst
+        assert worst < tol, ("per-row", key, worst)
     Hg = to_np(out).reshape(R, D)
     m["A_delta"] = rel_l2(gs["A_all"] - Hin, res["A"] - Hin)
     m["delta"] = rel_l2(Hg - Hin, res["out"] - Hin)
@@ -298,7 +347,9 @@ def check_layer_sublayers(inp, tau, attn_rematch, ffn_gate, rope_theta=0.0, gate
     for got, ref, key in ((gs["A_all"], res["A"], "A_delta"), (Hg, res["out"], "delta")):
         if dev.fp32:
             assert m[key] < tol, (key, m)
+            assert float(rel_rows(got - Hin, ref - Hin).max()) < 10 * tol, key
         else:
             floor = np.linalg.norm(synth.round_bf16(ref.astype(np.float32)) - ref)
             assert np.linalg.norm(got - ref) <= TOL * np.linalg.norm(ref - Hin) + 2.0 * floor, (key, m)
+            m[key + "_row_worst"] = check_rows_out(got, ref, Hin)
     return m, res, lay, out

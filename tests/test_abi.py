@@ -52,15 +52,27 @@ def test_workspace_layout_host_only(L):
     lo = binding.workspace_layout(d, 8, 32)
     R = 256
     assert lo.total == binding.workspace_size(d, 8, 32)
-    offs = [getattr(lo, f) for f, _ in binding.specfold_ws_layout._fields_]
+    variant = ("q_all", "all_idx", "n_all", "a_all", "fold_ffn", "rel_ffn", "src_ffn", "packed_ffn", "slot_ffn",
+               "n_ffn", "dep_rng_ffn", "dep_rows_ffn")
+    names = [f for f, _ in binding.specfold_ws_layout._fields_]
+    # the base path reserves no variant-path regions
+    assert all(getattr(lo, f) == 0 for f in variant)
+    offs = [getattr(lo, f) for f in names if f not in variant]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)
-    assert lo.x1 - lo.slot_of_row >= R * 4
+    assert lo.dep_rows - lo.dep_rng >= R * 8
+    assert lo.x1 - lo.sync >= 4 + 4 * 160
     assert lo.q - lo.x1 >= R * 3584 * 2
-    assert lo.g - lo.x2 >= R * 3584 * 2
-    assert lo.q_all - lo.g >= R * 18944 * 2
-    assert lo.a_all - lo.n_all >= 256 and lo.fold_ffn - lo.a_all >= R * 3584 * 2
-    assert lo.dep_rows_ffn - lo.dep_off_ffn >= (R + 1) * 4
+    assert lo.gemm_scratch - lo.x2 >= R * 3584 * 2 + R * 18944 * 2
+    # with a variant flag every region is reserved, in order
+    dv = binding.make_dims(3584, 28, 4, 128, 18944, 1e-6, binding.BF16, 0.0, 0, 1, 1)
+    lv = binding.workspace_layout(dv, 8, 32)
+    offs_v = [getattr(lv, f) for f in names]
+    assert all(o % 256 == 0 for o in offs_v) and offs_v == sorted(offs_v)
+    assert lv.q_all - lv.g >= R * 18944 * 2
+    assert lv.a_all - lv.n_all >= 256 and lv.fold_ffn - lv.a_all >= R * 3584 * 2
+    assert lv.dep_rows_ffn - lv.dep_rng_ffn >= R * 8
+    assert lv.total > lo.total
     # invalid shapes give 0 / an error code
     assert binding.workspace_size(_dims(hd=96), 8, 32) == 0
     assert binding.workspace_size(_dims(n_q=27), 8, 32) == 0

@@ -118,6 +118,22 @@ def test_layer_no_prefix():
     check_layer(synth.make_layer_inputs(w, seed=2), 0.05)
 
 
+@pytest.mark.parametrize("levels,L,tau", [
+    ((1, 8, 55, 64), 32, 0.05),   # 4096 rows: several rows per warp (rows re-read for RMSNorm1)
+    ((1, 1), 320, 0.05),          # more block positions than CTAs: positions grouped in turn
+    ((1,), 16, 0.05),             # the main branch alone: every row recomputed
+    ((1, 3, 9), 32, 0.0),         # tau = 0: nothing folds
+])
+def test_layer_gate_pack_shapes(levels, L, tau):
+    """The fused gate / resolve / pack launch on shapes that take its other
+    code paths, against the oracle (decisions, sources, packed list exact;
+    outputs within tolerance)."""
+    w = synth.small_workload(d=256, n_q=4, n_kv=2, hd=64, F=256, P=64, L=L, levels=levels)
+    m, _, _ = check_layer(synth.make_layer_inputs(w, seed=11), tau)
+    if tau == 0.0 or len(levels) == 1:
+        assert m["n"] == sum(levels) * L
+
+
 TOL_F32 = 1e-4   # relative L2 for the fp32 path (fp32 storage and accumulation)
 
 
@@ -192,14 +208,31 @@ def test_layer_3b():
 
 
 @pytest.mark.parametrize("frac,n_expect", [(0.0, 32), (0.25, 536), (1.0, 2048)])
-def test_layer_stress_sampled(frac, n_expect):
+def test_layer_stress_all_rows(frac, n_expect):
+    """The stress workload (prefix 8192, 64 branches) at three recompute
+    fractions: every output row, and every packed row's intermediates (so
+    every m-tile of each GEMM and every query tile of the attention), row by
+    row against the oracle."""
     inp = synth.make_layer_inputs("stress", seed=0, forced_frac=frac)
-    rng = np.random.default_rng(1)
-    R = inp.H.shape[0] * inp.H.shape[1]
-    rows = sorted(set(rng.choice(R, size=24, replace=False).tolist()) | {0, R - 1})
-    m, _, _ = check_layer(inp, 0.05, rows=rows)
+    m, _, _ = check_layer(inp, 0.05)
     assert m["n"] == n_expect
     print("stress", frac, m)
+
+
+# the draft-budget points of the 7B-like layer (level sizes; node 0 is the main branch)
+BUDGET_7B = {4: (1, 1, 2), 16: (1, 4, 11), 32: (1, 4, 6, 6, 6, 5, 4)}
+
+
+@pytest.mark.parametrize("B", [4, 16, 32])
+def test_layer_7b_budget(B):
+    """The 7B-like layer (prefix 512, L 32) over 4, 16 and 32 branches: all
+    rows against the oracle."""
+    base = synth.WORKLOADS["7b_layer"]
+    w = synth.Workload(f"7b_budget{B}", base.dims, P=base.P, L=base.L, levels=BUDGET_7B[B],
+                       max_fanout=4 if B == 16 else None, second_parent=True, reveals=base.reveals,
+                       ripple_len=base.ripple_len, taus=(0.05,), dtype="bf16")
+    m, _, _ = check_layer(synth.make_layer_inputs(w, seed=B), 0.05)
+    print("7b budget", B, m)
 
 
 def test_deterministic_bitwise():

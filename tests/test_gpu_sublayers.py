@@ -100,11 +100,13 @@ def test_sublayers_tiny_fp32():
         print(flags, m)
 
 
-def test_sublayers_7b():
-    """The 7B layer (d 3584, 28/4 x 128, F 18944, P 512, B 8, L 32) with both
-    variants."""
+@pytest.mark.parametrize("rematch,fgate,tau", [(0, 1, 0.05), (1, 0, 0.1), (1, 1, 0.05)])
+def test_sublayers_7b(rematch, fgate, tau):
+    """The 7B layer (d 3584, 28/4 x 128, F 18944, P 512, B 8, L 32) under each
+    variant on its own and both together: the FFN gate's unpack-and-fill path
+    without the correction, the correction without the FFN gate, and both."""
     inp = synth.make_layer_inputs("7b_layer", seed=0)
-    m, _, _, _ = check_layer_sublayers(inp, 0.05, 1, 1)
+    m, _, _, _ = check_layer_sublayers(inp, tau, rematch, fgate)
     print(m)
 
 
