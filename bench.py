@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--no-stress", action="store_true", help="skip the stress-workload recompute-fraction sweep")
     ap.add_argument("--no-budget", action="store_true", help="skip the draft-budget sweep")
     ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer stack tau sweep")
+    ap.add_argument("--no-3b", action="store_true", help="skip the 3B-class layer leg")
     return ap.parse_args()
 
 
@@ -398,6 +399,25 @@ def run_ours(args, rank, world):
            "d2h_bytes_per_step": int(Hout.numel() * 2), "steps": e2e_steps,
            "loop": f"{NBUF} buffer sets, input copy / layer / output copy on three streams, no L2 flush "
                    f"(weights > L2)"}
+    # the device-only rate under the e2e loop's L2 policy (back-to-back
+    # replays, no flush), so e2e is compared like with like
+    g_nf = lay.graph(H, parent, args.tau, Hout)
+    for _ in range(3):
+        g_nf.launch()
+    torch.cuda.synchronize()
+    barrier()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        g_nf.launch()
+    eb.record(stream)
+    eb.synchronize()
+    nf_ms = reduce_max(ea.elapsed_time(eb), world)
+    g_nf.close()
+    e2e["device_no_flush"] = {"value": round(aggregate_rate(B * L, e2e_steps, world, nf_ms), 1),
+                              "us_per_step": round(nf_ms / e2e_steps * 1e3, 2),
+                              "note": "the same replays with inputs resident and no copies, back to back (no L2 "
+                                      "flush), the e2e loop's L2 policy"}
 
     # recompute-fraction sweep (tau = 0 is the dense multi-branch verify)
     sweep = []
@@ -453,11 +473,13 @@ def run_ours(args, rank, world):
             del vlay
     budget = [] if (args.no_budget or args.workload != "7b_layer") else budget_sweep(args, lay.dims, W, pk, pv, flush,
                                                                                        barrier)
+    leg3b = None if (args.no_3b or args.workload != "7b_layer") else layer_leg(args, "3b_layer", flush, barrier)
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
     del lay
     torch.cuda.empty_cache()
     stack = None if args.no_stack else stack_sweep(args, flush, barrier)
     return {
+        "layer_3b": leg3b,
         "stack_sweep": stack,
         "budget_sweep": budget,
         "stress_sweep": stress,
@@ -547,6 +569,68 @@ def stage_times(lay, H, parent, tau, out, flush, steps):
             acc[si] += ev[si].elapsed_time(ev[si + 1])
     g.close()
     return {nm: acc[si] / steps * 1e3 for si, nm in enumerate(binding.STAGE_NAMES)}
+
+
+def layer_leg(args, name, flush, barrier):
+    """One more single-layer workload (the 3B-class layer: d 3072, 24/8 heads,
+    F 8192, prefix 4096, 32 branches): µs per step folded and dense, the
+    stage breakdown and each stage against its bound."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+    w = synth.WORKLOADS[name]
+    inp = synth.make_layer_inputs(w, seed=args.seed)
+    d = inp.dims
+    B, L, D = inp.H.shape
+    dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(torch.bfloat16)
+    H = to(inp.H)
+    parent = torch.from_numpy(inp.parent.astype(np.int32)).cuda()
+    W = {k: to(v) for k, v in inp.weights.items()}
+    cache = to(inp.prefix.cache)
+    o, P = inp.prefix.offset, inp.prefix.P
+    lay = binding.FoldedLayer(dims, W, B, L, cache[o:o + P, 0], cache[o:o + P, 1])
+    out = torch.empty_like(H)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    steps = max(20, min(args.steps, 200))
+    res = {"workload": workload_desc(w, w.taus[0])}
+    for tau, key in ((0.0, "dense"), (w.taus[0], "folded")):
+        g = lay.graph(H, parent, tau, out)
+        for _ in range(5):
+            flush()
+            g.launch()
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(steps):
+            flush()
+            a.record(stream)
+            g.launch()
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        g.close()
+        res[f"{key}_us"] = round(tot / steps * 1e3, 2)
+        if key == "folded":
+            nn = lay.n_packed()
+            st = stage_times(lay, H, parent, tau, out, flush, max(10, steps // 2))
+            res.update({"n_packed": nn, "rho": round(nn / (B * L), 4),
+                        "tokens_per_s": round(B * L * steps / (tot * 1e-3), 1),
+                        "stages_us": {k: round(v, 2) for k, v in st.items()}})
+            res["stage_roofline"] = {nm: stage_roofline(nm, d, nn, B * L, st[nm], peaks)
+                                     for nm in ("qkv", "out_proj_norm", "gate_up", "down")}
+            att_flops = 4.0 * nn * d.n_q * d.hd * (P + L)
+            tf = att_flops / (st["attention"] * 1e-6) / 1e12
+            res["stage_roofline"]["attention"] = {"bound": "tensor", "achieved": round(tf, 1),
+                                                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                                  "frac": round(tf / peaks["bf16_tflops"], 4)}
+    res["time_vs_dense"] = round(res["folded_us"] / res["dense_us"], 4)
+    assert lay.status() == 0, "device status set"
+    del lay, W, cache
+    torch.cuda.empty_cache()
+    return res
 
 
 def stress_sweep(args, flush, barrier):
@@ -719,6 +803,26 @@ def oracle_sample(inp, tau, rows_per_step, steps, budget_s=None):
     return done, t_total
 
 
+def oracle_one_core(workload, tau, seed, frac, budget_s):
+    """The oracle timed with every BLAS and OpenMP pool held to one thread,
+    in a child process (the pools size themselves when numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from diffusion_branch_speculative_gb300 import synth; "
+            "inp = synth.make_layer_inputs(%r, seed=%d, forced_frac=%r); "
+            "done, secs = bench.oracle_sample(inp, %r, 8, 1000, budget_s=%r); "
+            "print(json.dumps([done, secs]))") % (ROOT, workload, seed, frac, tau, budget_s)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        done, secs = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": round(done / secs, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{done} seeded output rows (8 per oracle call), numpy float64, one BLAS thread, "
+                          f"~{budget_s:.0f} s"}
+    except Exception as e:  # reported, not fatal
+        return {"unavailable": f"single-core oracle run failed: {type(e).__name__}"}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -730,6 +834,9 @@ def main():
         w = synth.WORKLOADS[args.workload]
         inp = synth.make_layer_inputs(w, seed=args.seed, forced_frac=args.frac)
         R = w.B * w.L
+        from oracle import specfold_oracle as orc
+        fold0, _ = orc.gate(inp.H, inp.parent, float(np.float32(args.tau)))
+        n_ref = int(orc.pack(fold0)[2])
         rows_per_step = 1
         oracle_sample(inp, args.tau, rows_per_step, max(1, min(args.warmup, 2)))
         done, secs = oracle_sample(inp, args.tau, rows_per_step, args.steps)
@@ -739,7 +846,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(w, args.tau, args.frac), "B": w.B, "L": w.L, "P": w.P,
-                       "tau": args.tau, "l2": "n/a (CPU)"},
+                       "tau": args.tau, "n_packed": n_ref, "recompute_fraction": round(n_ref / R, 4),
+                       "l2": "n/a (CPU)", "parallelism": f"replicas x{args.gpus}"},
             "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{rows_per_step} seeded output row(s) of the {R}-row step per timed step "
                                        f"(numpy float64, all BLAS threads)"},
@@ -759,7 +867,8 @@ def main():
         done, secs = oracle_sample(r["inp"], args.tau, rows_per_step, 1000, budget_s=15.0)
         cpu = {"value": round(done / secs, 3), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{done} seeded output rows ({rows_per_step} per oracle call) of the "
-                         f"{r['R']}-row step, numpy float64, ~15 s"}
+                         f"{r['R']}-row step, numpy float64, all BLAS threads, ~15 s",
+               "one_core": oracle_one_core(args.workload, args.tau, args.seed, args.frac, 10.0)}
     if rank == 0:
         w = r["w"]
         line = {
@@ -781,6 +890,7 @@ def main():
             "stress_sweep": r["stress_sweep"],
             "budget_sweep": r["budget_sweep"],
             "stack_sweep": r["stack_sweep"],
+            "layer_3b": r["layer_3b"],
         }
         print(json.dumps(line))
     if world > 1:

@@ -55,7 +55,9 @@ bool pdl_enabled() {
   return on;
 }
 
-int check_launch() { return cudaPeekAtLastError() == cudaSuccess ? SPECFOLD_OK : SPECFOLD_ECUDA; }
+// Reads and clears the launch error state, so a rejected launch is reported
+// by the call that made it and not again by every later one.
+int check_launch() { return cudaGetLastError() == cudaSuccess ? SPECFOLD_OK : SPECFOLD_ECUDA; }
 
 // ------------------------------------------------------------ TMA maps --
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

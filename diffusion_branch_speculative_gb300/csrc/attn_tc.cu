@@ -14,15 +14,19 @@
 // loops over the units of the packed-row count n read on the device, with
 // its pipeline running on across units.
 // S = Q K^T and O += P V run as tcgen05.mma into TMEM (two S buffers so the
-// next S overlaps the softmax, one O accumulator); four softmax warps own one
-// query row per thread, keep the running max and sum, rescale O in TMEM when
-// the reference max moves, and write P (bf16) to shared memory.
+// next S overlaps the softmax, one O accumulator).  The softmax keeps the
+// running max and sum, rescales O in TMEM when the reference max moves, and
+// writes P (bf16) over the block's K tile, which S has finished with: P is
+// double-buffered with the K/V stages, so the softmax of block t never waits
+// for the P V product of block t - 1 except to rescale O.
 //
-// Roles (256 threads): warps 0-2 load (TMA for prefix and Q, gathers for
-// block keys), warp 3 allocates TMEM and issues MMAs, warps 4-7 softmax
-// (warp w may only touch TMEM lanes 32*(w%4) .. +31).  Eight warps keep two
-// warps per SM sub-partition, so a softmax thread can hold its 128-float
-// output row in registers.
+// Roles (384 threads): warps 0-2 load (TMA for prefix and Q, gathers for
+// block keys), warp 3 allocates TMEM and issues MMAs, warps 4-11 softmax:
+// two threads per query row, warp w holding half (w - 4) / 4 of the keys of
+// a block and of the output columns (warp w may only touch TMEM lanes
+// 32*(w%4) .. +31), so every SM sub-partition runs two softmax warps.  The
+// two halves of a row exchange their maxima through shared memory once per
+// key block and their sums once per unit.
 #include "sf_device.cuh"
 #include "sf_internal.h"
 
@@ -34,7 +38,7 @@
 namespace sf {
 namespace {
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 384;
 constexpr int kLoaders = 96;
 constexpr int kSmBudget = 160;  // SM count the split sizing plans for (>= one GB300)
 constexpr int kAtom = 128 * 128;  // one 128-row x 128-byte swizzle block
@@ -84,11 +88,16 @@ struct ACfg {
   static constexpr int Q_BYTES = kAtom * NATOM;
   static constexpr int KV_BYTES = kAtom * NATOM;  // one K (or V) tile of 128 keys
   static constexpr int P_BYTES = 2 * kAtom;       // 128 rows x 128 keys bf16
+  // P of a block goes over that block's K tile when it fits (hd 128), else
+  // into one of two P buffers of its own (hd 64)
+  static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;          // stage s: K at +2s*KV, V at +(2s+1)*KV
+  static constexpr int OFF_KV = Q_BYTES;          // stage s: K (then P) at +2s*KV, V at +(2s+1)*KV
   static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
-  static constexpr int OFF_META = OFF_P + P_BYTES;          // int [2][128]
-  static constexpr int OFF_BAR = OFF_META + 2 * 128 * 4;
+  static constexpr int OFF_META = OFF_P + (P_IN_K ? 0 : 2 * P_BYTES);  // int [2][128]
+  static constexpr int p_off(int stage) { return P_IN_K ? OFF_KV + 2 * stage * KV_BYTES : OFF_P + stage * P_BYTES; }
+  static constexpr int OFF_XCH = OFF_META + 2 * 128 * 4;    // float [2][128]: a row's two halves' maxima / sums
+  static constexpr int OFF_BAR = OFF_XCH + 2 * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = 256;
@@ -163,12 +172,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&kv_full[i]), 1);
       mbar_init(smem_u32(&kv_empty[i]), 1);
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 128);
+      mbar_init(smem_u32(&s_free[i]), 256);
     }
-    mbar_init(smem_u32(p_full), 128);
+    mbar_init(smem_u32(p_full), 256);
     mbar_init(smem_u32(o_full), 1);
     mbar_init(smem_u32(q_empty), 1);
-    mbar_init(smem_u32(o_empty), 128);
+    mbar_init(smem_u32(o_empty), 256);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -182,7 +191,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sP = smem + C::OFF_P;
 
   // Every role walks the same units in the same order; gt counts this CTA's
   // key blocks over all units so far (it sets the ring stage and the phase
@@ -303,23 +311,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax --
-    // One query row per thread.  S is read from TMEM once per key block; the
-    // output accumulates in TMEM (P V with accumulate) against a reference
-    // max m_ref that is raised -- and O rescaled in place -- only when a row's
-    // max grows by more than 2^8, so the probabilities stay below 2^8.
+    // Two threads per query row: half hf of the row owns keys [64 hf, 64 hf +
+    // 64) of every block and output columns [hf HD/2, (hf + 1) HD/2).  S is
+    // read from TMEM once per key block; the output accumulates in TMEM (P V
+    // with accumulate) against a reference max m_ref, the same in both halves,
+    // that is raised -- and O rescaled in place -- only when the row's max
+    // grows by more than 2^8, so the probabilities stay below 2^8.
     const int qw = warp & 3;
+    const int hf = (warp - 4) >> 2;
     const int row = qw * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const uint32_t to = tmem + lane_off + C::COL_O;
+    constexpr int OH = HD / 2;  // output columns of a half
+    const uint32_t to = tmem + lane_off + C::COL_O + hf * OH;
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2][128]
+    const int pair_bar = 2 + qw;  // named barrier of the two warps sharing these rows
     int gt = 0, j = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
       const AUnit w = attn_unit(p, u, n, tiles_x, SP);
       if (w.NT == 0) {  // empty key range: a neutral partial
-        float* po = p.part_o + (w.pslot * 128 + row) * HD;
-        for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.part_ml[(w.pslot * 128 + row) * 2] = -INFINITY;
-        p.part_ml[(w.pslot * 128 + row) * 2 + 1] = 0.f;
+        float* po = p.part_o + (w.pslot * 128 + row) * HD + hf * OH;
+        for (int c = 0; c < OH; c += 4) *reinterpret_cast<float4*>(po + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hf == 0) {
+          p.part_ml[(w.pslot * 128 + row) * 2] = -INFINITY;
+          p.part_ml[(w.pslot * 128 + row) * 2 + 1] = 0.f;
+        }
         continue;
       }
       const int h = w.h;
@@ -333,28 +349,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const int gi = gt + t;
         const int jblk = w.jb + t;
         const int sb = gi & 1;
-        if (!mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        __syncwarp();
         const bool prefix = jblk < NBP;
-        if (!prefix && !mbar_wait(smem_u32(&kv_full[sb]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        // the waits of the block come before the first meeting of the two
+        // halves, which ANDs their outcomes: both leave together or neither
+        // (a wait that ran out must not strand the other half at a barrier)
+        bool okb = mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
+        if (okb && !prefix) okb = mbar_wait(smem_u32(&kv_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
         __syncwarp();
+        if (!named_bar_and(pair_bar, 64, okb)) { ok = false; break; }
         tc_fence_after();
-        const int key0 = jblk * 128;
-        const uint32_t ts = tmem + lane_off + sb * 128;
-        // visibility of the 128 keys as four 32-bit masks (bit e of km[c]: key
-        // 32c + e): prefix keys below P, block keys of this row's own branch
-        uint32_t km[4];
+        const int key0 = jblk * 128 + hf * 64;  // first key of this half
+        const uint32_t ts = tmem + lane_off + sb * 128 + hf * 64;
+        // visibility of the 64 keys as two 32-bit masks (bit e of km[c]: key
+        // 32c + e of the half): prefix keys below P, block keys of this row's
+        // own branch
+        uint32_t km[2];
         if (prefix) {
           const int lim = p.P - key0;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             const int v = lim - c * 32;
             km[c] = v >= 32 ? 0xffffffffu : (v <= 0 ? 0u : ((1u << v) - 1u));
           }
         } else {
-          const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128);
+          const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128 + hf * 64);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t mk = 0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -365,33 +385,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             km[c] = mk;
           }
         }
-        uint32_t sv[4][32];
+        uint32_t sv[2][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(ts + c * 32, sv[c]);
+        for (int c = 0; c < 2; ++c) tmem_ld32(ts + c * 32, sv[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_wait(sv[c]);
+        for (int c = 0; c < 2; ++c) tmem_ld_wait(sv[c]);
         tc_fence_before();
         mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
-        // a whole prefix block needs no mask; eight independent max chains
-        // (one warp per SM sub-partition: a single 128-deep chain would stall)
-        const bool allv = prefix && p.P - key0 >= 128;
+        // a whole prefix half-block needs no mask; eight independent max chains
+        const bool allv = prefix && p.P - key0 >= 64;
         float mx8[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) mx8[q] = -INFINITY;
         if (allv) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(sv[c][e]));
         } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               mx8[e & 7] = fmaxf(mx8[e & 7], ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // the row's max over both halves (the meeting above ordered the
+        // previous block's reads of the exchange slots before these writes)
+        xch[hf * 128 + row] = mx;
+        named_bar_sync(pair_bar, 64);
+        mx = fmaxf(mx, xch[(hf ^ 1) * 128 + row]);
         const float m_new = fmaxf(m_ref, mx * p.sl2);
         float alpha = 1.f;
         bool rescale = false;
@@ -403,15 +427,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           rescale = true;
         }
         l *= alpha;
-        if (t >= 1) {
-          // P V of the previous block must be done: it frees the P tile, and O
-          // may only be rescaled once it holds that block's contribution
-          if (!mbar_wait(smem_u32(o_full), (gi - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        // O may only be rescaled once it holds the previous block's P V; both
+        // halves of these rows take this branch together (same decisions)
+        if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
+          const bool okr = mbar_wait(smem_u32(o_full), (gi - 1) & 1, abort_flag, p.status);
           __syncwarp();
+          if (!named_bar_and(pair_bar, 64, okr)) { ok = false; break; }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, rescale)) {
+          {
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
+            for (int c = 0; c < OH / 32; ++c) {
               uint32_t r[32];
               tmem_ld32(to + c * 32, r);
               tmem_ld_wait(r);
@@ -422,22 +447,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             tmem_st_wait();
           }
         }
-        // probabilities -> bf16 P tile (K-major, 128-byte swizzle); the row sum
-        // in four independent partial sums, of the rounded values the P V
-        // product uses (so the output is an exactly normalised average of V
-        // rows, with no row-wide scale error from the rounding of P)
+        // probabilities -> bf16 P tile (K-major, 128-byte swizzle) over this
+        // block's K tile; the sum in four independent partial sums
+        uint8_t* sP = smem + C::p_off(sb);
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
           if (allv) {
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const float x0 = ex2(fmaf(__uint_as_float(sv[c][e]), p.sl2, -m_ref));
               const float x1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), p.sl2, -m_ref));
-              const uint32_t pr = pack_bf16x2(x0, x1);
-              ls[(e >> 1) & 3] += bf16lo(pr) + bf16hi(pr);
-              pk[e / 2] = pr;
+              ls[(e >> 1) & 3] += x0 + x1;
+              pk[e / 2] = pack_bf16x2(x0, x1);
             }
           } else {
 #pragma unroll
@@ -448,14 +471,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 const float x = ex2(fmaf(__uint_as_float(sv[c][e + uu]), p.sl2, -m_ref));
                 pv[uu] = ((km[c] >> (e + uu)) & 1u) ? x : 0.f;
               }
-              const uint32_t pr = pack_bf16x2(pv[0], pv[1]);
-              ls[(e >> 1) & 3] += bf16lo(pr) + bf16hi(pr);
-              pk[e / 2] = pr;
+              ls[(e >> 1) & 3] += pv[0] + pv[1];
+              pk[e / 2] = pack_bf16x2(pv[0], pv[1]);
             }
           }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const int kc = c * 4 + q4;  // 8-key chunk index, 0..15
+            const int kc = hf * 8 + c * 4 + q4;  // 8-key chunk index, 0..15
             const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
           }
@@ -466,14 +488,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         mbar_arrive(smem_u32(p_full));
       }
       if (!ok) break;
+      // the unit's last two P V products, in order: a parity wait tells only
+      // the latest phases apart, and the one before the last may still be
+      // running (the softmax waits for P V only to rescale)
       const int glast = gt + w.NT - 1;
-      if (!mbar_wait(smem_u32(o_full), glast & 1, abort_flag, p.status)) { ok = false; break; }
+      bool oku = w.NT < 2 || mbar_wait(smem_u32(o_full), (glast - 1) & 1, abort_flag, p.status);
+      oku = oku && mbar_wait(smem_u32(o_full), glast & 1, abort_flag, p.status);
       __syncwarp();
+      if (!named_bar_and(pair_bar, 64, oku)) { ok = false; break; }
       tc_fence_after();
+      // the row's sum over both halves
+      xch[hf * 128 + row] = l;
+      named_bar_sync(pair_bar, 64);
+      const float lrow = l + xch[(hf ^ 1) * 128 + row];
       if (SP > 1) {
-        float* po = p.part_o + (w.pslot * 128 + row) * HD;
+        float* po = p.part_o + (w.pslot * 128 + row) * HD + hf * OH;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < OH / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(to + c * 32, r);
           tmem_ld_wait(r);
@@ -483,14 +514,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
                             __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
         }
-        p.part_ml[(w.pslot * 128 + row) * 2] = m_ref;
-        p.part_ml[(w.pslot * 128 + row) * 2 + 1] = l;
+        if (hf == 0) {
+          p.part_ml[(w.pslot * 128 + row) * 2] = m_ref;
+          p.part_ml[(w.pslot * 128 + row) * 2 + 1] = lrow;
+        }
       } else {
-        const float inv = 1.f / l;
+        const float inv = 1.f / lrow;
         uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
-                                              static_cast<size_t>(h * g + hg) * HD);
+                                              static_cast<size_t>(h * g + hg) * HD + hf * OH);
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < OH / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(to + c * 32, r);
           tmem_ld_wait(r);
@@ -517,7 +550,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, HD, true);
       const uint32_t aQ = smem_u32(sQ);
-      const uint32_t aP = smem_u32(sP);
       int gt = 0, j = 0;
       bool ok = true;
       // P V of key block gi (first: the unit's first block, which overwrites O
@@ -526,6 +558,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (first && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(smem_u32(p_full), gi & 1, abort_flag, p.status)) return false;
         tc_fence_after();
+        const uint32_t aP = smem_u32(smem + C::p_off(gi & 1));
         const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (gi & 1) + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {

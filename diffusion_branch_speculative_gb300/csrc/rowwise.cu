@@ -745,7 +745,8 @@ struct GatePackArgs {
   uint32_t* bar;
   int32_t* cta_cnt;
   uint32_t* status;
-  int chunk;
+  int chunk;   // rows per CTA
+  int batch;   // rows per shared-memory batch
 };
 
 // Exclusive prefix sums of v[0 .. N) into out (may alias v); returns the
@@ -839,93 +840,108 @@ SF_DEV void gate_write(const GatePackArgs& a, int row, bool valid, float num, fl
 template <typename T, int MAXV, bool HOLD>
 __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_constant__ GatePackArgs a) {
   using V = VecT<T>;
-  extern __shared__ __align__(16) uint8_t gp_smem[];
+  extern __shared__ __align__(128) uint8_t gp_smem[];
   __shared__ int s_warp[32];
   __shared__ int s_nb, s_n, s_bad;
   __shared__ volatile int s_flag;
+  __shared__ volatile int s_abort;
+  __shared__ __align__(8) uint64_t s_bar;
   const int B = a.B, L = a.L, d = a.d, R = B * L;
-  const int nv = d / V::N;
+  const int nv = d / V::N;  // 16-byte vectors per row
+  const uint32_t rowb = static_cast<uint32_t>(d) * sizeof(T);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  // shared memory: gains [nv] uint4 | parent [B] | decisions [R, 16-rounded] | three int arrays
-  uint4* s_g = reinterpret_cast<uint4*>(gp_smem);
+  // shared memory: rows [batch][nv] | gains [nv] | parent [B] | decisions [R, 16-rounded] | three int arrays
+  uint4* s_rows = reinterpret_cast<uint4*>(gp_smem);
+  uint4* s_g = s_rows + static_cast<size_t>(a.batch) * nv;
   int* s_par = reinterpret_cast<int*>(s_g + nv);
   uint8_t* s_fold = reinterpret_cast<uint8_t*>(s_par + ((B + 3) & ~3));
   int* s_c1 = reinterpret_cast<int*>(s_fold + ((R + 15) & ~15));  // [max(B, chunk)]
   int* s_c2 = s_c1 + max(B, a.chunk);                              // [B]
   int* s_c3 = s_c2 + B;                                            // [B]
+  const uint32_t bar = smem_u32(&s_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    s_abort = 0;
+    s_bad = 0;
+  }
   // gains: weights, independent of earlier kernels
   for (int v = tid; v < nv; v += kGPThreads) s_g[v] = __ldg(reinterpret_cast<const uint4*>(a.g1) + v);
   pdl_wait();
-  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  // ---------------------------------------------------- phase 1: gate --
+  const int c0 = blockIdx.x * a.chunk, c1 = min(R, c0 + a.chunk);
+  const int nch = max(c1 - c0, 0);
+  const T* H = static_cast<const T*>(a.H);
+  float ss_hold = 0.f;
+  int act_here = 0;     // recomputed rows of this warp (lane 0)
+  int issued_bt = -1;   // last batch whose copies were issued (thread 0)
+  for (int bt = 0; bt * a.batch < nch; ++bt) {
+    const int r0 = c0 + bt * a.batch, nr = min(a.batch, c1 - r0);
+    if (bt > 0) {
+      __syncthreads();  // the previous batch's rows are consumed
+      if (s_abort) break;
+    }
+    if (tid == 0) {
+      issued_bt = bt;
+      // the child rows of this batch, one bulk copy each
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * rowb);
+      for (int t = 0; t < nr; ++t)
+        bulk_load(smem_u32(s_rows + static_cast<size_t>(t) * nv), H + static_cast<size_t>(r0 + t) * d, rowb, bar);
+    }
+    for (int t = w; t < nr; t += kGPWarps) {
+      const int r = r0 + t;
+      const int b = r / L, i = r - b * L;
+      const int p = b > 0 ? __ldg(a.parent + b) : -1;
+      const bool valid = b > 0 && p >= 0 && p < b;
+      // the parent row (usually an L2 hit) into registers while the child
+      // rows stream into shared memory
+      const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(valid ? p : 0) * L + i) * d);
+      uint4 pv[MAXV];
+      if (valid) {
+#pragma unroll
+        for (int u = 0; u < MAXV; ++u)
+          if (lane + 32 * u < nv) pv[u] = __ldg(q + lane + 32 * u);
+      }
+      if (!mbar_wait(bar, bt & 1, &s_abort, a.status)) break;
+      const uint4* c = s_rows + static_cast<size_t>(t) * nv;
+      float num = 0.f, den = 0.f, ss = 0.f;
+#pragma unroll
+      for (int u = 0; u < MAXV; ++u) {
+        const int v = lane + 32 * u;
+        if (v < nv) {
+          const uint4 cv = c[v];
+          if (valid) accum_gate<T>(cv, pv[u], num, den);
+          accum_sq<T>(cv, ss);
+        }
+      }
+      num = warp_sum(num);
+      den = warp_sum(den);
+      const bool f = valid && ((num < a.tau * a.tau * den) || (num == 0.f && a.tau > 0.f));
+      if (lane == 0) {
+        gate_write(a, r, valid, num, den);
+        act_here += f ? 0 : 1;
+      }
+      if constexpr (HOLD) ss_hold = warp_sum(ss);
+    }
+  }
+  // the draft graph, for the pack (and its validity, once)
   for (int b = tid; b < B; b += kGPThreads) {
     const int p = a.parent[b];
     s_par[b] = p;
     if ((b == 0 && p != -1) || (b > 0 && (p < 0 || p >= b))) s_bad = 1;
   }
-  __syncthreads();
-
-  // ---------------------------------------------------- phase 1: gate --
-  const int c0 = blockIdx.x * a.chunk, c1 = min(R, c0 + a.chunk);
-  const T* H = static_cast<const T*>(a.H);
-  uint4 cv[HOLD ? MAXV : 1];
-  float ss_hold = 0.f;
-  int act_here = 0;  // recomputed rows of this warp (lane 0)
-  for (int r = c0 + w; r < c1; r += kGPWarps) {
-    const int b = r / L, i = r - b * L;
-    const int p = b > 0 ? s_par[b] : -1;
-    const bool valid = b > 0 && p >= 0 && p < b;
-    const uint4* c = reinterpret_cast<const uint4*>(H + static_cast<size_t>(r) * d);
-    const uint4* q = reinterpret_cast<const uint4*>(H + (static_cast<size_t>(valid ? p : 0) * L + i) * d);
-    float num = 0.f, den = 0.f, ss = 0.f;
-    if constexpr (HOLD) {
-#pragma unroll
-      for (int u = 0; u < MAXV; ++u)
-        if (lane + 32 * u < nv) cv[u] = __ldg(c + lane + 32 * u);
-      if (valid) {
-#pragma unroll
-        for (int u0 = 0; u0 < MAXV; u0 += 8) {
-          uint4 pv[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u0 + u < MAXV && lane + 32 * (u0 + u) < nv) pv[u] = __ldg(q + lane + 32 * (u0 + u));
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (u0 + u < MAXV && lane + 32 * (u0 + u) < nv) accum_gate<T>(cv[u0 + u], pv[u], num, den);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < MAXV; ++u)
-        if (lane + 32 * u < nv) accum_sq<T>(cv[u], ss);
-    } else {
-      for (int v0 = 0; v0 < nv; v0 += 32 * kGPPass) {
-        uint4 xv[kGPPass], pv[kGPPass];
-#pragma unroll
-        for (int u = 0; u < kGPPass; ++u) {
-          const int v = v0 + lane + 32 * u;
-          if (v < nv) {
-            xv[u] = __ldg(c + v);
-            if (valid) pv[u] = __ldg(q + v);
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kGPPass; ++u) {
-          const int v = v0 + lane + 32 * u;
-          if (v < nv && valid) accum_gate<T>(xv[u], pv[u], num, den);
-        }
-      }
-    }
-    num = warp_sum(num);
-    den = warp_sum(den);
-    const bool f = valid && ((num < a.tau * a.tau * den) || (num == 0.f && a.tau > 0.f));
-    if (lane == 0) {
-      gate_write(a, r, valid, num, den);
-      act_here += f ? 0 : 1;
-    }
-    if constexpr (HOLD) ss_hold = warp_sum(ss);
-  }
   // this CTA's count of recomputed rows
   if (lane == 0) s_warp[w] = act_here;
   __syncthreads();
+  if (s_abort) {  // a copy never landed: give the last ones a short bound, then leave
+    if (tid == 0 && issued_bt >= 0) {
+      int never = 0;
+      mbar_wait(bar, issued_bt & 1, &never, nullptr, 10000000ull);
+    }
+    return;
+  }
   if (tid == 0) {
     int t = 0;
     for (int j = 0; j < kGPWarps; ++j) t += s_warp[j];
@@ -957,10 +973,9 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   }
   __syncthreads();
   const int n = s_n, nb = s_nb;
-  const int nch = c1 - c0;
   for (int t = tid; t < nch; t += kGPThreads) s_c1[t] = s_fold[c0 + t] ? 0 : 1;
   __syncthreads();
-  block_scan_excl(s_c1, s_c1, max(nch, 0), s_warp);  // local rank of each recomputed row
+  block_scan_excl(s_c1, s_c1, nch, s_warp);  // local rank of each recomputed row
   for (int t = tid; t < nch; t += kGPThreads) {
     const int r = c0 + t;
     const int b = r / L, i = r - b * L;
@@ -978,14 +993,11 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   T* X1 = static_cast<T*>(a.X1);
   if constexpr (HOLD) {
     const int r = c0 + w;
-    if (r < c1 && !s_fold[r]) {
+    if (w < nch && !s_fold[r]) {
       const float inv = rsqrtf(ss_hold / static_cast<float>(d) + a.eps);
+      const uint4* x = s_rows + static_cast<size_t>(w) * nv;
       uint4* y = reinterpret_cast<uint4*>(X1 + static_cast<size_t>(nb + s_c1[w]) * d);
-#pragma unroll
-      for (int u = 0; u < MAXV; ++u) {
-        const int v = lane + 32 * u;
-        if (v < nv) y[v] = scale_vec<T>(cv[u], s_g[v], inv);
-      }
+      for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(x[v], s_g[v], inv);
     }
   } else {
     for (int t = w; t < nch; t += kGPWarps) {
@@ -1091,10 +1103,12 @@ int launch_gate(int dtype, const void* H, const int32_t* parent, int B, int L, i
 
 size_t gate_pack_sync_bytes() { return 128 + sizeof(int32_t) * kGPMaxCtas; }
 
+constexpr int kGPMaxSmem = 200 * 1024;  // the launcher's bound on the kernel's dynamic shared memory
+
 template <typename T, int MAXV, bool HOLD>
 static int gate_pack_go(const GatePackArgs& a, int grid, size_t smem, cudaStream_t st) {
-  if (smem > 48 * 1024 && smem_limit_once(gate_pack_kernel<T, MAXV, HOLD>, static_cast<int>(smem)))
-    return SPECFOLD_ECUDA;
+  // the limit is raised once per device, to the largest size any shape asks for
+  if (smem > 48 * 1024 && smem_limit_once(gate_pack_kernel<T, MAXV, HOLD>, kGPMaxSmem)) return SPECFOLD_ECUDA;
   launch_k(gate_pack_kernel<T, MAXV, HOLD>, dim3(grid), dim3(kGPThreads), smem, st, a);
   count_launch();
   return check_launch();
@@ -1111,9 +1125,13 @@ int launch_gate_pack(int dtype, const void* H, const int32_t* parent, int B, int
   const int sms = std::max(1, std::min(num_sms(), kGPMaxCtas));
   const int chunk = (R + sms - 1) / sms;
   const int grid = (R + chunk - 1) / chunk;
-  const size_t smem = static_cast<size_t>(nv) * 16 + 4 * static_cast<size_t>((B + 3) & ~3) + ((R + 15) & ~15) +
+  // child rows staged in shared memory: up to 16 rows, 128 KB
+  const size_t rowb = static_cast<size_t>(d) * es;
+  const int batch = static_cast<int>(std::max<size_t>(1, std::min<size_t>(kGPWarps, (128u << 10) / rowb)));
+  const size_t smem = static_cast<size_t>(batch) * rowb + static_cast<size_t>(nv) * 16 +
+                      4 * static_cast<size_t>((B + 3) & ~3) + ((R + 15) & ~15) +
                       4 * static_cast<size_t>(std::max(B, chunk)) + 8 * static_cast<size_t>(B);
-  if (per_lane > 32 || smem > 200 * 1024) return SPECFOLD_EUNSUPPORTED;
+  if (per_lane > 16 || smem > static_cast<size_t>(kGPMaxSmem)) return SPECFOLD_EUNSUPPORTED;
   GatePackArgs a;
   memset(&a, 0, sizeof(a));
   a.H = H;
@@ -1139,12 +1157,16 @@ int launch_gate_pack(int dtype, const void* H, const int32_t* parent, int B, int
   a.cta_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(sync) + 128);
   a.status = status;
   a.chunk = chunk;
-  const bool hold = chunk <= kGPWarps && per_lane <= 16;
-#define SF_GP(TT)                                                                   \
-  if (hold && per_lane <= 4) return gate_pack_go<TT, 4, true>(a, grid, smem, st);   \
-  if (hold && per_lane <= 8) return gate_pack_go<TT, 8, true>(a, grid, smem, st);   \
-  if (hold) return gate_pack_go<TT, 16, true>(a, grid, smem, st);                   \
-  return gate_pack_go<TT, 1, false>(a, grid, smem, st)
+  a.batch = batch;
+  // the whole chunk stays staged for RMSNorm1 (one row per warp), or the
+  // rows are read again from L2 after the barrier
+  const bool hold = chunk <= batch;
+#define SF_GP(TT)                                                                          \
+  if (per_lane <= 4) return hold ? gate_pack_go<TT, 4, true>(a, grid, smem, st)           \
+                                 : gate_pack_go<TT, 4, false>(a, grid, smem, st);         \
+  if (per_lane <= 8) return hold ? gate_pack_go<TT, 8, true>(a, grid, smem, st)           \
+                                 : gate_pack_go<TT, 8, false>(a, grid, smem, st);         \
+  return hold ? gate_pack_go<TT, 16, true>(a, grid, smem, st) : gate_pack_go<TT, 16, false>(a, grid, smem, st)
   if (dtype == SPECFOLD_BF16) {
     SF_GP(__nv_bfloat16);
   }

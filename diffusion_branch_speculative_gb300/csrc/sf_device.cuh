@@ -104,8 +104,11 @@ SF_DEV bool grid_barrier(uint32_t* bar, uint32_t* status, volatile int* s_flag,
   if (threadIdx.x == 0) {
     const uint32_t nb = gridDim.x * gridDim.y * gridDim.z;
     const bool first = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
-    __threadfence();
-    const uint32_t old = atomicAdd(bar, first ? 0x80000000u - (nb - 1u) : 1u);
+    const uint32_t add = first ? 0x80000000u - (nb - 1u) : 1u;
+    uint32_t old;
+    // release: this CTA's writes (ordered before by the block barrier) are
+    // visible to whoever acquires the flipped word
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(add) : "memory");
     int ok = 1;
     const uint64_t t0 = globaltimer();
     while (true) {
@@ -117,13 +120,26 @@ SF_DEV bool grid_barrier(uint32_t* bar, uint32_t* status, volatile int* s_flag,
         if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT);
         break;
       }
-      __nanosleep(32);
     }
-    __threadfence();
     *s_flag = ok;
   }
   __syncthreads();
   return *s_flag != 0;
+}
+
+// Named barrier that also ANDs a predicate over the participating threads:
+// every one of them gets true only if all passed true.
+SF_DEV bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 SF_DEV void named_bar_sync(int id, int nthreads) {
@@ -180,6 +196,14 @@ SF_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// Untiled bulk copy global -> shared memory of `bytes` (a multiple of 16,
+// both addresses 16-byte aligned), completing on the mbarrier.
+SF_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 SF_DEV void prefetch_tmap(const CUtensorMap* map) {
