@@ -88,17 +88,18 @@ struct ACfg {
   static constexpr int Q_BYTES = kAtom * NATOM;
   static constexpr int KV_BYTES = kAtom * NATOM;  // one K (or V) tile of 128 keys
   static constexpr int P_BYTES = 2 * kAtom;       // 128 rows x 128 keys bf16
+  // three K/V stages, so a stage's next keys load while the two before it are
+  // still in use (the load of block t must not wait for the P V of block t-1)
+  static constexpr int KV_STAGES = 3;
   // P of a block goes over that block's K tile when it fits (hd 128), else
-  // into one of two P buffers of its own (hd 64)
+  // into a P buffer of its own per stage (hd 64)
   static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;          // stage s: K (then P) at +2s*KV, V at +(2s+1)*KV
-  static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
-  static constexpr int OFF_META = OFF_P + (P_IN_K ? 0 : 2 * P_BYTES);  // int [2][128]
+  static constexpr int OFF_KV = Q_BYTES;  // stage s: K (then P) at +2s*KV, V at +(2s+1)*KV
+  static constexpr int OFF_P = OFF_KV + 2 * KV_STAGES * KV_BYTES;
+  static constexpr int SMEM_TILES = OFF_P + (P_IN_K ? 0 : KV_STAGES * P_BYTES);
+  static constexpr int SMEM_BYTES = SMEM_TILES + 1024;  // and the 1024-byte alignment of the base
   static constexpr int p_off(int stage) { return P_IN_K ? OFF_KV + 2 * stage * KV_BYTES : OFF_P + stage * P_BYTES; }
-  static constexpr int OFF_XCH = OFF_META + 2 * 128 * 4;    // float [2][128]: a row's two halves' maxima / sums
-  static constexpr int OFF_BAR = OFF_XCH + 2 * 128 * 4;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = 256;
 };
@@ -138,21 +139,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // every derived pointer in the shared state space (shared, not generic,
   // loads and stores)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  int* meta = reinterpret_cast<int*>(smem + C::OFF_META);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  // barriers, flags and the halves' exchange slots in static shared memory
+  __shared__ __align__(8) uint64_t bars[16];
+  __shared__ uint32_t tmem_slot_s;
+  __shared__ volatile int abort_s;
+  __shared__ volatile int okflag[C::KV_STAGES];
+  __shared__ float xch[2 * 128];  // a row's two halves' maxima / sums
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_free = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_full = bars + 10;   // one completion per P V product
-  uint64_t* q_empty = bars + 11;  // the S products of a unit are done: Q may be replaced
-  uint64_t* o_empty = bars + 12;  // the softmax warps have read a unit's output
-  uint64_t* drain = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* okflag = abort_flag + 1;  // [2]
+  uint64_t* kv_full = bars + 1;   // [KV_STAGES]
+  uint64_t* kv_empty = bars + 4;  // [KV_STAGES]
+  uint64_t* s_full = bars + 7;    // [2]
+  uint64_t* s_free = bars + 9;    // [2]
+  uint64_t* p_full = bars + 11;
+  uint64_t* o_full = bars + 12;   // one completion per P V product
+  uint64_t* q_empty = bars + 13;  // the S products of a unit are done: Q may be replaced
+  uint64_t* o_empty = bars + 14;  // the softmax warps have read a unit's output
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = &tmem_slot_s;
+  volatile int* abort_flag = &abort_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();
@@ -168,9 +172,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::KV_STAGES; ++i) {
       mbar_init(smem_u32(&kv_full[i]), 1);
       mbar_init(smem_u32(&kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 256);
     }
@@ -223,8 +229,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       }
       for (int t = 0; t < w.NT; ++t, ++gt) {
         const int jblk = w.jb + t;
-        const int st = gt & 1;
-        if (lt == 0) okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+        const int st = gt % C::KV_STAGES;
+        if (lt == 0)
+          okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt / C::KV_STAGES) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
         named_bar_sync(1, kLoaders);
         if (!okflag[st]) {
           ok = false;
@@ -257,7 +264,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
         } else {
           for (int kr = lt; kr < 128; kr += kLoaders) {
-            int bb = -1;
             const uint4* krow = nullptr;
             const uint4* vrow = nullptr;
             if (jblk < NBP) {  // paged prefix token
@@ -277,14 +283,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
               if (e < w.keys_blk) {
                 const int b = w.b_lo + e / L;
                 const int s = p.src[b * L + (e - (e / L) * L)];
-                if (s >= 0 && s < p.R) {  // an invalid source leaves the key masked
-                  bb = b;
+                if (s >= 0 && s < p.R) {  // an invalid source reads as a zero key and value
                   const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
                   krow = reinterpret_cast<const uint4*>(p.bK + off);
                   vrow = reinterpret_cast<const uint4*>(p.bV + off);
                 }
               }
-              meta[st * 128 + kr] = bb;
             }
 #pragma unroll
             for (int c16 = 0; c16 < HD / 8; ++c16) {
@@ -306,7 +310,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       // let the copies already issued land before the CTA exits
       int never = 0;
       if (issued_tma >= 0)
-        mbar_wait(smem_u32(&kv_full[issued_tma & 1]), (issued_tma >> 1) & 1, &never, nullptr, 10000000ull);
+        mbar_wait(smem_u32(&kv_full[issued_tma % C::KV_STAGES]), (issued_tma / C::KV_STAGES) & 1, &never, nullptr,
+                  10000000ull);
       if (issued_q >= 0) mbar_wait(smem_u32(q_full), issued_q & 1, &never, nullptr, 10000000ull);
     }
   } else if (warp >= 4) {
@@ -323,7 +328,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     constexpr int OH = HD / 2;  // output columns of a half
     const uint32_t to = tmem + lane_off + C::COL_O + hf * OH;
-    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);  // [2][128]
     const int pair_bar = 2 + qw;  // named barrier of the two warps sharing these rows
     int gt = 0, j = 0;
     bool ok = true;
@@ -353,36 +357,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // the waits of the block come before the first meeting of the two
         // halves, which ANDs their outcomes: both leave together or neither
         // (a wait that ran out must not strand the other half at a barrier)
-        bool okb = mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
-        if (okb && !prefix) okb = mbar_wait(smem_u32(&kv_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
+        const bool okb = mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
         __syncwarp();
         if (!named_bar_and(pair_bar, 64, okb)) { ok = false; break; }
         tc_fence_after();
         const int key0 = jblk * 128 + hf * 64;  // first key of this half
         const uint32_t ts = tmem + lane_off + sb * 128 + hf * 64;
         // visibility of the 64 keys as two 32-bit masks (bit e of km[c]: key
-        // 32c + e of the half): prefix keys below P, block keys of this row's
-        // own branch
+        // 32c + e of the half): prefix keys below P; block keys of this row's
+        // own branch, one run of L keys
         uint32_t km[2];
-        if (prefix) {
-          const int lim = p.P - key0;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int v = lim - c * 32;
-            km[c] = v >= 32 ? 0xffffffffu : (v <= 0 ? 0u : ((1u << v) - 1u));
+        {
+          int lo, hi;  // visible keys [lo, hi) relative to this half's first key
+          if (prefix) {
+            lo = 0;
+            hi = p.P - key0;
+          } else {
+            lo = (my_b - w.b_lo) * L - ((jblk - NBP) * 128 + hf * 64);
+            hi = lo + L;
           }
-        } else {
-          const int4* mb4 = reinterpret_cast<const int4*>(meta + sb * 128 + hf * 64);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t mk = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int4 v = mb4[c * 8 + q];
-              mk |= (static_cast<uint32_t>(v.x == my_b) << (4 * q)) | (static_cast<uint32_t>(v.y == my_b) << (4 * q + 1)) |
-                    (static_cast<uint32_t>(v.z == my_b) << (4 * q + 2)) | (static_cast<uint32_t>(v.w == my_b) << (4 * q + 3));
-            }
-            km[c] = mk;
+            const int a0 = max(lo - c * 32, 0), a1 = min(hi - c * 32, 32);
+            km[c] = a1 > a0 ? ((a1 >= 32 ? 0xffffffffu : ((1u << a1) - 1u)) & ~((1u << a0) - 1u)) : 0u;
           }
         }
         uint32_t sv[2][32];
@@ -449,7 +446,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
         // probabilities -> bf16 P tile (K-major, 128-byte swizzle) over this
         // block's K tile; the sum in four independent partial sums
-        uint8_t* sP = smem + C::p_off(sb);
+        uint8_t* sP = smem + C::p_off(gi % C::KV_STAGES);
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -558,15 +555,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (first && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(smem_u32(p_full), gi & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t aP = smem_u32(smem + C::p_off(gi & 1));
-        const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * (gi & 1) + 1) * C::KV_BYTES);
+        const int kst = gi % C::KV_STAGES;
+        const uint32_t aP = smem_u32(smem + C::p_off(kst));
+        const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * kst + 1) * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
                      sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(o_full));
-        tc_commit(smem_u32(&kv_empty[gi & 1]));
+        tc_commit(smem_u32(&kv_empty[kst]));
         return true;
       };
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
@@ -575,11 +573,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (!mbar_wait(smem_u32(q_full), j & 1, abort_flag, p.status)) break;
         for (int t = 0; t < w.NT && ok; ++t) {
           const int gi = gt + t;
-          const int st = gi & 1;
-          if (!mbar_wait(smem_u32(&kv_full[st]), (gi >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          const int st = gi & 1;            // S buffer
+          const int kst = gi % C::KV_STAGES;  // K/V stage
+          if (!mbar_wait(smem_u32(&kv_full[kst]), (gi / C::KV_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&s_free[st]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * st) * C::KV_BYTES);
+          const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * kst) * C::KV_BYTES);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             tc_mma_f16(tmem + st * 128,
