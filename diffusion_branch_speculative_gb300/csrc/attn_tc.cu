@@ -110,13 +110,21 @@ struct AUnit {
   size_t pslot;
 };
 
-SF_DEV AUnit attn_unit(const AttnParams& p, int u, int n, int tiles_x, int SP) {
+// The unit's position (tile, head, split): arithmetic only, so the loader can
+// start the unit's Q load before the packed-row reads of attn_unit_keys.
+SF_DEV AUnit attn_unit_pos(const AttnParams& p, int u, int tiles_x, int SP) {
   AUnit w;
   w.x = u % tiles_x;
   const int rest = u / tiles_x;
   w.h = rest % p.n_kv;
   w.z = rest / p.n_kv;
   w.m0 = w.x * 128;
+  w.pslot = (static_cast<size_t>(w.h) * tiles_x + w.x) * SP + w.z;
+  return w;
+}
+
+// The unit's keys: the branches its rows span and its share of the key blocks.
+SF_DEV void attn_unit_keys(const AttnParams& p, AUnit& w, int n, int SP) {
   const int g = p.g, L = p.L, B = p.R / L;
   const int k_lo = w.m0 / g;
   const int k_hi = min(n - 1, (w.m0 + 127) / g);
@@ -127,7 +135,11 @@ SF_DEV AUnit attn_unit(const AttnParams& p, int u, int n, int tiles_x, int SP) {
   w.NB = NBP + (w.keys_blk + 127) / 128;
   w.jb = (w.z * w.NB) / SP;
   w.NT = ((w.z + 1) * w.NB) / SP - w.jb;
-  w.pslot = (static_cast<size_t>(w.h) * tiles_x + w.x) * SP + w.z;
+}
+
+SF_DEV AUnit attn_unit(const AttnParams& p, int u, int n, int tiles_x, int SP) {
+  AUnit w = attn_unit_pos(p, u, tiles_x, SP);
+  attn_unit_keys(p, w, n, SP);
   return w;
 }
 
@@ -215,11 +227,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       }
     }
     for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-      const AUnit w = attn_unit(p, u, n, tiles_x, SP);
-      if (w.NT == 0) continue;
+      AUnit w = attn_unit_pos(p, u, tiles_x, SP);
       const int h = w.h;
-      if (lt == 0) {
+      // a unit without keys (more splits than key blocks) loads nothing; NT
+      // is 0 only when SP > NB, and NB >= NBP + 1 always
+      const bool may_be_empty = SP > NBP + 1;
+      if (lt == 0 && !may_be_empty) {
         // the previous unit's S products must be done with the Q buffer
+        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status)) {
+          mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
+          for (int a = 0; a < C::NATOM; ++a)
+            tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + w.m0);
+          issued_q = j;
+        }
+      }
+      attn_unit_keys(p, w, n, SP);
+      if (w.NT == 0) continue;
+      if (lt == 0 && may_be_empty) {
         if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status)) {
           mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
           for (int a = 0; a < C::NATOM; ++a)
@@ -698,12 +722,12 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
   return best;
 }
 
-// Cost of the combine launch in key blocks (SPECFOLD_ATTN_COMBINE_COST
-// overrides it).
+// Cost of the combine launch in key blocks: writing and reading back the
+// fp32 partials plus a launch (SPECFOLD_ATTN_COMBINE_COST overrides it).
 float combine_cost() {
   static const float c = [] {
     const char* e = std::getenv("SPECFOLD_ATTN_COMBINE_COST");
-    return e ? static_cast<float>(std::atof(e)) : 3.f;
+    return e ? static_cast<float>(std::atof(e)) : 8.f;
   }();
   return c;
 }
@@ -757,11 +781,13 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   const int cap = attn_slot_cap(R, g, c.n_kv);
   const int tiles_max = std::min(((R * g + 127) / 128) * c.n_kv, kSpTable);  // n <= R
   int units_max = ((R * g + 127) / 128) * c.n_kv;  // every tile, unsplit
+  bool any_split = false;
   for (int t = 1; t <= tiles_max; ++t) {
     const int lim = std::min(16, cap / t);
     const int sp = lim >= 2 ? plan_splits(t, lim, p.num_sms, c.P, combine_cost()) : 1;
     p.sp_table[t - 1] = static_cast<uint8_t>(sp);
     units_max = std::max(units_max, t * sp);
+    any_split = any_split || sp > 1;
   }
   if (cap > 0) {
     if (!c.part || c.part_bytes < attn_partial_bytes(R, g, c.n_kv, HD)) return SPECFOLD_ECAPACITY;
@@ -774,7 +800,7 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   launch_k(attn_kernel<HD>, dim3(grid), dim3(kAttnThreads), C::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;
-  if (cap > 0) {
+  if (any_split) {  // no combine launch when no row count splits the key range
     const long long work = static_cast<long long>(R) * g * c.n_kv * (HD / 8);
     const int cg = static_cast<int>(std::min<long long>((work + 255) / 256, 8LL * num_sms()));
     launch_k(attn_combine_kernel<HD>, dim3(std::max(cg, 1)), dim3(256), 0, st, p);

@@ -434,27 +434,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   float* epi_stage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
-  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const int Mt = (n + kBM - 1) / kBM;
-  const int tiles = Mt * p.Nt;
-  const int KB = p.K / kBK;
-  const Sched sc = get_sched(p.sched, n, p.Nt, KB);
-  const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs) : sc.S;
-  const bool dsm = CL && S > 1;  // splits summed through distributed shared memory
-  const int U = CL ? tiles * S : sc.U;
-  auto unit = [&](int u) { return CL ? decode(u, Mt, S, p.Nt, KB, dsm) : decode_plain(u, sc, p.Nt); };
-  if (static_cast<int>(blockIdx.x) >= U) {
-    if constexpr (CL) {
-      if (dsm) {  // an idle CTA still takes part in its cluster's two barriers
-        cluster_sync_all();
-        cluster_sync_all();
-      }
-    }
-    return;
-  }
-
+  // Set-up that depends on no earlier kernel runs before the programmatic
+  // wait, overlapping the previous kernel's tail wherever this CTA is already
+  // resident: barriers, tensor-map prefetch, TMEM.  (A GEMM CTA shares an SM
+  // only with kernels that hold no TMEM -- the row and finish kernels --
+  // since attention and the other GEMMs take too much shared memory to fit
+  // beside it, so the allocation cannot wait on a kernel that waits on it.)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
@@ -479,6 +464,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int Mt = (n + kBM - 1) / kBM;
+  const int tiles = Mt * p.Nt;
+  const int KB = p.K / kBK;
+  const Sched sc = get_sched(p.sched, n, p.Nt, KB);
+  const int S = CL ? split_factor_cl(tiles, static_cast<int>(gridDim.x), KB, p.cs) : sc.S;
+  const bool dsm = CL && S > 1;  // splits summed through distributed shared memory
+  const int U = CL ? tiles * S : sc.U;
+  auto unit = [&](int u) { return CL ? decode(u, Mt, S, p.Nt, KB, dsm) : decode_plain(u, sc, p.Nt); };
+  if (static_cast<int>(blockIdx.x) >= U) {
+    if (warp == 1) tmem_dealloc(*tmem_slot, C::TMEM_COLS);
+    if constexpr (CL) {
+      if (dsm) {  // an idle CTA still takes part in its cluster's two barriers
+        cluster_sync_all();
+        cluster_sync_all();
+      }
+    }
+    return;
+  }
+
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
@@ -1150,8 +1157,10 @@ Plan plan_gemm(int Mcap, int N, int K, bool swiglu, bool ok128, bool ok256) {
 // Tile width of the residual projections (output and down).  With few
 // packed rows the K loop is split to fill the SMs, and every split writes an
 // fp32 partial of its whole tile: 128-wide tiles give twice the n-tiles, so
-// half the splits and half the partial traffic.  With many rows the tiles
-// fill the SMs unsplit and 256-wide tiles keep the MMA wider.
+// half the splits and half the partial traffic.  With many rows the GEMM is
+// compute-bound and 256-wide tiles read half the shared-memory operand
+// bytes per FLOP (a 128-wide tile's MMA runs near the shared-memory read
+// rate), so 128 is taken only for at most two m-tiles of rows.
 // SPECFOLD_RESID_BN=128 or 256 in the environment fixes the width.
 int resid_tile_width(int Mcap, int N) {
   static const int forced = [] {
@@ -1160,7 +1169,7 @@ int resid_tile_width(int Mcap, int N) {
   }();
   if (N % 256) return 128;
   if (forced == 128 || forced == 256) return forced;
-  return Mcap <= 4 * kBM ? 128 : 256;
+  return Mcap <= 2 * kBM ? 128 : 256;
 }
 
 template <int EPI>

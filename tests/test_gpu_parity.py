@@ -315,7 +315,7 @@ def test_graph_replay_matches_eager_and_tracks_inputs():
     n0 = binding.specfold_launch_count()
     g.launch()
     torch.cuda.synchronize()
-    assert binding.specfold_launch_count() - n0 >= 9
+    assert binding.specfold_launch_count() - n0 >= 6   # at least one launch per stage kernel
     assert torch.equal(out, eager)
     # new inputs written into the captured buffer are picked up by the replay
     inp2 = synth.make_layer_inputs("7b_layer", seed=7)
