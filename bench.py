@@ -57,6 +57,7 @@ def parse():
     ap.add_argument("--no-budget", action="store_true", help="skip the draft-budget sweep")
     ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer stack tau sweep")
     ap.add_argument("--no-3b", action="store_true", help="skip the 3B-class layer leg")
+    ap.add_argument("--no-gate-pack", action="store_true", help="skip the fused gate/pack size sweep")
     return ap.parse_args()
 
 
@@ -474,11 +475,13 @@ def run_ours(args, rank, world):
     budget = [] if (args.no_budget or args.workload != "7b_layer") else budget_sweep(args, lay.dims, W, pk, pv, flush,
                                                                                        barrier)
     leg3b = None if (args.no_3b or args.workload != "7b_layer") else layer_leg(args, "3b_layer", flush, barrier)
+    gp = None if (args.no_gate_pack or args.workload != "7b_layer") else gate_pack_sweep(args, flush, barrier)
     stress = [] if args.no_stress else stress_sweep(args, flush, barrier)
     del lay
     torch.cuda.empty_cache()
     stack = None if args.no_stack else stack_sweep(args, flush, barrier)
     return {
+        "gate_pack_sweep": gp,
         "layer_3b": leg3b,
         "stack_sweep": stack,
         "budget_sweep": budget,
@@ -631,6 +634,63 @@ def layer_leg(args, name, flush, barrier):
     del lay, W, cache
     torch.cuda.empty_cache()
     return res
+
+
+# draft graphs for the gate/pack sweep: fanout 8, level sizes summing to B
+GATE_PACK_LEVELS = {64: (1, 8, 55), 128: (1, 8, 64, 55), 256: (1, 8, 64, 183), 512: (1, 8, 64, 439)}
+
+
+def gate_pack_sweep(args, flush, barrier):
+    """The fused gate / resolve / pack launch alone (specfold_gate_pack), 7B
+    rows (d 3584, bf16), L 32, from the stress size (64 branches, 2048 rows) to
+    the row limit (512 branches, 16384 rows): µs per launch from CUDA events
+    around single launches after an L2 flush, and the achieved rate of its
+    algorithmic bytes (H read once, X1 written for the packed rows, the
+    row lists) against the measured copy peak."""
+    import torch
+
+    from diffusion_branch_speculative_gb300 import binding, synth
+    peaks = load_peaks()
+    d = synth.DIMS_7B
+    dims = binding.make_dims(d.d, d.n_q, d.n_kv, d.hd, d.F, d.eps, binding.BF16)
+    g1 = torch.ones(d.d, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    reps = 30
+    rows = []
+    for B in (64, 128, 256, 512):
+        for frac in ((1.0, 0.25) if B in (64, 512) else (1.0,)):
+            w = synth.Workload("gate_pack", d, P=0, L=32, levels=GATE_PACK_LEVELS[B], max_fanout=8,
+                               second_parent=False, reveals=(1,), ripple_len=2.0, taus=(0.05,), dtype="bf16")
+            br = synth.make_branches(w, np.random.default_rng(args.seed + B), forced_frac=frac)
+            H = torch.from_numpy(np.ascontiguousarray(br.H, np.float32)).cuda().to(torch.bfloat16)
+            parent = torch.from_numpy(br.graph.parent.astype(np.int32)).cuda()
+            R = B * 32
+            ws = binding.alloc_workspace(binding.workspace_size(dims, B, 32))
+            for _ in range(3):
+                binding.specfold_gate_pack(dims, g1, H, parent, 0.05, ws)
+            torch.cuda.synchronize()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for _ in range(reps):
+                flush()
+                a.record(stream)
+                binding.specfold_gate_pack(dims, g1, H, parent, 0.05, ws)
+                b.record(stream)
+                b.synchronize()
+                tot += a.elapsed_time(b)
+            assert binding.specfold_get_status(ws) == 0, "device status set"
+            lo = binding.workspace_layout(dims, B, 32)
+            n = int(ws[lo.n_packed:lo.n_packed + 4].view(torch.int32).item())
+            us = tot / reps * 1e3
+            byts = R * d.d * 2 + n * d.d * 2 + 13 * R
+            gbs = byts / (us * 1e-6) / 1e9
+            rows.append({"B": B, "rows": R, "forced_frac": frac, "n_packed": n, "us": round(us, 2),
+                         "algorithmic_bytes": int(byts), "achieved_gbs": round(gbs, 1),
+                         "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)})
+            del H, ws
+    torch.cuda.empty_cache()
+    return rows
 
 
 def stress_sweep(args, flush, barrier):
@@ -891,6 +951,7 @@ def main():
             "budget_sweep": r["budget_sweep"],
             "stack_sweep": r["stack_sweep"],
             "layer_3b": r["layer_3b"],
+            "gate_pack_sweep": r["gate_pack_sweep"],
         }
         print(json.dumps(line))
     if world > 1:

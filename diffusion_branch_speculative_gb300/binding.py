@@ -85,6 +85,7 @@ _SIG = {
     "specfold_status_string": (ctypes.c_char_p, [_I]),
     "specfold_launch_count": (ctypes.c_uint64, []),
     "specfold_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+    "specfold_gate_pack": (_I, [_P, _P, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "specfold_layer_graph_create": (_I, [_P, _P, _P, _P, _I, _I, specfold_kv_view, specfold_kv_view, _I,
                                          ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P]),
     "specfold_stack_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
@@ -344,6 +345,13 @@ def specfold_get_status(ws: torch.Tensor, stream=None) -> int:
 
 def specfold_launch_count() -> int:
     return int(lib().specfold_launch_count())
+
+
+def specfold_gate_pack(dims: specfold_dims, g1: torch.Tensor, H: torch.Tensor, parent: torch.Tensor, tau: float,
+                       ws: torch.Tensor, stream=None):
+    B, L, _ = H.shape
+    _check(lib().specfold_gate_pack(ctypes.byref(dims), _ptr(g1), _ptr(H), _ptr(parent), B, L, float(tau), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "specfold_gate_pack")
 
 
 def specfold_selftest_timeout(status: torch.Tensor, wait_ns: int, stream=None):

@@ -303,9 +303,15 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
                            const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
                            const int32_t* n_dev, int B, int L, void* O, uint32_t* status, void* part,
-                           size_t part_bytes, cudaStream_t st) {
+                           size_t part_bytes, cudaStream_t st, const specfold_weights* w_ffn = nullptr) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
+  if (w_ffn && d->dtype == SPECFOLD_BF16) {  // CTAs without work prefetch the FFN weights
+    a.ffn_w[0] = w_ffn->w_gate;
+    a.ffn_w[1] = w_ffn->w_up;
+    a.ffn_F = d->ffn_dim;
+    a.ffn_d = d->d_model;
+  }
   a.Q = Q;
   a.pk = pk;
   a.pv = pv;
@@ -559,7 +565,7 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   mark(3);
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
-                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st));
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st, w));
   mark(4);
   SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
                         at<void>(ws, lo.x2)));
@@ -638,6 +644,23 @@ int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1,
   // pack alone: no parent walk -- a folded non-root row is not recomputed
   return launch_select_pack(dtype, fold, nullptr, B, L, d, H, g1, eps, nullptr, packed_idx, slot_of_row, n_dev, X1,
                             nullptr, st);
+}
+
+int specfold_gate_pack(const specfold_dims* dims, const void* g1, const void* H, const int32_t* parent, int B, int L,
+                       float tau, void* ws, size_t ws_bytes, void* stream) {
+  SF_TRY(check_dims(dims));
+  SF_TRY(check_rows(B, L));
+  if (!g1 || !H || !parent || !ws) return SPECFOLD_EINVAL;
+  if (!(tau >= 0.f)) return SPECFOLD_EINVAL;
+  if (!a16(H) || !a16(g1) || !a16(ws)) return SPECFOLD_EALIGN;
+  specfold_ws_layout lo;
+  layout(dims, B, L, &lo);
+  if (ws_bytes < lo.total) return SPECFOLD_ECAPACITY;
+  return launch_gate_pack(dims->dtype, H, parent, B, L, dims->d_model, tau, g1, dims->rms_eps, at<uint8_t>(ws, lo.fold),
+                          at<float>(ws, lo.rel), at<int32_t>(ws, lo.src), at<int32_t>(ws, lo.packed_idx),
+                          at<int32_t>(ws, lo.slot_of_row), at<int32_t>(ws, lo.n_packed), at<void>(ws, lo.x1),
+                          at<int32_t>(ws, lo.dep_rng), at<int32_t>(ws, lo.dep_rows), at<void>(ws, lo.sync),
+                          at<uint32_t>(ws, lo.status), static_cast<cudaStream_t>(stream));
 }
 
 int specfold_qkv(const specfold_dims* dims, const specfold_weights* w, const void* X1, const int32_t* packed_idx,

@@ -70,6 +70,11 @@ struct AttnParams {
   uint8_t sp_table[1024];            // key-range splits by tile count (see plan_splits)
   float* part_o;    // [slot capacity][128][hd]
   float* part_ml;   // [slot capacity][128][2]
+  // CTAs without a unit prefetch into L2 the first pf_kb k-blocks (64
+  // columns) of every 128-row block of the SwiGLU weights, k-block by
+  // k-block, in the FFN GEMM's own boxes (pf_n maps; 0: none)
+  CUtensorMap pf_map[2];
+  int pf_n, pf_rb, pf_kb;
 };
 
 // Number of key-range splits for n packed rows, looked up from a table the
@@ -179,7 +184,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int tiles_x = (rows_total + 127) / 128;
   const int SP = attn_splits(p, rows_total);
   const int U = tiles_x * p.n_kv * SP;
-  if (static_cast<int>(blockIdx.x) >= U) return;
+  if (static_cast<int>(blockIdx.x) >= U) {
+    // no unit for this CTA: its SM would idle through the attention, so it
+    // pulls a share of the FFN weights' leading k-blocks into L2, in the order
+    // the FFN GEMM's CTAs stream them
+    if (p.pf_n > 0 && threadIdx.x == 0) {
+      // after the working CTAs' first loads have gone out (a prefetch flood
+      // ahead of them delays their first key blocks)
+      __nanosleep(3000);
+      const int idle = static_cast<int>(gridDim.x) - U, me = static_cast<int>(blockIdx.x) - U;
+      const int boxes = p.pf_n * p.pf_rb * p.pf_kb;
+      for (int q = me; q < boxes; q += idle) {
+        const int kb = q / (p.pf_n * p.pf_rb);
+        const int rest = q - kb * p.pf_n * p.pf_rb;
+        const int m = rest / p.pf_rb, rb = rest - m * p.pf_rb;
+        tma_prefetch_2d(&p.pf_map[m], kb * 64, rb * 128);
+      }
+    }
+    return;
+  }
   const int NBP = (p.P + 127) / 128;
 
   if (threadIdx.x == 0) {
@@ -722,6 +745,16 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
   return best;
 }
 
+// SPECFOLD_FFN_PREFETCH=0 in the environment turns the FFN weight prefetch
+// of the attention's idle CTAs off.
+bool ffn_prefetch_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("SPECFOLD_FFN_PREFETCH");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 // Cost of the combine launch in key blocks: writing and reading back the
 // fp32 partials plus a launch (SPECFOLD_ATTN_COMBINE_COST overrides it).
 float combine_cost() {
@@ -795,8 +828,23 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
     p.part_ml = p.part_o + static_cast<size_t>(cap) * 128 * HD;
   }
   if (smem_limit_once(attn_kernel<HD>, C::SMEM_BYTES)) return SPECFOLD_ECUDA;
+  // FFN weight prefetch by CTAs without a unit: the leading k-blocks of the
+  // gate and up weights, about 40 MB (well inside L2 next to the output
+  // projection's weights and the layer's activations)
+  if (c.ffn_w[0] && c.ffn_w[1] && c.ffn_F % 128 == 0 && c.ffn_d % 64 == 0 && ffn_prefetch_enabled()) {
+    bool ok = true;
+    for (int m = 0; m < 2; ++m)
+      ok = ok && make_map_2d(&p.pf_map[m], c.ffn_w[m], c.ffn_F, c.ffn_d, c.ffn_d, 128) == SPECFOLD_OK;
+    if (ok) {
+      p.pf_n = 2;
+      p.pf_rb = c.ffn_F / 128;
+      const long long box_bytes = 128LL * 64 * 2;
+      p.pf_kb = static_cast<int>(std::min<long long>(c.ffn_d / 64, (40LL << 20) / (2LL * p.pf_rb * box_bytes)));
+    }
+  }
   // persistent: at most one CTA per SM, each looping over the live units
-  const dim3 grid(std::min(units_max, p.num_sms));
+  // (every SM when CTAs without a unit have weights to prefetch)
+  const dim3 grid(p.pf_n > 0 ? p.num_sms : std::min(units_max, p.num_sms));
   launch_k(attn_kernel<HD>, dim3(grid), dim3(kAttnThreads), C::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;

@@ -139,6 +139,10 @@ struct AttnCall {
   uint32_t* status;
   void* part;             // split-KV partials (attn_partial_bytes)
   size_t part_bytes;
+  // optional: the SwiGLU weights [F, d] (gate, up); CTAs without a unit pull
+  // their leading k-blocks into L2 for the FFN GEMM
+  const void* ffn_w[2];
+  int ffn_F, ffn_d;
 };
 int attn_slot_cap(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);

@@ -216,6 +216,22 @@ int specfold_pack(int dtype, const uint8_t* fold, const void* H, const void* g1,
                   int B, int L, int d, int32_t* packed_idx, int32_t* slot_of_row,
                   int32_t* n_dev, void* X1, void* stream);
 
+/* S1 + S2 + S3 in one launch (the parent gate), as specfold_layer_forward
+ * runs them: the gate decisions and r, the sources, the packed list, n,
+ * RMSNorm1 of the packed rows and the folded rows grouped by source, all
+ * written into the layer workspace ws (offsets: specfold_workspace_layout;
+ * fields fold, rel, src, packed_idx, slot_of_row, n_packed, x1, dep_rng,
+ * dep_rows).  Same rules as the three calls above (explainer, "observation"
+ * and "mechanism" paragraphs, implementation note).  One CTA per SM at most,
+ * meeting once at a bounded grid barrier: if that wait runs out (another
+ * kernel holding SMs for over a second) the call sets SPECFOLD_DEV_TIMEOUT and
+ * the workspace must be zeroed again before its next use.  dims gives d, eps
+ * and the dtype; rows wider than 4096 bf16 (2048 fp32) elements, or draft
+ * graphs too large for the shared memory of one CTA, give
+ * SPECFOLD_EUNSUPPORTED (use the three calls above). */
+int specfold_gate_pack(const specfold_dims* dims, const void* g1, const void* H, const int32_t* parent, int B,
+                       int L, float tau, void* ws, size_t ws_bytes, void* stream);
+
 /* S4 QKV projection of the packed rows (one transformer layer's attention
  * input projections).  Q goes to the head-group-major layout
  * Q[h_kv][k*g + j][hd] (query head h_kv*g + j of packed row k, R*g rows per

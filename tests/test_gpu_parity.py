@@ -502,3 +502,61 @@ def test_layer_gate_source_3b_sampled():
     rng = np.random.default_rng(2)
     rows = np.unique(np.concatenate([np.arange(L), rng.choice(np.arange(L, B * L), 24, replace=False)]))
     check_layer(inp, 0.05, rows=rows, inter=False, gate_ref=1)
+
+
+# ------------------------------------------ S1-S3 in one launch (entry point) --
+
+def _gate_pack_case(levels, L, d, frac, tau=0.05, fanout=None):
+    base = synth.small_workload(d=d, n_q=4, n_kv=2, hd=64, F=256, P=0, L=L, levels=levels, max_fanout=fanout)
+    return synth.make_layer_inputs(base, seed=9, forced_frac=frac)
+
+
+@pytest.mark.parametrize("levels,L,d,frac", [
+    ((1, 8, 55), 32, 3584, 1.0),        # the stress size, every row recomputed
+    ((1, 8, 55), 32, 3584, 0.25),
+    ((1, 8, 64, 439), 32, 256, 0.25),   # 16384 rows (the row limit): many rows per CTA
+])
+def test_gate_pack_entry_point(levels, L, d, frac):
+    """specfold_gate_pack against the oracle: decisions, sources, packed list
+    and n exactly, RMSNorm1 row by row; the dependents lists are a partition
+    of the folded rows by source."""
+    inp = _gate_pack_case(levels, L, d, frac, fanout=8)
+    dev = DeviceInputs(inp)
+    B, L, D = inp.H.shape
+    R = B * L
+    ws = binding.alloc_workspace(binding.workspace_size(dev.dims, B, L))
+    binding.specfold_gate_pack(dev.dims, dev.W["g1"], dev.H, dev.parent, 0.05, ws)
+    torch.cuda.synchronize()
+    assert binding.specfold_get_status(ws) == 0
+    lo = binding.workspace_layout(dev.dims, B, L)
+
+    def view(name, dtype, n):
+        off = getattr(lo, name)
+        es = torch.empty((), dtype=dtype).element_size()
+        return ws[off:off + n * es].view(dtype)
+    fold = view("fold", torch.uint8, R).cpu().numpy().astype(bool)
+    f0, r0 = orc.gate(inp.H, inp.parent, np.float32(0.05))
+    near = orc.near_tau_rows(r0, float(np.float32(0.05)))
+    assert np.array_equal(fold.reshape(B, L)[~near], f0[~near])
+    f_use = fold.reshape(B, L)
+    src = view("src", torch.int32, R).cpu().numpy()
+    assert np.array_equal(src, orc.resolve(f_use, inp.parent))
+    idx, sl, n = orc.pack(f_use)
+    assert int(view("n_packed", torch.int32, 1).item()) == n
+    assert np.array_equal(view("packed_idx", torch.int32, R).cpu().numpy()[:n], idx)
+    assert np.array_equal(view("slot_of_row", torch.int32, R).cpu().numpy(), sl)
+    x1 = view("x1", torch.bfloat16, R * D).view(R, D)[:n].float().cpu().numpy()
+    ref = orc.rmsnorm(inp.H.reshape(R, D)[idx], inp.weights["g1"], inp.dims.eps)
+    from tests.gpu_cases import rel_rows
+    assert float(rel_rows(x1, ref).max()) < 5e-3
+    # dependents: every folded row exactly once, in the range of its source
+    rng = view("dep_rng", torch.int32, 2 * R).view(R, 2).cpu().numpy()
+    deps = view("dep_rows", torch.int32, R).cpu().numpy()
+    seen = np.zeros(R, int)
+    for s in idx:
+        b_, e_ = rng[s]
+        for r in deps[b_:e_]:
+            assert src[r] == s and r != s
+            seen[r] += 1
+    folded = np.nonzero(src != np.arange(R))[0]
+    assert np.all(seen[folded] == 1) and seen.sum() == len(folded)
