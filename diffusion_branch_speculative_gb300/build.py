@@ -82,8 +82,7 @@ def build(verbose_ptxas: bool = False, force: bool = False) -> str:
         raise RuntimeError(f"nvcc failed for: {failed}")
     if jobs or not os.path.exists(LIB) or _stale(LIB, objs):
         tmp = LIB + ".tmp"
-        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"] if False else \
-              [cc, *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)

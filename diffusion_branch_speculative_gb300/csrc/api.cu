@@ -41,6 +41,14 @@ int smem_limit_once(const void* kernel, int bytes) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SPECFOLD_ECUDA;
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({dev, kernel})) return SPECFOLD_OK;
+  // the kernel's static shared memory and the dynamic size together must fit
+  // the per-block limit: a shape past it is unsupported, not a launch error
+  cudaFuncAttributes fa;
+  int optin = 0;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return SPECFOLD_ECUDA;
+  if (static_cast<long long>(fa.sharedSizeBytes) + bytes > optin) return SPECFOLD_EUNSUPPORTED;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
     return SPECFOLD_ECUDA;
   done.insert({dev, kernel});
@@ -306,7 +314,10 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
                            size_t part_bytes, cudaStream_t st, const specfold_weights* w_ffn = nullptr) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
-  if (w_ffn && d->dtype == SPECFOLD_BF16) {  // CTAs without work prefetch the FFN weights
+  if (w_ffn && d->dtype == SPECFOLD_BF16) {  // CTAs without work prefetch the next GEMMs' weights
+    a.wo = w_ffn->w_o;
+    a.wo_rows = d->d_model;
+    a.wo_cols = d->n_q_heads * d->head_dim;
     a.ffn_w[0] = w_ffn->w_gate;
     a.ffn_w[1] = w_ffn->w_up;
     a.ffn_F = d->ffn_dim;

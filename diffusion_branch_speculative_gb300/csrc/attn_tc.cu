@@ -13,20 +13,23 @@
 // partials a combine kernel merges.  The kernel is persistent: one CTA per SM
 // loops over the units of the packed-row count n read on the device, with
 // its pipeline running on across units.
-// S = Q K^T and O += P V run as tcgen05.mma into TMEM (two S buffers so the
-// next S overlaps the softmax, one O accumulator).  The softmax keeps the
-// running max and sum, rescales O in TMEM when the reference max moves, and
-// writes P (bf16) over the block's K tile, which S has finished with: P is
-// double-buffered with the K/V stages, so the softmax of block t never waits
-// for the P V product of block t - 1 except to rescale O.
+// Each key block is worked in two halves of 64 keys, h = 0, 1, that run
+// independently within a unit: S_h = Q K_h^T and O_h += P_h V_h run as
+// tcgen05.mma into TMEM (two S buffers per half so the next S overlaps the
+// softmax, one O accumulator per half), and each half keeps its own running
+// max and sum, rescaling O_h in TMEM when its reference max moves.  P_h (bf16)
+// goes over the half's own K keys, which S_h has finished with (K is stored
+// half by half for that): P is double-buffered with the K/V stages, so the
+// softmax of block t never waits for the P V product of block t - 1 except
+// to rescale.  At the end of a unit the two halves merge their (O, max, sum)
+// the way split-KV partials merge.
 //
-// Roles (384 threads): warps 0-2 load (TMA for prefix and Q, gathers for
-// block keys), warp 3 allocates TMEM and issues MMAs, warps 4-11 softmax:
-// two threads per query row, warp w holding half (w - 4) / 4 of the keys of
-// a block and of the output columns (warp w may only touch TMEM lanes
-// 32*(w%4) .. +31), so every SM sub-partition runs two softmax warps.  The
-// two halves of a row exchange their maxima through shared memory once per
-// key block and their sums once per unit.
+// Roles (384 threads): warps 0-1 load (TMA for prefix and Q, gathers for
+// block keys), warps 2 and 3 issue half 0's and half 1's MMAs (warp 3 also
+// owns the TMEM allocation), warps 4-11 softmax: two threads per query row,
+// warp w working half (w - 4) / 4 (warp w may only touch TMEM lanes
+// 32*(w%4) .. +31), so every SM sub-partition runs one softmax warp of each
+// half.  The two threads of a row meet once per unit, to merge.
 #include "sf_device.cuh"
 #include "sf_internal.h"
 
@@ -39,7 +42,7 @@ namespace sf {
 namespace {
 
 constexpr int kAttnThreads = 384;
-constexpr int kLoaders = 96;
+constexpr int kLoaders = 64;
 constexpr int kSmBudget = 160;  // SM count the split sizing plans for (>= one GB300)
 constexpr int kAtom = 128 * 128;  // one 128-row x 128-byte swizzle block
 
@@ -70,9 +73,12 @@ struct AttnParams {
   uint8_t sp_table[1024];            // key-range splits by tile count (see plan_splits)
   float* part_o;    // [slot capacity][128][hd]
   float* part_ml;   // [slot capacity][128][2]
-  // CTAs without a unit prefetch into L2 the first pf_kb k-blocks (64
-  // columns) of every 128-row block of the SwiGLU weights, k-block by
-  // k-block, in the FFN GEMM's own boxes (pf_n maps; 0: none)
+  // CTAs without a unit prefetch into L2 the whole output-projection weight
+  // (pf_orb x pf_okb boxes of 128 rows x 64 columns; 0: none), then the
+  // first pf_kb k-blocks (64 columns) of every 128-row block of the SwiGLU
+  // weights, k-block by k-block (pf_n maps; 0: none)
+  CUtensorMap pf_omap;
+  int pf_orb, pf_okb;
   CUtensorMap pf_map[2];
   int pf_n, pf_rb, pf_kb;
 };
@@ -92,19 +98,28 @@ struct ACfg {
   static constexpr int NATOM = HD / 64;
   static constexpr int Q_BYTES = kAtom * NATOM;
   static constexpr int KV_BYTES = kAtom * NATOM;  // one K (or V) tile of 128 keys
-  static constexpr int P_BYTES = 2 * kAtom;       // 128 rows x 128 keys bf16
+  // K is stored half by half: keys [64h, 64h + 64) of the block take KH_BYTES
+  // at h * KH_BYTES, in NATOM 64-row swizzle atoms of 64 dims each, so half
+  // h's product S_h = Q K_h^T reads only its own region
+  static constexpr int KH_BYTES = KV_BYTES / 2;
+  static constexpr int KH_ATOM = 64 * 128;
+  static constexpr int PH_BYTES = kAtom;          // P of one half: 128 rows x 64 keys bf16
   // three K/V stages, so a stage's next keys load while the two before it are
   // still in use (the load of block t must not wait for the P V of block t-1)
   static constexpr int KV_STAGES = 3;
-  // P of a block goes over that block's K tile when it fits (hd 128), else
-  // into a P buffer of its own per stage (hd 64)
-  static constexpr bool P_IN_K = P_BYTES <= KV_BYTES;
+  // P of a half goes over that half's K keys when they have room (hd 128),
+  // else into P buffers of their own per stage (hd 64)
+  static constexpr bool P_IN_K = PH_BYTES <= KH_BYTES;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;  // stage s: K (then P) at +2s*KV, V at +(2s+1)*KV
   static constexpr int OFF_P = OFF_KV + 2 * KV_STAGES * KV_BYTES;
-  static constexpr int SMEM_TILES = OFF_P + (P_IN_K ? 0 : KV_STAGES * P_BYTES);
+  static constexpr int SMEM_TILES = OFF_P + (P_IN_K ? 0 : KV_STAGES * 2 * PH_BYTES);
   static constexpr int SMEM_BYTES = SMEM_TILES + 1024;  // and the 1024-byte alignment of the base
-  static constexpr int p_off(int stage) { return P_IN_K ? OFF_KV + 2 * stage * KV_BYTES : OFF_P + stage * P_BYTES; }
+  static constexpr int p_off(int stage, int h) {
+    return P_IN_K ? OFF_KV + 2 * stage * KV_BYTES + h * KH_BYTES : OFF_P + (2 * stage + h) * PH_BYTES;
+  }
+  // TMEM: S of half h, buffer b at columns (2h + b) * 64; O of half h at
+  // COL_O + h * HD
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = 256;
 };
@@ -157,21 +172,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // loads and stores)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   // barriers, flags and the halves' exchange slots in static shared memory
-  __shared__ __align__(8) uint64_t bars[16];
+  __shared__ __align__(8) uint64_t bars[24];
   __shared__ uint32_t tmem_slot_s;
   __shared__ volatile int abort_s;
   __shared__ volatile int okflag[C::KV_STAGES];
-  __shared__ float xch[2 * 128];  // a row's two halves' maxima / sums
+  // the halves' exchange at the end of a unit, one slot per row (1 KB: the
+  // static and dynamic shared memory together sit within a few hundred bytes
+  // of the per-block limit at hd 128)
+  __shared__ float2 xch[128];
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;   // [KV_STAGES]
-  uint64_t* kv_empty = bars + 4;  // [KV_STAGES]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* s_free = bars + 9;    // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_full = bars + 12;   // one completion per P V product
-  uint64_t* q_empty = bars + 13;  // the S products of a unit are done: Q may be replaced
-  uint64_t* o_empty = bars + 14;  // the softmax warps have read a unit's output
-  uint64_t* drain = bars + 15;
+  uint64_t* kv_empty = bars + 4;  // [KV_STAGES]: both halves' P V of the block are done
+  uint64_t* s_full = bars + 7;    // [half][2]
+  uint64_t* s_free = bars + 11;   // [half][2]
+  uint64_t* p_full = bars + 15;   // [half]
+  uint64_t* o_full = bars + 17;   // [half]: one completion per P V product of the half
+  uint64_t* q_empty = bars + 19;  // both halves' S products of a unit are done: Q may be replaced
+  uint64_t* o_empty = bars + 20;  // the softmax warps have read a unit's outputs
+  uint64_t* drain = bars + 21;    // [half]
   uint32_t* tmem_slot = &tmem_slot_s;
   volatile int* abort_flag = &abort_s;
 
@@ -186,17 +204,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int U = tiles_x * p.n_kv * SP;
   if (static_cast<int>(blockIdx.x) >= U) {
     // no unit for this CTA: its SM would idle through the attention, so it
-    // pulls a share of the FFN weights' leading k-blocks into L2, in the order
-    // the FFN GEMM's CTAs stream them
-    if (p.pf_n > 0 && threadIdx.x == 0) {
+    // pulls a share of the next GEMMs' weights into L2: the output
+    // projection's (needed right after the attention), then the FFN weights'
+    // leading k-blocks, in the order the FFN GEMM's CTAs stream them
+    if ((p.pf_orb > 0 || p.pf_n > 0) && threadIdx.x == 0) {
       // after the working CTAs' first loads have gone out (a prefetch flood
       // ahead of them delays their first key blocks)
       __nanosleep(3000);
       const int idle = static_cast<int>(gridDim.x) - U, me = static_cast<int>(blockIdx.x) - U;
-      const int boxes = p.pf_n * p.pf_rb * p.pf_kb;
+      const int boxes_o = p.pf_orb * p.pf_okb;
+      const int boxes = boxes_o + p.pf_n * p.pf_rb * p.pf_kb;
       for (int q = me; q < boxes; q += idle) {
-        const int kb = q / (p.pf_n * p.pf_rb);
-        const int rest = q - kb * p.pf_n * p.pf_rb;
+        if (q < boxes_o) {
+          const int kb = q / p.pf_orb, rb = q - kb * p.pf_orb;
+          tma_prefetch_2d(&p.pf_omap, kb * 64, rb * 128);
+          continue;
+        }
+        const int qf = q - boxes_o;
+        const int kb = qf / (p.pf_n * p.pf_rb);
+        const int rest = qf - kb * p.pf_n * p.pf_rb;
         const int m = rest / p.pf_rb, rb = rest - m * p.pf_rb;
         tma_prefetch_2d(&p.pf_map[m], kb * 64, rb * 128);
       }
@@ -209,17 +235,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     mbar_init(smem_u32(q_full), 1);
     for (int i = 0; i < C::KV_STAGES; ++i) {
       mbar_init(smem_u32(&kv_full[i]), 1);
-      mbar_init(smem_u32(&kv_empty[i]), 1);
+      mbar_init(smem_u32(&kv_empty[i]), 2);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), 256);
+      mbar_init(smem_u32(&s_free[i]), 128);
     }
-    mbar_init(smem_u32(p_full), 256);
-    mbar_init(smem_u32(o_full), 1);
-    mbar_init(smem_u32(q_empty), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&p_full[h]), 128);
+      mbar_init(smem_u32(&o_full[h]), 1);
+      mbar_init(smem_u32(&drain[h]), 1);
+    }
+    mbar_init(smem_u32(q_empty), 2);
     mbar_init(smem_u32(o_empty), 256);
-    mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -236,7 +264,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // Every role walks the same units in the same order; gt counts this CTA's
   // key blocks over all units so far (it sets the ring stage and the phase
   // of every per-block barrier), j its units with keys (Q and O barriers).
-  if (warp < 3) {
+  if (warp < 2) {
     // ------------------------------------------------------------ loaders --
     const int lt = threadIdx.x;
     int gt = 0, j = 0;
@@ -304,7 +332,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             const uint32_t fb = smem_u32(&kv_full[st]);
             mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
             for (int a = 0; a < C::NATOM; ++a) {
-              tma_load_3d(smem_u32(sK + a * kAtom), &p.mapK, fb, a * 64, h, z);
+              // K half by half (64-token boxes), V whole (128-token boxes)
+              tma_load_3d(smem_u32(sK + a * C::KH_ATOM), &p.mapK, fb, a * 64, h, z);
+              tma_load_3d(smem_u32(sK + C::KH_BYTES + a * C::KH_ATOM), &p.mapK, fb, a * 64, h, z + 64);
               tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h, z);
             }
             issued_tma = gt;
@@ -337,13 +367,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 }
               }
             }
+            const int kh = kr >> 6, kq = kr & 63;  // half of the block and row within it
 #pragma unroll
             for (int c16 = 0; c16 < HD / 8; ++c16) {
               const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
               const uint4 vv = vrow ? __ldg(vrow + c16) : make_uint4(0, 0, 0, 0);
-              const int off = (c16 >> 3) * kAtom + kr * 128 + (((c16 & 7) ^ (kr & 7)) << 4);
-              *reinterpret_cast<uint4*>(sK + off) = kv;
-              *reinterpret_cast<uint4*>(sV + off) = vv;
+              const int sw = ((c16 & 7) ^ (kr & 7)) << 4;
+              *reinterpret_cast<uint4*>(sK + kh * C::KH_BYTES + (c16 >> 3) * C::KH_ATOM + kq * 128 + sw) = kv;
+              *reinterpret_cast<uint4*>(sV + (c16 >> 3) * kAtom + kr * 128 + sw) = vv;
             }
           }
           fence_proxy_async_smem();
@@ -364,17 +395,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax --
     // Two threads per query row: half hf of the row owns keys [64 hf, 64 hf +
-    // 64) of every block and output columns [hf HD/2, (hf + 1) HD/2).  S is
-    // read from TMEM once per key block; the output accumulates in TMEM (P V
-    // with accumulate) against a reference max m_ref, the same in both halves,
-    // that is raised -- and O rescaled in place -- only when the row's max
-    // grows by more than 2^8, so the probabilities stay below 2^8.
+    // 64) of every block, with its own S products, its own output
+    // accumulator O_hf in TMEM (P_hf V_hf with accumulate), its own reference
+    // max m and sum l: within a unit the halves never wait for each other.
+    // A half raises m -- and rescales its O in place -- only when its max
+    // grows by more than 2^8, so its probabilities stay below 2^8.  At the end
+    // of the unit the halves meet once and merge: with M = max(m_0, m_1) and
+    // w_h = 2^(m_h - M), the row's output is (w_0 O_0 + w_1 O_1) / (w_0 l_0 +
+    // w_1 l_1), half hf writing output columns [hf HD/2, (hf + 1) HD/2).
     const int qw = warp & 3;
     const int hf = (warp - 4) >> 2;
     const int row = qw * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    constexpr int OH = HD / 2;  // output columns of a half
-    const uint32_t to = tmem + lane_off + C::COL_O + hf * OH;
+    constexpr int OH = HD / 2;  // output columns a thread writes
+    const uint32_t to_own = tmem + lane_off + C::COL_O + hf * HD;
     const int pair_bar = 2 + qw;  // named barrier of the two warps sharing these rows
     int gt = 0, j = 0;
     bool ok = true;
@@ -401,15 +435,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const int jblk = w.jb + t;
         const int sb = gi & 1;
         const bool prefix = jblk < NBP;
-        // the waits of the block come before the first meeting of the two
-        // halves, which ANDs their outcomes: both leave together or neither
-        // (a wait that ran out must not strand the other half at a barrier)
-        const bool okb = mbar_wait(smem_u32(&s_full[sb]), (gi >> 1) & 1, abort_flag, p.status);
-        __syncwarp();
-        if (!named_bar_and(pair_bar, 64, okb)) { ok = false; break; }
+        // every wait's outcome is made warp-uniform: a lane whose wait ran out
+        // takes its whole warp along
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[2 * hf + sb]), (gi >> 1) & 1, abort_flag, p.status))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const int key0 = jblk * 128 + hf * 64;  // first key of this half
-        const uint32_t ts = tmem + lane_off + sb * 128 + hf * 64;
+        const uint32_t ts = tmem + lane_off + (2 * hf + sb) * 64;
+        uint32_t sv[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tmem_ld32(ts + c * 32, sv[c]);
         // visibility of the 64 keys as two 32-bit masks (bit e of km[c]: key
         // 32c + e of the half): prefix keys below P; block keys of this row's
         // own branch, one run of L keys
@@ -429,13 +466,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             km[c] = a1 > a0 ? ((a1 >= 32 ? 0xffffffffu : ((1u << a1) - 1u)) & ~((1u << a0) - 1u)) : 0u;
           }
         }
-        uint32_t sv[2][32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) tmem_ld32(ts + c * 32, sv[c]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) tmem_ld_wait(sv[c]);
         tc_fence_before();
-        mbar_arrive(smem_u32(&s_free[sb]));   // the S buffer may be refilled now
+        mbar_arrive(smem_u32(&s_free[2 * hf + sb]));   // the S buffer may be refilled now
         // a whole prefix half-block needs no mask; eight independent max chains
         const bool allv = prefix && p.P - key0 >= 64;
         float mx8[8];
@@ -453,13 +487,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             for (int e = 0; e < 32; ++e)
               mx8[e & 7] = fmaxf(mx8[e & 7], ((km[c] >> e) & 1u) ? __uint_as_float(sv[c][e]) : -INFINITY);
         }
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // the row's max over both halves (the meeting above ordered the
-        // previous block's reads of the exchange slots before these writes)
-        xch[hf * 128 + row] = mx;
-        named_bar_sync(pair_bar, 64);
-        mx = fmaxf(mx, xch[(hf ^ 1) * 128 + row]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_ref, mx * p.sl2);
         float alpha = 1.f;
         bool rescale = false;
@@ -471,29 +500,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           rescale = true;
         }
         l *= alpha;
-        // O may only be rescaled once it holds the previous block's P V; both
-        // halves of these rows take this branch together (same decisions)
+        // O_hf may only be rescaled once it holds the previous block's P V
+        bool rescale_waited = false;
         if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
-          const bool okr = mbar_wait(smem_u32(o_full), (gi - 1) & 1, abort_flag, p.status);
-          __syncwarp();
-          if (!named_bar_and(pair_bar, 64, okr)) { ok = false; break; }
-          tc_fence_after();
-          {
-#pragma unroll
-            for (int c = 0; c < OH / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(to + c * 32, r);
-              tmem_ld_wait(r);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(to + c * 32, r);
-            }
-            tmem_st_wait();
+          rescale_waited = true;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(to_own + c * 32, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(to_own + c * 32, r);
+          }
+          tmem_st_wait();
         }
-        // probabilities -> bf16 P tile (K-major, 128-byte swizzle) over this
-        // block's K tile; the sum in four independent partial sums
-        uint8_t* sP = smem + C::p_off(gi % C::KV_STAGES);
+        // probabilities -> bf16 P_hf tile (128 rows x 64 keys, K-major,
+        // 128-byte swizzle); the sum in four independent partial sums
+        uint8_t* sP = smem + C::p_off(gi % C::KV_STAGES, hf);
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -521,68 +550,106 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
-            const int kc = hf * 8 + c * 4 + q4;  // 8-key chunk index, 0..15
-            const int off = (kc >> 3) * kAtom + row * 128 + (((kc & 7) ^ (row & 7)) << 4);
+            const int kc = c * 4 + q4;  // 8-key chunk of the half, 0..7
+            const int off = row * 128 + ((kc ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(sP + off) = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
           }
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // A parity wait is exact only while its barrier cannot run two phases
+        // ahead.  o_full completes once per P V; P V of block gi - 2 is done
+        // once S(gi) is (the MMA warp issues S(gi) after it), and P V of block
+        // gi cannot start before this thread's p_full below.  So the wait for
+        // P V of block gi - 1 is exact here, and the unit's last block takes
+        // it before handing over its P: afterwards only the last P V is out,
+        // and the wait for it after the loop is exact too.
+        if (t == w.NT - 1 && t >= 1 && !rescale_waited) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+        }
         tc_fence_before();
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(p_full));
+        mbar_arrive(smem_u32(&p_full[hf]));
       }
-      if (!ok) break;
-      // the unit's last two P V products, in order: a parity wait tells only
-      // the latest phases apart, and the one before the last may still be
-      // running (the softmax waits for P V only to rescale)
+      // the half's last P V product (the one before it is done, see above)
       const int glast = gt + w.NT - 1;
-      bool oku = w.NT < 2 || mbar_wait(smem_u32(o_full), (glast - 1) & 1, abort_flag, p.status);
-      oku = oku && mbar_wait(smem_u32(o_full), glast & 1, abort_flag, p.status);
+      const bool oku = ok && mbar_wait(smem_u32(&o_full[hf]), glast & 1, abort_flag, p.status);
+      // the halves' meeting at the end of the unit: both leave together or
+      // neither (a wait that ran out must not strand the other half at a
+      // barrier).  Half 1 hands its (m, l) to half 0, which computes the merge
+      // weights w_h = 2^(m_h - M) (divided by the row's sum when the output is
+      // final) and hands half 1 its pair back.  The first barrier also orders
+      // half 0's reads of the previous unit's hand-back before this write.
+      if (hf == 1) xch[row] = make_float2(m_ref, l);
+      tc_fence_before();
       __syncwarp();
       if (!named_bar_and(pair_bar, 64, oku)) { ok = false; break; }
       tc_fence_after();
-      // the row's sum over both halves
-      xch[hf * 128 + row] = l;
+      float a0 = 0.f, a1 = 0.f, M = 0.f, lrow = 0.f;
+      if (hf == 0) {
+        const float2 o1 = xch[row];
+        M = fmaxf(m_ref, o1.x);
+        const float w0 = m_ref == -INFINITY ? 0.f : ex2(m_ref - M);
+        const float w1 = o1.x == -INFINITY ? 0.f : ex2(o1.x - M);
+        lrow = w0 * l + w1 * o1.y;
+        const float sc = SP > 1 ? 1.f : 1.f / lrow;  // split: the partial stays unnormalised
+        a0 = w0 * sc;
+        a1 = w1 * sc;
+        xch[row] = make_float2(a0, a1);
+      }
       named_bar_sync(pair_bar, 64);
-      const float lrow = l + xch[(hf ^ 1) * 128 + row];
+      if (hf == 1) {
+        const float2 f = xch[row];
+        a0 = f.x;
+        a1 = f.y;
+      }
+      const uint32_t t0 = tmem + lane_off + C::COL_O + hf * OH;  // columns [hf OH, (hf + 1) OH) of O_0
+      const uint32_t t1 = t0 + HD;                                // ... and of O_1
       if (SP > 1) {
         float* po = p.part_o + (w.pslot * 128 + row) * HD + hf * OH;
 #pragma unroll
         for (int c = 0; c < OH / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(to + c * 32, r);
-          tmem_ld_wait(r);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(t0 + c * 32, r0);
+          tmem_ld32(t1 + c * 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            reinterpret_cast<float4*>(po + c * 32)[q4] =
-                make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
-                            __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[e] = a0 * __uint_as_float(r0[4 * q4 + e]) + a1 * __uint_as_float(r1[4 * q4 + e]);
+            reinterpret_cast<float4*>(po + c * 32)[q4] = make_float4(o[0], o[1], o[2], o[3]);
+          }
         }
         if (hf == 0) {
-          p.part_ml[(w.pslot * 128 + row) * 2] = m_ref;
+          p.part_ml[(w.pslot * 128 + row) * 2] = M;
           p.part_ml[(w.pslot * 128 + row) * 2 + 1] = lrow;
         }
       } else {
-        const float inv = 1.f / lrow;
         uint4* dst = reinterpret_cast<uint4*>(p.O + static_cast<size_t>(k) * (p.n_q * HD) +
                                               static_cast<size_t>(h * g + hg) * HD + hf * OH);
 #pragma unroll
         for (int c = 0; c < OH / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(to + c * 32, r);
-          tmem_ld_wait(r);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(t0 + c * 32, r0);
+          tmem_ld32(t1 + c * 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
           if (valid) {
+            auto ov = [&](int e) { return a0 * __uint_as_float(r0[e]) + a1 * __uint_as_float(r1[e]); };
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8)
-              dst[c * 4 + q8] = make_uint4(
-                  pack_bf16x2(__uint_as_float(r[8 * q8]) * inv, __uint_as_float(r[8 * q8 + 1]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * q8 + 2]) * inv, __uint_as_float(r[8 * q8 + 3]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * q8 + 4]) * inv, __uint_as_float(r[8 * q8 + 5]) * inv),
-                  pack_bf16x2(__uint_as_float(r[8 * q8 + 6]) * inv, __uint_as_float(r[8 * q8 + 7]) * inv));
+              dst[c * 4 + q8] = make_uint4(pack_bf16x2(ov(8 * q8), ov(8 * q8 + 1)), pack_bf16x2(ov(8 * q8 + 2), ov(8 * q8 + 3)),
+                                           pack_bf16x2(ov(8 * q8 + 4), ov(8 * q8 + 5)),
+                                           pack_bf16x2(ov(8 * q8 + 6), ov(8 * q8 + 7)));
           }
         }
       }
-      // the accumulator is free for the next unit's first P V product
+      // the accumulators are free for the next unit's first P V products
       tc_fence_before();
       mbar_arrive(smem_u32(o_empty));
       gt += w.NT;
@@ -590,27 +657,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     }
   } else {
     // ---------------------------------------------------------------- MMA --
+    // warp 2 issues half 0's products, warp 3 half 1's: S_h = Q K_h^T
+    // (N = 64) into S buffer (h, gi & 1) and O_h += P_h V_h (K = 64 keys)
+    const int hm = warp - 2;
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, HD, true);
       const uint32_t aQ = smem_u32(sQ);
+      const uint32_t tO = tmem + C::COL_O + hm * HD;
       int gt = 0, j = 0;
       bool ok = true;
-      // P V of key block gi (first: the unit's first block, which overwrites O
-      // once the softmax warps have read the previous unit's output)
+      // P_h V_h of key block gi (first: the unit's first block, which
+      // overwrites O_h: the softmax warps have read the previous unit's
+      // outputs by then, see the o_empty wait below)
       auto issue_pv = [&](int gi, bool first) -> bool {
-        if (first && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(smem_u32(p_full), gi & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(smem_u32(&p_full[hm]), gi & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const int kst = gi % C::KV_STAGES;
-        const uint32_t aP = smem_u32(smem + C::p_off(kst));
+        const uint32_t aP = smem_u32(smem + C::p_off(kst, hm));
         const uint32_t aV = smem_u32(smem + C::OFF_KV + (2 * kst + 1) * C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          tc_mma_f16(tmem + C::COL_O, sdesc_sw128(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                     sdesc_sw128(aV + kk * 2048, kAtom, 1024), idPV, (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk) {
+          tc_mma_f16(tO, sdesc_sw128(aP + kk * 32, 16, 1024), sdesc_sw128(aV + (4 * hm + kk) * 2048, kAtom, 1024),
+                     idPV, (!first || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(o_full));
+        tc_commit(smem_u32(&o_full[hm]));
         tc_commit(smem_u32(&kv_empty[kst]));
         return true;
       };
@@ -620,30 +691,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         if (!mbar_wait(smem_u32(q_full), j & 1, abort_flag, p.status)) break;
         for (int t = 0; t < w.NT && ok; ++t) {
           const int gi = gt + t;
-          const int st = gi & 1;            // S buffer
+          const int sb = gi & 1;              // S buffer
           const int kst = gi % C::KV_STAGES;  // K/V stage
           if (!mbar_wait(smem_u32(&kv_full[kst]), (gi / C::KV_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&s_free[st]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&s_free[2 * hm + sb]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          // Before the unit's second S (or its only P V): both halves have
+          // read the previous unit's outputs.  Waiting here, and not just
+          // before the first P V, keeps p_full exact: with S(1) not yet
+          // issued, the softmax can hand over at most block 0's P before the
+          // p_full wait below.
+          if (t == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * kst) * C::KV_BYTES);
+          const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * kst) * C::KV_BYTES + hm * C::KH_BYTES);
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
-            tc_mma_f16(tmem + st * 128,
+            tc_mma_f16(tmem + (2 * hm + sb) * 64,
                        sdesc_sw128(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                       sdesc_sw128(aK + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                       sdesc_sw128(aK + (kk >> 2) * C::KH_ATOM + (kk & 3) * 32, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&s_full[st]));
+          tc_commit(smem_u32(&s_full[2 * hm + sb]));
           if (t == w.NT - 1) tc_commit(smem_u32(q_empty));  // Q is read by no later product of this unit
           if (t >= 1 && !issue_pv(gi - 1, t == 1)) { ok = false; break; }
         }
         if (!ok) break;
+        if (w.NT == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) break;
         if (!issue_pv(gt + w.NT - 1, w.NT == 1)) break;
         gt += w.NT;
         ++j;
       }
-      tc_commit(smem_u32(drain));
+      tc_commit(smem_u32(&drain[hm]));
       int never = 0;
-      mbar_wait(smem_u32(drain), 0, &never, nullptr, 10000000ull);
+      mbar_wait(smem_u32(&drain[hm]), 0, &never, nullptr, 10000000ull);
     }
     __syncwarp();
   }
@@ -745,8 +823,14 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
   return best;
 }
 
-// SPECFOLD_FFN_PREFETCH=0 in the environment turns the FFN weight prefetch
-// of the attention's idle CTAs off.
+// SPECFOLD_FFN_PREFETCH=0 in the environment turns the weight prefetch of the
+// attention's idle CTAs (output projection and FFN) off;
+// SPECFOLD_PREFETCH_WO=0 leaves the output projection's weight out, and
+// SPECFOLD_FFN_PREFETCH_MB sets the FFN share (default 40 MB).
+static int env_int(const char* name, int dflt) {
+  const char* e = std::getenv(name);
+  return e ? std::atoi(e) : dflt;
+}
 bool ffn_prefetch_enabled() {
   static const bool on = [] {
     const char* e = std::getenv("SPECFOLD_FFN_PREFETCH");
@@ -778,7 +862,8 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
     // contiguous: the map spans the P prefix tokens; paged: the whole pool
     const uint64_t tokens = c.pk.block_table ? static_cast<uint64_t>(c.pk.num_pages) * c.pk.page_size : c.P;
     const uint64_t vtokens = c.pv.block_table ? static_cast<uint64_t>(c.pv.num_pages) * c.pv.page_size : c.P;
-    rc = make_map_3d(&p.mapK, c.pk.ptr, HD, c.n_kv, tokens, c.pk.head_stride, c.pk.token_stride, 128);
+    // K in 64-token boxes (the kernel stores a block's K half by half)
+    rc = make_map_3d(&p.mapK, c.pk.ptr, HD, c.n_kv, tokens, c.pk.head_stride, c.pk.token_stride, 64);
     if (rc) return rc;
     rc = make_map_3d(&p.mapV, c.pv.ptr, HD, c.n_kv, vtokens, c.pv.head_stride, c.pv.token_stride, 128);
     if (rc) return rc;
@@ -827,10 +912,17 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
     p.part_o = static_cast<float*>(c.part);
     p.part_ml = p.part_o + static_cast<size_t>(cap) * 128 * HD;
   }
-  if (smem_limit_once(attn_kernel<HD>, C::SMEM_BYTES)) return SPECFOLD_ECUDA;
+  if (const int rc = smem_limit_once(attn_kernel<HD>, C::SMEM_BYTES)) return rc;
   // FFN weight prefetch by CTAs without a unit: the leading k-blocks of the
   // gate and up weights, about 40 MB (well inside L2 next to the output
   // projection's weights and the layer's activations)
+  static const int pf_wo = env_int("SPECFOLD_PREFETCH_WO", 1);
+  static const int pf_ffn_mb = env_int("SPECFOLD_FFN_PREFETCH_MB", 40);
+  if (pf_wo && c.wo && c.wo_rows % 128 == 0 && c.wo_cols % 64 == 0 && ffn_prefetch_enabled() &&
+      make_map_2d(&p.pf_omap, c.wo, c.wo_rows, c.wo_cols, c.wo_cols, 128) == SPECFOLD_OK) {
+    p.pf_orb = c.wo_rows / 128;
+    p.pf_okb = c.wo_cols / 64;
+  }
   if (c.ffn_w[0] && c.ffn_w[1] && c.ffn_F % 128 == 0 && c.ffn_d % 64 == 0 && ffn_prefetch_enabled()) {
     bool ok = true;
     for (int m = 0; m < 2; ++m)
@@ -839,12 +931,14 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
       p.pf_n = 2;
       p.pf_rb = c.ffn_F / 128;
       const long long box_bytes = 128LL * 64 * 2;
-      p.pf_kb = static_cast<int>(std::min<long long>(c.ffn_d / 64, (40LL << 20) / (2LL * p.pf_rb * box_bytes)));
+      p.pf_kb = static_cast<int>(
+          std::min<long long>(c.ffn_d / 64, (static_cast<long long>(std::max(pf_ffn_mb, 0)) << 20) / (2LL * p.pf_rb * box_bytes)));
+      if (p.pf_kb <= 0) p.pf_n = 0;
     }
   }
   // persistent: at most one CTA per SM, each looping over the live units
   // (every SM when CTAs without a unit have weights to prefetch)
-  const dim3 grid(p.pf_n > 0 ? p.num_sms : std::min(units_max, p.num_sms));
+  const dim3 grid(p.pf_n > 0 || p.pf_orb > 0 ? p.num_sms : std::min(units_max, p.num_sms));
   launch_k(attn_kernel<HD>, dim3(grid), dim3(kAttnThreads), C::SMEM_BYTES, st, p);
   count_launch();
   if (check_launch()) return SPECFOLD_ECUDA;

@@ -744,26 +744,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 // Slice j of J of the dependents is filled (the dependents of a source are
 // split evenly between J threads when the folded rows far outnumber the
 // packed ones, so a few sources with many dependents do not serialise).
+// The caller passes the source row s = row_idx[k] and its dependents' range
+// rg; the source's input columns go out with the first four folded rows'
+// indices, then those rows' inputs (four at a time).
 template <int BN, int EPI>
-SF_DEV void fill_dependents(const GemmParams& p, int k, int c, const float (&yb)[8], int j = 0, int J = 1) {
-  const int s = p.row_idx[k];
-  const int2 rg = reinterpret_cast<const int2*>(p.dep_rng)[s];
+SF_DEV void fill_dependents(const GemmParams& p, int s, int2 rg, int c, const float (&yb)[8], int j = 0, int J = 1) {
   const int len = rg.y - rg.x;
   const int d0 = rg.x + (len * j) / J, d1 = rg.x + (len * (j + 1)) / J;
   if (d1 <= d0) return;
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
-  float hs[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) hs[e] = 0.f;
-  add_bf16<8>(p.hin + static_cast<size_t>(s) * p.ldy + c, hs);
+  const uint4 hsv = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(s) * p.ldy + c));
   for (int j0 = d0; j0 < d1; j0 += 4) {
     uint4 hr[4];
     int rr[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      rr[q] = j0 + q < d1 ? p.dep_rows[j0 + q] : -1;
+    for (int q = 0; q < 4; ++q) rr[q] = j0 + q < d1 ? p.dep_rows[j0 + q] : -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
       if (rr[q] >= 0) hr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(rr[q]) * p.ldy + c));
-    }
+    float hs[8];
+    hs[0] = bf16lo(hsv.x); hs[1] = bf16hi(hsv.x); hs[2] = bf16lo(hsv.y); hs[3] = bf16hi(hsv.y);
+    hs[4] = bf16lo(hsv.z); hs[5] = bf16hi(hsv.z); hs[6] = bf16lo(hsv.w); hs[7] = bf16hi(hsv.w);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if (rr[q] < 0) continue;
@@ -778,7 +779,9 @@ SF_DEV void fill_dependents(const GemmParams& p, int k, int c, const float (&yb)
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
+// (At most 128 registers a thread, so that a block of it fits on an SM beside
+// the GEMM CTA it follows and starts early under programmatic launch.)
+__global__ void __launch_bounds__(256, 2) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
@@ -803,16 +806,34 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
     const int nt = c / TW, tc = c - nt * TW;
     const int m = k / kBM, row = k - m * kBM;
     int S = 1, slot0 = 0;
-    if (!tile_split(sc, m, nt, p.Nt, S, slot0)) {
+    const bool split = tile_split(sc, m, nt, p.Nt, S, slot0);
+    // fold-fill: the source row's index first; its dependents' range and the
+    // residual go out with the first batch of partials
+    int srow = 0;
+    int2 rg = make_int2(0, 0);
+    uint4 resv = make_uint4(0, 0, 0, 0);
+    auto fill_info = [&]() {
+      if constexpr (EPI == EPI_RESID_SCATTER) {
+        if (fill) {
+          rg = reinterpret_cast<const int2*>(p.dep_rng)[srow];
+          if (split)
+            resv = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
+                                                        static_cast<size_t>(k) * p.ldr + c));
+        }
+      }
+    };
+    if constexpr (EPI == EPI_RESID_SCATTER)
+      if (fill) srow = p.row_idx[k];
+    if (!split) {
+      fill_info();
       if constexpr (EPI == EPI_RESID_SCATTER) {
         // unsplit tile: the GEMM epilogue wrote Y[s]; fill the dependents only
-        const int2 rg = fill ? reinterpret_cast<const int2*>(p.dep_rng)[p.row_idx[k]] : make_int2(0, 0);
         if (rg.y > rg.x) {
           float yb[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) yb[e] = 0.f;
-          add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + c, yb);
-          fill_dependents<BN, EPI>(p, k, c, yb, jsl, J);
+          add_bf16<8>(static_cast<const __nv_bfloat16*>(p.Y) + static_cast<size_t>(srow) * p.ldy + c, yb);
+          fill_dependents<BN, EPI>(p, srow, rg, c, yb, jsl, J);
         }
       }
       continue;
@@ -837,6 +858,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
           }
         }
       }
+      if (s0 == 0) fill_info();
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (s0 + q < S) {
@@ -863,13 +885,13 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
     if constexpr (EPI == EPI_RESID_SCATTER) {
       if (fill) {
         // the residual add and the bf16 rounding of the stored row, then the fill
-        const int cc = nt * TW + tc;
-        add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(k) * p.ldr + cc, v);
-        if (jsl == 0) store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(p.row_idx[k]) * p.ldy + cc, v);
+        v[0] += bf16lo(resv.x); v[1] += bf16hi(resv.x); v[2] += bf16lo(resv.y); v[3] += bf16hi(resv.y);
+        v[4] += bf16lo(resv.z); v[5] += bf16hi(resv.z); v[6] += bf16lo(resv.w); v[7] += bf16hi(resv.w);
+        if (jsl == 0) store_bf16<8>(static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(srow) * p.ldy + c, v);
         float yb[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) yb[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-        fill_dependents<BN, EPI>(p, k, cc, yb, jsl, J);
+        fill_dependents<BN, EPI>(p, srow, rg, c, yb, jsl, J);
         continue;
       }
     }
@@ -877,35 +899,51 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const __grid_constan
   }
 }
 
-// Output-projection finish (S6 + S7): one block per packed row k.  When the
-// GEMM was split, sums the partials in split order, adds the residual row
-// H[row_idx[k]] and writes A[k] (bf16); when it was not, A[k] is already
-// written by the GEMM epilogue.  Either way the block then RMS-normalises the
-// bf16 row: X2[k] = A[k] * g2 / sqrt(mean(A[k]^2) + eps).
+// Output-projection finish (S6 + S7): one block per packed row k, one thread
+// per 8 output columns (GPT groups of 8 when the row is wider than the
+// block).  When the GEMM was split, sums the partials in split order, adds the
+// residual row H[row_idx[k]] and writes A[k] (bf16); when it was not, A[k] is
+// already written by the GEMM epilogue.  Either way the block then
+// RMS-normalises the bf16 row: X2[k] = A[k] * g2 / sqrt(mean(A[k]^2) + eps).
+// The gains are weights, read before the wait on the GEMM; after it, the
+// packed-row count and the row index come in one round trip, the residual row
+// and the first four splits of every partial in the next.  At most 64
+// registers a thread, so that a block fits on an SM beside the GEMM CTA it
+// follows and starts early under programmatic launch.
 template <int BN, int GPT>
-__global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_constant__ GemmParams p, int gemm_grid,
+__global__ void __launch_bounds__(512, 2) outproj_finish_kernel(const __grid_constant__ GemmParams p, int gemm_grid,
                                                              const __nv_bfloat16* __restrict__ g2, float eps,
                                                              __nv_bfloat16* __restrict__ X2) {
-  __shared__ float s_red[8];
+  __shared__ float s_red[16];
+  const int k = blockIdx.x;
+  const int groups = p.N / 8;
+  const int nthr = static_cast<int>(blockDim.x);
+  uint4 gv[GPT];
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int gi = threadIdx.x + nthr * j;
+    gv[j] = gi < groups ? __ldg(reinterpret_cast<const uint4*>(g2 + gi * 8)) : make_uint4(0, 0, 0, 0);
+  }
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const int k = blockIdx.x;
+  const int r = p.row_idx[k];  // k < Mcap: in bounds; used only when k < n
   if (k >= n) return;
   const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
-  const int groups = p.N / 8;
   const int m = k / kBM, row = k - m * kBM;
   __nv_bfloat16* Arow = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(k) * p.ldy;
   float v[GPT][8];
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < GPT; ++j) {
-    const int gi = threadIdx.x + 256 * j;
+    const int gi = threadIdx.x + nthr * j;
     if (gi >= groups) break;
     const int c = gi * 8;
     const int nt = c / BN, tc = c - nt * BN;
     int S = 1, slot0 = 0;
     if (tile_split(sc, m, nt, p.Nt, S, slot0)) {
+      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
+                                                            static_cast<size_t>(r) * p.ldr + c));
       const float* base = p.partial + static_cast<size_t>(slot0) * kBM * BN + static_cast<size_t>(row) * BN + tc;
       float acc[8];
 #pragma unroll
@@ -926,7 +964,8 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
             acc[4] += a4[q][1].x; acc[5] += a4[q][1].y; acc[6] += a4[q][1].z; acc[7] += a4[q][1].w;
           }
       }
-      add_bf16<8>(static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(p.row_idx[k]) * p.ldr + c, acc);
+      acc[0] += bf16lo(rv.x); acc[1] += bf16hi(rv.x); acc[2] += bf16lo(rv.y); acc[3] += bf16hi(rv.y);
+      acc[4] += bf16lo(rv.z); acc[5] += bf16hi(rv.z); acc[6] += bf16lo(rv.w); acc[7] += bf16hi(rv.w);
       store_bf16<8>(Arow + c, acc);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[j][e] = __bfloat162float(__float2bfloat16_rn(acc[e]));
@@ -943,15 +982,14 @@ __global__ void __launch_bounds__(256) outproj_finish_kernel(const __grid_consta
   if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) tot += s_red[w];
+  for (int w = 0; w < nthr / 32; ++w) tot += s_red[w];
   const float inv = rsqrtf(tot / static_cast<float>(p.N) + eps);
 #pragma unroll
   for (int j = 0; j < GPT; ++j) {
-    const int gi = threadIdx.x + 256 * j;
+    const int gi = threadIdx.x + nthr * j;
     if (gi >= groups) break;
     const int c = gi * 8;
-    const uint4 gu = __ldg(reinterpret_cast<const uint4*>(g2 + c));
+    const uint4 gu = gv[j];
     float o[8];
     o[0] = v[j][0] * inv * bf16lo(gu.x); o[1] = v[j][1] * inv * bf16hi(gu.x);
     o[2] = v[j][2] * inv * bf16lo(gu.y); o[3] = v[j][3] * inv * bf16hi(gu.y);
@@ -1056,9 +1094,8 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
     }
   }
 
-  if (smem_limit_once(gemm_kernel<BN, EPI, false>, Cf::SMEM_BYTES) ||
-      smem_limit_once(gemm_kernel<BN, EPI, true>, Cf::SMEM_BYTES))
-    return SPECFOLD_ECUDA;
+  if (const int rc = smem_limit_once(gemm_kernel<BN, EPI, false>, Cf::SMEM_BYTES)) return rc;
+  if (const int rc = smem_limit_once(gemm_kernel<BN, EPI, true>, Cf::SMEM_BYTES)) return rc;
   // schedule table for the plain grid (a clustered launch computes its own
   // split and sums it inside the GEMM)
   const bool any_split = fill_sched(p, c.Mcap, min(num_sms(), kMaxGrid));
@@ -1081,16 +1118,16 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
   if constexpr (EPI == EPI_RESID_PACKED) {
     if (rn) {
       const int groups = c.N / 8;
-      if (groups > 4 * 256 || c.N % 8) return SPECFOLD_EUNSUPPORTED;
-      const dim3 g(c.Mcap), b(256);
+      if (groups > 2 * 512 || c.N % 8) return SPECFOLD_EUNSUPPORTED;
+      // one thread per group up to 512 groups, two beyond
+      const int threads = std::min(512, (groups + 31) / 32 * 32);
+      const dim3 g(c.Mcap), b(threads);
       const __nv_bfloat16* g2 = static_cast<const __nv_bfloat16*>(rn->gain);
       __nv_bfloat16* x2 = static_cast<__nv_bfloat16*>(rn->out);
-      if (groups <= 256)
+      if (groups <= threads)
         launch_k(outproj_finish_kernel<BN, 1>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
-      else if (groups <= 512)
-        launch_k(outproj_finish_kernel<BN, 2>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       else
-        launch_k(outproj_finish_kernel<BN, 4>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
+        launch_k(outproj_finish_kernel<BN, 2>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       count_launch();
       return check_launch();
     }
@@ -1276,7 +1313,7 @@ int run_linear_noalloc(const void* X, const void* W, int M, int N, int K, void* 
   p.g = 1;
   p.partial = static_cast<float*>(scratch);  // written in full before it is read: nothing to clear
   p.status = nullptr;
-  if (smem_limit_once(gemm_kernel<BN, EPI_STORE, false>, Cf::SMEM_BYTES)) return SPECFOLD_ECUDA;
+  if (const int rc = smem_limit_once(gemm_kernel<BN, EPI_STORE, false>, Cf::SMEM_BYTES)) return rc;
   const bool any_split = fill_sched(p, M, grid);
   launch_k(gemm_kernel<BN, EPI_STORE, false>, dim3(grid), dim3(kGemmThreads), Cf::SMEM_BYTES, st, p);
   count_launch();

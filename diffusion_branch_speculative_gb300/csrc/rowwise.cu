@@ -794,6 +794,31 @@ SF_DEV int chain_end_smem(const uint8_t* f, const int* par, int b, int i, int L,
   return s;
 }
 
+// The dependents lists of block position i for a draft graph of at most 32
+// branches, in one warp (lane b = branch b): the same outputs as the block
+// loop at the end of gate_pack_kernel, with each source's folded rows in
+// ascending branch order.
+SF_DEV void deps_warp(const GatePackArgs& a, const uint8_t* f, const int* par, int i, int L, int B, int lane) {
+  const bool on = lane < B;
+  const int sb = on ? (f[lane * L + i] ? chain_end_smem(f, par, lane, i, L, B) : lane) : -1;
+  const unsigned grp = __match_any_sync(0xffffffffu, sb);  // lanes that share this source
+  const bool is_src = on && sb == lane;
+  const int cnt = is_src ? __popc(grp) - 1 : 0;
+  int inc = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  const int start = inc - cnt;  // first slot of this source's group
+  if (is_src) reinterpret_cast<int2*>(a.dep_rng)[lane * L + i] = make_int2(i * B + start, i * B + start + cnt);
+  const int sstart = __shfl_sync(0xffffffffu, start, on ? sb : 0);
+  if (on && !is_src) {
+    const int rank = __popc(grp & ((1u << lane) - 1u) & ~(1u << sb));
+    a.dep_rows[i * B + sstart + rank] = lane * L + i;
+  }
+}
+
 template <typename T>
 SF_DEV void accum_gate(const uint4& c, const uint4& q, float& num, float& den) {
   using V = VecT<T>;
@@ -846,6 +871,7 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   __shared__ volatile int s_flag;
   __shared__ volatile int s_abort;
   __shared__ __align__(8) uint64_t s_bar;
+  __shared__ __align__(8) uint64_t s_gbar;  // the gains' copy
   const int B = a.B, L = a.L, d = a.d, R = B * L;
   const int nv = d / V::N;  // 16-byte vectors per row
   const uint32_t rowb = static_cast<uint32_t>(d) * sizeof(T);
@@ -858,15 +884,18 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   int* s_c1 = reinterpret_cast<int*>(s_fold + ((R + 15) & ~15));  // [max(B, chunk)]
   int* s_c2 = s_c1 + max(B, a.chunk);                              // [B]
   int* s_c3 = s_c2 + B;                                            // [B]
-  const uint32_t bar = smem_u32(&s_bar);
+  const uint32_t bar = smem_u32(&s_bar), gbar = smem_u32(&s_gbar);
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(gbar, 1);
     fence_mbar_init();
     s_abort = 0;
     s_bad = 0;
+    // gains: weights, independent of earlier kernels; needed only by the
+    // RMSNorm after the grid barrier, so nothing waits for them until then
+    mbar_arrive_expect_tx(gbar, rowb);
+    bulk_load(smem_u32(s_g), a.g1, rowb, gbar);
   }
-  // gains: weights, independent of earlier kernels
-  for (int v = tid; v < nv; v += kGPThreads) s_g[v] = __ldg(reinterpret_cast<const uint4*>(a.g1) + v);
   pdl_wait();
   __syncthreads();
 
@@ -936,9 +965,10 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   if (lane == 0) s_warp[w] = act_here;
   __syncthreads();
   if (s_abort) {  // a copy never landed: give the last ones a short bound, then leave
-    if (tid == 0 && issued_bt >= 0) {
+    if (tid == 0) {
       int never = 0;
-      mbar_wait(bar, issued_bt & 1, &never, nullptr, 10000000ull);
+      if (issued_bt >= 0) mbar_wait(bar, issued_bt & 1, &never, nullptr, 10000000ull);
+      mbar_wait(gbar, 0, &never, nullptr, 10000000ull);
     }
     return;
   }
@@ -948,7 +978,13 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
     a.cta_cnt[blockIdx.x] = t;
     if (blockIdx.x == 0 && s_bad && a.status) atomicOr(a.status, SPECFOLD_DEV_BAD_PARENT);
   }
-  if (!grid_barrier(a.bar, a.status, &s_flag)) return;
+  if (!grid_barrier(a.bar, a.status, &s_flag)) {
+    if (tid == 0) {  // the gains' copy targets this CTA's shared memory
+      int never = 0;
+      mbar_wait(gbar, 0, &never, nullptr, 10000000ull);
+    }
+    return;
+  }
   pdl_trigger();
 
   // ---------------------------------------------------- phase 2: pack --
@@ -989,18 +1025,24 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
     a.n_dev[0] = n;
     if (a.n_hist) a.n_hist[0] = n;
   }
+  // with at most 32 branches and a warp to spare, the last warp builds the
+  // dependents lists of this CTA's block positions while the others write X1
+  const bool deps_by_warp = HOLD && B <= 32 && nch < kGPWarps;
+  if (deps_by_warp && w == kGPWarps - 1)
+    for (int i = blockIdx.x; i < L; i += gridDim.x) deps_warp(a, s_fold, s_par, i, L, B, lane);
   // RMSNorm1 of this CTA's recomputed rows: X1[k] = H[r] * g1 / rms(H[r])
   T* X1 = static_cast<T*>(a.X1);
   if constexpr (HOLD) {
     const int r = c0 + w;
-    if (w < nch && !s_fold[r]) {
+    if (w < nch && !s_fold[r] && mbar_wait(gbar, 0, &s_abort, a.status)) {
       const float inv = rsqrtf(ss_hold / static_cast<float>(d) + a.eps);
       const uint4* x = s_rows + static_cast<size_t>(w) * nv;
       uint4* y = reinterpret_cast<uint4*>(X1 + static_cast<size_t>(nb + s_c1[w]) * d);
       for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(x[v], s_g[v], inv);
     }
   } else {
-    for (int t = w; t < nch; t += kGPWarps) {
+    const bool g_ok = mbar_wait(gbar, 0, &s_abort, a.status);
+    for (int t = w; t < nch && g_ok; t += kGPWarps) {
       const int r = c0 + t;
       if (s_fold[r]) continue;
       const uint4* x = reinterpret_cast<const uint4*>(H + static_cast<size_t>(r) * d);
@@ -1019,6 +1061,7 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
       for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(__ldg(x + v), s_g[v], inv);
     }
   }
+  if (deps_by_warp) return;
   // folded rows grouped by source, one block position at a time
   for (int i = blockIdx.x; i < L; i += gridDim.x) {
     __syncthreads();  // the arrays are free again
@@ -1108,7 +1151,8 @@ constexpr int kGPMaxSmem = 200 * 1024;  // the launcher's bound on the kernel's 
 template <typename T, int MAXV, bool HOLD>
 static int gate_pack_go(const GatePackArgs& a, int grid, size_t smem, cudaStream_t st) {
   // the limit is raised once per device, to the largest size any shape asks for
-  if (smem > 48 * 1024 && smem_limit_once(gate_pack_kernel<T, MAXV, HOLD>, kGPMaxSmem)) return SPECFOLD_ECUDA;
+  if (smem > 48 * 1024)
+    if (const int rc = smem_limit_once(gate_pack_kernel<T, MAXV, HOLD>, kGPMaxSmem)) return rc;
   launch_k(gate_pack_kernel<T, MAXV, HOLD>, dim3(grid), dim3(kGPThreads), smem, st, a);
   count_launch();
   return check_launch();

@@ -143,6 +143,8 @@ struct AttnCall {
   // their leading k-blocks into L2 for the FFN GEMM
   const void* ffn_w[2];
   int ffn_F, ffn_d;
+  const void* wo;        // output-projection weight [wo_rows, wo_cols], prefetched before the FFN's
+  int wo_rows, wo_cols;
 };
 int attn_slot_cap(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);

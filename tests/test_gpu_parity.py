@@ -515,6 +515,8 @@ def _gate_pack_case(levels, L, d, frac, tau=0.05, fanout=None):
     ((1, 8, 55), 32, 3584, 1.0),        # the stress size, every row recomputed
     ((1, 8, 55), 32, 3584, 0.25),
     ((1, 8, 64, 439), 32, 256, 0.25),   # 16384 rows (the row limit): many rows per CTA
+    ((1, 2, 3, 2), 32, 3584, 0.25),     # 8 branches, depth 3: the dependents lists built by one warp
+    ((1, 4, 11, 16), 32, 3584, 0.5),    # 32 branches: the largest graph the one-warp lists take
 ])
 def test_gate_pack_entry_point(levels, L, d, frac):
     """specfold_gate_pack against the oracle: decisions, sources, packed list
