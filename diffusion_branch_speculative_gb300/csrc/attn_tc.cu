@@ -824,9 +824,10 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
 }
 
 // SPECFOLD_FFN_PREFETCH=0 in the environment turns the weight prefetch of the
-// attention's idle CTAs (output projection and FFN) off;
-// SPECFOLD_PREFETCH_WO=0 leaves the output projection's weight out, and
-// SPECFOLD_FFN_PREFETCH_MB sets the FFN share (default 40 MB).
+// attention's idle CTAs off; SPECFOLD_FFN_PREFETCH_MB sets its FFN share
+// (default 40 MB); SPECFOLD_PREFETCH_WO=1 adds the output projection's weight
+// ahead of it (off by default: at the 7B layer it slowed the attention by
+// more than it saved in the projection).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   return e ? std::atoi(e) : dflt;
@@ -916,7 +917,7 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   // FFN weight prefetch by CTAs without a unit: the leading k-blocks of the
   // gate and up weights, about 40 MB (well inside L2 next to the output
   // projection's weights and the layer's activations)
-  static const int pf_wo = env_int("SPECFOLD_PREFETCH_WO", 1);
+  static const int pf_wo = env_int("SPECFOLD_PREFETCH_WO", 0);
   static const int pf_ffn_mb = env_int("SPECFOLD_FFN_PREFETCH_MB", 40);
   if (pf_wo && c.wo && c.wo_rows % 128 == 0 && c.wo_cols % 64 == 0 && ffn_prefetch_enabled() &&
       make_map_2d(&p.pf_omap, c.wo, c.wo_rows, c.wo_cols, c.wo_cols, 128) == SPECFOLD_OK) {

@@ -612,12 +612,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         mbar_arrive(smem_u32(&acce[ab]));
         continue;
       }
+      const int row0 = w.m * kBM + q * 32;          // first packed row of this warp
+      const int rows_here = min(32, n - row0);      // valid rows (may be <= 0)
+      if constexpr (EPI == EPI_SWIGLU || EPI == EPI_STORE) {
+        if (!w.split) {
+          // Straight from TMEM: thread `lane` owns row row0 + lane and writes
+          // each 32-column chunk of it as 64 contiguous bytes (four 16-byte
+          // stores), with no shared-memory transpose and no per-element
+          // branch (the transposed path's dependent chains left the last
+          // tile's SwiGLU epilogue exposed for several microseconds)
+          __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(row0 + lane) * p.ldy;
+          constexpr int NCH = EPI == EPI_SWIGLU ? BN / 64 : BN / 32;
+#pragma unroll 1
+          for (int ch = 0; ch < NCH; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tb + ch * 32, r);
+            uint32_t pk[16];
+            if constexpr (EPI == EPI_SWIGLU) {
+              uint32_t r2[32];
+              tmem_ld32(tb + BN / 2 + ch * 32, r2);
+              tmem_ld_wait(r);
+              tmem_ld_wait(r2);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                pk[e / 2] = pack_bf16x2(silu(__uint_as_float(r[e])) * __uint_as_float(r2[e]),
+                                        silu(__uint_as_float(r[e + 1])) * __uint_as_float(r2[e + 1]));
+            } else {
+              tmem_ld_wait(r);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+            }
+            if (lane < rows_here) {
+              const int c = (EPI == EPI_SWIGLU ? w.nt * (BN / 2) : w.nt * BN) + ch * 32;
+              uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) dst[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&acce[ab]));
+          continue;
+        }
+      }
       // Each 32-column chunk of the warp's 32 rows goes through a padded smem
       // transpose so that lane j then handles column j of one row at a time:
       // every store (and residual load) of the warp is one contiguous segment.
       float* stg = epi_stage + q * (32 * 33);
-      const int row0 = w.m * kBM + q * 32;          // first packed row of this warp
-      const int rows_here = min(32, n - row0);      // valid rows (may be <= 0)
       // lane j holds the row index of the warp's row j (broadcast by shuffle)
       int ridx = 0;
       if constexpr (EPI == EPI_QKV || EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER)
