@@ -314,7 +314,8 @@ def run_ours(args, rank, world):
     clocks = sampler.stop(t0, t1)
     # per-stage breakdown (graph with event-record nodes at stage boundaries)
     _, _, _, stages, _ = timed_steps(args.tau, max(50, min(args.steps, 500)), 5, stage_events=True)
-    assert lay.status() == 0, "device status set"
+    st = lay.status()
+    assert st == 0, f"device status {st:#x}: {binding.timeout_sites(st)}"
     n = lay.n_packed()
     total_ms_max = reduce_max(total_ms, world)
     value = aggregate_rate(B * L, args.steps, world, total_ms_max)
@@ -630,7 +631,8 @@ def layer_leg(args, name, flush, barrier):
                                                   "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                                                   "frac": round(tf / peaks["bf16_tflops"], 4)}
     res["time_vs_dense"] = round(res["folded_us"] / res["dense_us"], 4)
-    assert lay.status() == 0, "device status set"
+    st = lay.status()
+    assert st == 0, f"device status {st:#x}: {binding.timeout_sites(st)}"
     del lay, W, cache
     torch.cuda.empty_cache()
     return res

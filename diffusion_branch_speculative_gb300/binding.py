@@ -20,6 +20,21 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "specfold.h")
 
 OK, EINVAL, EALIGN, ECAPACITY, EUNSUPPORTED, ECUDA, EDEVICE = 0, -1, -2, -3, -4, -5, -6
 DEV_TIMEOUT, DEV_BAD_PARENT, DEV_BAD_PAGE = 1, 2, 4
+DEV_SITE_SHIFT = 8  # with DEV_TIMEOUT: bit DEV_SITE_SHIFT + site names the wait that ran out
+DEV_SITES = ("attention loader: Q buffer free", "attention loader: K/V stage free", "attention softmax: S ready",
+             "attention softmax: P V before a rescale", "attention softmax: P V before the last P",
+             "attention softmax: last P V", "attention MMA: P ready", "attention MMA: Q loaded",
+             "attention MMA: K/V loaded", "attention MMA: S buffer free", "attention MMA: accumulators free",
+             "GEMM producer: stage free", "GEMM MMA: accumulator free", "GEMM MMA: stage loaded",
+             "GEMM epilogue: accumulator ready", "gate/pack: row copies", "gate/pack: gains copy",
+             "gate/pack: grid barrier", "timeout probe")
+
+
+def timeout_sites(status: int) -> list:
+    """The waits a device status word says ran out (empty without DEV_TIMEOUT)."""
+    if not status & DEV_TIMEOUT:
+        return []
+    return [nm for i, nm in enumerate(DEV_SITES) if status >> (DEV_SITE_SHIFT + i) & 1]
 BF16, F32 = 0, 1
 STAGE_EVENTS = 9
 STAGE_NAMES = ("gate", "select_pack", "qkv", "attention", "out_proj_norm", "gate_up", "down", "fold_fill")

@@ -81,6 +81,7 @@ struct AttnParams {
   int pf_orb, pf_okb;
   CUtensorMap pf_map[2];
   int pf_n, pf_rb, pf_kb;
+  int pf_pace_ns;  // pause between one idle CTA's prefetches (queues stay short for the working CTAs' loads)
 };
 
 // Number of key-range splits for n packed rows, looked up from a table the
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   // loads and stores)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   // barriers, flags and the halves' exchange slots in static shared memory
-  __shared__ __align__(8) uint64_t bars[24];
+  __shared__ __align__(8) uint64_t bars[25];
   __shared__ uint32_t tmem_slot_s;
   __shared__ volatile int abort_s;
   __shared__ volatile int okflag[C::KV_STAGES];
@@ -185,11 +186,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   uint64_t* kv_empty = bars + 4;  // [KV_STAGES]: both halves' P V of the block are done
   uint64_t* s_full = bars + 7;    // [half][2]
   uint64_t* s_free = bars + 11;   // [half][2]
-  uint64_t* p_full = bars + 15;   // [half]
-  uint64_t* o_full = bars + 17;   // [half]: one completion per P V product of the half
-  uint64_t* q_empty = bars + 19;  // both halves' S products of a unit are done: Q may be replaced
-  uint64_t* o_empty = bars + 20;  // the softmax warps have read a unit's outputs
-  uint64_t* drain = bars + 21;    // [half]
+  // [half][gi & 1]: two, alternating by block like the S buffers, so that a
+  // barrier never runs two phases ahead of the MMA warp that waits on it
+  // (the softmax may hand over P of blocks t and t + 1 before that warp, which
+  // issued S(t + 1) first, gets to its wait for P(t))
+  uint64_t* p_full = bars + 15;
+  uint64_t* o_full = bars + 19;   // [half]: one completion per P V product of the half
+  uint64_t* q_empty = bars + 21;  // both halves' S products of a unit are done: Q may be replaced
+  uint64_t* o_empty = bars + 22;  // the softmax warps have read a unit's outputs
+  uint64_t* drain = bars + 23;    // [half]
   uint32_t* tmem_slot = &tmem_slot_s;
   volatile int* abort_flag = &abort_s;
 
@@ -214,7 +219,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const int idle = static_cast<int>(gridDim.x) - U, me = static_cast<int>(blockIdx.x) - U;
       const int boxes_o = p.pf_orb * p.pf_okb;
       const int boxes = boxes_o + p.pf_n * p.pf_rb * p.pf_kb;
+      // the pauses of one CTA add up to at most 8 us, whatever its share of
+      // the boxes: the attention's launch ends only when this loop does
+      const int share = (boxes - me + idle - 1) / idle;
+      const int pace = min(p.pf_pace_ns, 8000 / max(share, 1));
       for (int q = me; q < boxes; q += idle) {
+        if (pace > 0 && q != me) __nanosleep(pace);
         if (q < boxes_o) {
           const int kb = q / p.pf_orb, rb = q - kb * p.pf_orb;
           tma_prefetch_2d(&p.pf_omap, kb * 64, rb * 128);
@@ -241,8 +251,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), 128);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&p_full[i]), 128);
     for (int h = 0; h < 2; ++h) {
-      mbar_init(smem_u32(&p_full[h]), 128);
       mbar_init(smem_u32(&o_full[h]), 1);
       mbar_init(smem_u32(&drain[h]), 1);
     }
@@ -285,17 +295,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const bool may_be_empty = SP > NBP + 1;
       if (lt == 0 && !may_be_empty) {
         // the previous unit's S products must be done with the Q buffer
-        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status)) {
+        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnQEmpty)) {
           mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
           for (int a = 0; a < C::NATOM; ++a)
             tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + w.m0);
           issued_q = j;
         }
       }
-      attn_unit_keys(p, w, n, SP);
+      // An unsplit unit starts with the whole prefix, so its first block goes
+      // out before the packed-row reads that size its block keys (their
+      // round trip then overlaps that block's load)
+      bool keys_known = SP > 1 || NBP == 0;
+      if (keys_known) {
+        attn_unit_keys(p, w, n, SP);
+      } else {
+        w.jb = 0;
+        w.NT = NBP + 1;  // a lower bound: at least one block of branch keys follows
+      }
       if (w.NT == 0) continue;
       if (lt == 0 && may_be_empty) {
-        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status)) {
+        if (j == 0 || mbar_wait(smem_u32(q_empty), (j - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnQEmpty)) {
           mbar_arrive_expect_tx(smem_u32(q_full), C::Q_BYTES);
           for (int a = 0; a < C::NATOM; ++a)
             tma_load_2d(smem_u32(sQ + a * kAtom), &p.mapQ, smem_u32(q_full), a * 64, h * p.R * g + w.m0);
@@ -303,10 +322,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
       }
       for (int t = 0; t < w.NT; ++t, ++gt) {
+        if (!keys_known && t == 1) {
+          attn_unit_keys(p, w, n, SP);  // the same NT every other role computed
+          keys_known = true;
+        }
         const int jblk = w.jb + t;
         const int st = gt % C::KV_STAGES;
         if (lt == 0)
-          okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt / C::KV_STAGES) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+          okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt / C::KV_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitLimitNs,
+                               kSiteAttnKvEmpty) ? 1 : 0;
         named_bar_sync(1, kLoaders);
         if (!okflag[st]) {
           ok = false;
@@ -437,7 +461,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         const bool prefix = jblk < NBP;
         // every wait's outcome is made warp-uniform: a lane whose wait ran out
         // takes its whole warp along
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[2 * hf + sb]), (gi >> 1) & 1, abort_flag, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[2 * hf + sb]), (gi >> 1) & 1, abort_flag, p.status, kWaitLimitNs,
+                                                         kSiteAttnSFull))) {
           ok = false;
           break;
         }
@@ -504,7 +529,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         bool rescale_waited = false;
         if (t >= 1 && __any_sync(0xffffffffu, rescale)) {
           rescale_waited = true;
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnRescale))) {
             ok = false;
             break;
           }
@@ -564,18 +589,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // it before handing over its P: afterwards only the last P V is out,
         // and the wait for it after the loop is exact too.
         if (t == w.NT - 1 && t >= 1 && !rescale_waited) {
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&o_full[hf]), (gi - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnLastP))) {
             ok = false;
             break;
           }
         }
         tc_fence_before();
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&p_full[hf]));
+        mbar_arrive(smem_u32(&p_full[2 * hf + sb]));
       }
       // the half's last P V product (the one before it is done, see above)
       const int glast = gt + w.NT - 1;
-      const bool oku = ok && mbar_wait(smem_u32(&o_full[hf]), glast & 1, abort_flag, p.status);
+      const bool oku = ok && mbar_wait(smem_u32(&o_full[hf]), glast & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnEnd);
       // the halves' meeting at the end of the unit: both leave together or
       // neither (a wait that ran out must not strand the other half at a
       // barrier).  Half 1 hands its (m, l) to half 0, which computes the merge
@@ -671,7 +696,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       // overwrites O_h: the softmax warps have read the previous unit's
       // outputs by then, see the o_empty wait below)
       auto issue_pv = [&](int gi, bool first) -> bool {
-        if (!mbar_wait(smem_u32(&p_full[hm]), gi & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(smem_u32(&p_full[2 * hm + (gi & 1)]), (gi >> 1) & 1, abort_flag, p.status, kWaitLimitNs,
+                       kSiteAttnPFull))
+          return false;
         tc_fence_after();
         const int kst = gi % C::KV_STAGES;
         const uint32_t aP = smem_u32(smem + C::p_off(kst, hm));
@@ -688,19 +715,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
         const AUnit w = attn_unit(p, u, n, tiles_x, SP);
         if (w.NT == 0) continue;
-        if (!mbar_wait(smem_u32(q_full), j & 1, abort_flag, p.status)) break;
+        if (!mbar_wait(smem_u32(q_full), j & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnQFull)) break;
         for (int t = 0; t < w.NT && ok; ++t) {
           const int gi = gt + t;
           const int sb = gi & 1;              // S buffer
           const int kst = gi % C::KV_STAGES;  // K/V stage
-          if (!mbar_wait(smem_u32(&kv_full[kst]), (gi / C::KV_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
-          if (!mbar_wait(smem_u32(&s_free[2 * hm + sb]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&kv_full[kst]), (gi / C::KV_STAGES) & 1, abort_flag, p.status, kWaitLimitNs,
+                         kSiteAttnKvFull)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&s_free[2 * hm + sb]), ((gi >> 1) & 1) ^ 1, abort_flag, p.status, kWaitLimitNs,
+                         kSiteAttnSFree)) { ok = false; break; }
           // Before the unit's second S (or its only P V): both halves have
           // read the previous unit's outputs.  Waiting here, and not just
           // before the first P V, keeps p_full exact: with S(1) not yet
           // issued, the softmax can hand over at most block 0's P before the
           // p_full wait below.
-          if (t == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (t == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnOEmpty)) { ok = false; break; }
           tc_fence_after();
           const uint32_t aK = smem_u32(smem + C::OFF_KV + (2 * kst) * C::KV_BYTES + hm * C::KH_BYTES);
 #pragma unroll
@@ -714,7 +743,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
           if (t >= 1 && !issue_pv(gi - 1, t == 1)) { ok = false; break; }
         }
         if (!ok) break;
-        if (w.NT == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status)) break;
+        if (w.NT == 1 && j >= 1 && !mbar_wait(smem_u32(o_empty), (j - 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteAttnOEmpty)) break;
         if (!issue_pv(gt + w.NT - 1, w.NT == 1)) break;
         gt += w.NT;
         ++j;
@@ -827,7 +856,8 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
 // attention's idle CTAs off; SPECFOLD_FFN_PREFETCH_MB sets its FFN share
 // (default 40 MB); SPECFOLD_PREFETCH_WO=1 adds the output projection's weight
 // ahead of it (off by default: at the 7B layer it slowed the attention by
-// more than it saved in the projection).
+// more than it saved in the projection); SPECFOLD_PREFETCH_PACE_NS sets the
+// pause between one idle CTA's prefetches (default 400 ns).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   return e ? std::atoi(e) : dflt;
@@ -919,6 +949,8 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   // projection's weights and the layer's activations)
   static const int pf_wo = env_int("SPECFOLD_PREFETCH_WO", 0);
   static const int pf_ffn_mb = env_int("SPECFOLD_FFN_PREFETCH_MB", 40);
+  static const int pf_pace = env_int("SPECFOLD_PREFETCH_PACE_NS", 400);
+  p.pf_pace_ns = std::max(pf_pace, 0);
   if (pf_wo && c.wo && c.wo_rows % 128 == 0 && c.wo_cols % 64 == 0 && ffn_prefetch_enabled() &&
       make_map_2d(&p.pf_omap, c.wo, c.wo_rows, c.wo_cols, c.wo_cols, 128) == SPECFOLD_OK) {
     p.pf_orb = c.wo_rows / 128;

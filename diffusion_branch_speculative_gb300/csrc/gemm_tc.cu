@@ -340,80 +340,107 @@ SF_DEV Unit decode(int u, int Mt, int S, int Nt, int KB, bool dsm) {
 // epilogue on groups of 8 columns.  The row indices were staged next to the
 // partial tile, so every global load of an item (residual row) is issued
 // before its distributed-shared-memory loads and the two latencies overlap.
-template <int BN, int EPI>
-SF_DEV void dsm_reduce(const GemmParams& p, const uint8_t* smem, int n, int Mt, int S) {
+// SC is the split count; a thread issues the loads of ITEMS items (2·SC
+// distributed-shared-memory vectors each, 16 in all) before it sums any of
+// them, so their latencies overlap too.
+template <int BN, int EPI, int SC>
+SF_DEV void dsm_reduce_sc(const GemmParams& p, const uint8_t* smem, int n, int Mt) {
   constexpr int TW = EPI == EPI_SWIGLU ? BN / 2 : BN;  // output columns per tile
   constexpr int SROW = Cfg<BN>::SROW;
+  constexpr int HALVES = EPI == EPI_SWIGLU ? 2 : 1;    // gate and up columns
+  constexpr int ITEMS = (8 / SC) / HALVES > 0 ? (8 / SC) / HALVES : 1;
   const int* s_ridx = reinterpret_cast<const int*>(smem + kBM * SROW * 4);
-  const int s = static_cast<int>(blockIdx.x) % S;
+  const int s = static_cast<int>(blockIdx.x) % SC;
   const uint32_t rank0 = cluster_ctarank() - static_cast<uint32_t>(s);
-  const int tile = static_cast<int>(blockIdx.x) / S;
+  const int tile = static_cast<int>(blockIdx.x) / SC;
   const int m = tile % Mt, nt = tile / Mt;
   const int rows = min(kBM, n - m * kBM);
-  const int share = TW / S;
-  const int groups = share / 8;
+  constexpr int share = TW / SC;
+  constexpr int groups = share / 8;
   const uint32_t sbase = smem_u32(smem);
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
   const __nv_bfloat16* Rz = static_cast<const __nv_bfloat16*>(p.resid);
-  for (int idx = threadIdx.x; idx < rows * groups; idx += kGemmThreads) {
-    const int r = idx / groups;
-    const int tc = s * share + (idx - r * groups) * 8;
-    const int k = m * kBM + r;
-    const int c = nt * TW + tc;
-    uint4 res = make_uint4(0, 0, 0, 0);
-    if constexpr (EPI == EPI_RESID_PACKED)
-      res = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(s_ridx[r]) * p.ldr + c));
-    if constexpr (EPI == EPI_RESID_SCATTER)
-      res = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(k) * p.ldr + c));
-    const uint32_t off = sbase + static_cast<uint32_t>((r * SROW + tc) * 4);
-    float4 a[kMaxClusterSplit][2], b[kMaxClusterSplit][2];
+  const int total = rows * groups;
+  for (int idx0 = threadIdx.x; idx0 < total; idx0 += ITEMS * kGemmThreads) {
+    float4 a[ITEMS][SC][2], b[ITEMS][SC][2];
+    uint4 res[ITEMS];
+    // every load of the thread's items first
 #pragma unroll
-    for (int j = 0; j < kMaxClusterSplit; ++j) {
-      if (j < S) {
+    for (int it = 0; it < ITEMS; ++it) {
+      const int idx = idx0 + it * kGemmThreads;
+      if (idx >= total) break;
+      const int r = idx / groups;
+      const int tc = s * share + (idx - r * groups) * 8;
+      const int k = m * kBM + r;
+      const int c = nt * TW + tc;
+      res[it] = make_uint4(0, 0, 0, 0);
+      if constexpr (EPI == EPI_RESID_PACKED)
+        res[it] = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(s_ridx[r]) * p.ldr + c));
+      if constexpr (EPI == EPI_RESID_SCATTER)
+        res[it] = __ldg(reinterpret_cast<const uint4*>(Rz + static_cast<size_t>(k) * p.ldr + c));
+      const uint32_t off = sbase + static_cast<uint32_t>((r * SROW + tc) * 4);
+#pragma unroll
+      for (int j = 0; j < SC; ++j) {
         const uint32_t ra = dsmem_addr(off, rank0 + j);
-        a[j][0] = ld_dsmem_f4(ra);
-        a[j][1] = ld_dsmem_f4(ra + 16);
+        a[it][j][0] = ld_dsmem_f4(ra);
+        a[it][j][1] = ld_dsmem_f4(ra + 16);
         if constexpr (EPI == EPI_SWIGLU) {
-          b[j][0] = ld_dsmem_f4(ra + (BN / 2) * 4);
-          b[j][1] = ld_dsmem_f4(ra + (BN / 2) * 4 + 16);
+          b[it][j][0] = ld_dsmem_f4(ra + (BN / 2) * 4);
+          b[it][j][1] = ld_dsmem_f4(ra + (BN / 2) * 4 + 16);
         }
       }
     }
-    float v[8], u[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = u[e] = 0.f;
+    for (int it = 0; it < ITEMS; ++it) {
+      const int idx = idx0 + it * kGemmThreads;
+      if (idx >= total) break;
+      const int r = idx / groups;
+      const int tc = s * share + (idx - r * groups) * 8;
+      const int k = m * kBM + r;
+      const int c = nt * TW + tc;
+      float v[8], u[8];
 #pragma unroll
-    for (int j = 0; j < kMaxClusterSplit; ++j) {
-      if (j < S) {
-        v[0] += a[j][0].x; v[1] += a[j][0].y; v[2] += a[j][0].z; v[3] += a[j][0].w;
-        v[4] += a[j][1].x; v[5] += a[j][1].y; v[6] += a[j][1].z; v[7] += a[j][1].w;
+      for (int e = 0; e < 8; ++e) v[e] = u[e] = 0.f;
+#pragma unroll
+      for (int j = 0; j < SC; ++j) {
+        v[0] += a[it][j][0].x; v[1] += a[it][j][0].y; v[2] += a[it][j][0].z; v[3] += a[it][j][0].w;
+        v[4] += a[it][j][1].x; v[5] += a[it][j][1].y; v[6] += a[it][j][1].z; v[7] += a[it][j][1].w;
         if constexpr (EPI == EPI_SWIGLU) {
-          u[0] += b[j][0].x; u[1] += b[j][0].y; u[2] += b[j][0].z; u[3] += b[j][0].w;
-          u[4] += b[j][1].x; u[5] += b[j][1].y; u[6] += b[j][1].z; u[7] += b[j][1].w;
+          u[0] += b[it][j][0].x; u[1] += b[it][j][0].y; u[2] += b[it][j][0].z; u[3] += b[it][j][0].w;
+          u[4] += b[it][j][1].x; u[5] += b[it][j][1].y; u[6] += b[it][j][1].z; u[7] += b[it][j][1].w;
         }
       }
-    }
-    if constexpr (EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
-      v[0] += bf16lo(res.x); v[1] += bf16hi(res.x); v[2] += bf16lo(res.y); v[3] += bf16hi(res.y);
-      v[4] += bf16lo(res.z); v[5] += bf16hi(res.z); v[6] += bf16lo(res.w); v[7] += bf16hi(res.w);
-      const int rdst = EPI == EPI_RESID_PACKED ? k : s_ridx[r];
-      store_bf16<8>(Y + static_cast<size_t>(rdst) * p.ldy + c, v);
-    } else if constexpr (EPI == EPI_QKV) {
-      const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
-      if (c < nq) {
-        const int head = c / p.hd, j = c - head * p.hd;
-        const int hk = head / p.g, hg = head - hk * p.g;
-        store_bf16<8>(Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + j, v);
+      if constexpr (EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
+        const uint4 rs = res[it];
+        v[0] += bf16lo(rs.x); v[1] += bf16hi(rs.x); v[2] += bf16lo(rs.y); v[3] += bf16hi(rs.y);
+        v[4] += bf16lo(rs.z); v[5] += bf16hi(rs.z); v[6] += bf16lo(rs.w); v[7] += bf16hi(rs.w);
+        const int rdst = EPI == EPI_RESID_PACKED ? k : s_ridx[r];
+        store_bf16<8>(Y + static_cast<size_t>(rdst) * p.ldy + c, v);
+      } else if constexpr (EPI == EPI_QKV) {
+        const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+        if (c < nq) {
+          const int head = c / p.hd, jh = c - head * p.hd;
+          const int hk = head / p.g, hg = head - hk * p.g;
+          store_bf16<8>(Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + jh, v);
+        } else {
+          const bool is_k = c < nq + nkv;
+          const int cc = is_k ? c - nq : c - nq - nkv;
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
+          store_bf16<8>(dst + static_cast<size_t>(s_ridx[r]) * nkv + cc, v);
+        }
       } else {
-        const bool is_k = c < nq + nkv;
-        const int cc = is_k ? c - nq : c - nq - nkv;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv);
-        store_bf16<8>(dst + static_cast<size_t>(s_ridx[r]) * nkv + cc, v);
+        epi_chunk<EPI, 8>(p, k, c, v, u);
       }
-    } else {
-      epi_chunk<EPI, 8>(p, k, c, v, u);
     }
   }
+}
+
+// The split count of a clustered launch divides the cluster size (2, 4 or 8).
+template <int BN, int EPI>
+SF_DEV void dsm_reduce(const GemmParams& p, const uint8_t* smem, int n, int Mt, int S) {
+  if (S == 2) dsm_reduce_sc<BN, EPI, 2>(p, smem, n, Mt);
+  else if (S == 4) dsm_reduce_sc<BN, EPI, 4>(p, smem, n, Mt);
+  else if (S == 8) dsm_reduce_sc<BN, EPI, 8>(p, smem, n, Mt);
 }
 
 template <int BN, int EPI, bool CL>
@@ -513,7 +540,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, abort_flag, p.status)) {
+          if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, abort_flag, p.status, kWaitLimitNs, kSiteGemmEmpty)) {
             ok = false;
             break;
           }
@@ -544,13 +571,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++t) {
         const Unit w = unit(u);
         const int ab = t & 1;
-        if (!mbar_wait(smem_u32(&acce[ab]), ((t >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait(smem_u32(&acce[ab]), ((t >> 1) & 1) ^ 1, abort_flag, p.status, kWaitLimitNs, kSiteGemmAccEmpty)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + ab * BN;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(smem_u32(&full[st]), ph, abort_flag, p.status)) {
+          if (!mbar_wait(smem_u32(&full[st]), ph, abort_flag, p.status, kWaitLimitNs, kSiteGemmFull)) {
             ok = false;
             break;
           }
@@ -581,7 +608,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++t) {
       const Unit w = unit(u);
       const int ab = t & 1;
-      if (et == 0) *s_ok = mbar_wait(smem_u32(&accf[ab]), (t >> 1) & 1, abort_flag, p.status) ? 1 : 0;
+      if (et == 0) *s_ok = mbar_wait(smem_u32(&accf[ab]), (t >> 1) & 1, abort_flag, p.status, kWaitLimitNs, kSiteGemmAccFull) ? 1 : 0;
       named_bar_sync(1, 128);
       const bool ok = *s_ok != 0;
       named_bar_sync(1, 128);

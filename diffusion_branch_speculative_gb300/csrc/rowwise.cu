@@ -933,7 +933,7 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
         for (int u = 0; u < MAXV; ++u)
           if (lane + 32 * u < nv) pv[u] = __ldg(q + lane + 32 * u);
       }
-      if (!mbar_wait(bar, bt & 1, &s_abort, a.status)) break;
+      if (!mbar_wait(bar, bt & 1, &s_abort, a.status, kWaitLimitNs, kSiteGpRows)) break;
       const uint4* c = s_rows + static_cast<size_t>(t) * nv;
       float num = 0.f, den = 0.f, ss = 0.f;
 #pragma unroll
@@ -1034,14 +1034,14 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   T* X1 = static_cast<T*>(a.X1);
   if constexpr (HOLD) {
     const int r = c0 + w;
-    if (w < nch && !s_fold[r] && mbar_wait(gbar, 0, &s_abort, a.status)) {
+    if (w < nch && !s_fold[r] && mbar_wait(gbar, 0, &s_abort, a.status, kWaitLimitNs, kSiteGpGains)) {
       const float inv = rsqrtf(ss_hold / static_cast<float>(d) + a.eps);
       const uint4* x = s_rows + static_cast<size_t>(w) * nv;
       uint4* y = reinterpret_cast<uint4*>(X1 + static_cast<size_t>(nb + s_c1[w]) * d);
       for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(x[v], s_g[v], inv);
     }
   } else {
-    const bool g_ok = mbar_wait(gbar, 0, &s_abort, a.status);
+    const bool g_ok = mbar_wait(gbar, 0, &s_abort, a.status, kWaitLimitNs, kSiteGpGains);
     for (int t = w; t < nch && g_ok; t += kGPWarps) {
       const int r = c0 + t;
       if (s_fold[r]) continue;
@@ -1097,7 +1097,7 @@ __global__ void timeout_probe_kernel(uint32_t* status, uint64_t wait_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     // Nothing arrives on this barrier: the wait has to run out.
-    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, wait_ns);
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, wait_ns, kSiteProbe);
   }
   __syncthreads();
 }

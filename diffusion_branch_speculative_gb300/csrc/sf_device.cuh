@@ -58,8 +58,18 @@ SF_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Wait for the phase with this parity to complete.  Gives up when *abort is
 // set by another thread or after kWaitLimitNs; in the latter case it sets
 // *abort and the device status bit.  Returns false when it gave up.
+// The wait sites named in the status word (bit SPECFOLD_DEV_SITE_SHIFT + site).
+enum WaitSite : int {
+  kSiteAttnQEmpty = 0, kSiteAttnKvEmpty, kSiteAttnSFull, kSiteAttnRescale, kSiteAttnLastP, kSiteAttnEnd,
+  kSiteAttnPFull, kSiteAttnQFull, kSiteAttnKvFull, kSiteAttnSFree, kSiteAttnOEmpty,
+  kSiteGemmEmpty, kSiteGemmAccEmpty, kSiteGemmFull, kSiteGemmAccFull,
+  kSiteGpRows, kSiteGpGains, kSiteGpBarrier, kSiteProbe,
+  kSiteNone = -1
+};
+SF_DEV uint32_t site_bits(int site) { return site >= 0 ? (1u << (SPECFOLD_DEV_SITE_SHIFT + site)) : 0u; }
+
 SF_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* status,
-                      uint64_t limit_ns = kWaitLimitNs) {
+                      uint64_t limit_ns = kWaitLimitNs, int site = kSiteNone) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -67,7 +77,7 @@ SF_DEV bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32
     if (*abort) return false;
     if (globaltimer() - t0 > limit_ns) {
       *abort = 1;
-      if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT);
+      if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT | site_bits(site));
       return false;
     }
   }
@@ -117,7 +127,7 @@ SF_DEV bool grid_barrier(uint32_t* bar, uint32_t* status, volatile int* s_flag,
       if ((cur ^ old) & 0x80000000u) break;
       if (globaltimer() - t0 > limit_ns) {
         ok = 0;
-        if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT);
+        if (status) atomicOr(status, SPECFOLD_DEV_TIMEOUT | site_bits(kSiteGpBarrier));
         break;
       }
     }

@@ -62,6 +62,21 @@ extern "C" {
 #define SPECFOLD_DEV_TIMEOUT    1u  /* a bounded wait inside a kernel ran out; outputs invalid */
 #define SPECFOLD_DEV_BAD_PARENT 2u  /* parent[b] outside [0, b) for b > 0, or parent[0] != -1 */
 #define SPECFOLD_DEV_BAD_PAGE   4u  /* a paged prefix view's block table names a page outside the pool */
+/* With SPECFOLD_DEV_TIMEOUT, bit (SPECFOLD_DEV_SITE_SHIFT + site) names the
+ * wait that ran out (the other waits of that kernel then give up without a
+ * bit of their own), for a report:
+ *   attention  0 loader: Q buffer free       1 loader: K/V stage free
+ *              2 softmax: S ready            3 softmax: P V before a rescale
+ *              4 softmax: P V before the last P   5 softmax: last P V
+ *              6 MMA: P ready                7 MMA: Q loaded
+ *              8 MMA: K/V loaded             9 MMA: S buffer free
+ *             10 MMA: accumulators free
+ *   GEMM      11 producer: stage free       12 MMA: accumulator free
+ *             13 MMA: stage loaded          14 epilogue: accumulator ready
+ *   gate/pack 15 row copies                 16 gains copy
+ *             17 grid barrier
+ *   probe     18 specfold_timeout_probe's wait */
+#define SPECFOLD_DEV_SITE_SHIFT 8
 
 #define SPECFOLD_MAX_ROWS 16384     /* largest B*L */
 

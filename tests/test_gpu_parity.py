@@ -250,6 +250,7 @@ def test_timeout_selftest_reports_and_context_survives():
     binding.specfold_selftest_timeout(status, 20_000_000)
     torch.cuda.synchronize()
     assert int(status.item()) & binding.DEV_TIMEOUT
+    assert binding.timeout_sites(int(status.item())) == ["timeout probe"]
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum().item()) == 8.0
 
