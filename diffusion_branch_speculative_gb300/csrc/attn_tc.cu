@@ -219,10 +219,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       const int idle = static_cast<int>(gridDim.x) - U, me = static_cast<int>(blockIdx.x) - U;
       const int boxes_o = p.pf_orb * p.pf_okb;
       const int boxes = boxes_o + p.pf_n * p.pf_rb * p.pf_kb;
-      // the pauses of one CTA add up to at most 8 us, whatever its share of
-      // the boxes: the attention's launch ends only when this loop does
+      // Paced only when many idle CTAs share the boxes (a few each): then a
+      // burst of prefetches queues ahead of the working CTAs' first loads.
+      // With a long share per CTA the pauses would outlast the attention
+      // (whose launch ends only when this loop does), so it runs unpaced.
       const int share = (boxes - me + idle - 1) / idle;
-      const int pace = min(p.pf_pace_ns, 8000 / max(share, 1));
+      const int pace = share <= 32 ? p.pf_pace_ns : 0;
       for (int q = me; q < boxes; q += idle) {
         if (pace > 0 && q != me) __nanosleep(pace);
         if (q < boxes_o) {
