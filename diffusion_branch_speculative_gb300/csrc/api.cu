@@ -239,6 +239,7 @@ static void layout(const specfold_dims* d, int B, int L, specfold_ws_layout* o) 
 struct Scratch {
   float* partial;
   size_t partial_len;
+  uint32_t* fill_bar;  // grid-barrier word of the down projection's two-pass finish
 };
 
 static Scratch layer_scratch(void* ws, const specfold_dims* d, int B, int L, const specfold_ws_layout& lo) {
@@ -248,6 +249,9 @@ static Scratch layer_scratch(void* ws, const specfold_dims* d, int B, int L, con
   (void)L;
   s.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + lo.gemm_scratch);
   s.partial_len = gemm_partial_floats();
+  // a word of the gate/pack sync header that the gate/pack barrier leaves alone
+  // (that barrier uses the first word, and both return their word to zero)
+  s.fill_bar = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + lo.sync + 64);
   return s;
 }
 
@@ -382,6 +386,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   auto mark = [&](int i) {
     if (ev) record_stage_event(ev[i], st);
   };
+  uint32_t* fill_bar = s.fill_bar;
   if (!x2_ready)
     SF_TRY(launch_rmsnorm_rows(d->dtype, A, nullptr, n_dev, R, d->d_model, w->g2, d->rms_eps, X2, st));
   GemmCall c;
@@ -421,6 +426,10 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
     c.dep_rng = dep_rng;
     c.dep_rows = dep_rows;
     c.hin = H_in;
+    if (fill_bar) {
+      c.fill_src = src;
+      c.fill_bar = fill_bar;
+    }
   } else {
     dep_rng = nullptr;
   }

@@ -873,7 +873,8 @@ bool ffn_prefetch_enabled() {
 }
 
 // Cost of the combine launch in key blocks: writing and reading back the
-// fp32 partials plus a launch (SPECFOLD_ATTN_COMBINE_COST overrides it).
+// fp32 partials plus a launch (SPECFOLD_ATTN_COMBINE_COST overrides it;
+// SPECFOLD_ATTN_SPLITS=k forces k key ranges wherever the partial slots allow).
 float combine_cost() {
   static const float c = [] {
     const char* e = std::getenv("SPECFOLD_ATTN_COMBINE_COST");
@@ -933,9 +934,11 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   const int tiles_max = std::min(((R * g + 127) / 128) * c.n_kv, kSpTable);  // n <= R
   int units_max = ((R * g + 127) / 128) * c.n_kv;  // every tile, unsplit
   bool any_split = false;
+  static const int forced_sp = env_int("SPECFOLD_ATTN_SPLITS", 0);  // > 0: that split count wherever it fits
   for (int t = 1; t <= tiles_max; ++t) {
     const int lim = std::min(16, cap / t);
-    const int sp = lim >= 2 ? plan_splits(t, lim, p.num_sms, c.P, combine_cost()) : 1;
+    int sp = lim >= 2 ? plan_splits(t, lim, p.num_sms, c.P, combine_cost()) : 1;
+    if (forced_sp > 0) sp = std::max(1, std::min(forced_sp, std::max(lim, 1)));
     p.sp_table[t - 1] = static_cast<uint8_t>(sp);
     units_max = std::max(units_max, t * sp);
     any_split = any_split || sp > 1;

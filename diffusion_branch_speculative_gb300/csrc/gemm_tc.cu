@@ -79,6 +79,8 @@ struct GemmParams {
   const int32_t* dep_rng;   // RESID_SCATTER: fold-fill of dependents in the finish kernel
   const int32_t* dep_rows;
   const __nv_bfloat16* hin;
+  const int32_t* fill_src;  // RESID_SCATTER: the two-pass finish (fold-fill by folded row, from src)
+  uint32_t* fill_bar;       // its grid-barrier word
   // work decomposition per m-tile count Mt (row Mt - 1): S, full, r, St, U
   // (see Sched); filled by the host for this launch's grid
   int sched[kSchedRows][5];
@@ -966,6 +968,114 @@ __global__ void __launch_bounds__(256, 2) splitk_reduce_kernel(const __grid_cons
   }
 }
 
+// Down-projection finish with the fold-fill (S9 + S10), in two passes of one
+// grid of one CTA per SM (all resident at once).  Pass 1 sums the fp32
+// partials of every split tile in split order, adds the residual and writes
+// row k to H_out[row_idx[k]] (the GEMM epilogue wrote whole tiles).  After a
+// bounded grid barrier, pass 2 gives every folded row r its source's output
+// plus its own input difference, H_out[r] = H_out[s] + (H_in[r] - H_in[s])
+// with s = src[r], one thread per (row, 8 columns) and four items' loads in
+// flight, so a source with many folded rows does not serialise their loads.
+// The next kernel may launch only after the barrier (every CTA of this grid
+// is resident by then).
+constexpr int kFinThreads = 512;
+template <int BN>
+__global__ void __launch_bounds__(kFinThreads, 1) down_finish_kernel(const __grid_constant__ GemmParams p) {
+  __shared__ volatile int s_flag;
+  pdl_wait();
+  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
+  const int groups = (p.Nt * BN) / 8;
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+  // ---- pass 1: split tiles
+  if (sc.S > 1 || sc.St > 1) {
+    const long long total = static_cast<long long>(n) * groups;
+    for (long long idx = tid; idx < total; idx += nthr) {
+      const int k = static_cast<int>(idx / groups);
+      const int c = static_cast<int>(idx - static_cast<long long>(k) * groups) * 8;
+      const int nt = c / BN, tc = c - nt * BN;
+      const int m = k / kBM, row = k - m * kBM;
+      int S = 1, slot0 = 0;
+      if (!tile_split(sc, m, nt, p.Nt, S, slot0)) continue;
+      const int srow = p.row_idx[k];
+      const uint4 resv = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
+                                                             static_cast<size_t>(k) * p.ldr + c));
+      const float* base = p.partial + static_cast<size_t>(slot0) * kBM * BN + static_cast<size_t>(row) * BN + tc;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.f;
+      for (int s0 = 0; s0 < S; s0 += 8) {
+        float4 a[8][2];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (s0 + q < S) {
+            const float4* src = reinterpret_cast<const float4*>(base + static_cast<size_t>(s0 + q) * kBM * BN);
+            a[q][0] = __ldcg(src);
+            a[q][1] = __ldcg(src + 1);
+          }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (s0 + q < S) {
+            v[0] += a[q][0].x; v[1] += a[q][0].y; v[2] += a[q][0].z; v[3] += a[q][0].w;
+            v[4] += a[q][1].x; v[5] += a[q][1].y; v[6] += a[q][1].z; v[7] += a[q][1].w;
+          }
+      }
+      // four consecutive threads consumed one 128-byte line of every split
+      __syncwarp(__activemask());
+      {
+        const float* line = base - (threadIdx.x & 3) * 8;
+        for (int s = threadIdx.x & 3; s < S; s += 4) l2_discard_line(line + static_cast<size_t>(s) * kBM * BN);
+      }
+      v[0] += bf16lo(resv.x); v[1] += bf16hi(resv.x); v[2] += bf16lo(resv.y); v[3] += bf16hi(resv.y);
+      v[4] += bf16lo(resv.z); v[5] += bf16hi(resv.z); v[6] += bf16lo(resv.w); v[7] += bf16hi(resv.w);
+      store_bf16<8>(Y + static_cast<size_t>(srow) * p.ldy + c, v);
+    }
+  }
+  if (!grid_barrier(p.fill_bar, p.status, &s_flag)) return;
+  pdl_trigger();
+  // ---- pass 2: every folded row from its source's stored output
+  const long long total2 = static_cast<long long>(p.Mcap) * groups;
+  for (long long idx0 = tid; idx0 < total2; idx0 += 4 * nthr) {
+    int r[4], c[4], s[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long idx = idx0 + q * nthr;
+      r[q] = -1;
+      if (idx < total2) {
+        r[q] = static_cast<int>(idx / groups);
+        c[q] = static_cast<int>(idx - static_cast<long long>(r[q]) * groups) * 8;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s[q] = r[q] >= 0 ? __ldg(p.fill_src + r[q]) : -1;
+    uint4 ys[4], hr[4], hs[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (r[q] >= 0 && s[q] != r[q] && s[q] >= 0 && s[q] < p.Mcap) {
+        ys[q] = __ldcg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(s[q]) * p.ldy + c[q]));
+        hr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(r[q]) * p.ldy + c[q]));
+        hs[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(s[q]) * p.ldy + c[q]));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (!(r[q] >= 0 && s[q] != r[q] && s[q] >= 0 && s[q] < p.Mcap)) continue;
+      float o[8];
+      o[0] = bf16lo(ys[q].x) + (bf16lo(hr[q].x) - bf16lo(hs[q].x));
+      o[1] = bf16hi(ys[q].x) + (bf16hi(hr[q].x) - bf16hi(hs[q].x));
+      o[2] = bf16lo(ys[q].y) + (bf16lo(hr[q].y) - bf16lo(hs[q].y));
+      o[3] = bf16hi(ys[q].y) + (bf16hi(hr[q].y) - bf16hi(hs[q].y));
+      o[4] = bf16lo(ys[q].z) + (bf16lo(hr[q].z) - bf16lo(hs[q].z));
+      o[5] = bf16hi(ys[q].z) + (bf16hi(hr[q].z) - bf16hi(hs[q].z));
+      o[6] = bf16lo(ys[q].w) + (bf16lo(hr[q].w) - bf16lo(hs[q].w));
+      o[7] = bf16hi(ys[q].w) + (bf16hi(hr[q].w) - bf16hi(hs[q].w));
+      store_bf16<8>(Y + static_cast<size_t>(r[q]) * p.ldy + c[q], o);
+    }
+  }
+}
+
 // Output-projection finish (S6 + S7): one block per packed row k, one thread
 // per 8 output columns (GPT groups of 8 when the row is wider than the
 // block).  When the GEMM was split, sums the partials in split order, adds the
@@ -1158,6 +1268,10 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
       p.dep_rng = c.dep_rng;
       p.dep_rows = c.dep_rows;
       p.hin = static_cast<const __nv_bfloat16*>(c.hin);
+      if (c.fill_src && c.fill_bar) {
+        p.fill_src = c.fill_src;
+        p.fill_bar = c.fill_bar;
+      }
     }
   }
 
@@ -1195,6 +1309,13 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
         launch_k(outproj_finish_kernel<BN, 1>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       else
         launch_k(outproj_finish_kernel<BN, 2>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
+      count_launch();
+      return check_launch();
+    }
+  }
+  if constexpr (EPI == EPI_RESID_SCATTER) {
+    if (p.fill_src) {  // the two-pass finish: split sums, then the fold-fill by folded row
+      launch_k(down_finish_kernel<BN>, dim3(grid), dim3(kFinThreads), 0, st, p);
       count_launch();
       return check_launch();
     }

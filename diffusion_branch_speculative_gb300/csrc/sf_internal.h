@@ -111,6 +111,11 @@ struct GemmCall {
   const int32_t* dep_rng;
   const int32_t* dep_rows;
   const void* hin;
+  // RESID_SCATTER, optional (with dep_rng): the provenance table src[r] and a
+  // zeroed grid-barrier word; the finish then fills by folded row in a second
+  // pass after a grid barrier
+  const int32_t* fill_src;
+  uint32_t* fill_bar;
 };
 size_t gemm_partial_floats();
 // Optional RMSNorm of the finished rows of an EPI_RESID_PACKED GEMM (the

@@ -154,7 +154,8 @@ typedef struct {
   size_t slot_of_row;  /* int32  [R] (-1 for folded rows) */
   size_t dep_rng;      /* int32  [R][2] for a recomputed row s: {beg, end}, the folded rows */
   size_t dep_rows;     /* int32  [R]    dep_rows[beg .. end) whose source is s */
-  size_t sync;         /* uint32 grid-barrier word, then int32 per-CTA counts (library use) */
+  size_t sync;         /* grid-barrier words (bytes 0 and 64), then int32 per-CTA counts from byte 128
+                          (library use; each word returns to zero after every complete call) */
   size_t x1;           /* [R, d]        RMSNorm1 of packed rows */
   size_t q;            /* [n_kv, R*g, hd]  queries, head-group major */
   size_t block_k;      /* [R, n_kv, hd]  keys of recomputed rows (row r) */
