@@ -315,9 +315,11 @@ static int stage_qkv(const specfold_dims* d, const specfold_weights* w, const vo
 static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_view pk, specfold_kv_view pv, int P,
                            const void* bK, const void* bV, const int32_t* src, const int32_t* packed_idx,
                            const int32_t* n_dev, int B, int L, void* O, uint32_t* status, void* part,
-                           size_t part_bytes, cudaStream_t st, const specfold_weights* w_ffn = nullptr) {
+                           size_t part_bytes, cudaStream_t st, const specfold_weights* w_ffn = nullptr,
+                           bool n_early = false) {
   AttnCall a;
   memset(&a, 0, sizeof(a));
+  a.n_early = n_early;
   if (w_ffn && d->dtype == SPECFOLD_BF16) {  // CTAs without work prefetch the next GEMMs' weights
     a.wo = w_ffn->w_o;
     a.wo_rows = d->d_model;
@@ -350,9 +352,11 @@ static int stage_attention(const specfold_dims* d, const void* Q, specfold_kv_vi
 
 static int stage_out_proj(const specfold_dims* d, const specfold_weights* w, const void* O,
                           const int32_t* packed_idx, const int32_t* n_dev, const void* H_in, int R, void* A,
-                          const Scratch& s, uint32_t* status, cudaStream_t st, void* X2_fused = nullptr) {
+                          const Scratch& s, uint32_t* status, cudaStream_t st, void* X2_fused = nullptr,
+                          bool n_early = false) {
   GemmCall c;
   memset(&c, 0, sizeof(c));
+  c.n_early = n_early;
   c.epi = EPI_RESID_PACKED;
   c.A = O;
   c.Mcap = R;
@@ -382,7 +386,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
                      const int32_t* n_dev, const void* H_in, const int32_t* src, const uint8_t* fold, int R,
                      void* H_out, void* X2, void* G, const Scratch& s, uint32_t* status, cudaStream_t st,
                      void* const* ev, int ev0, bool x2_ready, const int32_t* dep_rng = nullptr,
-                     const int32_t* dep_rows = nullptr) {
+                     const int32_t* dep_rows = nullptr, bool n_early = false) {
   auto mark = [&](int i) {
     if (ev) record_stage_event(ev[i], st);
   };
@@ -391,6 +395,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
     SF_TRY(launch_rmsnorm_rows(d->dtype, A, nullptr, n_dev, R, d->d_model, w->g2, d->rms_eps, X2, st));
   GemmCall c;
   memset(&c, 0, sizeof(c));
+  c.n_early = n_early;
   c.epi = EPI_SWIGLU;
   c.A = X2;
   c.Mcap = R;
@@ -407,6 +412,7 @@ static int stage_ffn(const specfold_dims* d, const specfold_weights* w, const vo
   SF_TRY(gemm_call(d->dtype, c, st));
   mark(ev0 + 1);
   memset(&c, 0, sizeof(c));
+  c.n_early = n_early;
   c.epi = EPI_RESID_SCATTER;
   c.A = G;
   c.Mcap = R;
@@ -564,8 +570,8 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
   if (dims->gate_ref == 0)
     rc = launch_gate_pack(dims->dtype, H_in, parent, B, L, dims->d_model, tau, w->g1, dims->rms_eps, fold,
                           at<float>(ws, lo.rel), src, pidx, at<int32_t>(ws, lo.slot_of_row), n_dev,
-                          at<void>(ws, lo.x1), at<int32_t>(ws, lo.dep_rng), at<int32_t>(ws, lo.dep_rows),
-                          at<void>(ws, lo.sync), status, st, fold_hist, n_hist);
+                          at<void>(ws, lo.x1), nullptr, nullptr,  // no dependents lists: the down
+                          at<void>(ws, lo.sync), status, st, fold_hist, n_hist);  // finish fills from src
   if (rc == SPECFOLD_OK) {
     mark(1);  // the fused launch is the "gate" stage; "select_pack" is empty
   } else {
@@ -583,16 +589,19 @@ static int enqueue_layer(const specfold_dims* dims, const specfold_weights* w, c
     SF_TRY(launch_rope(dims->dtype, at<void>(ws, lo.q), at<void>(ws, lo.block_k), pidx, n_dev, R, L, P,
                        dims->n_q_heads, dims->n_kv_heads, dims->head_dim, dims->rope_theta, st));
   mark(3);
+  // from here on n_dev and packed_idx were written at least two launches
+  // back (the QKV GEMM sits between), by a kernel that completed before the
+  // QKV GEMM's programmatic wait returned: later kernels read them early
   SF_TRY(stage_attention(dims, at<void>(ws, lo.q), prefK, prefV, P, at<void>(ws, lo.block_k),
                          at<void>(ws, lo.block_v), src, pidx, n_dev, B, L, at<void>(ws, lo.attn_o), status,
-                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st, w));
+                         at<void>(ws, lo.attn_scratch), lo.total - lo.attn_scratch, st, w, true));
   mark(4);
   SF_TRY(stage_out_proj(dims, w, at<void>(ws, lo.attn_o), pidx, n_dev, H_in, R, at<void>(ws, lo.a), s, status, st,
-                        at<void>(ws, lo.x2)));
+                        at<void>(ws, lo.x2), true));
   mark(5);
   return stage_ffn(dims, w, at<void>(ws, lo.a), pidx, n_dev, H_in, src, fold, R, H_out, at<void>(ws, lo.x2),
                    at<void>(ws, lo.g), s, status, st, stage_events, 5, true, at<int32_t>(ws, lo.dep_rng),
-                   at<int32_t>(ws, lo.dep_rows));
+                   at<int32_t>(ws, lo.dep_rows), true);
 }
 
 }  // namespace sf

@@ -82,6 +82,7 @@ struct AttnParams {
   CUtensorMap pf_map[2];
   int pf_n, pf_rb, pf_kb;
   int pf_pace_ns;  // pause between one idle CTA's prefetches (queues stay short for the working CTAs' loads)
+  int n_early;     // n_dev may be read before the programmatic wait (its producer is known complete)
 };
 
 // Number of key-range splits for n packed rows, looked up from a table the
@@ -199,10 +200,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   volatile int* abort_flag = &abort_s;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_pre = p.n_early ? __ldcg(p.n_dev) : 0;
   pdl_wait();
   pdl_trigger();
   const int g = p.g, L = p.L;
-  const int n = min(max(p.n_dev[0], 0), p.R);
+  const int n = min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.R);
   const int rows_total = n * g;
   const int tiles_x = (rows_total + 127) / 128;
   const int SP = attn_splits(p, rows_total);
@@ -928,6 +930,7 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   p.n_q = c.n_q;
   p.sl2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   p.status = c.status;
+  p.n_early = c.n_early ? 1 : 0;
   p.num_sms = num_sms();
   // split counts per live tile count, within the partials' slot capacity
   const int cap = attn_slot_cap(R, g, c.n_kv);

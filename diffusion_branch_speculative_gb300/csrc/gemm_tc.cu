@@ -81,6 +81,7 @@ struct GemmParams {
   const __nv_bfloat16* hin;
   const int32_t* fill_src;  // RESID_SCATTER: the two-pass finish (fold-fill by folded row, from src)
   uint32_t* fill_bar;       // its grid-barrier word
+  int n_early;              // n_dev and row_idx may be read before the programmatic wait
   // work decomposition per m-tile count Mt (row Mt - 1): S, full, r, St, U
   // (see Sched); filled by the host for this launch's grid
   int sched[kSchedRows][5];
@@ -463,6 +464,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   float* epi_stage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // n through L2, early, when its producer is known complete (n_early)
+  const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
   // Set-up that depends on no earlier kernel runs before the programmatic
   // wait, overlapping the previous kernel's tail wherever this CTA is already
   // resident: barriers, tensor-map prefetch, TMEM.  (A GEMM CTA shares an SM
@@ -495,7 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_after();
   pdl_wait();
   pdl_trigger();
-  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const int Mt = (n + kBM - 1) / kBM;
   const int tiles = Mt * p.Nt;
   const int KB = p.K / kBK;
@@ -851,9 +854,10 @@ template <int BN, int EPI>
 // (At most 128 registers a thread, so that a block of it fits on an SM beside
 // the GEMM CTA it follows and starts early under programmatic launch.)
 __global__ void __launch_bounds__(256, 2) splitk_reduce_kernel(const __grid_constant__ GemmParams p, int gemm_grid) {
+  const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
   pdl_wait();
   pdl_trigger();
-  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   bool fill = false;
   if constexpr (EPI == EPI_RESID_SCATTER) fill = p.dep_rng != nullptr;
@@ -982,8 +986,9 @@ constexpr int kFinThreads = 512;
 template <int BN>
 __global__ void __launch_bounds__(kFinThreads, 1) down_finish_kernel(const __grid_constant__ GemmParams p) {
   __shared__ volatile int s_flag;
+  const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
   pdl_wait();
-  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
   const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   const int groups = (p.Nt * BN) / 8;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1101,10 +1106,14 @@ __global__ void __launch_bounds__(512, 2) outproj_finish_kernel(const __grid_con
     const int gi = threadIdx.x + nthr * j;
     gv[j] = gi < groups ? __ldg(reinterpret_cast<const uint4*>(g2 + gi * 8)) : make_uint4(0, 0, 0, 0);
   }
+  // n and this row's index through L2, early, when their producer is known
+  // complete (n_early); else after the wait
+  const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
+  const int r_pre = p.n_early ? __ldcg(p.row_idx + k) : 0;
   pdl_wait();
   pdl_trigger();
-  const int n = p.n_dev ? min(max(p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const int r = p.row_idx[k];  // k < Mcap: in bounds; used only when k < n
+  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const int r = p.n_early ? r_pre : p.row_idx[k];  // k < Mcap: in bounds; used only when k < n
   if (k >= n) return;
   const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   const int m = k / kBM, row = k - m * kBM;
@@ -1262,6 +1271,7 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
   if (c.partial_len < gemm_partial_floats()) return SPECFOLD_ECAPACITY;
   p.partial = c.partial;
   p.status = c.status;
+  p.n_early = c.n_early ? 1 : 0;
   if constexpr (EPI == EPI_RESID_SCATTER) {
     if (c.dep_rng) {
       if (!c.dep_rows || !c.hin || c.ldy != c.N) return SPECFOLD_EINVAL;

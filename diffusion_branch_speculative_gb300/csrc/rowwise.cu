@@ -1027,7 +1027,7 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
   }
   // with at most 32 branches and a warp to spare, the last warp builds the
   // dependents lists of this CTA's block positions while the others write X1
-  const bool deps_by_warp = HOLD && B <= 32 && nch < kGPWarps;
+  const bool deps_by_warp = a.dep_rng && HOLD && B <= 32 && nch < kGPWarps;
   if (deps_by_warp && w == kGPWarps - 1)
     for (int i = blockIdx.x; i < L; i += gridDim.x) deps_warp(a, s_fold, s_par, i, L, B, lane);
   // RMSNorm1 of this CTA's recomputed rows: X1[k] = H[r] * g1 / rms(H[r])
@@ -1061,7 +1061,7 @@ __global__ void __launch_bounds__(kGPThreads, 1) gate_pack_kernel(const __grid_c
       for (int v = lane; v < nv; v += 32) y[v] = scale_vec<T>(__ldg(x + v), s_g[v], inv);
     }
   }
-  if (deps_by_warp) return;
+  if (deps_by_warp || !a.dep_rng) return;  // lists built, or not asked for
   // folded rows grouped by source, one block position at a time
   for (int i = blockIdx.x; i < L; i += gridDim.x) {
     __syncthreads();  // the arrays are free again

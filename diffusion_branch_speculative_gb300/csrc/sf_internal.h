@@ -116,6 +116,10 @@ struct GemmCall {
   // pass after a grid barrier
   const int32_t* fill_src;
   uint32_t* fill_bar;
+  // n_dev (and row_idx) were written at least two launches back, by a kernel
+  // that had completed before this launch could start: read them through L2
+  // before the programmatic wait instead of after it
+  bool n_early;
 };
 size_t gemm_partial_floats();
 // Optional RMSNorm of the finished rows of an EPI_RESID_PACKED GEMM (the
@@ -150,6 +154,7 @@ struct AttnCall {
   int ffn_F, ffn_d;
   const void* wo;        // output-projection weight [wo_rows, wo_cols], prefetched before the FFN's
   int wo_rows, wo_cols;
+  bool n_early;          // as GemmCall::n_early
 };
 int attn_slot_cap(int R, int g, int n_kv);
 size_t attn_partial_bytes(int R, int g, int n_kv, int hd);

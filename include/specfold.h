@@ -153,7 +153,9 @@ typedef struct {
   size_t packed_idx;   /* int32  [R] (first n valid) */
   size_t slot_of_row;  /* int32  [R] (-1 for folded rows) */
   size_t dep_rng;      /* int32  [R][2] for a recomputed row s: {beg, end}, the folded rows */
-  size_t dep_rows;     /* int32  [R]    dep_rows[beg .. end) whose source is s */
+  size_t dep_rows;     /* int32  [R]    dep_rows[beg .. end) whose source is s (written by
+                          specfold_gate_pack and specfold_pack; the layer call's fused gate/pack
+                          leaves both unwritten: its down-projection finish fills from src) */
   size_t sync;         /* grid-barrier words (bytes 0 and 64), then int32 per-CTA counts from byte 128
                           (library use; each word returns to zero after every complete call) */
   size_t x1;           /* [R, d]        RMSNorm1 of packed rows */
