@@ -646,6 +646,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
       const int row0 = w.m * kBM + q * 32;          // first packed row of this warp
       const int rows_here = min(32, n - row0);      // valid rows (may be <= 0)
+      if constexpr (EPI == EPI_QKV) {
+        if (!w.split) {
+          // straight from TMEM as for SwiGLU below: thread `lane` owns row
+          // row0 + lane; a 32-column chunk lies in one head (hd % 32 == 0), so
+          // its 32 values go out as 64 contiguous bytes, to the head-group
+          // major Q or to the K/V row of the packed row's source row
+          const int k = row0 + lane;
+          const bool valid = lane < rows_here;
+          const int ridx_row = valid ? p.row_idx[k] : 0;
+          const int nq = p.n_q * p.hd, nkv = p.n_kv * p.hd;
+          __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tb + ch * 32, r);
+            tmem_ld_wait(r);
+            if (valid) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+              const int cbase = w.nt * BN + ch * 32;
+              __nv_bfloat16* dst;
+              if (cbase < nq) {
+                const int head = cbase / p.hd;
+                const int hk = head / p.g, hg = head - hk * p.g;
+                dst = Y + ((static_cast<size_t>(hk) * p.R + k) * p.g + hg) * p.hd + (cbase - head * p.hd);
+              } else {
+                const bool is_k = cbase < nq + nkv;
+                dst = static_cast<__nv_bfloat16*>(is_k ? p.Yk : p.Yv) + static_cast<size_t>(ridx_row) * nkv +
+                      (is_k ? cbase - nq : cbase - nq - nkv);
+              }
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) d4[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&acce[ab]));
+          continue;
+        }
+      }
       if constexpr (EPI == EPI_SWIGLU || EPI == EPI_STORE) {
         if (!w.split) {
           // Straight from TMEM: thread `lane` owns row row0 + lane and writes
@@ -1310,12 +1351,16 @@ int run_gemm(const GemmCall& c, cudaStream_t st, const RowNorm* rn, int cs = 0, 
     if (rn) {
       const int groups = c.N / 8;
       if (groups > 2 * 512 || c.N % 8) return SPECFOLD_EUNSUPPORTED;
-      // one thread per group up to 512 groups, two beyond
-      const int threads = std::min(512, (groups + 31) / 32 * 32);
+      // one thread per group up to 512 groups, two beyond; with many rows
+      // (over four m-tiles) two groups a thread in half as many threads, so
+      // more rows' blocks fit on an SM at once (the finish is then bound by
+      // its rows in flight, not by one row's latency)
+      const int gpt = c.Mcap > 4 * kBM || groups > 512 ? 2 : 1;
+      const int threads = std::min(512, ((groups + gpt - 1) / gpt + 31) / 32 * 32);
       const dim3 g(c.Mcap), b(threads);
       const __nv_bfloat16* g2 = static_cast<const __nv_bfloat16*>(rn->gain);
       __nv_bfloat16* x2 = static_cast<__nv_bfloat16*>(rn->out);
-      if (groups <= threads)
+      if (gpt == 1)
         launch_k(outproj_finish_kernel<BN, 1>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
       else
         launch_k(outproj_finish_kernel<BN, 2>, dim3(g), dim3(b), 0, st, p, grid, g2, rn->eps, x2);
