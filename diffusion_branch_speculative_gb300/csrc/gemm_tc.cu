@@ -687,6 +687,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           continue;
         }
       }
+      if constexpr (EPI == EPI_RESID_PACKED || EPI == EPI_RESID_SCATTER) {
+        if (!w.split) {
+          // straight from TMEM as for QKV above: thread `lane` owns row
+          // row0 + lane, adds its residual row's chunk (64 contiguous bytes,
+          // two chunks' loads in flight) and writes 64 contiguous bytes --
+          // packed row k (output projection) or row row_idx[k] (down)
+          const int k = row0 + lane;
+          const bool valid = lane < rows_here;
+          const int ridx_row = valid ? p.row_idx[k] : 0;
+          const int rres = EPI == EPI_RESID_PACKED ? ridx_row : k;   // residual row
+          const int rdst = EPI == EPI_RESID_PACKED ? k : ridx_row;   // output row
+          const __nv_bfloat16* Rz = static_cast<const __nv_bfloat16*>(p.resid) + static_cast<size_t>(rres) * p.ldr;
+          __nv_bfloat16* Yr = static_cast<__nv_bfloat16*>(p.Y) + static_cast<size_t>(rdst) * p.ldy;
+#pragma unroll 1
+          for (int ch = 0; ch < BN / 32; ch += 2) {
+            uint4 rv[2][4];
+            if (valid) {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                  rv[h2][q4] = __ldg(reinterpret_cast<const uint4*>(Rz + w.nt * BN + (ch + h2) * 32) + q4);
+            }
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tb + ch * 32, r0);
+            tmem_ld32(tb + (ch + 1) * 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+            if (valid) {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t* rr = h2 ? r1 : r0;
+                uint4* d4 = reinterpret_cast<uint4*>(Yr + w.nt * BN + (ch + h2) * 32);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const uint4 u = rv[h2][q4];
+                  const int e0 = q4 * 8;
+                  d4[q4] = make_uint4(
+                      pack_bf16x2(__uint_as_float(rr[e0 + 0]) + bf16lo(u.x), __uint_as_float(rr[e0 + 1]) + bf16hi(u.x)),
+                      pack_bf16x2(__uint_as_float(rr[e0 + 2]) + bf16lo(u.y), __uint_as_float(rr[e0 + 3]) + bf16hi(u.y)),
+                      pack_bf16x2(__uint_as_float(rr[e0 + 4]) + bf16lo(u.z), __uint_as_float(rr[e0 + 5]) + bf16hi(u.z)),
+                      pack_bf16x2(__uint_as_float(rr[e0 + 6]) + bf16lo(u.w), __uint_as_float(rr[e0 + 7]) + bf16hi(u.w)));
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&acce[ab]));
+          continue;
+        }
+      }
       if constexpr (EPI == EPI_SWIGLU || EPI == EPI_STORE) {
         if (!w.split) {
           // Straight from TMEM: thread `lane` owns row row0 + lane and writes
