@@ -82,6 +82,8 @@ struct AttnParams {
   CUtensorMap pf_map[2];
   int pf_n, pf_rb, pf_kb;
   int pf_pace_ns;  // pause between one idle CTA's prefetches (queues stay short for the working CTAs' loads)
+  int pf_blk_ns;   // expected time of one key block of a working unit (sizes an idle CTA's prefetch budget)
+  int pf_delay_ns;  // an idle CTA's pause before its first prefetch
   int n_early;     // n_dev may be read before the programmatic wait (its producer is known complete)
 };
 
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     if ((p.pf_orb > 0 || p.pf_n > 0) && threadIdx.x == 0) {
       // after the working CTAs' first loads have gone out (a prefetch flood
       // ahead of them delays their first key blocks)
-      __nanosleep(3000);
+      __nanosleep(p.pf_delay_ns);
       const int idle = static_cast<int>(gridDim.x) - U, me = static_cast<int>(blockIdx.x) - U;
       const int boxes_o = p.pf_orb * p.pf_okb;
       const int boxes = boxes_o + p.pf_n * p.pf_rb * p.pf_kb;
@@ -227,7 +229,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
       // (whose launch ends only when this loop does), so it runs unpaced.
       const int share = (boxes - me + idle - 1) / idle;
       const int pace = share <= 32 ? p.pf_pace_ns : 0;
-      for (int q = me; q < boxes; q += idle) {
+      // The launch lasts as long as its longest CTA, and one SM issues a
+      // box prefetch only every ~0.2 us: a few idle CTAs with the whole
+      // share each would outlast the working units.  So each one stops
+      // after the boxes that fit in a working unit's expected time (its
+      // fixed cost of about four key blocks, then its own key blocks, less
+      // the start delay above); together the idle CTAs still cover
+      // the leading boxes, in the order the FFN GEMM streams them.
+      const int NBu = ((p.P + 127) / 128 + SP) / SP + 1;
+      const long long budget_ns = (4LL + NBu) * p.pf_blk_ns - p.pf_delay_ns;
+      const int per_box_ns = pace > 0 ? pace + 50 : 250;
+      const int cap = budget_ns > 0 ? static_cast<int>(budget_ns / per_box_ns) : 0;
+      int issued = 0;
+      for (int q = me; q < boxes && issued < cap; q += idle, ++issued) {
         if (pace > 0 && q != me) __nanosleep(pace);
         if (q < boxes_o) {
           const int kb = q / p.pf_orb, rb = q - kb * p.pf_orb;
@@ -861,7 +875,11 @@ int plan_splits(int tiles, int sp_lim, int num_sms, int P, float combine) {
 // (default 40 MB); SPECFOLD_PREFETCH_WO=1 adds the output projection's weight
 // ahead of it (off by default: at the 7B layer it slowed the attention by
 // more than it saved in the projection); SPECFOLD_PREFETCH_PACE_NS sets the
-// pause between one idle CTA's prefetches (default 400 ns).
+// pause between one idle CTA's prefetches (default 400 ns), and
+// SPECFOLD_PREFETCH_BLOCK_NS the expected time of one key block of a working
+// unit (default 1500 ns), which bounds how long an idle CTA keeps
+// prefetching; SPECFOLD_PREFETCH_DELAY_NS the pause before an idle CTA's
+// first prefetch (default 3000 ns).
 static int env_int(const char* name, int dflt) {
   const char* e = std::getenv(name);
   return e ? std::atoi(e) : dflt;
@@ -958,7 +976,11 @@ int run_attn(const AttnCall& c, cudaStream_t st) {
   static const int pf_wo = env_int("SPECFOLD_PREFETCH_WO", 0);
   static const int pf_ffn_mb = env_int("SPECFOLD_FFN_PREFETCH_MB", 40);
   static const int pf_pace = env_int("SPECFOLD_PREFETCH_PACE_NS", 400);
+  static const int pf_blk = env_int("SPECFOLD_PREFETCH_BLOCK_NS", 1500);
+  static const int pf_delay = env_int("SPECFOLD_PREFETCH_DELAY_NS", 3000);
+  p.pf_delay_ns = std::min(std::max(pf_delay, 0), 1000000);
   p.pf_pace_ns = std::max(pf_pace, 0);
+  p.pf_blk_ns = std::max(pf_blk, 0);
   if (pf_wo && c.wo && c.wo_rows % 128 == 0 && c.wo_cols % 64 == 0 && ffn_prefetch_enabled() &&
       make_map_2d(&p.pf_omap, c.wo, c.wo_rows, c.wo_cols, c.wo_cols, 128) == SPECFOLD_OK) {
     p.pf_orb = c.wo_rows / 128;
