@@ -207,12 +207,13 @@ def test_layer_3b():
     print("3b", m)
 
 
-@pytest.mark.parametrize("frac,n_expect", [(0.0, 32), (0.25, 536), (1.0, 2048)])
+@pytest.mark.parametrize("frac,n_expect", [(0.0, 32), (0.1, 234), (0.25, 536), (0.5, 1040), (1.0, 2048)])
 def test_layer_stress_all_rows(frac, n_expect):
-    """The stress workload (prefix 8192, 64 branches) at three recompute
+    """The stress workload (prefix 8192, 64 branches) at five recompute
     fractions: every output row, and every packed row's intermediates (so
     every m-tile of each GEMM and every query tile of the attention), row by
-    row against the oracle."""
+    row against the oracle.  n = 234 splits every attention tile's key
+    range in two (104 units); n = 1040 runs 228 whole tiles, two waves."""
     inp = synth.make_layer_inputs("stress", seed=0, forced_frac=frac)
     m, _, _ = check_layer(inp, 0.05)
     assert m["n"] == n_expect
