@@ -1,6 +1,6 @@
 """CUDA path vs the CPU oracle, through the C-ABI (GPU only).
 
-Bars (the benchmark spec): gate decisions, provenance and packed index lists are
+Bars: gate decisions, provenance and packed index lists are
 bit-exact (rows within 1e-4 relative of tau are reported and take the GPU's
 decision on both sides); bf16 outputs are within 2e-2 relative L2.
 """
