@@ -87,6 +87,13 @@ struct AttnParams {
   int n_early;     // n_dev may be read before the programmatic wait (its producer is known complete)
 };
 
+// 16-byte asynchronous copy global -> shared that reads `bytes` (16 or 0)
+// and zero-fills the rest; completion by cp_async_wait_all in this thread.
+SF_DEV void cp_async16_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+SF_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Number of key-range splits for n packed rows, looked up from a table the
 // host fills per launch (sp_table[tiles - 1]; beyond it, no split).  See
 // plan_splits for the rule.
@@ -382,17 +389,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
             issued_tma = gt;
           }
         } else {
-          for (int kr = lt; kr < 128; kr += kLoaders) {
-            const uint4* krow = nullptr;
-            const uint4* vrow = nullptr;
+          // Gathered rows: first every row's source (the page table or src
+          // read, one round trip for all of this thread's rows), then each
+          // 16-byte chunk copied asynchronously straight to its swizzled
+          // place, zero-filled for a missing row, all in flight at once.
+          constexpr int RPT = 128 / kLoaders;  // rows per thread
+          const __nv_bfloat16* krow[RPT];
+          const __nv_bfloat16* vrow[RPT];
+#pragma unroll
+          for (int q = 0; q < RPT; ++q) {
+            const int kr = lt + q * kLoaders;
+            krow[q] = vrow[q] = nullptr;
             if (jblk < NBP) {  // paged prefix token
               const int tk = jblk * 128 + kr;
               if (tk < p.P) {
                 const int page = p.table[tk / p.page_size];
                 if (page >= 0 && page < p.num_pages) {
                   const size_t tok = static_cast<size_t>(page) * p.page_size + tk % p.page_size;
-                  krow = reinterpret_cast<const uint4*>(p.pkp + tok * p.k_ts + static_cast<size_t>(h) * p.k_hs);
-                  vrow = reinterpret_cast<const uint4*>(p.pvp + tok * p.v_ts + static_cast<size_t>(h) * p.v_hs);
+                  krow[q] = p.pkp + tok * p.k_ts + static_cast<size_t>(h) * p.k_hs;
+                  vrow[q] = p.pvp + tok * p.v_ts + static_cast<size_t>(h) * p.v_hs;
                 } else {
                   atomicOr(p.status, SPECFOLD_DEV_BAD_PAGE);
                 }
@@ -404,21 +419,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
                 const int s = p.src[b * L + (e - (e / L) * L)];
                 if (s >= 0 && s < p.R) {  // an invalid source reads as a zero key and value
                   const size_t off = (static_cast<size_t>(s) * p.n_kv + h) * HD;
-                  krow = reinterpret_cast<const uint4*>(p.bK + off);
-                  vrow = reinterpret_cast<const uint4*>(p.bV + off);
+                  krow[q] = p.bK + off;
+                  vrow[q] = p.bV + off;
                 }
               }
             }
+          }
+#pragma unroll
+          for (int q = 0; q < RPT; ++q) {
+            const int kr = lt + q * kLoaders;
             const int kh = kr >> 6, kq = kr & 63;  // half of the block and row within it
+            const uint32_t nk = krow[q] ? 16u : 0u, nv = vrow[q] ? 16u : 0u;
+            const __nv_bfloat16* ks = krow[q] ? krow[q] : p.bK;  // any valid address when nothing is read
+            const __nv_bfloat16* vs = vrow[q] ? vrow[q] : p.bV;
 #pragma unroll
             for (int c16 = 0; c16 < HD / 8; ++c16) {
-              const uint4 kv = krow ? __ldg(krow + c16) : make_uint4(0, 0, 0, 0);
-              const uint4 vv = vrow ? __ldg(vrow + c16) : make_uint4(0, 0, 0, 0);
               const int sw = ((c16 & 7) ^ (kr & 7)) << 4;
-              *reinterpret_cast<uint4*>(sK + kh * C::KH_BYTES + (c16 >> 3) * C::KH_ATOM + kq * 128 + sw) = kv;
-              *reinterpret_cast<uint4*>(sV + (c16 >> 3) * kAtom + kr * 128 + sw) = vv;
+              cp_async16_zfill(smem_u32(sK + kh * C::KH_BYTES + (c16 >> 3) * C::KH_ATOM + kq * 128 + sw), ks + c16 * 8, nk);
+              cp_async16_zfill(smem_u32(sV + (c16 >> 3) * kAtom + kr * 128 + sw), vs + c16 * 8, nv);
             }
           }
+          cp_async_wait_all();
           fence_proxy_async_smem();
           named_bar_sync(1, kLoaders);
           if (lt == 0) mbar_arrive(smem_u32(&kv_full[st]));
