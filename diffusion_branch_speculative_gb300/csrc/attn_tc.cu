@@ -210,8 +210,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_pre = p.n_early ? __ldcg(p.n_dev) : 0;
-  pdl_wait();
-  pdl_trigger();
+  // Without n_early every thread waits for the previous kernel here.  With
+  // it, only the loaders wait, just before the queries and the branch keys,
+  // which that kernel (the QKV GEMM) wrote.  Everything else read before
+  // that -- n, the packed rows, src -- was written by a kernel that completed
+  // before the QKV GEMM's own wait returned, and the prefix is an input of
+  // the layer.  (The QKV GEMM and this kernel cannot share an SM, so the
+  // TMEM allocation below finds that GEMM's columns already freed.)
+  if (!p.n_early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int g = p.g, L = p.L;
   const int n = min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.R);
   const int rows_total = n * g;
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
   const int SP = attn_splits(p, rows_total);
   const int U = tiles_x * p.n_kv * SP;
   if (static_cast<int>(blockIdx.x) >= U) {
+    if (p.n_early) pdl_trigger();  // it reads nothing the previous kernel wrote
     // no unit for this CTA: its SM would idle through the attention, so it
     // pulls a share of the next GEMMs' weights into L2: the output
     // projection's (needed right after the attention), then the FFN weights'
@@ -312,6 +322,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         prefetch_tmap(&p.mapV);
       }
     }
+    // the first unit's first prefix block (a fresh stage, no wait for it to
+    // empty) goes out before the wait for the previous kernel; its other
+    // blocks follow the queries (when that kernel is long done, the queries
+    // should not queue behind all three)
+    int pre = 0;
+    if (p.n_early && lt == 0 && SP == 1 && NBP > 0 && !p.table) {
+      const int h0 = attn_unit_pos(p, blockIdx.x, tiles_x, SP).h;
+      pre = 1;
+      for (int t = 0; t < pre; ++t) {
+        uint8_t* sK = smem + C::OFF_KV + (2 * t) * C::KV_BYTES;
+        uint8_t* sV = sK + C::KV_BYTES;
+        const uint32_t fb = smem_u32(&kv_full[t]);
+        mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+        for (int a = 0; a < C::NATOM; ++a) {
+          tma_load_3d(smem_u32(sK + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, t * 128);
+          tma_load_3d(smem_u32(sK + C::KH_BYTES + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, t * 128 + 64);
+          tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h0, t * 128);
+        }
+        issued_tma = t;
+      }
+    }
+    if (p.n_early) {
+      pdl_wait();
+      pdl_trigger();  // (as every thread does at the top without n_early)
+    }
     for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
       AUnit w = attn_unit_pos(p, u, tiles_x, SP);
       const int h = w.h;
@@ -353,9 +388,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         }
         const int jblk = w.jb + t;
         const int st = gt % C::KV_STAGES;
+        const bool early_blk = gt < pre;  // issued before the wait (thread 0 only)
         if (lt == 0)
-          okflag[st] = mbar_wait(smem_u32(&kv_empty[st]), ((gt / C::KV_STAGES) & 1) ^ 1, abort_flag, p.status, kWaitLimitNs,
-                               kSiteAttnKvEmpty) ? 1 : 0;
+          okflag[st] = early_blk || mbar_wait(smem_u32(&kv_empty[st]), ((gt / C::KV_STAGES) & 1) ^ 1, abort_flag, p.status,
+                                              kWaitLimitNs, kSiteAttnKvEmpty) ? 1 : 0;
         named_bar_sync(1, kLoaders);
         if (!okflag[st]) {
           ok = false;
@@ -367,7 +403,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
         // one page or not whole (pool tokens past P may hold anything)
         const bool use_tma = jblk < NBP && (!p.table || (p.page_tma && (jblk + 1) * 128 <= p.P));
         if (use_tma) {
-          if (lt == 0) {
+          if (lt == 0 && !early_blk) {
             int z = jblk * 128;
             if (p.table) {
               const int page = p.table[(jblk * 128) / p.page_size];
