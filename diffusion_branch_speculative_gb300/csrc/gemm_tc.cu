@@ -1073,18 +1073,45 @@ __global__ void __launch_bounds__(256, 2) splitk_reduce_kernel(const __grid_cons
 // with s = src[r], one thread per (row, 8 columns) and four items' loads in
 // flight, so a source with many folded rows does not serialise their loads.
 // The next kernel may launch only after the barrier (every CTA of this grid
-// is resident by then).
+// is resident by then).  With n_early, a thread's first two pass-2 items
+// have their sources and input rows read before the wait: src comes from
+// the gate/pack kernel and H_in is the layer's input, neither written by the
+// GEMM, so after the barrier only the source's output is left to read.
 constexpr int kFinThreads = 512;
 template <int BN>
 __global__ void __launch_bounds__(kFinThreads, 1) down_finish_kernel(const __grid_constant__ GemmParams p) {
   __shared__ volatile int s_flag;
   const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
-  pdl_wait();
-  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
-  const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   const int groups = (p.Nt * BN) / 8;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long total2 = static_cast<long long>(p.Mcap) * groups;
+  constexpr int PRE = 2;
+  int pr[PRE], pc[PRE], ps[PRE];
+  uint4 phr[PRE], phs[PRE];
+  const bool pre = p.n_early != 0;
+#pragma unroll
+  for (int q = 0; q < PRE; ++q) {
+    const long long idx = tid + q * nthr;
+    pr[q] = -1;
+    ps[q] = -1;
+    pc[q] = 0;
+    if (pre && idx < total2) {
+      pr[q] = static_cast<int>(idx / groups);
+      pc[q] = static_cast<int>(idx - static_cast<long long>(pr[q]) * groups) * 8;
+      ps[q] = __ldg(p.fill_src + pr[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < PRE; ++q) {
+    if (pr[q] >= 0 && ps[q] != pr[q] && ps[q] >= 0 && ps[q] < p.Mcap) {
+      phr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(pr[q]) * p.ldy + pc[q]));
+      phs[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(ps[q]) * p.ldy + pc[q]));
+    }
+  }
+  pdl_wait();
+  const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
+  const Sched sc = get_sched(p.sched, n, p.Nt, p.K / kBK);
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.Y);
   // ---- pass 1: split tiles
   if (sc.S > 1 || sc.St > 1) {
@@ -1133,27 +1160,35 @@ __global__ void __launch_bounds__(kFinThreads, 1) down_finish_kernel(const __gri
   if (!grid_barrier(p.fill_bar, p.status, &s_flag)) return;
   pdl_trigger();
   // ---- pass 2: every folded row from its source's stored output
-  const long long total2 = static_cast<long long>(p.Mcap) * groups;
   for (long long idx0 = tid; idx0 < total2; idx0 += 4 * nthr) {
+    const bool first = pre && idx0 == tid;  // items 0 and 1 read before the wait
     int r[4], c[4], s[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const long long idx = idx0 + q * nthr;
       r[q] = -1;
-      if (idx < total2) {
+      if (q < PRE && first) {
+        r[q] = pr[q];
+        c[q] = pc[q];
+      } else if (idx < total2) {
         r[q] = static_cast<int>(idx / groups);
         c[q] = static_cast<int>(idx - static_cast<long long>(r[q]) * groups) * 8;
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s[q] = r[q] >= 0 ? __ldg(p.fill_src + r[q]) : -1;
+    for (int q = 0; q < 4; ++q) s[q] = q < PRE && first ? ps[q] : r[q] >= 0 ? __ldg(p.fill_src + r[q]) : -1;
     uint4 ys[4], hr[4], hs[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if (r[q] >= 0 && s[q] != r[q] && s[q] >= 0 && s[q] < p.Mcap) {
         ys[q] = __ldcg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(s[q]) * p.ldy + c[q]));
-        hr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(r[q]) * p.ldy + c[q]));
-        hs[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(s[q]) * p.ldy + c[q]));
+        if (q < PRE && first) {
+          hr[q] = phr[q];
+          hs[q] = phs[q];
+        } else {
+          hr[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(r[q]) * p.ldy + c[q]));
+          hs[q] = __ldg(reinterpret_cast<const uint4*>(p.hin + static_cast<size_t>(s[q]) * p.ldy + c[q]));
+        }
       }
     }
 #pragma unroll
@@ -1179,9 +1214,12 @@ __global__ void __launch_bounds__(kFinThreads, 1) down_finish_kernel(const __gri
 // residual row H[row_idx[k]] and writes A[k] (bf16); when it was not, A[k] is
 // already written by the GEMM epilogue.  Either way the block then
 // RMS-normalises the bf16 row: X2[k] = A[k] * g2 / sqrt(mean(A[k]^2) + eps).
-// The gains are weights, read before the wait on the GEMM; after it, the
-// packed-row count and the row index come in one round trip, the residual row
-// and the first four splits of every partial in the next.  At most 64
+// The gains are weights, read before the wait on the GEMM.  With n_early the
+// packed-row count and the row index come through L2 before the wait too,
+// and so does the residual row (the layer's input, which the GEMM does not
+// write); after the wait only the partials' round trip is left.  Without it
+// n and the row index come in one round trip after the wait, the residual
+// row and the first four splits of every partial in the next.  At most 64
 // registers a thread, so that a block fits on an SM beside the GEMM CTA it
 // follows and starts early under programmatic launch.
 template <int BN, int GPT>
@@ -1202,6 +1240,17 @@ __global__ void __launch_bounds__(512, 2) outproj_finish_kernel(const __grid_con
   // complete (n_early); else after the wait
   const int n_pre = p.n_early && p.n_dev ? __ldcg(p.n_dev) : 0;
   const int r_pre = p.n_early ? __ldcg(p.row_idx + k) : 0;
+  // the residual row, early (row_idx[k] is a row of H only for k < n)
+  const bool rv_early = p.n_early && k < min(max(n_pre, 0), p.Mcap);
+  uint4 rv_pre[GPT];
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int gi = threadIdx.x + nthr * j;
+    rv_pre[j] = rv_early && gi < groups
+                    ? __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
+                                                           static_cast<size_t>(r_pre) * p.ldr + gi * 8))
+                    : make_uint4(0, 0, 0, 0);
+  }
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
@@ -1220,8 +1269,9 @@ __global__ void __launch_bounds__(512, 2) outproj_finish_kernel(const __grid_con
     const int nt = c / BN, tc = c - nt * BN;
     int S = 1, slot0 = 0;
     if (tile_split(sc, m, nt, p.Nt, S, slot0)) {
-      const uint4 rv = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
-                                                            static_cast<size_t>(r) * p.ldr + c));
+      const uint4 rv = rv_early ? rv_pre[j]
+                                : __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.resid) +
+                                                                       static_cast<size_t>(r) * p.ldr + c));
       const float* base = p.partial + static_cast<size_t>(slot0) * kBM * BN + static_cast<size_t>(row) * BN + tc;
       float acc[8];
 #pragma unroll
