@@ -496,6 +496,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The FFN GEMMs' weight tiles: the first unit's first kPreB stages of B go
+  // out before the wait when n is known early (the weights are an input; A,
+  // the previous kernel's output, follows after the wait on the same
+  // barriers).  Their predecessors (the output-projection finish, the gate/up
+  // GEMM's tail) leave DRAM time to spare.
+  constexpr int kPreB = 2;
+  int preb = 0;
+  auto b_coords = [&](const Unit& w, const CUtensorMap*& mlo, const CUtensorMap*& mhi, int& ylo, int& yhi) {
+    if constexpr (EPI == EPI_SWIGLU) {
+      mlo = &p.mapB[0];
+      mhi = &p.mapB[1];
+      ylo = yhi = w.nt * (BN / 2);
+    } else {
+      const int c0 = w.nt * BN;
+      int j = 0;
+      while (j + 1 < p.nb && c0 >= p.col0[j + 1]) ++j;
+      mlo = mhi = &p.mapB[j];
+      ylo = c0 - p.col0[j];
+      yhi = ylo + BN / 2;
+    }
+  };
+  if constexpr (!CL && (EPI == EPI_SWIGLU || EPI == EPI_RESID_SCATTER)) {
+    if (p.n_early && warp == 0 && lane == 0) {
+      const int n0 = p.n_dev ? min(max(n_pre, 0), p.Mcap) : p.Mcap;
+      const Sched sc0 = get_sched(p.sched, n0, p.Nt, p.K / kBK);
+      if (static_cast<int>(blockIdx.x) < sc0.U) {
+        const Unit w = decode_plain(static_cast<int>(blockIdx.x), sc0, p.Nt);
+        const CUtensorMap* mlo;
+        const CUtensorMap* mhi;
+        int ylo, yhi;
+        b_coords(w, mlo, mhi, ylo, yhi);
+        preb = min(min(kPreB, C::STAGES), w.kb1 - w.kb0);
+        for (int it = 0; it < preb; ++it) {  // fresh stages: nothing to wait for
+          uint8_t* sb = smem + it * C::STAGE_BYTES + C::A_BYTES;
+          const uint32_t fb = smem_u32(&full[it]);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sb), mlo, fb, (w.kb0 + it) * kBK, ylo);
+          tma_load_2d(smem_u32(sb + (BN / 2) * 128), mhi, fb, (w.kb0 + it) * kBK, yhi);
+        }
+      }
+    }
+  }
   pdl_wait();
   pdl_trigger();
   const int n = p.n_dev ? min(max(p.n_early ? n_pre : p.n_dev[0], 0), p.Mcap) : p.Mcap;
@@ -530,28 +572,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const CUtensorMap* mlo;
         const CUtensorMap* mhi;
         int ylo, yhi;
-        if constexpr (EPI == EPI_SWIGLU) {
-          mlo = &p.mapB[0];
-          mhi = &p.mapB[1];
-          ylo = yhi = w.nt * (BN / 2);
-        } else {
-          const int c0 = w.nt * BN;
-          int j = 0;
-          while (j + 1 < p.nb && c0 >= p.col0[j + 1]) ++j;
-          mlo = mhi = &p.mapB[j];
-          ylo = c0 - p.col0[j];
-          yhi = ylo + BN / 2;
-        }
+        b_coords(w, mlo, mhi, ylo, yhi);
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int st = it % C::STAGES;
+          uint8_t* sa = smem + st * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          const uint32_t fb = smem_u32(&full[st]);
+          if (static_cast<int>(it) < preb) {  // B already on its way (before the wait)
+            tma_load_2d(smem_u32(sa), &p.mapA, fb, kb * kBK, w.m * kBM);
+            continue;
+          }
           const uint32_t ph = (it / C::STAGES) & 1;
           if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1, abort_flag, p.status, kWaitLimitNs, kSiteGemmEmpty)) {
             ok = false;
             break;
           }
-          uint8_t* sa = smem + st * C::STAGE_BYTES;
-          uint8_t* sb = sa + C::A_BYTES;
-          const uint32_t fb = smem_u32(&full[st]);
           mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           tma_load_2d(smem_u32(sa), &p.mapA, fb, kb * kBK, w.m * kBM);
           tma_load_2d(smem_u32(sb), mlo, fb, kb * kBK, ylo);
