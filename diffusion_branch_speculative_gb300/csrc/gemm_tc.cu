@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // the previous kernel's output, follows after the wait on the same
   // barriers).  Their predecessors (the output-projection finish, the gate/up
   // GEMM's tail) leave DRAM time to spare.
-  constexpr int kPreB = 2;
+  constexpr int kPreB = 4;
   int preb = 0;
   auto b_coords = [&](const Unit& w, const CUtensorMap*& mlo, const CUtensorMap*& mhi, int& ylo, int& yhi) {
     if constexpr (EPI == EPI_SWIGLU) {
