@@ -35,6 +35,15 @@
  *     throughout (CUDA-core fp32 FMA for the projections and attention, the
  *     tiny fp32 configuration).  All activations, weights and the prefix view
  *     use that type.
+ *   - Kernels are launched with programmatic dependent launch, so each may
+ *     start before the previous kernel in the stream has ended.  Inputs that
+ *     no kernel of the call writes (weights, gains, the draft graph, the
+ *     prefix view) may then be read before a kernel waits for its
+ *     predecessor.  Everything a call reads must be complete in stream order
+ *     before the call.  A caller's kernel that runs just before a call and
+ *     releases its dependents early (griddepcontrol.launch_dependents) must
+ *     not write those inputs after doing so.  Ordinary kernels, copies and
+ *     memsets are complete before the call's first kernel starts.
  *   - Matrices are row-major.  Weights use the [out, in] layout.
  *   - Alignment: every pointer is 16-byte aligned; the prefix view strides are
  *     multiples of 8 elements (SPECFOLD_EALIGN otherwise).
