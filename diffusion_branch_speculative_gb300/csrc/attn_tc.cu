@@ -326,22 +326,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const __grid_cons
     // empty) goes out before the wait for the previous kernel; its other
     // blocks follow the queries (when that kernel is long done, the queries
     // should not queue behind all three)
-    int pre = 0;
+    int pre = 0;  // blocks issued before the wait (thread 0 only)
     if (p.n_early && lt == 0 && SP == 1 && NBP > 0 && !p.table) {
       const int h0 = attn_unit_pos(p, blockIdx.x, tiles_x, SP).h;
-      pre = 1;
-      for (int t = 0; t < pre; ++t) {
-        uint8_t* sK = smem + C::OFF_KV + (2 * t) * C::KV_BYTES;
-        uint8_t* sV = sK + C::KV_BYTES;
-        const uint32_t fb = smem_u32(&kv_full[t]);
-        mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
-        for (int a = 0; a < C::NATOM; ++a) {
-          tma_load_3d(smem_u32(sK + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, t * 128);
-          tma_load_3d(smem_u32(sK + C::KH_BYTES + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, t * 128 + 64);
-          tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h0, t * 128);
-        }
-        issued_tma = t;
+      uint8_t* sK = smem + C::OFF_KV;  // stage 0, block 0
+      uint8_t* sV = sK + C::KV_BYTES;
+      const uint32_t fb = smem_u32(&kv_full[0]);
+      mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+      for (int a = 0; a < C::NATOM; ++a) {
+        tma_load_3d(smem_u32(sK + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, 0);
+        tma_load_3d(smem_u32(sK + C::KH_BYTES + a * C::KH_ATOM), &p.mapK, fb, a * 64, h0, 64);
+        tma_load_3d(smem_u32(sV + a * kAtom), &p.mapV, fb, a * 64, h0, 0);
       }
+      issued_tma = 0;
+      pre = 1;
     }
     if (p.n_early) {
       pdl_wait();
